@@ -1,0 +1,286 @@
+/*
+ * oracle.c -- plain, slow fp64 CPU reference for the fused MoE expert layer
+ * with per-token multi-LoRA adapters.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call, link or
+ * load this file or the library built from it; only the tests, the smoke
+ * check and the benchmark's CPU-baseline leg do.  It shares no code, header,
+ * table or helper with the CUDA library: every step below is written out from
+ * the definitions on the source pages, with no blocking, fusion or
+ * reordering beyond what those definitions state.
+ *
+ * Sources (pages this implements):
+ *  [P1] "Amazon SageMaker 및 Amazon Bedrock에서 vLLM을 활용한 MoE 모델 Multi-LoRA
+ *       서빙 최적화" (aitrends.kr), section "섹션별 상세" paragraph 1 (the LoRA
+ *       shrink and expand are folded into each expert's projection) and
+ *       section "이미지 분석 / Diagram" (an adapter path on both the gate_up
+ *       and the down projection).
+ *  [P3] "[vllm] vLLM ROCm 환경에서 Shared-Expert Fusion을 통한 MoE 추론 성능
+ *       최적화" (blog.secrett2633.cloud), section "코드 분석" items 1 (shared
+ *       experts appended after the routed top-k slots, ids starting at the
+ *       routed expert count, weight shared_expert_weight) and 2 (align runs
+ *       over w13.shape[0] experts), and section "교훈" item 2 (the shared
+ *       weight 1/routed_scaling_factor keeps the fused form equal to the
+ *       separate shared MLP).
+ *
+ * Readings where the pages are silent (each is listed in the design notes):
+ *  - activation: plain SwiGLU silu(g)*u, w13 rows [0,I) are gate, [I,2I) up;
+ *  - one LoRA pair per (adapter, expert) on gate_up (A13 [r,H], B13 [2I,r])
+ *    and on down (A2 [r,I], B2 [H,r]); the delta s*B(Ax) is added to the
+ *    projection output before SwiGLU / before the combine;
+ *  - top-k order: descending key, ties to the lower expert id;
+ *  - softmax routing selects on the raw logits (monotone in the softmax) and
+ *    weights by the softmax of the selected logits when renormalising, else
+ *    by the full softmax;
+ *  - sigmoid+bias routing selects on sigmoid(l)+b, computed in fp32 (the
+ *    precision the GPU takes the same integer decision in), and weights by
+ *    sigmoid(l) (bias-free), renormalised over the routed slots only;
+ *  - align: experts in ascending id, slots of one expert in ascending flat
+ *    slot index f = m*K' + k, each expert's list padded with the sentinel
+ *    M*K' to a multiple of block_m; the tail of sorted_ids beyond the padded
+ *    total is the sentinel and the tail of expert_ids is -1;
+ *  - token_lora_idx outside [-1, L) is treated as -1 (no adapter).
+ *
+ * Bf16 tensors arrive as raw 16-bit patterns and are widened exactly to
+ * double.  All arithmetic is double precision except the fp32 routing key.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_OK 0
+#define ORACLE_BAD_ARG 1
+
+static double bf16_bits_to_double(uint16_t bits) {
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* Is candidate (key_a, id_a) ranked before (key_b, id_b)?  Descending key,
+ * ties to the lower id. */
+static int ranks_before_f(float key_a, int id_a, float key_b, int id_b) {
+    if (key_a != key_b) return key_a > key_b;
+    return id_a < id_b;
+}
+
+/*
+ * Top-k routing with forced shared-expert slots ([P3] "코드 분석" 1).
+ * Output per token: K' = top_k + n_shared ids and weights.  Routed slots
+ * k < top_k hold the selected experts in rank order; shared slot top_k + j
+ * holds expert E + j with weight 1/routed_scaling_factor ([P3] "교훈" 2).
+ * Weights are returned in double.
+ */
+int oracle_moe_route(const float* logits, const float* bias, int M, int E,
+                     int top_k, int scoring, int renormalize, int n_shared,
+                     float routed_scaling_factor, int32_t* topk_ids,
+                     double* topk_w) {
+    if (M < 0 || E <= 0 || top_k <= 0 || top_k > E || n_shared < 0) return ORACLE_BAD_ARG;
+    if (scoring != 0 && scoring != 1) return ORACLE_BAD_ARG;
+    if (n_shared > 0 && !(routed_scaling_factor > 0.0f)) return ORACLE_BAD_ARG;
+    const int KT = top_k + n_shared;
+    float* key = (float*)malloc(sizeof(float) * (size_t)E);
+    int* taken = (int*)malloc(sizeof(int) * (size_t)E);
+    if (!key || !taken) { free(key); free(taken); return ORACLE_BAD_ARG; }
+    for (int m = 0; m < M; ++m) {
+        const float* l = logits + (size_t)m * E;
+        for (int e = 0; e < E; ++e) {
+            if (scoring == 0) {
+                key[e] = l[e];
+            } else {
+                /* the routing decision is an integer taken in fp32 */
+                float sg = 1.0f / (1.0f + expf(-l[e]));
+                key[e] = sg + (bias ? bias[e] : 0.0f);
+            }
+            taken[e] = 0;
+        }
+        int32_t* ids = topk_ids + (size_t)m * KT;
+        double* w = topk_w + (size_t)m * KT;
+        /* selection: k passes, each taking the best remaining candidate */
+        for (int k = 0; k < top_k; ++k) {
+            int best = -1;
+            for (int e = 0; e < E; ++e) {
+                if (taken[e]) continue;
+                if (best < 0 || ranks_before_f(key[e], e, key[best], best)) best = e;
+            }
+            taken[best] = 1;
+            ids[k] = best;
+        }
+        if (scoring == 0) {
+            double lmax = -INFINITY;
+            for (int e = 0; e < E; ++e) if ((double)l[e] > lmax) lmax = (double)l[e];
+            double denom = 0.0;
+            if (renormalize) {
+                for (int k = 0; k < top_k; ++k) denom += exp((double)l[ids[k]] - lmax);
+            } else {
+                for (int e = 0; e < E; ++e) denom += exp((double)l[e] - lmax);
+            }
+            for (int k = 0; k < top_k; ++k) w[k] = exp((double)l[ids[k]] - lmax) / denom;
+        } else {
+            double sum = 0.0;
+            for (int k = 0; k < top_k; ++k) {
+                w[k] = 1.0 / (1.0 + exp(-(double)l[ids[k]]));
+                sum += w[k];
+            }
+            if (renormalize) for (int k = 0; k < top_k; ++k) w[k] /= sum;
+        }
+        for (int j = 0; j < n_shared; ++j) {
+            ids[top_k + j] = E + j;
+            w[top_k + j] = 1.0 / (double)routed_scaling_factor;
+        }
+    }
+    free(key);
+    free(taken);
+    return ORACLE_OK;
+}
+
+/* Upper bound of the padded length: every non-empty expert adds at most
+ * block_m - 1 sentinels, and there are at most min(E_tot, M*K') of them. */
+long oracle_moe_align_max_padded(int M, int K_total, int E_tot, int block_m) {
+    long slots = (long)M * K_total;
+    long nonempty = slots < E_tot ? slots : E_tot;
+    long bound = slots + nonempty * (block_m - 1);
+    return (bound + block_m - 1) / block_m * block_m;
+}
+
+/*
+ * Sort and pad slots by expert ([P3] "코드 분석" 2: over E_tot =
+ * w13.shape[0] experts, shared ones included).
+ */
+int oracle_moe_align(const int32_t* topk_ids, int M, int K_total, int E_tot,
+                     int block_m, int32_t* sorted_ids, int32_t* expert_ids,
+                     int32_t* num_post_padded) {
+    if (M < 0 || K_total <= 0 || E_tot <= 0 || block_m <= 0) return ORACLE_BAD_ARG;
+    const long slots = (long)M * K_total;
+    const long max_padded = oracle_moe_align_max_padded(M, K_total, E_tot, block_m);
+    const int32_t sentinel = (int32_t)slots;
+    long pos = 0;
+    for (int e = 0; e < E_tot; ++e) {
+        long start = pos;
+        for (long f = 0; f < slots; ++f)
+            if (topk_ids[f] == e) sorted_ids[pos++] = (int32_t)f;
+        while ((pos - start) % block_m != 0) sorted_ids[pos++] = sentinel;
+        for (long b = start / block_m; b < pos / block_m; ++b) expert_ids[b] = e;
+    }
+    *num_post_padded = (int32_t)pos;
+    for (long p = pos; p < max_padded; ++p) sorted_ids[p] = sentinel;
+    for (long b = pos / block_m; b < max_padded / block_m; ++b) expert_ids[b] = -1;
+    return ORACLE_OK;
+}
+
+static double silu(double z) { return z / (1.0 + exp(-z)); }
+
+/*
+ * One expert applied to one token, with the token's adapter folded into both
+ * projections ([P1] "섹션별 상세" 1, "Diagram").  Writes d[0..H).
+ * scratch must hold 2I + I + 2r doubles.
+ */
+static void expert_with_lora(const double* xm, const uint16_t* w13, const uint16_t* w2,
+                             const uint16_t* A13, const uint16_t* B13,
+                             const uint16_t* A2, const uint16_t* B2,
+                             int e, int l, int H, int I, int E_tot, int r,
+                             double scaling, double* scratch, double* d) {
+    double* h = scratch;          /* [2I]: gate then up */
+    double* a = h + 2 * (size_t)I; /* [I]  */
+    double* t = a + I;            /* [r]  */
+    double* t2 = t + r;           /* [r]  */
+    const uint16_t* W13 = w13 + (size_t)e * 2 * I * H;
+    for (int j = 0; j < 2 * I; ++j) {
+        double s = 0.0;
+        for (int i = 0; i < H; ++i) s += xm[i] * bf16_bits_to_double(W13[(size_t)j * H + i]);
+        h[j] = s;
+    }
+    if (l >= 0) {
+        const uint16_t* A = A13 + ((size_t)l * E_tot + e) * r * H;
+        const uint16_t* B = B13 + ((size_t)l * E_tot + e) * 2 * I * r;
+        for (int q = 0; q < r; ++q) {
+            double s = 0.0;
+            for (int i = 0; i < H; ++i) s += xm[i] * bf16_bits_to_double(A[(size_t)q * H + i]);
+            t[q] = s;
+        }
+        for (int j = 0; j < 2 * I; ++j) {
+            double s = 0.0;
+            for (int q = 0; q < r; ++q) s += t[q] * bf16_bits_to_double(B[(size_t)j * r + q]);
+            h[j] += scaling * s;
+        }
+    }
+    for (int j = 0; j < I; ++j) a[j] = silu(h[j]) * h[I + j];
+    const uint16_t* W2 = w2 + (size_t)e * H * I;
+    for (int o = 0; o < H; ++o) {
+        double s = 0.0;
+        for (int j = 0; j < I; ++j) s += a[j] * bf16_bits_to_double(W2[(size_t)o * I + j]);
+        d[o] = s;
+    }
+    if (l >= 0) {
+        const uint16_t* A = A2 + ((size_t)l * E_tot + e) * r * I;
+        const uint16_t* B = B2 + ((size_t)l * E_tot + e) * H * r;
+        for (int q = 0; q < r; ++q) {
+            double s = 0.0;
+            for (int j = 0; j < I; ++j) s += a[j] * bf16_bits_to_double(A[(size_t)q * I + j]);
+            t2[q] = s;
+        }
+        for (int o = 0; o < H; ++o) {
+            double s = 0.0;
+            for (int q = 0; q < r; ++q) s += t2[q] * bf16_bits_to_double(B[(size_t)o * r + q]);
+            d[o] += scaling * s;
+        }
+    }
+}
+
+/*
+ * The layer: y[m] = out_scale * sum_k topk_w[m,k] * Expert_{topk_ids[m,k]}(x[m])
+ * with token m's adapter l = token_lora_idx[m] applied inside every expert
+ * (l = -1: none).  A LoRA pointer set of NULL (or L == 0) means no adapters.
+ * y is written in double, [M, H].
+ */
+int oracle_moe_forward(const uint16_t* x, const uint16_t* w13, const uint16_t* w2,
+                       const uint16_t* A13, const uint16_t* B13,
+                       const uint16_t* A2, const uint16_t* B2,
+                       const int32_t* token_lora_idx, const int32_t* topk_ids,
+                       const float* topk_w, int M, int H, int I, int E_tot,
+                       int K_total, int L, int r, float scaling,
+                       float out_scale, double* y) {
+    if (M < 0 || H <= 0 || I <= 0 || E_tot <= 0 || K_total <= 0 || L < 0 || r < 0)
+        return ORACLE_BAD_ARG;
+    const int has_lora = A13 && B13 && A2 && B2 && token_lora_idx && L > 0 && r > 0;
+    int bad = 0;
+#pragma omp parallel
+    {
+        double* xm = (double*)malloc(sizeof(double) * (size_t)H);
+        double* d = (double*)malloc(sizeof(double) * (size_t)H);
+        double* acc = (double*)malloc(sizeof(double) * (size_t)H);
+        double* scratch = (double*)malloc(sizeof(double) * (3 * (size_t)I + 2 * (size_t)(r > 0 ? r : 1)));
+        if (!xm || !d || !acc || !scratch) {
+#pragma omp atomic write
+            bad = 1;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int m = 0; m < M; ++m) {
+                int l = has_lora ? token_lora_idx[m] : -1;
+                if (l < -1 || l >= L) l = -1;
+                for (int i = 0; i < H; ++i) xm[i] = bf16_bits_to_double(x[(size_t)m * H + i]);
+                for (int o = 0; o < H; ++o) acc[o] = 0.0;
+                for (int k = 0; k < K_total; ++k) {
+                    int e = topk_ids[(size_t)m * K_total + k];
+                    double w = (double)topk_w[(size_t)m * K_total + k];
+                    if (e < 0 || e >= E_tot) {
+#pragma omp atomic write
+                        bad = 1;
+                        continue;
+                    }
+                    expert_with_lora(xm, w13, w2, A13, B13, A2, B2, e, l, H, I, E_tot, r,
+                                     (double)scaling, scratch, d);
+                    for (int o = 0; o < H; ++o) acc[o] += w * d[o];
+                }
+                for (int o = 0; o < H; ++o) y[(size_t)m * H + o] = (double)out_scale * acc[o];
+            }
+        }
+        free(xm);
+        free(d);
+        free(acc);
+        free(scratch);
+    }
+    return bad ? ORACLE_BAD_ARG : ORACLE_OK;
+}

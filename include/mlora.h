@@ -1,0 +1,187 @@
+/*
+ * mlora.h -- C ABI of libmlora.so: the fused Mixture-of-Experts expert layer
+ * with per-token multi-LoRA adapters, as hand-written CUDA kernels for
+ * sm_103a (GB300).
+ *
+ * The operation (pages cited by title and section):
+ *  - "Amazon SageMaker 및 Amazon Bedrock에서 vLLM을 활용한 MoE 모델 Multi-LoRA
+ *    서빙 최적화", section "섹션별 상세" paragraph 1: every token carries its own
+ *    adapter; the adapter's LoRA shrink (x A^T) and expand ((.) B^T) are
+ *    folded into each routed expert's projections; section "이미지 분석 /
+ *    Diagram": an adapter path on both the gate_up and the down projection;
+ *    paragraph 2: layers without adapters exit at once, and the layer runs
+ *    under CUDA graphs.
+ *  - "[vllm] vLLM ROCm 환경에서 Shared-Expert Fusion을 통한 MoE 추론 성능 최적화",
+ *    section "코드 분석" item 1: shared experts are appended after the routed
+ *    top-k slots with ids E..E+n_shared-1; item 2: the sort-and-pad (align)
+ *    runs over E_tot = w13.shape[0] experts; section "교훈" item 2: the
+ *    shared slot weight 1/routed_scaling_factor keeps the fused layer equal
+ *    to the separate shared MLP once the sum is scaled by that factor.
+ *
+ * Conventions for every entry point:
+ *  - Tensor pointers are DEVICE pointers owned by the caller: contiguous,
+ *    row-major, 16-byte aligned.  The library never allocates or frees
+ *    device memory and never synchronises the stream, except
+ *    mlora_moe_read_status, which waits for the stream by design.
+ *  - `stream` is a cudaStream_t passed as void*; NULL is the legacy default
+ *    stream.  All work is enqueued on it, so every call can be captured into
+ *    a CUDA graph (mlora_moe_read_status excepted).
+ *  - bf16 tensors are passed as void*.
+ *  - Arguments are validated on the host before anything is enqueued; a
+ *    failed check returns a non-zero status and enqueues nothing.  Values
+ *    that live in device memory (expert ids, adapter ids) are checked on the
+ *    device: a bad value is skipped (expert id) or treated as "no adapter"
+ *    (adapter id) and recorded in the device status word that
+ *    mlora_moe_read_status returns.  Kernels never trap.
+ *  - Errors reported by the CUDA runtime at launch map to MLORA_ERR_CUDA;
+ *    asynchronous faults surface at the caller's next synchronisation.
+ */
+#ifndef MLORA_H
+#define MLORA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum mlora_status {
+    MLORA_OK = 0,
+    MLORA_ERR_INVALID_ARG = 1, /* NULL or misaligned pointer, bad enum value */
+    MLORA_ERR_SHAPE = 2,       /* sizes out of range or inconsistent */
+    MLORA_ERR_UNSUPPORTED = 3, /* valid in principle, not built (e.g. rank > 64) */
+    MLORA_ERR_WORKSPACE = 4,   /* workspace NULL, misaligned or too small */
+    MLORA_ERR_CUDA = 5         /* the CUDA runtime or driver reported an error */
+} mlora_status;
+
+enum { MLORA_SCORE_SOFTMAX = 0, MLORA_SCORE_SIGMOID_BIAS = 1 };
+
+/* Bits of the device status word (mlora_moe_read_status). */
+#define MLORA_DEV_TIMEOUT 1u        /* a pipeline wait gave up after ~2 s; outputs invalid */
+#define MLORA_DEV_BAD_EXPERT_ID 2u  /* a topk id was outside [0, E_tot); that slot was dropped */
+#define MLORA_DEV_BAD_LORA_IDX 4u   /* a token_lora_idx was outside [-1, L); treated as -1 */
+
+#define MLORA_MAX_EXPERTS 1024 /* E (routing) and E_tot (align, forward) */
+#define MLORA_MAX_TOPK 64      /* K' = top_k + n_shared */
+#define MLORA_MAX_RANK 64      /* LoRA rank: a multiple of 8 in [8, 64] */
+#define MLORA_MAX_ALIGN_BLOCK 1024
+#define MLORA_FORWARD_BLOCK_M 128 /* block_m used inside mlora_moe_forward */
+
+/*
+ * Top-k routing with optional forced shared-expert slots.
+ *
+ * logits  [M, E] fp32.  bias [E] fp32, read only for SIGMOID_BIAS (may be
+ * NULL there: zero bias).  Writes, for K' = top_k + n_shared,
+ * topk_ids [M, K'] int32 and topk_w [M, K'] fp32:
+ *  - SOFTMAX: the top_k experts by logit (the softmax is monotone), in
+ *    descending order, ties to the lower id; weights are the softmax over the
+ *    selected logits when renormalize != 0, else the full softmax's entries.
+ *  - SIGMOID_BIAS: the top_k experts by sigmoid(l) + bias, computed in fp32,
+ *    same order and tie rule; weights sigmoid(l) (no bias), divided by their
+ *    sum over the routed slots when renormalize != 0.
+ *  - slot top_k + j (j < n_shared) gets id E + j and weight
+ *    1 / routed_scaling_factor.
+ * Constraints: 0 <= M, 1 <= top_k <= E <= MLORA_MAX_EXPERTS, 0 <= n_shared,
+ * K' <= MLORA_MAX_TOPK, routed_scaling_factor > 0 when n_shared > 0.
+ * Logits must be finite.
+ */
+mlora_status mlora_moe_route(const float* logits, const float* bias, int M, int E, int top_k, int scoring,
+                             int renormalize, int n_shared, float routed_scaling_factor, int32_t* topk_ids,
+                             float* topk_w, void* stream);
+
+/*
+ * Length of the sorted_ids buffer mlora_moe_align writes:
+ * round_up(M*K' + min(E_tot, M*K') * (block_m - 1), block_m).  expert_ids
+ * holds max_padded / block_m entries.  Returns 0 for invalid arguments.
+ */
+size_t mlora_moe_align_max_padded(int M, int K_total, int E_tot, int block_m);
+
+/*
+ * Sort and pad the M*K' routed slots by expert (align).
+ *
+ * topk_ids [M, K_total] int32 with values in [0, E_tot).  Slot f = m*K'+k.
+ * Writes sorted_ids [max_padded]: experts in ascending id, each expert's
+ * slots in ascending f, padded with the sentinel M*K' to a multiple of
+ * block_m; positions past the padded total hold the sentinel.
+ * expert_ids [max_padded / block_m]: the expert of each block, -1 past the
+ * end.  num_post_padded [1]: the padded total.  Bit-exact and deterministic
+ * for a given block_m.  Slots whose id is out of range are skipped.
+ * Constraints: 0 <= M, 1 <= K_total <= MLORA_MAX_TOPK,
+ * 1 <= E_tot <= MLORA_MAX_EXPERTS, 1 <= block_m <= MLORA_MAX_ALIGN_BLOCK,
+ * M*K_total < 2^31 - E_tot*block_m.
+ */
+mlora_status mlora_moe_align(const int32_t* topk_ids, int M, int K_total, int E_tot, int block_m,
+                             int32_t* sorted_ids, int32_t* expert_ids, int32_t* num_post_padded, void* stream);
+
+/*
+ * Bytes of device workspace mlora_moe_forward needs for these sizes (with
+ * L = 0 or rank = 0 for a layer without adapters).  Returns 0 for invalid
+ * sizes.  The workspace is 256-byte aligned and caller-owned; it may be
+ * reused by consecutive calls on the same stream.
+ */
+size_t mlora_moe_workspace_size(int M, int H, int I, int E_tot, int K_total, int L, int rank);
+
+/*
+ * The layer:
+ *   y[m] = out_scale * sum_{k<K'} topk_w[m,k] * Expert_{topk_ids[m,k]}(x[m]; l_m)
+ * with l_m = token_lora_idx[m] and, for expert e,
+ *   h = x W13_e^T + s (x A13_{l,e}^T) B13_{l,e}^T        (2I values; LoRA only if l >= 0)
+ *   a = silu(h[0:I]) * h[I:2I]                           (SwiGLU; silu(z) = z / (1 + e^-z))
+ *   d = a W2_e^T + s (a A2_{l,e}^T) B2_{l,e}^T           (H values)
+ * Shapes (bf16 unless noted): x [M, H]; w13 [E_tot, 2I, H] (rows [0,I) gate,
+ * [I,2I) up); w2 [E_tot, H, I]; A13 [L, E_tot, rank, H]; B13 [L, E_tot, 2I,
+ * rank]; A2 [L, E_tot, rank, I]; B2 [L, E_tot, H, rank]; token_lora_idx [M]
+ * int32 (-1: no adapter); topk_ids [M, K'] int32 in [0, E_tot); topk_w
+ * [M, K'] fp32; y [M, H] bf16.  s = scaling.  With shared-expert fusion the
+ * route call appends the shared slots and out_scale is the routed scaling
+ * factor; n_shared is the number of those trailing slots (0 <= n_shared <
+ * K_total; only validated, the slots are ordinary experts here).
+ * If any of A13, B13, A2, B2, token_lora_idx is NULL, or L == 0, or rank ==
+ * 0, the layer runs without adapters and launches no LoRA work.  When the
+ * adapter pointers are given but no token uses an adapter, the LoRA kernels
+ * exit on the device and the result equals the adapter-free layer exactly.
+ * Constraints: H, I multiples of 8 (16-byte rows), H, I >= 8;
+ * rank in {8, 16, ..., 64}; E_tot <= MLORA_MAX_EXPERTS; K' <= MLORA_MAX_TOPK;
+ * workspace_bytes >= mlora_moe_workspace_size(...).
+ * Intermediates: the adapter shrink result is kept as bf16 (s * x A^T), the
+ * SwiGLU output as bf16, each slot's expert output as bf16, all
+ * accumulation in fp32; y is rounded to bf16 (nearest even).
+ */
+mlora_status mlora_moe_forward(const void* x, const void* w13, const void* w2, const void* A13, const void* B13,
+                               const void* A2, const void* B2, const int32_t* token_lora_idx,
+                               const int32_t* topk_ids, const float* topk_w, int M, int H, int I, int E_tot,
+                               int K_total, int L, int rank, float scaling, int n_shared, float out_scale, void* y,
+                               void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Copies the device status word of the last forward that used `workspace`
+ * (MLORA_DEV_* bits, 0 = clean) to *host_status after waiting for `stream`.
+ */
+mlora_status mlora_moe_read_status(const void* workspace, uint32_t* host_status, void* stream);
+
+/*
+ * Measurement hook.  Sets, for the calling host thread, MLORA_STAGE_EVENTS
+ * cudaEvent_t handles (passed as void*) that every later mlora_moe_forward
+ * on this thread records on its stream at the stage boundaries:
+ *   [0] before align, [1] after align, [2] after the row gather,
+ *   [3] after the gate_up shrink, [4] after the gate_up GEMM,
+ *   [5] after the down shrink, [6] after the down GEMM, [7] after combine.
+ * Stages that do not run record adjacent events.  The events are recorded
+ * with cudaEventRecordExternal, so they also become event nodes when the
+ * forward is captured into a CUDA graph.  events == NULL (or count == 0)
+ * switches the hook off.  The caller owns the events and keeps them alive
+ * while the hook is set.  Returns MLORA_ERR_INVALID_ARG when
+ * 0 < count < MLORA_STAGE_EVENTS.
+ */
+#define MLORA_STAGE_EVENTS 8
+mlora_status mlora_set_stage_events(void* const* events, int count);
+
+/* Static, human-readable name of a status code. */
+const char* mlora_status_string(mlora_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLORA_H */

@@ -1,0 +1,192 @@
+"""ctypes binding of libmlora.so (include/mlora.h), same names as the C ABI.
+
+Argument marshalling only: every step of the layer runs in the library's
+CUDA kernels.  Tensors are torch CUDA tensors (PyTorch provides device
+memory and streams); outputs not passed in are allocated with torch before
+the call.  A missing library raises at import of the first call: there is
+no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from typing import Optional
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libmlora.so")
+HEADER = os.path.join(os.path.dirname(HERE), "include", "mlora.h")
+
+MLORA_OK = 0
+STATUS_NAMES = {0: "MLORA_OK", 1: "MLORA_ERR_INVALID_ARG", 2: "MLORA_ERR_SHAPE", 3: "MLORA_ERR_UNSUPPORTED",
+                4: "MLORA_ERR_WORKSPACE", 5: "MLORA_ERR_CUDA"}
+SCORE_SOFTMAX = 0
+SCORE_SIGMOID_BIAS = 1
+DEV_TIMEOUT = 1
+DEV_BAD_EXPERT_ID = 2
+DEV_BAD_LORA_IDX = 4
+FORWARD_BLOCK_M = 128
+
+
+class MloraError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} failed: {STATUS_NAMES.get(status, status)}")
+        self.status = status
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load libmlora.so and declare its C signatures.  Raises if not built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with `python -m moe_layer_lora_gb300.build` "
+                           "(the layer has no fallback implementation)")
+    lib = ctypes.CDLL(path)
+    P, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.mlora_moe_route.argtypes = [P, P, i, i, i, i, i, i, f, P, P, P]
+    lib.mlora_moe_route.restype = i
+    lib.mlora_moe_align_max_padded.argtypes = [i, i, i, i]
+    lib.mlora_moe_align_max_padded.restype = sz
+    lib.mlora_moe_align.argtypes = [P, i, i, i, i, P, P, P, P]
+    lib.mlora_moe_align.restype = i
+    lib.mlora_moe_workspace_size.argtypes = [i] * 7
+    lib.mlora_moe_workspace_size.restype = sz
+    lib.mlora_moe_forward.argtypes = [P] * 10 + [i] * 7 + [f, i, f, P, P, sz, P]
+    lib.mlora_moe_forward.restype = i
+    lib.mlora_moe_read_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), P]
+    lib.mlora_moe_read_status.restype = i
+    lib.mlora_set_stage_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), i]
+    lib.mlora_set_stage_events.restype = i
+    lib.mlora_status_string.argtypes = [i]
+    lib.mlora_status_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def declared_functions(header: str = HEADER):
+    """Names of the functions include/mlora.h declares."""
+    with open(header) as fh:
+        text = fh.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mlora_[a-z_]+)\s*\(", text)))
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(fn: str, status: int):
+    if status != MLORA_OK:
+        raise MloraError(fn, status)
+
+
+def _need(t: torch.Tensor, dtype, name: str):
+    if not t.is_cuda or t.dtype != dtype or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor")
+
+
+def mlora_moe_route(logits: torch.Tensor, bias: Optional[torch.Tensor], top_k: int, scoring: int,
+                    renormalize: int = 1, n_shared: int = 0, routed_scaling_factor: float = 1.0,
+                    topk_ids: Optional[torch.Tensor] = None, topk_w: Optional[torch.Tensor] = None,
+                    stream=None):
+    _need(logits, torch.float32, "logits")
+    M, E = logits.shape
+    KT = top_k + n_shared
+    if topk_ids is None:
+        topk_ids = torch.empty((M, KT), dtype=torch.int32, device=logits.device)
+    if topk_w is None:
+        topk_w = torch.empty((M, KT), dtype=torch.float32, device=logits.device)
+    if bias is not None:
+        _need(bias, torch.float32, "bias")
+    st = load().mlora_moe_route(_ptr(logits), _ptr(bias), M, E, top_k, scoring, renormalize, n_shared,
+                                float(routed_scaling_factor), _ptr(topk_ids), _ptr(topk_w), _stream(stream))
+    _check("mlora_moe_route", st)
+    return topk_ids, topk_w
+
+
+def mlora_moe_align_max_padded(M: int, K_total: int, E_tot: int, block_m: int) -> int:
+    return int(load().mlora_moe_align_max_padded(M, K_total, E_tot, block_m))
+
+
+def mlora_moe_align(topk_ids: torch.Tensor, E_tot: int, block_m: int, stream=None):
+    """Returns (sorted_ids, expert_ids, num_post_padded[1]) as CUDA tensors."""
+    _need(topk_ids, torch.int32, "topk_ids")
+    M, KT = topk_ids.shape
+    mp = mlora_moe_align_max_padded(M, KT, E_tot, block_m)
+    dev = topk_ids.device
+    sorted_ids = torch.empty(mp, dtype=torch.int32, device=dev)
+    expert_ids = torch.empty(mp // block_m, dtype=torch.int32, device=dev)
+    npp = torch.empty(1, dtype=torch.int32, device=dev)
+    st = load().mlora_moe_align(_ptr(topk_ids), M, KT, E_tot, block_m, _ptr(sorted_ids), _ptr(expert_ids),
+                                _ptr(npp), _stream(stream))
+    _check("mlora_moe_align", st)
+    return sorted_ids, expert_ids, npp
+
+
+def mlora_moe_workspace_size(M: int, H: int, I: int, E_tot: int, K_total: int, L: int, rank: int) -> int:
+    return int(load().mlora_moe_workspace_size(M, H, I, E_tot, K_total, L, rank))
+
+
+def mlora_moe_forward(x, w13, w2, A13, B13, A2, B2, token_lora_idx, topk_ids, topk_w, scaling: float,
+                      n_shared: int = 0, out_scale: float = 1.0, y: Optional[torch.Tensor] = None,
+                      workspace: Optional[torch.Tensor] = None, stream=None):
+    """The fused MoE-LoRA layer; returns y [M, H] bf16 (see include/mlora.h)."""
+    _need(x, torch.bfloat16, "x")
+    M, H = x.shape
+    E_tot, twoI, _ = w13.shape
+    I = twoI // 2
+    KT = topk_ids.shape[1]
+    lora = all(t is not None for t in (A13, B13, A2, B2, token_lora_idx))
+    L, r = (A13.shape[0], A13.shape[2]) if lora else (0, 0)
+    if y is None:
+        y = torch.empty((M, H), dtype=torch.bfloat16, device=x.device)
+    need = mlora_moe_workspace_size(M, H, I, E_tot, KT, L, r)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=x.device)
+    st = load().mlora_moe_forward(
+        _ptr(x), _ptr(w13), _ptr(w2), _ptr(A13) if lora else None, _ptr(B13) if lora else None,
+        _ptr(A2) if lora else None, _ptr(B2) if lora else None, _ptr(token_lora_idx) if lora else None,
+        _ptr(topk_ids), _ptr(topk_w), M, H, I, E_tot, KT, L, r, float(scaling), int(n_shared),
+        float(out_scale), _ptr(y), _ptr(workspace), workspace.numel(), _stream(stream))
+    _check("mlora_moe_forward", st)
+    return y
+
+
+def mlora_moe_read_status(workspace: torch.Tensor, stream=None) -> int:
+    out = ctypes.c_uint32(0)
+    st = load().mlora_moe_read_status(_ptr(workspace), ctypes.byref(out), _stream(stream))
+    _check("mlora_moe_read_status", st)
+    return int(out.value)
+
+
+STAGE_EVENTS = 8
+STAGE_NAMES = ("align", "gather", "shrink_gate_up", "gate_up", "shrink_down", "down", "combine")
+
+
+def mlora_set_stage_events(events) -> None:
+    """Record the given torch.cuda.Event objects (STAGE_EVENTS of them, made
+    with enable_timing=True) at the forward's stage boundaries on this
+    thread; None switches the hook off."""
+    if events is None:
+        _check("mlora_set_stage_events", load().mlora_set_stage_events(None, 0))
+        return
+    handles = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    _check("mlora_set_stage_events", load().mlora_set_stage_events(handles, len(events)))
+
+
+def mlora_status_string(status: int) -> str:
+    return load().mlora_status_string(status).decode()

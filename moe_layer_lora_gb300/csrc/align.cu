@@ -1,0 +1,231 @@
+// align.cu -- sort and pad the routed slots by expert (moe_align).
+//
+// "[vllm] vLLM ROCm 환경에서 Shared-Expert Fusion을 통한 MoE 추론 성능 최적화",
+// section "코드 분석" item 2: the sort runs over E_tot = w13.shape[0] experts,
+// shared ones included.  Output contract (bit-exact): experts ascending,
+// each expert's slots f = m*K'+k ascending, each list padded with the
+// sentinel M*K' to a multiple of block_m, sentinel / -1 tails.
+//
+// One CTA of 1024 threads: shared-memory histogram, a block scan of the
+// padded counts, then a stable scatter in chunks of 1024 slots.  Within a
+// chunk a slot's rank is (slots of its expert in earlier warps) + (earlier
+// lanes of its warp with the same expert, from __match_any_sync); the
+// per-warp per-expert counts live in a small shared table.
+//
+// Inside the forward the same pass also records, per sorted position, the
+// token's adapter, and per block of kBlockM positions the ascending list of
+// distinct adapters, numbered globally into "shrink tiles" (block, adapter):
+// one masked LoRA tile per pair.
+#include "internal.cuh"
+
+namespace mlora {
+namespace {
+
+constexpr int kThreads = 1024;
+constexpr int kWarps = kThreads / 32;
+
+// Exclusive block scan of one int per thread; returns the exclusive prefix
+// and writes the block total to *total.  Uses 33 ints of scratch.
+__device__ int block_exclusive_scan(int v, int* scratch, int* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int inc = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, inc, off);
+        if (lane >= off) inc += n;
+    }
+    if (lane == 31) scratch[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+        int s = scratch[lane];
+        int si = s;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, si, off);
+            if (lane >= off) si += n;
+        }
+        scratch[lane] = si - s;  // exclusive warp offsets
+        if (lane == 31) scratch[32] = si;
+    }
+    __syncthreads();
+    const int excl = scratch[warp] + inc - v;
+    *total = scratch[32];
+    __syncthreads();
+    return excl;
+}
+
+template <bool kWithLora>
+__global__ void __launch_bounds__(kThreads, 1)
+    align_kernel(const int32_t* __restrict__ ids, int S, int E_tot, int BM, int max_padded,
+                 int32_t* __restrict__ sorted, int32_t* __restrict__ expert_ids, int32_t* __restrict__ n_pad_out,
+                 uint32_t* __restrict__ status, AlignExtra ex) {
+    extern __shared__ int smem_i[];
+    int* cnt = smem_i;                                               // [E_tot]
+    int* cursor = cnt + E_tot;                                       // [E_tot]
+    int* scratch = cursor + E_tot;                                   // [33]
+    uint16_t* wcnt = reinterpret_cast<uint16_t*>(scratch + 40);      // [kWarps][E_tot]
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    for (int e = tid; e < E_tot; e += kThreads) cnt[e] = 0;
+    for (int i = tid; i < kWarps * E_tot; i += kThreads) wcnt[i] = 0;
+    __syncthreads();
+
+    // 1. histogram
+    for (int f = tid; f < S; f += kThreads) {
+        const int e = ids[f];
+        if (static_cast<unsigned>(e) < static_cast<unsigned>(E_tot)) {
+            atomicAdd(&cnt[e], 1);
+        } else if (status) {
+            atomicOr(status, MLORA_DEV_BAD_EXPERT_ID);
+        }
+    }
+    __syncthreads();
+
+    // 2. exclusive scan of the padded counts (E_tot <= 1024: one expert per thread)
+    const int c = tid < E_tot ? cnt[tid] : 0;
+    const int padded = (c + BM - 1) / BM * BM;
+    int total;
+    const int start = block_exclusive_scan(padded, scratch, &total);
+    if (tid < E_tot) cursor[tid] = start;
+    if (tid == 0) *n_pad_out = total;
+
+    // 3. block -> expert map, per-expert padding, tails
+    if (tid < E_tot) {
+        for (int b = start / BM; b < (start + padded) / BM; ++b) expert_ids[b] = tid;
+        for (int p = start + c; p < start + padded; ++p) {
+            sorted[p] = S;
+            if (kWithLora) ex.lora_of[p] = -1;
+        }
+    }
+    for (int p = total + tid; p < max_padded; p += kThreads) sorted[p] = S;
+    for (int b = total / BM + tid; b < max_padded / BM; b += kThreads) expert_ids[b] = -1;
+    __syncthreads();
+
+    // 4. stable scatter, 1024 slots per pass
+    const unsigned lt_mask = (1u << lane) - 1u;
+    for (int base = 0; base < S; base += kThreads) {
+        const int f = base + tid;
+        const int e = f < S ? ids[f] : -1;
+        const bool valid = static_cast<unsigned>(e) < static_cast<unsigned>(E_tot);
+        const int key = valid ? e : -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, key);
+        const int rank = __popc(peers & lt_mask);
+        const int n_same = __popc(peers);
+        const bool leader = (peers & lt_mask) == 0;
+        if (valid && leader) wcnt[warp * E_tot + e] = static_cast<uint16_t>(n_same);
+        __syncthreads();
+        int pos = 0;
+        if (valid && leader) {
+            int pre = 0;
+            for (int w2 = 0; w2 < warp; ++w2) pre += wcnt[w2 * E_tot + e];
+            pos = cursor[e] + pre;
+        }
+        pos = __shfl_sync(0xffffffffu, pos, __ffs(peers) - 1);
+        if (valid) {
+            const int p = pos + rank;
+            sorted[p] = f;
+            if (kWithLora) {
+                int l = -1;
+                if (ex.token_lora_idx) {
+                    l = ex.token_lora_idx[f / ex.K_total];
+                    if (l < -1 || l >= ex.L) {
+                        if (status) atomicOr(status, MLORA_DEV_BAD_LORA_IDX);
+                        l = -1;
+                    }
+                }
+                ex.lora_of[p] = l;
+            }
+        }
+        __syncthreads();
+        if (valid && leader) {
+            atomicAdd(&cursor[e], n_same);
+            wcnt[warp * E_tot + e] = 0;
+        }
+        __syncthreads();
+    }
+
+    if (!kWithLora) return;
+
+    // 5. distinct adapters of each block (ascending), one warp per block
+    const int nblocks = total / BM;
+    for (int b = warp; b < nblocks; b += kWarps) {
+        int prev = -1, count = 0;
+        for (;;) {
+            int cand = 0x7fffffff;
+            for (int r = lane; r < BM; r += 32) {
+                const int l = ex.lora_of[b * BM + r];
+                if (l > prev && l < cand) cand = l;
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) cand = min(cand, __shfl_xor_sync(0xffffffffu, cand, off));
+            if (cand == 0x7fffffff) break;
+            if (lane == 0) ex.blk_lora[static_cast<long>(b) * ex.cap + count] = cand;
+            ++count;
+            prev = cand;
+        }
+        if (lane == 0) ex.blk_nad[b] = count;
+    }
+    __syncthreads();
+
+    // 6. number the (block, adapter) tiles
+    int running = 0;
+    for (int cb = 0; cb < nblocks; cb += kThreads) {
+        const int b = cb + tid;
+        const int v = b < nblocks ? ex.blk_nad[b] : 0;
+        int chunk_total;
+        const int excl = block_exclusive_scan(v, scratch, &chunk_total);
+        if (b < nblocks) {
+            const int t0 = running + excl;
+            ex.blk_lt_start[b] = t0;
+            for (int i = 0; i < v; ++i) {
+                ex.lt_block[t0 + i] = b;
+                ex.lt_lora[t0 + i] = ex.blk_lora[static_cast<long>(b) * ex.cap + i];
+            }
+        }
+        running += chunk_total;
+    }
+    if (tid == 0) *ex.lt_total = running;
+}
+
+}  // namespace
+
+long align_max_padded(long S, int E_tot, int block_m) {
+    const long nonempty = S < E_tot ? S : E_tot;
+    const long bound = S + nonempty * (block_m - 1);
+    return (bound + block_m - 1) / block_m * block_m;
+}
+
+cudaError_t launch_align(const int32_t* ids, long S, int E_tot, int block_m, long max_padded, int32_t* sorted,
+                         int32_t* expert_ids, int32_t* n_pad, uint32_t* status, const AlignExtra* extra,
+                         cudaStream_t s) {
+    const size_t smem = sizeof(int) * (2 * static_cast<size_t>(E_tot) + 40) +
+                        sizeof(uint16_t) * static_cast<size_t>(kWarps) * E_tot;
+    static unsigned long long attr_set[2] = {0ull, 0ull};  // one bit per device
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
+    if (extra) {
+        if (!(attr_set[1] & bit)) {
+            err = cudaFuncSetAttribute(align_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
+            if (err != cudaSuccess) return err;
+            attr_set[1] |= bit;
+        }
+        align_kernel<true><<<1, kThreads, smem, s>>>(ids, static_cast<int>(S), E_tot, block_m,
+                                                     static_cast<int>(max_padded), sorted, expert_ids, n_pad, status,
+                                                     *extra);
+    } else {
+        if (!(attr_set[0] & bit)) {
+            err = cudaFuncSetAttribute(align_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
+            if (err != cudaSuccess) return err;
+            attr_set[0] |= bit;
+        }
+        AlignExtra none{};
+        align_kernel<false><<<1, kThreads, smem, s>>>(ids, static_cast<int>(S), E_tot, block_m,
+                                                      static_cast<int>(max_padded), sorted, expert_ids, n_pad, status,
+                                                      none);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace mlora

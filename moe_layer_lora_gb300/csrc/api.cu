@@ -1,0 +1,367 @@
+// api.cu -- the extern "C" entry points of libmlora.so: host-side argument
+// validation, workspace layout, TMA tensor-map encoding and the launch
+// sequence of the fused MoE-LoRA layer.
+//
+// Forward, all on the caller's stream, no host synchronisation, no
+// allocation (capturable in a CUDA graph):
+//   memset(status) -> align (+ per-block adapter lists) -> gather x rows
+//   -> [shrink gate_up] -> gate_up GEMM (+ expand, SwiGLU)
+//   -> [shrink down]    -> down GEMM (+ expand) -> weighted combine
+// The bracketed shrink launches are skipped when the call carries no
+// adapters; when adapters are given but no token uses one, the shrink grid
+// finds zero tiles on the device and the GEMMs skip the expand chunks, so
+// the layer exits early without a host round trip ("Amazon SageMaker 및
+// Amazon Bedrock에서 vLLM을 활용한 MoE 모델 Multi-LoRA 서빙 최적화", section
+// "섹션별 상세" paragraph 2).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+
+#include "internal.cuh"
+
+namespace mlora {
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// bf16 tensor map with 128-byte swizzle; dims innermost first, strides in
+// bytes for dims 1..rank-1.
+bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+              const cuuint32_t* box) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank), const_cast<void*>(base), dims,
+              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t round256(size_t b) { return (b + 255) & ~size_t(255); }
+
+mlora_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MLORA_OK : MLORA_ERR_CUDA; }
+
+thread_local cudaEvent_t g_stage_events[MLORA_STAGE_EVENTS];
+thread_local bool g_stage_events_on = false;
+
+cudaError_t mark_stage(int i, cudaStream_t s) {
+    if (!g_stage_events_on) return cudaSuccess;
+    return cudaEventRecordWithFlags(g_stage_events[i], s, cudaEventRecordExternal);
+}
+
+}  // namespace
+
+int device_sm_count() {
+    static int counts[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    if (dev >= 0 && dev < 64 && counts[dev] > 0) return counts[dev];
+    int n = 1;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+    if (dev >= 0 && dev < 64) counts[dev] = n;
+    return n;
+}
+
+Sizes make_sizes(int M, int H, int I, int E_tot, int K_total, int L, int rank) {
+    Sizes z{};
+    z.M = M;
+    z.H = H;
+    z.I = I;
+    z.E_tot = E_tot;
+    z.K_total = K_total;
+    z.L = L;
+    z.rank = rank;
+    z.lora = L > 0 && rank > 0;
+    z.S = static_cast<long>(M) * K_total;
+    z.max_padded = align_max_padded(z.S, E_tot, kBlockM);
+    z.max_blocks = z.max_padded / kBlockM;
+    z.cap = z.lora ? std::min(L, kBlockM) : 0;
+    z.max_lt = z.max_blocks * z.cap;
+    return z;
+}
+
+Workspace carve_workspace(const Sizes& z, void* base) {
+    Workspace w{};
+    size_t off = 0;
+    auto take = [&](size_t bytes) -> char* {
+        const size_t o = off;
+        off += round256(bytes);
+        return base ? static_cast<char*>(base) + o : nullptr;
+    };
+    char* header = take(256);
+    w.status = reinterpret_cast<uint32_t*>(header);
+    w.n_pad = reinterpret_cast<int32_t*>(header ? header + 4 : nullptr);
+    w.lt_total = reinterpret_cast<int32_t*>(header ? header + 8 : nullptr);
+    w.sorted_ids = reinterpret_cast<int32_t*>(take(4 * z.max_padded));
+    w.expert_ids = reinterpret_cast<int32_t*>(take(4 * z.max_blocks));
+    if (z.lora) {
+        w.lora_of = reinterpret_cast<int32_t*>(take(4 * z.max_padded));
+        w.blk_nad = reinterpret_cast<int32_t*>(take(4 * z.max_blocks));
+        w.blk_lt_start = reinterpret_cast<int32_t*>(take(4 * z.max_blocks));
+        w.blk_lora = reinterpret_cast<int32_t*>(take(4 * z.max_blocks * z.cap));
+        w.lt_block = reinterpret_cast<int32_t*>(take(4 * z.max_lt));
+        w.lt_lora = reinterpret_cast<int32_t*>(take(4 * z.max_lt));
+    }
+    w.x_perm = take(2 * static_cast<size_t>(z.max_padded) * z.H);
+    w.act = take(2 * static_cast<size_t>(z.max_padded) * z.I);
+    if (z.lora) w.lora_t = take(2 * static_cast<size_t>(z.max_lt) * kBlockM * kLoraTileCols);
+    w.y_slot = take(2 * static_cast<size_t>(z.S) * z.H);
+    w.bytes = off;
+    return w;
+}
+
+}  // namespace mlora
+
+using namespace mlora;
+
+extern "C" {
+
+const char* mlora_status_string(mlora_status status) {
+    switch (status) {
+        case MLORA_OK: return "ok";
+        case MLORA_ERR_INVALID_ARG: return "invalid argument";
+        case MLORA_ERR_SHAPE: return "invalid shape";
+        case MLORA_ERR_UNSUPPORTED: return "unsupported configuration";
+        case MLORA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        case MLORA_ERR_CUDA: return "CUDA error";
+    }
+    return "unknown status";
+}
+
+mlora_status mlora_moe_route(const float* logits, const float* bias, int M, int E, int top_k, int scoring,
+                             int renormalize, int n_shared, float routed_scaling_factor, int32_t* topk_ids,
+                             float* topk_w, void* stream) {
+    if (scoring != MLORA_SCORE_SOFTMAX && scoring != MLORA_SCORE_SIGMOID_BIAS) return MLORA_ERR_INVALID_ARG;
+    if (M < 0 || E < 1 || E > MLORA_MAX_EXPERTS || top_k < 1 || top_k > E || n_shared < 0 ||
+        top_k + n_shared > MLORA_MAX_TOPK)
+        return MLORA_ERR_SHAPE;
+    if (n_shared > 0 && !(routed_scaling_factor > 0.0f)) return MLORA_ERR_INVALID_ARG;
+    if (M == 0) return MLORA_OK;
+    if (!logits || !topk_ids || !topk_w) return MLORA_ERR_INVALID_ARG;
+    const float inv_rsf = n_shared > 0 ? 1.0f / routed_scaling_factor : 0.0f;
+    return cuda_status(launch_route(logits, scoring == MLORA_SCORE_SIGMOID_BIAS ? bias : nullptr, M, E, top_k,
+                                    scoring, renormalize, n_shared, inv_rsf, topk_ids, topk_w,
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+size_t mlora_moe_align_max_padded(int M, int K_total, int E_tot, int block_m) {
+    if (M < 0 || K_total < 1 || E_tot < 1 || block_m < 1 || block_m > MLORA_MAX_ALIGN_BLOCK) return 0;
+    return static_cast<size_t>(align_max_padded(static_cast<long>(M) * K_total, E_tot, block_m));
+}
+
+mlora_status mlora_moe_align(const int32_t* topk_ids, int M, int K_total, int E_tot, int block_m,
+                             int32_t* sorted_ids, int32_t* expert_ids, int32_t* num_post_padded, void* stream) {
+    if (M < 0 || K_total < 1 || K_total > MLORA_MAX_TOPK || E_tot < 1 || E_tot > MLORA_MAX_EXPERTS ||
+        block_m < 1 || block_m > MLORA_MAX_ALIGN_BLOCK)
+        return MLORA_ERR_SHAPE;
+    const long S = static_cast<long>(M) * K_total;
+    if (S + static_cast<long>(E_tot) * block_m >= 0x7fffffffL) return MLORA_ERR_SHAPE;
+    if (!num_post_padded || (S > 0 && (!topk_ids || !sorted_ids || !expert_ids))) return MLORA_ERR_INVALID_ARG;
+    const long mp = align_max_padded(S, E_tot, block_m);
+    return cuda_status(launch_align(topk_ids, S, E_tot, block_m, mp, sorted_ids, expert_ids, num_post_padded,
+                                    nullptr, nullptr, static_cast<cudaStream_t>(stream)));
+}
+
+static mlora_status check_forward_sizes(int M, int H, int I, int E_tot, int K_total, int L, int rank) {
+    if (M < 0 || H < 8 || I < 8 || (H % 8) || (I % 8) || E_tot < 1 || E_tot > MLORA_MAX_EXPERTS || K_total < 1 ||
+        K_total > MLORA_MAX_TOPK || L < 0 || rank < 0)
+        return MLORA_ERR_SHAPE;
+    if (L > 0 && rank > 0 && (rank % 8 || rank > MLORA_MAX_RANK)) return MLORA_ERR_UNSUPPORTED;
+    const long S = static_cast<long>(M) * K_total;
+    if (S + static_cast<long>(E_tot) * kBlockM >= 0x7fffffffL) return MLORA_ERR_SHAPE;
+    if (static_cast<long>(L) * E_tot >= 0x7fffffffL) return MLORA_ERR_SHAPE;
+    const Sizes z = make_sizes(M, H, I, E_tot, K_total, L, rank);
+    if (z.max_lt * kBlockM >= 0x7fffffffL) return MLORA_ERR_SHAPE;
+    return MLORA_OK;
+}
+
+size_t mlora_moe_workspace_size(int M, int H, int I, int E_tot, int K_total, int L, int rank) {
+    if (check_forward_sizes(M, H, I, E_tot, K_total, L, rank) != MLORA_OK) return 0;
+    return carve_workspace(make_sizes(M, H, I, E_tot, K_total, L, rank), nullptr).bytes;
+}
+
+mlora_status mlora_moe_forward(const void* x, const void* w13, const void* w2, const void* A13, const void* B13,
+                               const void* A2, const void* B2, const int32_t* token_lora_idx,
+                               const int32_t* topk_ids, const float* topk_w, int M, int H, int I, int E_tot,
+                               int K_total, int L, int rank, float scaling, int n_shared, float out_scale, void* y,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+    const bool lora = A13 && B13 && A2 && B2 && token_lora_idx && L > 0 && rank > 0;
+    const int L_eff = lora ? L : 0, r_eff = lora ? rank : 0;
+    mlora_status st = check_forward_sizes(M, H, I, E_tot, K_total, L, rank);
+    if (st != MLORA_OK) return st;
+    if (n_shared < 0 || n_shared >= K_total || n_shared >= E_tot) return MLORA_ERR_SHAPE;
+    if (M == 0) return MLORA_OK;
+    if (!x || !w13 || !w2 || !topk_ids || !topk_w || !y) return MLORA_ERR_INVALID_ARG;
+    const void* ptrs[] = {x, w13, w2, topk_ids, topk_w, y};
+    for (const void* ptr : ptrs)
+        if (!aligned16(ptr)) return MLORA_ERR_INVALID_ARG;
+    if (lora) {
+        const void* lp[] = {A13, B13, A2, B2};
+        for (const void* ptr : lp)
+            if (!aligned16(ptr)) return MLORA_ERR_INVALID_ARG;
+        if (reinterpret_cast<uintptr_t>(token_lora_idx) & 3u) return MLORA_ERR_INVALID_ARG;
+    }
+    const Sizes z = make_sizes(M, H, I, E_tot, K_total, L_eff, r_eff);
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return MLORA_ERR_WORKSPACE;
+    const Workspace ws = carve_workspace(z, workspace);
+    if (workspace_bytes < ws.bytes) return MLORA_ERR_WORKSPACE;
+
+    // ---- tensor maps (dims innermost first) ----
+    GemmParams gu{}, dn{}, sh13{}, sh2{};
+    const cuuint64_t H_ = H, I_ = I, E_ = E_tot, MP = z.max_padded;
+    bool ok = true;
+    {
+        const cuuint64_t dx[2] = {H_, MP}, sx[1] = {H_ * 2};
+        const cuuint32_t bx[2] = {64, 128};
+        ok &= make_map(&gu.tm_a, ws.x_perm, 2, dx, sx, bx);
+        const cuuint64_t da[2] = {I_, MP}, sa[1] = {I_ * 2};
+        ok &= make_map(&dn.tm_a, ws.act, 2, da, sa, bx);
+        const cuuint64_t d13[4] = {H_, I_, 2, E_}, s13[3] = {H_ * 2, I_ * H_ * 2, 2 * I_ * H_ * 2};
+        const cuuint32_t b13[4] = {64, 128, 1, 1};
+        ok &= make_map(&gu.tm_b, w13, 4, d13, s13, b13);
+        const cuuint64_t d2[3] = {I_, H_, E_}, s2[2] = {I_ * 2, H_ * I_ * 2};
+        const cuuint32_t b2[3] = {64, 256, 1};
+        ok &= make_map(&dn.tm_b, w2, 3, d2, s2, b2);
+        if (lora) {
+            const cuuint64_t R = rank, LE = static_cast<cuuint64_t>(L) * E_tot;
+            const cuuint32_t rp = static_cast<cuuint32_t>((rank + 15) / 16 * 16);
+            const cuuint64_t dt[2] = {64, static_cast<cuuint64_t>(z.max_lt) * kBlockM}, st_[1] = {128};
+            ok &= make_map(&gu.tm_t, ws.lora_t, 2, dt, st_, bx);
+            dn.tm_t = gu.tm_t;
+            const cuuint64_t dA13[3] = {H_, R, LE}, sA13[2] = {H_ * 2, R * H_ * 2};
+            const cuuint32_t bA[3] = {64, rp, 1};
+            sh13.tm_a = gu.tm_a;
+            ok &= make_map(&sh13.tm_b, A13, 3, dA13, sA13, bA);
+            const cuuint64_t dA2[3] = {I_, R, LE}, sA2[2] = {I_ * 2, R * I_ * 2};
+            sh2.tm_a = dn.tm_a;
+            ok &= make_map(&sh2.tm_b, A2, 3, dA2, sA2, bA);
+            const cuuint64_t dB13[4] = {R, I_, 2, LE}, sB13[3] = {R * 2, I_ * R * 2, 2 * I_ * R * 2};
+            ok &= make_map(&gu.tm_lb, B13, 4, dB13, sB13, b13);
+            const cuuint64_t dB2[3] = {R, H_, LE}, sB2[2] = {R * 2, H_ * R * 2};
+            ok &= make_map(&dn.tm_lb, B2, 3, dB2, sB2, b2);
+        }
+    }
+    if (!ok) return MLORA_ERR_CUDA;
+
+    auto fill_common = [&](GemmParams& p) {
+        p.n_pad = ws.n_pad;
+        p.expert_ids = ws.expert_ids;
+        p.sorted_ids = ws.sorted_ids;
+        p.lora_of = ws.lora_of;
+        p.blk_nad = ws.blk_nad;
+        p.blk_lora = ws.blk_lora;
+        p.blk_lt_start = ws.blk_lt_start;
+        p.lt_block = ws.lt_block;
+        p.lt_lora = ws.lt_lora;
+        p.lt_total = ws.lt_total;
+        p.status = ws.status;
+        p.E_tot = E_tot;
+        p.cap = z.cap;
+        p.rank = r_eff;
+        p.S = static_cast<int>(z.S);
+        p.has_lora = lora ? 1 : 0;
+        p.scaling = scaling;
+    };
+    fill_common(gu);
+    fill_common(dn);
+    fill_common(sh13);
+    fill_common(sh2);
+    gu.out = ws.act;
+    gu.K = H;
+    gu.n_out = I;
+    dn.out = ws.y_slot;
+    dn.K = I;
+    dn.n_out = H;
+    sh13.out = ws.lora_t;
+    sh13.K = H;
+    sh13.n_out = r_eff;
+    sh2.out = ws.lora_t;
+    sh2.K = I;
+    sh2.n_out = r_eff;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t err = cudaMemsetAsync(ws.status, 0, 16, s);
+    if (err != cudaSuccess) return MLORA_ERR_CUDA;
+    if (mark_stage(0, s) != cudaSuccess) return MLORA_ERR_CUDA;
+    AlignExtra ex{};
+    if (lora) {
+        ex.token_lora_idx = token_lora_idx;
+        ex.L = L;
+        ex.K_total = K_total;
+        ex.cap = z.cap;
+        ex.lora_of = ws.lora_of;
+        ex.blk_nad = ws.blk_nad;
+        ex.blk_lora = ws.blk_lora;
+        ex.blk_lt_start = ws.blk_lt_start;
+        ex.lt_block = ws.lt_block;
+        ex.lt_lora = ws.lt_lora;
+        ex.lt_total = ws.lt_total;
+    }
+    err = launch_align(topk_ids, z.S, E_tot, kBlockM, z.max_padded, ws.sorted_ids, ws.expert_ids, ws.n_pad,
+                       ws.status, lora ? &ex : nullptr, s);
+    if (err != cudaSuccess || mark_stage(1, s) != cudaSuccess) return MLORA_ERR_CUDA;
+    err = launch_gather_rows(x, H, ws.sorted_ids, ws.n_pad, z.S, K_total, z.max_padded, ws.x_perm, s);
+    if (err != cudaSuccess || mark_stage(2, s) != cudaSuccess) return MLORA_ERR_CUDA;
+    if (lora) {
+        err = launch_gemm(kShrink, sh13, z.max_lt, s);
+        if (err != cudaSuccess) return MLORA_ERR_CUDA;
+    }
+    if (mark_stage(3, s) != cudaSuccess) return MLORA_ERR_CUDA;
+    err = launch_gemm(kGateUp, gu, z.max_blocks * ((I + 127) / 128), s);
+    if (err != cudaSuccess || mark_stage(4, s) != cudaSuccess) return MLORA_ERR_CUDA;
+    if (lora) {
+        err = launch_gemm(kShrink, sh2, z.max_lt, s);
+        if (err != cudaSuccess) return MLORA_ERR_CUDA;
+    }
+    if (mark_stage(5, s) != cudaSuccess) return MLORA_ERR_CUDA;
+    err = launch_gemm(kDown, dn, z.max_blocks * ((H + 255) / 256), s);
+    if (err != cudaSuccess || mark_stage(6, s) != cudaSuccess) return MLORA_ERR_CUDA;
+    err = launch_combine(ws.y_slot, topk_ids, topk_w, M, H, K_total, E_tot, out_scale, y, s);
+    if (err != cudaSuccess || mark_stage(7, s) != cudaSuccess) return MLORA_ERR_CUDA;
+    return MLORA_OK;
+}
+
+mlora_status mlora_set_stage_events(void* const* events, int count) {
+    if (!events || count == 0) {
+        g_stage_events_on = false;
+        return MLORA_OK;
+    }
+    if (count < MLORA_STAGE_EVENTS) return MLORA_ERR_INVALID_ARG;
+    for (int i = 0; i < MLORA_STAGE_EVENTS; ++i) {
+        if (!events[i]) return MLORA_ERR_INVALID_ARG;
+        g_stage_events[i] = static_cast<cudaEvent_t>(events[i]);
+    }
+    g_stage_events_on = true;
+    return MLORA_OK;
+}
+
+mlora_status mlora_moe_read_status(const void* workspace, uint32_t* host_status, void* stream) {
+    if (!workspace || !host_status) return MLORA_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(host_status, workspace, sizeof(uint32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return MLORA_ERR_CUDA;
+    return cuda_status(cudaStreamSynchronize(s));
+}
+
+}  // extern "C"

@@ -1,0 +1,113 @@
+// internal.cuh -- declarations shared by the translation units of libmlora.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "mlora.h"
+
+namespace mlora {
+
+constexpr int kBlockM = MLORA_FORWARD_BLOCK_M;  // token rows per GEMM tile (MMA M)
+constexpr int kBlockK = 64;                     // bf16 elements per 128-byte swizzle row
+constexpr int kLoraTileCols = 64;               // shrink result row, padded to one swizzle row
+
+// Per-forward buffers carved out of the caller's workspace.
+struct Workspace {
+    uint32_t* status;      // [0] device status word
+    int32_t* n_pad;        // padded slot total written by align
+    int32_t* lt_total;     // number of (block, adapter) shrink tiles
+    int32_t* sorted_ids;   // [max_padded]
+    int32_t* expert_ids;   // [max_blocks]
+    int32_t* lora_of;      // [max_padded] adapter of each sorted position (-1: none / pad)
+    int32_t* blk_nad;      // [max_blocks] distinct adapters in the block
+    int32_t* blk_lt_start; // [max_blocks] first shrink tile of the block
+    int32_t* blk_lora;     // [max_blocks * cap] the block's adapters, ascending
+    int32_t* lt_block;     // [max_lt] block of each shrink tile
+    int32_t* lt_lora;      // [max_lt] adapter of each shrink tile
+    void* x_perm;          // [max_padded, H] bf16: x rows gathered in sorted order
+    void* act;             // [max_padded, I] bf16: SwiGLU output in sorted order
+    void* lora_t;          // [max_lt * 128, 64] bf16: s * shrink, one masked tile per (block, adapter)
+    void* y_slot;          // [M*K', H] bf16: each slot's expert output
+    size_t bytes;
+};
+
+struct Sizes {
+    int M, H, I, E_tot, K_total, L, rank;
+    bool lora;
+    long S;           // M * K_total
+    long max_padded;  // with block_m = kBlockM
+    long max_blocks;
+    int cap;          // adapters per block list: min(L, kBlockM)
+    long max_lt;
+};
+
+Sizes make_sizes(int M, int H, int I, int E_tot, int K_total, int L, int rank);
+Workspace carve_workspace(const Sizes& z, void* base);  // base == nullptr: sizing only
+
+long align_max_padded(long S, int E_tot, int block_m);
+
+// Extra outputs of align used only inside the forward.
+struct AlignExtra {
+    const int32_t* token_lora_idx;
+    int L;
+    int K_total;
+    int cap;
+    int32_t* lora_of;
+    int32_t* blk_nad;
+    int32_t* blk_lora;
+    int32_t* blk_lt_start;
+    int32_t* lt_block;
+    int32_t* lt_lora;
+    int32_t* lt_total;
+};
+
+cudaError_t launch_route(const float* logits, const float* bias, int M, int E, int top_k, int scoring,
+                         int renormalize, int n_shared, float inv_rsf, int32_t* ids, float* w, cudaStream_t s);
+
+cudaError_t launch_align(const int32_t* ids, long S, int E_tot, int block_m, long max_padded, int32_t* sorted,
+                         int32_t* expert_ids, int32_t* n_pad, uint32_t* status, const AlignExtra* extra,
+                         cudaStream_t s);
+
+cudaError_t launch_gather_rows(const void* x, int H, const int32_t* sorted, const int32_t* n_pad, long S,
+                               int K_total, long max_padded, void* x_perm, cudaStream_t s);
+
+cudaError_t launch_combine(const void* y_slot, const int32_t* topk_ids, const float* topk_w, int M, int H,
+                           int K_total, int E_tot, float out_scale, void* y, cudaStream_t s);
+
+// ------------------------------------------------------------ grouped GEMM --
+enum GemmMode : int { kGateUp = 0, kDown = 1, kShrink = 2 };
+
+struct alignas(64) GemmParams {
+    CUtensorMap tm_a;   // token rows [rows, K], box {64, 128}
+    CUtensorMap tm_b;   // weight rows (w13 / w2 / A13 / A2 view)
+    CUtensorMap tm_t;   // LoRA shrink tiles [tiles*128, 64], box {64, 128}
+    CUtensorMap tm_lb;  // LoRA expand weights (B13 / B2 view)
+    const int32_t* n_pad;
+    const int32_t* expert_ids;
+    const int32_t* sorted_ids;
+    const int32_t* lora_of;
+    const int32_t* blk_nad;
+    const int32_t* blk_lora;
+    const int32_t* blk_lt_start;
+    const int32_t* lt_block;
+    const int32_t* lt_lora;
+    const int32_t* lt_total;
+    void* out;
+    uint32_t* status;
+    int K;          // reduction length
+    int n_out;      // valid output columns (I for gate_up, H for down, rank for shrink)
+    int E_tot;
+    int cap;
+    int rank;
+    int S;          // sentinel slot value M*K'
+    int has_lora;
+    float scaling;
+};
+
+cudaError_t launch_gemm(GemmMode mode, const GemmParams& p, long max_tiles, cudaStream_t s);
+
+int device_sm_count();
+
+}  // namespace mlora

@@ -1,0 +1,100 @@
+// rows.cu -- the two bandwidth-bound row kernels around the grouped GEMMs:
+//  * gather: x rows copied into sorted (expert-grouped) order so each GEMM
+//    tile reads 128 consecutive rows with one TMA box;
+//  * combine: y[m] = out_scale * sum_k topk_w[m,k] * y_slot[m*K'+k], the
+//    weighted top-k sum ("[vllm] vLLM ROCm 환경에서 Shared-Expert Fusion을 통한
+//    MoE 추론 성능 최적화", section "코드 분석" item 1: the routing weights,
+//    shared slots included, weight each slot's expert output).
+// Both move 16-byte vectors; one warp owns one row.
+#include <cuda_bf16.h>
+
+#include "internal.cuh"
+#include "ptx.cuh"
+
+namespace mlora {
+namespace {
+
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ x, int H8,
+                                                          const int32_t* __restrict__ sorted,
+                                                          const int32_t* __restrict__ n_pad, int S, int K_total,
+                                                          uint4* __restrict__ x_perm) {
+    const int lane = threadIdx.x & 31;
+    const int warps = blockDim.x >> 5;
+    const int np = *n_pad;
+    for (int p = blockIdx.x * warps + (threadIdx.x >> 5); p < np; p += gridDim.x * warps) {
+        const int f = sorted[p];
+        if (f >= S) continue;  // padding row: never stored downstream
+        const uint4* src = x + static_cast<size_t>(f / K_total) * H8;
+        uint4* dst = x_perm + static_cast<size_t>(p) * H8;
+        for (int i = lane; i < H8; i += 32) dst[i] = __ldg(src + i);
+    }
+}
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float (&f)[8]) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 t = __bfloat1622float2(h[i]);
+        f[2 * i] = t.x;
+        f[2 * i + 1] = t.y;
+    }
+}
+
+__global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ y_slot,
+                                                      const int32_t* __restrict__ topk_ids,
+                                                      const float* __restrict__ topk_w, int M, int H8, int K_total,
+                                                      int E_tot, float out_scale, uint4* __restrict__ y) {
+    const long total = static_cast<long>(M) * H8;
+    for (long idx = blockIdx.x * static_cast<long>(blockDim.x) + threadIdx.x; idx < total;
+         idx += static_cast<long>(gridDim.x) * blockDim.x) {
+        const int m = static_cast<int>(idx / H8);
+        const int c = static_cast<int>(idx - static_cast<long>(m) * H8);
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int k = 0; k < K_total; ++k) {
+            const long f = static_cast<long>(m) * K_total + k;
+            const int e = __ldg(topk_ids + f);
+            if (static_cast<unsigned>(e) >= static_cast<unsigned>(E_tot)) continue;  // dropped slot
+            const float wk = __ldg(topk_w + f);
+            float v[8];
+            bf16x8_to_f32(__ldg(y_slot + f * H8 + c), v);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] = fmaf(wk, v[i], acc[i]);
+        }
+        uint4 o;
+        o.x = pack_bf16x2(out_scale * acc[0], out_scale * acc[1]);
+        o.y = pack_bf16x2(out_scale * acc[2], out_scale * acc[3]);
+        o.z = pack_bf16x2(out_scale * acc[4], out_scale * acc[5]);
+        o.w = pack_bf16x2(out_scale * acc[6], out_scale * acc[7]);
+        y[idx] = o;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_gather_rows(const void* x, int H, const int32_t* sorted, const int32_t* n_pad, long S,
+                               int K_total, long max_padded, void* x_perm, cudaStream_t s) {
+    if (max_padded == 0) return cudaSuccess;
+    const int warps_per_block = 8;
+    long blocks = (max_padded + warps_per_block - 1) / warps_per_block;
+    const long cap = 8L * device_sm_count();
+    if (blocks > cap) blocks = cap;
+    gather_rows_kernel<<<static_cast<unsigned>(blocks), 32 * warps_per_block, 0, s>>>(
+        static_cast<const uint4*>(x), H / 8, sorted, n_pad, static_cast<int>(S), K_total,
+        static_cast<uint4*>(x_perm));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const void* y_slot, const int32_t* topk_ids, const float* topk_w, int M, int H,
+                           int K_total, int E_tot, float out_scale, void* y, cudaStream_t s) {
+    const long total = static_cast<long>(M) * (H / 8);
+    if (total == 0) return cudaSuccess;
+    long blocks = (total + 255) / 256;
+    const long cap = 16L * device_sm_count();
+    if (blocks > cap) blocks = cap;
+    combine_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(static_cast<const uint4*>(y_slot), topk_ids,
+                                                                 topk_w, M, H / 8, K_total, E_tot, out_scale,
+                                                                 static_cast<uint4*>(y));
+    return cudaGetLastError();
+}
+
+}  // namespace mlora

@@ -1,9 +1,13 @@
 """Seeded synthetic inputs for the fused MoE-LoRA layer.
 
 This module only draws numbers: it holds none of the layer's arithmetic, and
-both the CUDA path and the fp64 oracle read the very same host tensors it
-returns.  Every draw comes from a CPU ``torch.Generator`` seeded per tensor,
-so one tensor can be regenerated without the others.  Floating-point samples
+both the CUDA path and the fp64 oracle read the very same tensors it
+returns.  Every draw comes from a ``torch.Generator`` seeded per tensor, so one
+tensor can be regenerated without the others.  Router logits, the expert
+bias, x and the adapter ids come from CPU generators; the weight tensors
+come from a generator on ``device`` (a CUDA device draws gigabytes in
+milliseconds), so the same spec gives different weights on CPU and GPU,
+and both sides of a comparison always read the tensors of one draw.  Floating-point samples
 are drawn in fp32 and rounded to bf16 (round-to-nearest-even); router logits
 and the expert bias stay fp32.
 
@@ -97,12 +101,12 @@ def spec(name: str, **overrides) -> Spec:
     return Spec(name=name, **base)
 
 
-def _gen(seed: int, slot: int) -> torch.Generator:
-    return torch.Generator().manual_seed(seed * 64 + slot)
+def _gen(seed: int, slot: int, device="cpu") -> torch.Generator:
+    return torch.Generator(device=device).manual_seed(seed * 64 + slot)
 
 
-def _normal_bf16(shape, std: float, seed: int, slot: int) -> torch.Tensor:
-    t = torch.randn(*shape, generator=_gen(seed, slot), dtype=torch.float32)
+def _normal_bf16(shape, std: float, seed: int, slot: int, device="cpu") -> torch.Tensor:
+    t = torch.randn(*shape, generator=_gen(seed, slot, device), dtype=torch.float32, device=device)
     if std != 1.0:
         t.mul_(std)
     return t.to(torch.bfloat16)
@@ -149,8 +153,8 @@ def token_adapters(s: Spec) -> Optional[torch.Tensor]:
     return idx.to(torch.int32).contiguous()
 
 
-def make(s: Spec, with_weights: bool = True) -> Inputs:
-    """Draw every input of one layer call."""
+def make(s: Spec, with_weights: bool = True, device="cpu") -> Inputs:
+    """Draw every input of one layer call (weights on ``device``)."""
     Et, H, I = s.E_tot, s.H, s.I
     logits = torch.randn(s.M, s.E, generator=_gen(s.seed, 0), dtype=torch.float32)
     bias = None
@@ -163,13 +167,13 @@ def make(s: Spec, with_weights: bool = True) -> Inputs:
     x = _normal_bf16((s.M, H), 1.0, s.seed, 2)
     w13 = w2 = A13 = B13 = A2 = B2 = None
     if with_weights:
-        w13 = _normal_bf16((Et, 2 * I, H), H ** -0.5, s.seed, 3)
-        w2 = _normal_bf16((Et, H, I), I ** -0.5, s.seed, 4)
+        w13 = _normal_bf16((Et, 2 * I, H), H ** -0.5, s.seed, 3, device)
+        w2 = _normal_bf16((Et, H, I), I ** -0.5, s.seed, 4, device)
         if s.has_lora:
-            A13 = _normal_bf16((s.L, Et, s.r, H), H ** -0.5, s.seed, 5)
-            B13 = _normal_bf16((s.L, Et, 2 * I, s.r), 0.1, s.seed, 6)
-            A2 = _normal_bf16((s.L, Et, s.r, I), I ** -0.5, s.seed, 7)
-            B2 = _normal_bf16((s.L, Et, H, s.r), 0.1, s.seed, 8)
+            A13 = _normal_bf16((s.L, Et, s.r, H), H ** -0.5, s.seed, 5, device)
+            B13 = _normal_bf16((s.L, Et, 2 * I, s.r), 0.1, s.seed, 6, device)
+            A2 = _normal_bf16((s.L, Et, s.r, I), I ** -0.5, s.seed, 7, device)
+            B2 = _normal_bf16((s.L, Et, H, s.r), 0.1, s.seed, 8, device)
     return Inputs(s, logits.contiguous(), bias, x, w13, w2, A13, B13, A2, B2, token_adapters(s))
 
 
@@ -177,7 +181,7 @@ def bits(t: Optional[torch.Tensor]) -> Optional[np.ndarray]:
     """Raw bf16 bit patterns of a CPU bf16 tensor as a numpy uint16 array."""
     if t is None:
         return None
-    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
 def from_bits(a: np.ndarray) -> torch.Tensor:
@@ -186,5 +190,5 @@ def from_bits(a: np.ndarray) -> torch.Tensor:
 
 
 def to_f64(t: torch.Tensor) -> np.ndarray:
-    """Exact widening of a bf16 (or fp32) CPU tensor to float64 numpy."""
-    return t.to(torch.float64).numpy()
+    """Exact widening of a bf16 (or fp32) tensor to float64 numpy."""
+    return t.detach().cpu().to(torch.float64).numpy()

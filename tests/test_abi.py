@@ -1,0 +1,105 @@
+"""The C-ABI library loads on a machine without a GPU, exports every symbol
+include/mlora.h declares, and rejects bad arguments on the host before any
+CUDA call (only calls that fail validation or are no-ops run here)."""
+import ctypes
+
+import pytest
+
+import moe_layer_lora_gb300 as ml
+from moe_layer_lora_gb300 import _lib
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from moe_layer_lora_gb300 import build
+    build.build()
+    return _lib.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _lib.declared_functions()
+    assert len(names) == 8, names
+    raw = ctypes.CDLL(_lib.LIB_PATH)
+    for n in names:
+        assert hasattr(raw, n), n
+
+
+def test_stage_event_hook_validation(lib):
+    assert lib.mlora_set_stage_events(None, 0) == 0
+    arr = (ctypes.c_void_p * 3)(None, None, None)
+    assert lib.mlora_set_stage_events(arr, 3) == 1
+
+
+def test_status_strings(lib):
+    assert ml.mlora_status_string(0) == "ok"
+    assert "shape" in ml.mlora_status_string(2)
+    assert ml.mlora_status_string(99) == "unknown status"
+
+
+def test_route_validation(lib):
+    P = None
+    f = lib.mlora_moe_route
+    assert f(P, P, 4, 0, 1, 0, 1, 0, 1.0, P, P, P) == 2            # E = 0
+    assert f(P, P, 4, 8, 9, 0, 1, 0, 1.0, P, P, P) == 2            # top_k > E
+    assert f(P, P, 4, 8, 2, 7, 1, 0, 1.0, P, P, P) == 1            # bad scoring enum
+    assert f(P, P, 4, 8, 2, 1, 1, 1, 0.0, P, P, P) == 1            # rsf <= 0 with shared slots
+    assert f(P, P, 4, 2000, 2, 0, 1, 0, 1.0, P, P, P) == 2         # E > max
+    assert f(P, P, 4, 128, 60, 0, 1, 8, 1.0, P, P, P) == 2         # K' > max
+    assert f(P, P, 4, 8, 2, 0, 1, 0, 1.0, P, P, P) == 1            # NULL tensors
+    assert f(P, P, 0, 8, 2, 0, 1, 0, 1.0, P, P, P) == 0            # M = 0: nothing to do
+
+
+def test_align_validation(lib):
+    P = None
+    f = lib.mlora_moe_align
+    assert f(P, 4, 2, 8, 0, P, P, P, P) == 2                       # block_m = 0
+    assert f(P, 4, 2, 0, 16, P, P, P, P) == 2                      # E_tot = 0
+    assert f(P, 4, 2, 8, 2048, P, P, P, P) == 2                    # block_m > max
+    assert f(P, 4, 2, 8, 16, P, P, P, P) == 1                      # NULL buffers
+    assert lib.mlora_moe_align_max_padded(3, 2, 3, 4) == 16
+    assert lib.mlora_moe_align_max_padded(0, 2, 3, 4) == 0
+    assert lib.mlora_moe_align_max_padded(3, 2, 3, 0) == 0
+
+
+def test_align_max_padded_matches_oracle(lib):
+    import oracle
+    for args in [(3, 2, 3, 4), (16, 2, 8, 128), (64, 4, 32, 16), (8192, 4, 32, 128), (1, 9, 129, 128), (0, 1, 1, 1)]:
+        assert lib.mlora_moe_align_max_padded(*args) == oracle.moe_align_max_padded(*args)
+
+
+def _fwd(lib, M=4, H=64, I=64, E=4, K=2, L=0, r=0, n_shared=0, ptrs=True, ws=None, wsb=1 << 30, A13=None):
+    P = ctypes.c_void_p(4096) if ptrs else None
+    return lib.mlora_moe_forward(P, P, P, A13, A13, A13, A13, A13, P, P, M, H, I, E, K, L, r, 1.0, n_shared, 1.0,
+                                 P, ws if ws is not None else ctypes.c_void_p(1 << 20), wsb, None)
+
+
+def test_forward_validation(lib):
+    assert _fwd(lib, H=60) == 2                                    # H % 8
+    assert _fwd(lib, I=4) == 2                                     # I < 8
+    assert _fwd(lib, E=2000) == 2                                  # E_tot > max
+    assert _fwd(lib, K=0) == 2                                     # K' = 0
+    assert _fwd(lib, n_shared=2) == 2                              # n_shared >= K'
+    good = ctypes.c_void_p(4096)
+    assert _fwd(lib, L=2, r=12, A13=good) == 3                     # rank not a multiple of 8
+    assert _fwd(lib, L=2, r=128, A13=good) == 3                    # rank > 64
+    assert _fwd(lib, ptrs=False) == 1                              # NULL tensors
+    assert _fwd(lib, ws=ctypes.c_void_p(4096 + 16)) == 4           # misaligned workspace
+    assert _fwd(lib, wsb=16) == 4                                  # too small
+    assert _fwd(lib, M=0) == 0                                     # empty batch: no-op
+
+
+def test_forward_misaligned_pointer(lib):
+    bad = ctypes.c_void_p(4096 + 8)
+    P = ctypes.c_void_p(4096)
+    st = lib.mlora_moe_forward(bad, P, P, None, None, None, None, None, P, P, 4, 64, 64, 4, 2, 0, 0, 1.0, 0, 1.0,
+                               P, ctypes.c_void_p(1 << 20), 1 << 30, None)
+    assert st == 1
+
+
+def test_workspace_size(lib):
+    base = ml.mlora_moe_workspace_size(64, 2880, 2880, 32, 4, 0, 0)
+    with_lora = ml.mlora_moe_workspace_size(64, 2880, 2880, 32, 4, 8, 16)
+    assert 0 < base < with_lora
+    assert base % 256 == 0 and with_lora % 256 == 0
+    assert ml.mlora_moe_workspace_size(64, 2881, 2880, 32, 4, 0, 0) == 0
+    assert ml.mlora_moe_workspace_size(8192, 2880, 2880, 32, 4, 8, 32) < 2 << 30

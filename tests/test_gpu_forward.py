@@ -1,0 +1,177 @@
+"""The fused MoE-LoRA layer on the GPU against the fp64 oracle.
+
+Small cases compare every output; the full-size layers compare sampled token
+rows (the oracle computes one token at a time; every row of the GPU output
+comes from the same launch configuration the benchmark times).  Tolerance:
+relative Frobenius error <= 1e-2 and max abs error <= 5e-2 * rms(oracle)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import pins
+import moe_layer_lora_gb300 as ml
+from moe_layer_lora_gb300 import workloads as wl
+import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+
+def _layer(spec, rows=None, label=""):
+    inp = wl.make(spec, device="cuda")
+    d = gu.DeviceInputs(inp)
+    ids, w = gu.gpu_route(d)
+    ws = torch.empty(ml.mlora_moe_workspace_size(spec.M, spec.H, spec.I, spec.E_tot, spec.K_total,
+                                                 spec.L if spec.has_lora else 0, spec.r if spec.has_lora else 0),
+                     dtype=torch.uint8, device="cuda")
+    y = gu.gpu_forward(d, ids, w, workspace=ws)
+    torch.cuda.synchronize()
+    assert ml.mlora_moe_read_status(ws) == 0
+    ids_ref, w_ref = gu.oracle_route(inp)
+    gu.check_route(ids, w, ids_ref, w_ref)
+    y_ref = gu.oracle_forward(inp, ids_ref, w_ref, rows=rows)
+    yg = y if rows is None else y[torch.as_tensor(rows, device="cuda")]
+    errs = gu.check_y(yg, y_ref, label or spec.name)
+    return inp, d, ids, w, y, ids_ref, w_ref, errs
+
+
+def test_tiny():
+    _layer(wl.spec("tiny"))
+
+
+def test_decode_full():
+    _layer(wl.spec("decode"))
+
+
+def test_prefill_sampled():
+    s = wl.spec("prefill")
+    idx = wl.token_adapters(s).numpy()
+    none_rows = np.flatnonzero(idx == -1)
+    rows = gu.sample_rows(s.M, 40, 1, must=[0, s.M - 1, none_rows[0], none_rows[-1]])
+    _layer(s, rows=rows)
+
+
+@pytest.mark.parametrize("M", [1, 32, 128])
+def test_shared_fusion_matches_unfused(M):
+    """Fused shared slot (weight 1/rsf, output scaled by rsf) against the
+    unfused form: rsf * routed MoE (oracle) + separate shared MLP."""
+    s = wl.spec("shared", M=M)
+    rows = None if M <= 32 else gu.sample_rows(M, 32, 2, must=[0, M - 1])
+    inp, d, ids, w, y, ids_ref, w_ref, _ = _layer(s, rows=rows)
+    sel = slice(None) if rows is None else rows
+    k = s.top_k
+    routed = oracle.moe_forward(wl.bits(inp.x)[sel], gu._hbits(inp.w13), gu._hbits(inp.w2), None, None, None, None,
+                                None, np.ascontiguousarray(ids_ref[sel, :k]),
+                                np.ascontiguousarray(w_ref[sel, :k]).astype(np.float32), 0.0, 1.0)
+    shared = pins.shared_mlp_dense(wl.to_f64(inp.x)[sel], wl.to_f64(inp.w13[s.E]), wl.to_f64(inp.w2[s.E]))
+    unfused = s.routed_scaling_factor * routed + shared
+    yg = y if rows is None else y[torch.as_tensor(rows, device="cuda")]
+    gu.check_y(yg, unfused, f"shared M={M} vs unfused")
+
+
+def test_stress_sampled_and_early_exit():
+    s = wl.spec("stress")
+    idx = wl.token_adapters(s).numpy()
+    rows = gu.sample_rows(s.M, 40, 3, must=[int(np.flatnonzero(idx == -1)[0]), int(np.flatnonzero(idx == 0)[0])])
+    inp, d, ids, w, y, ids_ref, w_ref, _ = _layer(s, rows=rows)
+    # every token without an adapter: the LoRA work exits on the device and
+    # the output equals the adapter-free layer bit for bit
+    none = torch.full((s.M,), -1, dtype=torch.int32, device="cuda")
+    y_none = gu.gpu_forward(d, ids, w, idx=none)
+    y_base = gu.gpu_forward(d, ids, w, lora=False)
+    torch.cuda.synchronize()
+    assert torch.equal(y_none, y_base)
+    y_ref = gu.oracle_forward(inp, ids_ref, w_ref, rows=rows, lora=False)
+    gu.check_y(y_base[torch.as_tensor(rows, device="cuda")], y_ref, "stress all -1")
+
+
+@pytest.mark.parametrize("over", [
+    dict(M=37, H=136, I=72, E=5, top_k=3, L=3, r=24, seed=101),             # ragged K, N, rank
+    dict(M=5, H=64, I=64, E=6, top_k=2, L=2, r=48, seed=102),               # rank 48
+    dict(M=130, H=256, I=128, E=3, top_k=1, L=1, r=16, seed=103),           # >128 slots of one expert
+    dict(M=9, H=8, I=8, E=4, top_k=4, L=5, r=64, seed=104),                 # tiny H/I, top_k = E
+    dict(M=300, H=200, I=328, E=16, top_k=2, L=70, r=8, seed=105),          # L > 64 adapters
+    dict(M=64, H=512, I=256, E=8, top_k=2, n_shared=2, routed_scaling_factor=2.0,
+         scoring=wl.SCORE_SIGMOID_BIAS, L=4, r=16, seed=106),               # shared slots with adapters
+    dict(M=16, H=256, I=128, E=8, top_k=2, L=0, r=0, lora_mode="none", seed=107),  # no adapters
+    dict(M=24, H=384, I=136, E=8, top_k=2, renormalize=0, L=4, r=32, seed=108),
+])
+def test_edges(over):
+    _layer(wl.spec("tiny", **over), label=str(over))
+
+
+def test_empty_batch():
+    s = wl.spec("tiny")
+    inp = wl.make(s, device="cuda")
+    d = gu.DeviceInputs(inp)
+    e = torch.empty((0, s.H), dtype=torch.bfloat16, device="cuda")
+    ids = torch.empty((0, s.K_total), dtype=torch.int32, device="cuda")
+    w = torch.empty((0, s.K_total), dtype=torch.float32, device="cuda")
+    y = ml.mlora_moe_forward(e, d.w13, d.w2, d.A13, d.B13, d.A2, d.B2,
+                             torch.empty(0, dtype=torch.int32, device="cuda"), ids, w, 2.0)
+    assert y.shape == (0, s.H)
+
+
+def test_bad_device_values_are_flagged():
+    """Out-of-range adapter ids act as 'no adapter', out-of-range expert ids
+    drop their slot; both set a bit of the device status word."""
+    s = wl.spec("tiny")
+    inp = wl.make(s, device="cuda")
+    d = gu.DeviceInputs(inp)
+    ids, w = gu.gpu_route(d)
+    ws = torch.empty(ml.mlora_moe_workspace_size(s.M, s.H, s.I, s.E_tot, s.K_total, s.L, s.r), dtype=torch.uint8,
+                     device="cuda")
+    bad_idx = d.idx.clone()
+    bad_idx[3] = s.L + 7
+    y = gu.gpu_forward(d, ids, w, idx=bad_idx, workspace=ws)
+    assert ml.mlora_moe_read_status(ws) == ml.DEV_BAD_LORA_IDX
+    fixed = inp.token_lora_idx.numpy().copy()
+    fixed[3] = -1
+    ids_ref, w_ref = gu.oracle_route(inp)
+    gu.check_y(y, gu.oracle_forward(inp, ids_ref, w_ref, idx=fixed), "bad adapter id")
+    bad_ids = ids.clone()
+    bad_ids[5, 1] = s.E_tot + 3
+    y2 = gu.gpu_forward(d, bad_ids, w, workspace=ws)
+    assert ml.mlora_moe_read_status(ws) == ml.DEV_BAD_EXPERT_ID
+    w_drop = w_ref.copy()
+    w_drop[5, 1] = 0.0
+    gu.check_y(y2, gu.oracle_forward(inp, ids_ref, w_drop), "dropped slot")
+
+
+def test_graph_capture_replay():
+    """Route + forward captured once, replayed on new inputs written into the
+    same buffers; each replay matches an eager call."""
+    s = wl.spec("tiny", M=48, seed=111)
+    inp = wl.make(s, device="cuda")
+    d = gu.DeviceInputs(inp)
+    ids = torch.empty((s.M, s.K_total), dtype=torch.int32, device="cuda")
+    w = torch.empty((s.M, s.K_total), dtype=torch.float32, device="cuda")
+    y = torch.empty((s.M, s.H), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(ml.mlora_moe_workspace_size(s.M, s.H, s.I, s.E_tot, s.K_total, s.L, s.r), dtype=torch.uint8,
+                     device="cuda")
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        ml.mlora_moe_route(d.logits, None, s.top_k, s.scoring, topk_ids=ids, topk_w=w, stream=stream)
+        ml.mlora_moe_forward(d.x, d.w13, d.w2, d.A13, d.B13, d.A2, d.B2, d.idx, ids, w, s.scaling, y=y,
+                             workspace=ws, stream=stream)
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        ml.mlora_moe_route(d.logits, None, s.top_k, s.scoring, topk_ids=ids, topk_w=w, stream=stream)
+        ml.mlora_moe_forward(d.x, d.w13, d.w2, d.A13, d.B13, d.A2, d.B2, d.idx, ids, w, s.scaling, y=y,
+                             workspace=ws, stream=stream)
+    for seed in (5, 6):
+        new = wl.make(wl.spec("tiny", M=48, seed=seed), with_weights=False)
+        d.logits.copy_(new.logits)
+        d.x.copy_(new.x)
+        d.idx.copy_(new.token_lora_idx)
+        g.replay()
+        torch.cuda.synchronize()
+        y_graph = y.clone()
+        ids_e, w_e = ml.mlora_moe_route(d.logits, None, s.top_k, s.scoring)
+        y_eager = ml.mlora_moe_forward(d.x, d.w13, d.w2, d.A13, d.B13, d.A2, d.B2, d.idx, ids_e, w_e, s.scaling)
+        torch.cuda.synchronize()
+        assert torch.equal(y_graph, y_eager)
+        inp.logits, inp.x, inp.token_lora_idx = new.logits, new.x, new.token_lora_idx
+        ids_ref, w_ref = gu.oracle_route(inp)
+        gu.check_y(y_graph, gu.oracle_forward(inp, ids_ref, w_ref), f"graph replay seed {seed}")

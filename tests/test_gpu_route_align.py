@@ -1,0 +1,110 @@
+"""GPU routing and align against the oracle: ids and the sorted, padded
+permutation bit-exact, routing weights within fp32 rounding."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import moe_layer_lora_gb300 as ml
+from moe_layer_lora_gb300 import workloads as wl
+import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+
+def _route_case(spec):
+    inp = wl.make(spec, with_weights=False)
+    d_logits = gu.dev(inp.logits)
+    d_bias = gu.dev(inp.bias)
+    ids_ref, w_ref = gu.oracle_route(inp)
+    if spec.scoring == wl.SCORE_SIGMOID_BIAS:
+        _assert_unambiguous(inp, ids_ref)
+    ids, w = ml.mlora_moe_route(d_logits, d_bias, spec.top_k, spec.scoring, spec.renormalize, spec.n_shared,
+                                spec.routed_scaling_factor)
+    torch.cuda.synchronize()
+    gu.check_route(ids, w, ids_ref, w_ref)
+    return ids_ref
+
+
+def _assert_unambiguous(inp, ids_ref):
+    """The integer decision is taken in fp32 on both sides with each side's
+    own expf; the seeded inputs must keep every key that decides the order
+    more than 8 ulp from its neighbour so that a 1-2 ulp expf difference
+    cannot change the result."""
+    s = inp.spec
+    l = inp.logits.numpy().astype(np.float32)
+    key = (np.float32(1) / (np.float32(1) + np.exp(-l))) + inp.bias.numpy()[None, :]
+    srt = -np.sort(-key, axis=1)[:, : s.top_k + 1]
+    gaps = srt[:, :-1] - srt[:, 1:]
+    ulp = np.spacing(np.abs(srt[:, :-1])).astype(np.float64)
+    assert (gaps > 8 * ulp).all(), "seeded input has a near-tie in the sigmoid+bias keys"
+
+
+@pytest.mark.parametrize("name", wl.WORKLOADS)
+def test_route_workloads(name):
+    _route_case(wl.spec(name))
+
+
+@pytest.mark.parametrize("M", [1, 32, 128])
+def test_route_shared_sweep(M):
+    _route_case(wl.spec("shared", M=M))
+
+
+@pytest.mark.parametrize("over", [
+    dict(renormalize=0),
+    dict(scoring=wl.SCORE_SIGMOID_BIAS, renormalize=0, E=64, top_k=6),
+    dict(E=1024, top_k=8, M=33),
+    dict(E=3, top_k=3, M=5),
+    dict(E=40, top_k=5, n_shared=2, routed_scaling_factor=2.0, M=17),
+    dict(E=1, top_k=1, M=9),
+    dict(E=200, top_k=64, M=3),
+])
+def test_route_edges(over):
+    _route_case(wl.spec("tiny", **over))
+
+
+def test_route_ties_lower_id():
+    logits = torch.tensor([[1.0, 2.0, 2.0, 0.5, 2.0, 2.0]] * 3, dtype=torch.float32)
+    ids, w = ml.mlora_moe_route(logits.cuda(), None, 4, wl.SCORE_SOFTMAX)
+    assert ids.cpu().tolist() == [[1, 2, 4, 5]] * 3
+    ids_ref, w_ref = oracle.moe_route(logits.numpy(), None, 4, 0, 1)
+    gu.check_route(ids, w, ids_ref, w_ref)
+
+
+def _align_case(ids_np, E_tot, BM):
+    s_ref, e_ref, n_ref = oracle.moe_align(ids_np, E_tot, BM)
+    s, e, n = ml.mlora_moe_align(torch.from_numpy(ids_np).cuda(), E_tot, BM)
+    torch.cuda.synchronize()
+    assert int(n.item()) == n_ref
+    assert np.array_equal(s.cpu().numpy(), s_ref)
+    assert np.array_equal(e.cpu().numpy(), e_ref)
+
+
+@pytest.mark.parametrize("name", wl.WORKLOADS)
+@pytest.mark.parametrize("BM", [16, 32, 64, 128])
+def test_align_workloads(name, BM):
+    spec = wl.spec(name)
+    ids_ref, _ = gu.oracle_route(wl.make(spec, with_weights=False))
+    _align_case(ids_ref, spec.E_tot, BM)
+
+
+def test_align_edges():
+    rng = np.random.default_rng(0)
+    # one expert takes every slot: many blocks of the same expert
+    _align_case(np.full((300, 1), 2, np.int32), 4, 16)
+    # block_m = 1 (no padding) and a large block
+    ids = np.stack([rng.permutation(7)[:3] for _ in range(50)]).astype(np.int32)
+    _align_case(ids, 7, 1)
+    _align_case(ids, 7, 1024)
+    # the largest expert count
+    ids = rng.integers(0, 1024, size=(700, 4), dtype=np.int32)
+    _align_case(ids, 1024, 8)
+    # more slots than one pass of the scatter, ragged tail
+    ids = rng.integers(0, 5, size=(3001, 3), dtype=np.int32)
+    _align_case(ids, 5, 64)
+
+
+def test_align_empty():
+    s, e, n = ml.mlora_moe_align(torch.zeros((0, 4), dtype=torch.int32, device="cuda"), 8, 16)
+    torch.cuda.synchronize()
+    assert int(n.item()) == 0 and s.numel() == 0 and e.numel() == 0

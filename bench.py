@@ -81,6 +81,15 @@ def reduce_max(value: float, world: int, device) -> float:
     return float(t.item())
 
 
+def aggregate(step_ms, tokens_per_rank: int, world: int, device):
+    """Whole-job throughput: the slowest rank's total time over the tokens
+    every rank processed (weak scaling: each rank runs its own batch)."""
+    total_ms = reduce_max(float(sum(step_ms)), world, device)
+    steps = len(step_ms)
+    ms_per_step = total_ms / steps
+    return total_ms, ms_per_step, tokens_per_rank * world / (ms_per_step / 1e3)
+
+
 def barrier(world: int):
     if world > 1:
         import torch.distributed as dist
@@ -190,10 +199,17 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def kernel_source_hash() -> str:
+STAGE_SOURCES = {
+    "gate_up": ("gemm.cu", "ptx.cuh", "internal.cuh"),
+    "down": ("gemm.cu", "ptx.cuh", "internal.cuh"),
+}
+
+
+def kernel_source_hash(stage: str) -> str:
+    """Hash of the sources a stage's kernel is built from."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "moe_layer_lora_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in STAGE_SOURCES.get(stage, sorted(os.listdir(csrc))):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -209,7 +225,7 @@ def profiled_traffic(stage: str, workload: str):
         return None
     m_hash = re.search(r"kernel source hash:\s*`?([0-9a-f]{16})", text)
     m_val = re.search(r"dram bytes per launch:\s*`?([0-9.eE+]+)", text)
-    if not m_hash or not m_val or m_hash.group(1) != kernel_source_hash():
+    if not m_hash or not m_val or m_hash.group(1) != kernel_source_hash(stage):
         return None
     return float(m_val.group(1))
 
@@ -349,7 +365,7 @@ def run_gpu(args, s: wl.Spec, rank: int, world: int, local_rank: int):
         if status != 0:
             raise RuntimeError(f"device status {status:#x} after the timed steps")
 
-    total_ms = reduce_max(float(sum(step_ms)), world, device)
+    total_ms, _, _ = aggregate(step_ms, s.M, world, device)
     e2e_s = reduce_max(e2e_s, world, device)
     stage_avg = {n: float(np.mean(v)) for n, v in stage_ms.items()}
     return dict(inp=inp, alg=alg, total_ms=total_ms, step_ms=step_ms, stage_avg=stage_avg, e2e_s=e2e_s, bi=bi,

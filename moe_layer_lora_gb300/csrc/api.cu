@@ -17,6 +17,8 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -65,9 +67,27 @@ mlora_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MLORA_OK : M
 thread_local cudaEvent_t g_stage_events[MLORA_STAGE_EVENTS];
 thread_local bool g_stage_events_on = false;
 
+// Inside stream capture the events become graph event-record nodes (the
+// external flag); outside capture they are recorded normally.
 cudaError_t mark_stage(int i, cudaStream_t s) {
     if (!g_stage_events_on) return cudaSuccess;
-    return cudaEventRecordWithFlags(g_stage_events[i], s, cudaEventRecordExternal);
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t err = cudaStreamIsCapturing(s, &cs);
+    if (err != cudaSuccess) return err;
+    if (cs == cudaStreamCaptureStatusActive)
+        return cudaEventRecordWithFlags(g_stage_events[i], s, cudaEventRecordExternal);
+    return cudaEventRecord(g_stage_events[i], s);
+}
+
+// MLORA_DEBUG=1 in the environment prints the CUDA error behind an
+// MLORA_ERR_CUDA return to stderr.
+mlora_status cuda_fail(cudaError_t e, const char* where) {
+    static const bool verbose = [] {
+        const char* v = getenv("MLORA_DEBUG");
+        return v && *v && *v != '0';
+    }();
+    if (verbose) fprintf(stderr, "libmlora: %s: %s\n", where, cudaGetErrorString(e));
+    return MLORA_ERR_CUDA;
 }
 
 }  // namespace
@@ -262,7 +282,7 @@ mlora_status mlora_moe_forward(const void* x, const void* w13, const void* w2, c
             ok &= make_map(&dn.tm_lb, B2, 3, dB2, sB2, b2);
         }
     }
-    if (!ok) return MLORA_ERR_CUDA;
+    if (!ok) return cuda_fail(cudaErrorInvalidValue, "tensor map encoding");
 
     auto fill_common = [&](GemmParams& p) {
         p.n_pad = ws.n_pad;
@@ -302,8 +322,8 @@ mlora_status mlora_moe_forward(const void* x, const void* w13, const void* w2, c
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t err = cudaMemsetAsync(ws.status, 0, 16, s);
-    if (err != cudaSuccess) return MLORA_ERR_CUDA;
-    if (mark_stage(0, s) != cudaSuccess) return MLORA_ERR_CUDA;
+    if (err != cudaSuccess) return cuda_fail(err, "status reset");
+    if ((err = mark_stage(0, s)) != cudaSuccess) return cuda_fail(err, "stage event");
     AlignExtra ex{};
     if (lora) {
         ex.token_lora_idx = token_lora_idx;
@@ -320,25 +340,24 @@ mlora_status mlora_moe_forward(const void* x, const void* w13, const void* w2, c
     }
     err = launch_align(topk_ids, z.S, E_tot, kBlockM, z.max_padded, ws.sorted_ids, ws.expert_ids, ws.n_pad,
                        ws.status, lora ? &ex : nullptr, s);
-    if (err != cudaSuccess || mark_stage(1, s) != cudaSuccess) return MLORA_ERR_CUDA;
+    if (err != cudaSuccess) return cuda_fail(err, "align");
+    if ((err = mark_stage(1, s)) != cudaSuccess) return cuda_fail(err, "stage event");
     err = launch_gather_rows(x, H, ws.sorted_ids, ws.n_pad, z.S, K_total, z.max_padded, ws.x_perm, s);
-    if (err != cudaSuccess || mark_stage(2, s) != cudaSuccess) return MLORA_ERR_CUDA;
-    if (lora) {
-        err = launch_gemm(kShrink, sh13, z.max_lt, s);
-        if (err != cudaSuccess) return MLORA_ERR_CUDA;
-    }
-    if (mark_stage(3, s) != cudaSuccess) return MLORA_ERR_CUDA;
+    if (err != cudaSuccess) return cuda_fail(err, "gather");
+    if ((err = mark_stage(2, s)) != cudaSuccess) return cuda_fail(err, "stage event");
+    if (lora && (err = launch_gemm(kShrink, sh13, z.max_lt, s)) != cudaSuccess) return cuda_fail(err, "shrink gate_up");
+    if ((err = mark_stage(3, s)) != cudaSuccess) return cuda_fail(err, "stage event");
     err = launch_gemm(kGateUp, gu, z.max_blocks * ((I + 127) / 128), s);
-    if (err != cudaSuccess || mark_stage(4, s) != cudaSuccess) return MLORA_ERR_CUDA;
-    if (lora) {
-        err = launch_gemm(kShrink, sh2, z.max_lt, s);
-        if (err != cudaSuccess) return MLORA_ERR_CUDA;
-    }
-    if (mark_stage(5, s) != cudaSuccess) return MLORA_ERR_CUDA;
+    if (err != cudaSuccess) return cuda_fail(err, "gate_up");
+    if ((err = mark_stage(4, s)) != cudaSuccess) return cuda_fail(err, "stage event");
+    if (lora && (err = launch_gemm(kShrink, sh2, z.max_lt, s)) != cudaSuccess) return cuda_fail(err, "shrink down");
+    if ((err = mark_stage(5, s)) != cudaSuccess) return cuda_fail(err, "stage event");
     err = launch_gemm(kDown, dn, z.max_blocks * ((H + 255) / 256), s);
-    if (err != cudaSuccess || mark_stage(6, s) != cudaSuccess) return MLORA_ERR_CUDA;
+    if (err != cudaSuccess) return cuda_fail(err, "down");
+    if ((err = mark_stage(6, s)) != cudaSuccess) return cuda_fail(err, "stage event");
     err = launch_combine(ws.y_slot, topk_ids, topk_w, M, H, K_total, E_tot, out_scale, y, s);
-    if (err != cudaSuccess || mark_stage(7, s) != cudaSuccess) return MLORA_ERR_CUDA;
+    if (err != cudaSuccess) return cuda_fail(err, "combine");
+    if ((err = mark_stage(7, s)) != cudaSuccess) return cuda_fail(err, "stage event");
     return MLORA_OK;
 }
 

@@ -58,18 +58,9 @@ def oracle_route(inp: wl.Inputs):
                             s.scoring, s.renormalize, s.n_shared, s.routed_scaling_factor)
 
 
-_HOST = {}
-
-
 def _hbits(t):
-    """Host bit copy of a (possibly device) bf16 tensor, cached per tensor."""
-    if t is None:
-        return None
-    key = (id(t), t.data_ptr())
-    if key not in _HOST:
-        _HOST.clear() if len(_HOST) > 16 else None
-        _HOST[key] = wl.bits(t)
-    return _HOST[key]
+    """Host bit copy of a (possibly device) bf16 tensor."""
+    return None if t is None else wl.bits(t)
 
 
 def oracle_forward(inp: wl.Inputs, ids, w, rows=None, lora=True, idx=None):
@@ -80,7 +71,9 @@ def oracle_forward(inp: wl.Inputs, ids, w, rows=None, lora=True, idx=None):
     use = lora and s.has_lora
     sel = slice(None) if rows is None else np.asarray(rows)
     x = wl.bits(inp.x)[sel]
-    tli = inp.token_lora_idx.numpy() if idx is None else np.asarray(idx, np.int32)
+    tli = None
+    if use:
+        tli = inp.token_lora_idx.numpy() if idx is None else np.asarray(idx, np.int32)
     b = _hbits
     return oracle.moe_forward(x, b(inp.w13), b(inp.w2), b(inp.A13) if use else None,
                               b(inp.B13) if use else None, b(inp.A2) if use else None,

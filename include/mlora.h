@@ -155,6 +155,40 @@ mlora_status mlora_moe_forward(const void* x, const void* w13, const void* w2, c
                                void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * mlora_moe_forward_static -- the same layer as mlora_moe_forward, for
+ * callers that cannot allocate device memory where they run it (their
+ * device memory belongs to another allocator they must not bypass, they may
+ * not allocate after start-up, or they only hold pointers to tensors).
+ * The pages have no counterpart to this entry point; it is a deployment
+ * convenience of this library.
+ *
+ * Arguments are those of mlora_moe_forward without the workspace: the
+ * scratch is a fixed device array inside the library, of
+ * MLORA_STATIC_WORKSPACE_BYTES, reserved on every GPU that loads the
+ * library's kernels and held until the process exits.  Nothing is
+ * allocated or freed by the call.
+ *  - Sizes whose mlora_moe_workspace_size exceeds the array return
+ *    MLORA_ERR_WORKSPACE and enqueue nothing (64 MiB holds, e.g., the
+ *    M=64, H=I=2880, E=32, top_k=4, L=8, rank=16 layer).
+ *  - The first call on a device looks up the array's device address
+ *    (once per device, with that device current); make that first call
+ *    before any stream capture on the device.
+ *  - Every call shares the one array and it keeps the last call's
+ *    contents.  The call clears what must start at zero (its status word)
+ *    itself; everything else is written before it is read.  Calls whose
+ *    work overlaps on the GPU (different streams, or concurrent host
+ *    threads) race on the array: serialise them.
+ *  - mlora_moe_read_status on the array is not offered; the device status
+ *    bits are only readable through mlora_moe_forward's workspace.
+ */
+#define MLORA_STATIC_WORKSPACE_BYTES (64u << 20)
+mlora_status mlora_moe_forward_static(const void* x, const void* w13, const void* w2, const void* A13,
+                                      const void* B13, const void* A2, const void* B2,
+                                      const int32_t* token_lora_idx, const int32_t* topk_ids, const float* topk_w,
+                                      int M, int H, int I, int E_tot, int K_total, int L, int rank, float scaling,
+                                      int n_shared, float out_scale, void* y, void* stream);
+
+/*
  * Copies the device status word of the last forward that used `workspace`
  * (MLORA_DEV_* bits, 0 = clean) to *host_status after waiting for `stream`.
  */

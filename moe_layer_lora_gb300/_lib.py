@@ -166,6 +166,36 @@ def mlora_moe_forward(x, w13, w2, A13, B13, A2, B2, token_lora_idx, topk_ids, to
     return y
 
 
+STATIC_WORKSPACE_BYTES = 64 << 20
+
+
+def mlora_moe_forward_static(x, w13, w2, A13, B13, A2, B2, token_lora_idx, topk_ids, topk_w, scaling: float,
+                             n_shared: int = 0, out_scale: float = 1.0, y: Optional[torch.Tensor] = None,
+                             stream=None):
+    """The layer with the library's fixed scratch array instead of a
+    workspace: for callers that cannot allocate device memory where they
+    run it.  Only y is allocated here (by torch) when not passed in."""
+    lib = load()
+    fn = lib.mlora_moe_forward_static
+    if fn.argtypes is None:
+        P, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        fn.argtypes = [P] * 10 + [i] * 7 + [f, i, f, P, P]
+        fn.restype = i
+    _need(x, torch.bfloat16, "x")
+    M, H = x.shape
+    E_tot, twoI, _ = w13.shape
+    lora = all(t is not None for t in (A13, B13, A2, B2, token_lora_idx))
+    L, r = (A13.shape[0], A13.shape[2]) if lora else (0, 0)
+    if y is None:
+        y = torch.empty((M, H), dtype=torch.bfloat16, device=x.device)
+    st = fn(_ptr(x), _ptr(w13), _ptr(w2), _ptr(A13) if lora else None, _ptr(B13) if lora else None,
+            _ptr(A2) if lora else None, _ptr(B2) if lora else None, _ptr(token_lora_idx) if lora else None,
+            _ptr(topk_ids), _ptr(topk_w), M, H, twoI // 2, E_tot, topk_ids.shape[1], L, r, float(scaling),
+            int(n_shared), float(out_scale), _ptr(y), _stream(stream))
+    _check("mlora_moe_forward_static", st)
+    return y
+
+
 def mlora_moe_read_status(workspace: torch.Tensor, stream=None) -> int:
     out = ctypes.c_uint32(0)
     st = load().mlora_moe_read_status(_ptr(workspace), ctypes.byref(out), _stream(stream))

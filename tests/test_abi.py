@@ -18,7 +18,9 @@ def lib():
 
 def test_exports_every_declared_symbol(lib):
     names = _lib.declared_functions()
-    assert len(names) == 8, names
+    for core in ("mlora_moe_route", "mlora_moe_align", "mlora_moe_align_max_padded", "mlora_moe_workspace_size",
+                 "mlora_moe_forward", "mlora_moe_read_status", "mlora_set_stage_events", "mlora_status_string"):
+        assert core in names, core
     raw = ctypes.CDLL(_lib.LIB_PATH)
     for n in names:
         assert hasattr(raw, n), n

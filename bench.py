@@ -289,6 +289,7 @@ def run_gpu(args, s: wl.Spec, rank: int, world: int, local_rank: int):
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(ml.STAGE_EVENTS)]
     for e in ev:
         e.record(stream)  # creates the event handles
+    ml.mlora_set_stage_events(None)
     step_start = torch.cuda.Event(enable_timing=True)
     step_end = torch.cuda.Event(enable_timing=True)
 
@@ -299,28 +300,45 @@ def run_gpu(args, s: wl.Spec, rank: int, world: int, local_rank: int):
                              s.scaling, s.n_shared, s.out_scale, y=y, workspace=ws, stream=stream)
 
     with torch.cuda.stream(stream):
-        ml.mlora_set_stage_events(ev)
         step()
         stream.synchronize()
         status = ml.mlora_moe_read_status(ws, stream=stream)
         if status != 0:
             raise RuntimeError(f"device status {status:#x} after the first step")
-        graph = None
+        # two graphs of the same step: a plain one for the headline time and
+        # one with event nodes at the stage boundaries for per-kernel times
+        plain = inst = None
         if not args.no_graph:
-            graph = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(graph, stream=stream):
+            plain = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(plain, stream=stream):
                 step()
-        run = graph.replay if graph is not None else step
+            ml.mlora_set_stage_events(ev)
+            inst = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(inst, stream=stream):
+                step()
+            ml.mlora_set_stage_events(None)
+        run = plain.replay if plain is not None else step
+
+        def run_inst():
+            if inst is not None:
+                inst.replay()
+            else:
+                ml.mlora_set_stage_events(ev)
+                step()
+                ml.mlora_set_stage_events(None)
+
         for _ in range(args.warmup):
             flush.fill_(1)
             run()
+            flush.fill_(1)
+            run_inst()
         stream.synchronize()
         ids_host = ids.cpu().numpy()
         alg = algorithmic(s, ids_host, inp.token_lora_idx.numpy() if s.has_lora else None)
 
         barrier(world)
         torch.cuda.synchronize(device)
-        step_ms, stage_ms = [], {n: [] for n in ml.STAGE_NAMES}
+        step_ms, inst_ms, stage_ms = [], [], {n: [] for n in ml.STAGE_NAMES}
         with ClockSampler(local_rank) as clocks:
             for _ in range(args.steps):
                 flush.fill_(1)
@@ -329,11 +347,20 @@ def run_gpu(args, s: wl.Spec, rank: int, world: int, local_rank: int):
                 step_end.record(stream)
                 stream.synchronize()
                 step_ms.append(step_start.elapsed_time(step_end))
+            torch.cuda.synchronize(device)
+            barrier(world)
+            # per-kernel times: as many steps of the instrumented graph
+            for _ in range(args.steps):
+                flush.fill_(1)
+                step_start.record(stream)
+                run_inst()
+                step_end.record(stream)
+                stream.synchronize()
+                inst_ms.append(step_start.elapsed_time(step_end))
                 for i, n in enumerate(ml.STAGE_NAMES):
                     stage_ms[n].append(ev[i].elapsed_time(ev[i + 1]))
         torch.cuda.synchronize(device)
         barrier(world)
-        ml.mlora_set_stage_events(None)
         launches_per_step = 1 + 5 + (2 if s.has_lora else 0)  # route, align, gather, gate_up, down, combine, shrinks
 
         # end to end through the public API with host buffers: H2D of the
@@ -368,7 +395,8 @@ def run_gpu(args, s: wl.Spec, rank: int, world: int, local_rank: int):
     total_ms, _, _ = aggregate(step_ms, s.M, world, device)
     e2e_s = reduce_max(e2e_s, world, device)
     stage_avg = {n: float(np.mean(v)) for n, v in stage_ms.items()}
-    return dict(inp=inp, alg=alg, total_ms=total_ms, step_ms=step_ms, stage_avg=stage_avg, e2e_s=e2e_s, bi=bi,
+    return dict(inp=inp, alg=alg, total_ms=total_ms, step_ms=step_ms, inst_ms=float(np.mean(inst_ms)),
+                stage_avg=stage_avg, e2e_s=e2e_s, bi=bi,
                 bo=bo, clocks=clocks.summary(), launches=launches_per_step * args.steps)
 
 
@@ -421,6 +449,7 @@ def main(argv=None):
                          "traffic": profiled_traffic(dom, s.name),
                          "kernel_ms": dom_ms},
             "layer": {"hbm_frac": layer_hbm_frac, "tensor_frac": layer_tc_frac,
+                      "ms_per_step_with_stage_events": res["inst_ms"],
                       "algorithmic_bytes": alg["layer_bytes"], "algorithmic_flops": alg["layer_flops"],
                       "experts_touched": alg["experts"], "adapter_pairs_touched": alg["pairs"],
                       "stage_us": {k: v * 1e3 for k, v in res["stage_avg"].items()}},

@@ -12,11 +12,13 @@
 // lanes of its warp with the same expert, from __match_any_sync); the
 // per-warp per-expert counts live in a small shared table.
 //
-// Inside the forward the same pass also records, per sorted position, the
-// token's adapter, and per block of kBlockM positions the ascending list of
-// distinct adapters, numbered globally into "shrink tiles" (block, adapter):
-// one masked LoRA tile per pair.
+// Inside the forward the same pass also records the real (non-padding) row
+// count of every block and, with adapters, per sorted position the token's
+// adapter and per block of kBlockM positions the ascending list of distinct
+// adapters, numbered globally into "shrink tiles" (block, adapter): one
+// masked LoRA tile per pair.
 #include "internal.cuh"
+#include "ptx.cuh"
 
 namespace mlora {
 namespace {
@@ -60,11 +62,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                  int32_t* __restrict__ sorted, int32_t* __restrict__ expert_ids, int32_t* __restrict__ n_pad_out,
                  uint32_t* __restrict__ status, AlignExtra ex) {
     extern __shared__ int smem_i[];
-    int* cnt = smem_i;                                               // [E_tot]
-    int* cursor = cnt + E_tot;                                       // [E_tot]
-    int* scratch = cursor + E_tot;                                   // [33]
-    uint16_t* wcnt = reinterpret_cast<uint16_t*>(scratch + 40);      // [kWarps][E_tot]
+    int* cnt = smem_i;                                            // [E_tot] slots per expert
+    int* first = cnt + E_tot;                                     // [E_tot] padded start of each expert
+    int* cursor = first + E_tot;                                  // [E_tot] next free position
+    int* scratch = cursor + E_tot;                                // [40]
+    uint16_t* wcnt = reinterpret_cast<uint16_t*>(scratch + 40);   // [kWarps][E_tot]
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    griddep_wait();
+    griddep_launch_dependents();
 
     for (int e = tid; e < E_tot; e += kThreads) cnt[e] = 0;
     for (int i = tid; i < kWarps * E_tot; i += kThreads) wcnt[i] = 0;
@@ -81,25 +86,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncthreads();
 
-    // 2. exclusive scan of the padded counts (E_tot <= 1024: one expert per thread)
+    // 2. exclusive scan of the padded counts (E_tot <= 1024: one expert per
+    //    thread), the block -> expert map and the real rows of each block
     const int c = tid < E_tot ? cnt[tid] : 0;
     const int padded = (c + BM - 1) / BM * BM;
     int total;
     const int start = block_exclusive_scan(padded, scratch, &total);
-    if (tid < E_tot) cursor[tid] = start;
-    if (tid == 0) *n_pad_out = total;
-
-    // 3. block -> expert map, per-expert padding, tails
     if (tid < E_tot) {
-        for (int b = start / BM; b < (start + padded) / BM; ++b) expert_ids[b] = tid;
-        for (int p = start + c; p < start + padded; ++p) {
+        first[tid] = start;
+        cursor[tid] = start;
+        for (int b = start / BM; b < (start + padded) / BM; ++b) {
+            expert_ids[b] = tid;
+            if (ex.blk_rows) ex.blk_rows[b] = min(BM, c - (b - start / BM) * BM);
+        }
+    }
+    if (tid == 0) *n_pad_out = total;
+    for (int p = total + tid; p < max_padded; p += kThreads) sorted[p] = S;
+    for (int b = total / BM + tid; b < max_padded / BM; b += kThreads) expert_ids[b] = -1;
+    __syncthreads();
+
+    // 3. per-expert padding, one warp per expert
+    for (int e = warp; e < E_tot; e += kWarps) {
+        const int n = cnt[e];
+        const int pad_end = first[e] + (n + BM - 1) / BM * BM;
+        for (int p = first[e] + n + lane; p < pad_end; p += 32) {
             sorted[p] = S;
             if (kWithLora) ex.lora_of[p] = -1;
         }
     }
-    for (int p = total + tid; p < max_padded; p += kThreads) sorted[p] = S;
-    for (int b = total / BM + tid; b < max_padded / BM; b += kThreads) expert_ids[b] = -1;
-    __syncthreads();
 
     // 4. stable scatter, 1024 slots per pass
     const unsigned lt_mask = (1u << lane) - 1u;
@@ -125,13 +139,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int p = pos + rank;
             sorted[p] = f;
             if (kWithLora) {
-                int l = -1;
-                if (ex.token_lora_idx) {
-                    l = ex.token_lora_idx[f / ex.K_total];
-                    if (l < -1 || l >= ex.L) {
-                        if (status) atomicOr(status, MLORA_DEV_BAD_LORA_IDX);
-                        l = -1;
-                    }
+                int l = ex.token_lora_idx[f / ex.K_total];
+                if (l < -1 || l >= ex.L) {
+                    if (status) atomicOr(status, MLORA_DEV_BAD_LORA_IDX);
+                    l = -1;
                 }
                 ex.lora_of[p] = l;
             }
@@ -146,16 +157,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (!kWithLora) return;
 
-    // 5. distinct adapters of each block (ascending), one warp per block
+    // 5. distinct adapters of each block (ascending), one warp per block;
+    //    the block's adapter ids are read once into registers
+    constexpr int kMaxPerLane = MLORA_FORWARD_BLOCK_M / 32;
     const int nblocks = total / BM;
     for (int b = warp; b < nblocks; b += kWarps) {
+        int mine[kMaxPerLane];
+#pragma unroll
+        for (int i = 0; i < kMaxPerLane; ++i) {
+            const int r = lane + 32 * i;
+            mine[i] = r < BM ? ex.lora_of[b * BM + r] : -1;
+        }
         int prev = -1, count = 0;
         for (;;) {
             int cand = 0x7fffffff;
-            for (int r = lane; r < BM; r += 32) {
-                const int l = ex.lora_of[b * BM + r];
-                if (l > prev && l < cand) cand = l;
-            }
+#pragma unroll
+            for (int i = 0; i < kMaxPerLane; ++i)
+                if (mine[i] > prev && mine[i] < cand) cand = mine[i];
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) cand = min(cand, __shfl_xor_sync(0xffffffffu, cand, off));
             if (cand == 0x7fffffff) break;
@@ -198,32 +216,36 @@ long align_max_padded(long S, int E_tot, int block_m) {
 cudaError_t launch_align(const int32_t* ids, long S, int E_tot, int block_m, long max_padded, int32_t* sorted,
                          int32_t* expert_ids, int32_t* n_pad, uint32_t* status, const AlignExtra* extra,
                          cudaStream_t s) {
-    const size_t smem = sizeof(int) * (2 * static_cast<size_t>(E_tot) + 40) +
+    const size_t smem = sizeof(int) * (3 * static_cast<size_t>(E_tot) + 40) +
                         sizeof(uint16_t) * static_cast<size_t>(kWarps) * E_tot;
     static unsigned long long attr_set[2] = {0ull, 0ull};  // one bit per device
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
-    if (extra) {
+    const bool with_lora = extra && extra->token_lora_idx;
+    AlignExtra ex{};
+    if (extra) ex = *extra;
+    if (with_lora) {
         if (!(attr_set[1] & bit)) {
             err = cudaFuncSetAttribute(align_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
             if (err != cudaSuccess) return err;
             attr_set[1] |= bit;
         }
-        align_kernel<true><<<1, kThreads, smem, s>>>(ids, static_cast<int>(S), E_tot, block_m,
+        err = launch_pdl(align_kernel<true>, dim3(1), dim3(kThreads), smem, s, ids, static_cast<int>(S), E_tot, block_m,
                                                      static_cast<int>(max_padded), sorted, expert_ids, n_pad, status,
-                                                     *extra);
+                                                     ex);
+        if (err != cudaSuccess) return err;
     } else {
         if (!(attr_set[0] & bit)) {
             err = cudaFuncSetAttribute(align_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
             if (err != cudaSuccess) return err;
             attr_set[0] |= bit;
         }
-        AlignExtra none{};
-        align_kernel<false><<<1, kThreads, smem, s>>>(ids, static_cast<int>(S), E_tot, block_m,
+        err = launch_pdl(align_kernel<false>, dim3(1), dim3(kThreads), smem, s, ids, static_cast<int>(S), E_tot, block_m,
                                                       static_cast<int>(max_padded), sorted, expert_ids, n_pad, status,
-                                                      none);
+                                                      ex);
+        if (err != cudaSuccess) return err;
     }
     return cudaGetLastError();
 }

@@ -135,6 +135,7 @@ Workspace carve_workspace(const Sizes& z, void* base) {
     w.lt_total = reinterpret_cast<int32_t*>(header ? header + 8 : nullptr);
     w.sorted_ids = reinterpret_cast<int32_t*>(take(4 * z.max_padded));
     w.expert_ids = reinterpret_cast<int32_t*>(take(4 * z.max_blocks));
+    w.blk_rows = reinterpret_cast<int32_t*>(take(4 * z.max_blocks));
     if (z.lora) {
         w.lora_of = reinterpret_cast<int32_t*>(take(4 * z.max_padded));
         w.blk_nad = reinterpret_cast<int32_t*>(take(4 * z.max_blocks));
@@ -253,10 +254,13 @@ mlora_status mlora_moe_forward(const void* x, const void* w13, const void* w2, c
     bool ok = true;
     {
         const cuuint64_t dx[2] = {H_, MP}, sx[1] = {H_ * 2};
-        const cuuint32_t bx[2] = {64, 128};
+        const cuuint32_t bx[2] = {64, kRowBox};
+        const cuuint32_t bxf[2] = {64, 128};
         ok &= make_map(&gu.tm_a, ws.x_perm, 2, dx, sx, bx);
+        ok &= make_map(&gu.tm_a_full, ws.x_perm, 2, dx, sx, bxf);
         const cuuint64_t da[2] = {I_, MP}, sa[1] = {I_ * 2};
         ok &= make_map(&dn.tm_a, ws.act, 2, da, sa, bx);
+        ok &= make_map(&dn.tm_a_full, ws.act, 2, da, sa, bxf);
         const cuuint64_t d13[4] = {H_, I_, 2, E_}, s13[3] = {H_ * 2, I_ * H_ * 2, 2 * I_ * H_ * 2};
         const cuuint32_t b13[4] = {64, 128, 1, 1};
         ok &= make_map(&gu.tm_b, w13, 4, d13, s13, b13);
@@ -268,13 +272,17 @@ mlora_status mlora_moe_forward(const void* x, const void* w13, const void* w2, c
             const cuuint32_t rp = static_cast<cuuint32_t>((rank + 15) / 16 * 16);
             const cuuint64_t dt[2] = {64, static_cast<cuuint64_t>(z.max_lt) * kBlockM}, st_[1] = {128};
             ok &= make_map(&gu.tm_t, ws.lora_t, 2, dt, st_, bx);
+            ok &= make_map(&gu.tm_t_full, ws.lora_t, 2, dt, st_, bxf);
             dn.tm_t = gu.tm_t;
+            dn.tm_t_full = gu.tm_t_full;
             const cuuint64_t dA13[3] = {H_, R, LE}, sA13[2] = {H_ * 2, R * H_ * 2};
             const cuuint32_t bA[3] = {64, rp, 1};
             sh13.tm_a = gu.tm_a;
+            sh13.tm_a_full = gu.tm_a_full;
             ok &= make_map(&sh13.tm_b, A13, 3, dA13, sA13, bA);
             const cuuint64_t dA2[3] = {I_, R, LE}, sA2[2] = {I_ * 2, R * I_ * 2};
             sh2.tm_a = dn.tm_a;
+            sh2.tm_a_full = dn.tm_a_full;
             ok &= make_map(&sh2.tm_b, A2, 3, dA2, sA2, bA);
             const cuuint64_t dB13[4] = {R, I_, 2, LE}, sB13[3] = {R * 2, I_ * R * 2, 2 * I_ * R * 2};
             ok &= make_map(&gu.tm_lb, B13, 4, dB13, sB13, b13);
@@ -287,6 +295,7 @@ mlora_status mlora_moe_forward(const void* x, const void* w13, const void* w2, c
     auto fill_common = [&](GemmParams& p) {
         p.n_pad = ws.n_pad;
         p.expert_ids = ws.expert_ids;
+        p.blk_rows = ws.blk_rows;
         p.sorted_ids = ws.sorted_ids;
         p.lora_of = ws.lora_of;
         p.blk_nad = ws.blk_nad;
@@ -307,6 +316,8 @@ mlora_status mlora_moe_forward(const void* x, const void* w13, const void* w2, c
     fill_common(dn);
     fill_common(sh13);
     fill_common(sh2);
+    gu.pdl_early = lora ? 1 : 0;
+    dn.pdl_early = lora ? 1 : 0;
     gu.out = ws.act;
     gu.K = H;
     gu.n_out = I;
@@ -325,6 +336,7 @@ mlora_status mlora_moe_forward(const void* x, const void* w13, const void* w2, c
     if (err != cudaSuccess) return cuda_fail(err, "status reset");
     if ((err = mark_stage(0, s)) != cudaSuccess) return cuda_fail(err, "stage event");
     AlignExtra ex{};
+    ex.blk_rows = ws.blk_rows;
     if (lora) {
         ex.token_lora_idx = token_lora_idx;
         ex.L = L;
@@ -339,18 +351,46 @@ mlora_status mlora_moe_forward(const void* x, const void* w13, const void* w2, c
         ex.lt_total = ws.lt_total;
     }
     err = launch_align(topk_ids, z.S, E_tot, kBlockM, z.max_padded, ws.sorted_ids, ws.expert_ids, ws.n_pad,
-                       ws.status, lora ? &ex : nullptr, s);
+                       ws.status, &ex, s);
     if (err != cudaSuccess) return cuda_fail(err, "align");
     if ((err = mark_stage(1, s)) != cudaSuccess) return cuda_fail(err, "stage event");
     err = launch_gather_rows(x, H, ws.sorted_ids, ws.n_pad, z.S, K_total, z.max_padded, ws.x_perm, s);
     if (err != cudaSuccess) return cuda_fail(err, "gather");
     if ((err = mark_stage(2, s)) != cudaSuccess) return cuda_fail(err, "stage event");
-    if (lora && (err = launch_gemm(kShrink, sh13, z.max_lt, s)) != cudaSuccess) return cuda_fail(err, "shrink gate_up");
+    // the shrink: CUDA cores (beside the consuming GEMM) while it is small,
+    // tensor cores beyond
+    const bool rows_shrink = z.S * r_eff <= kShrinkRowsMaxWork;
+    ShrinkParams sr13{}, sr2{};
+    if (lora) {
+        for (ShrinkParams* sp : {&sr13, &sr2}) {
+            sp->rank = r_eff;
+            sp->E_tot = E_tot;
+            sp->scaling = scaling;
+            sp->lt_block = ws.lt_block;
+            sp->lt_lora = ws.lt_lora;
+            sp->lt_total = ws.lt_total;
+            sp->expert_ids = ws.expert_ids;
+            sp->lora_of = ws.lora_of;
+            sp->blk_rows = ws.blk_rows;
+            sp->T = ws.lora_t;
+        }
+        sr13.X = ws.x_perm;
+        sr13.A = A13;
+        sr13.K = H;
+        sr2.X = ws.act;
+        sr2.A = A2;
+        sr2.K = I;
+        err = rows_shrink ? launch_shrink_rows(sr13, z.max_lt, s) : launch_gemm(kShrink, sh13, z.max_lt, s);
+        if (err != cudaSuccess) return cuda_fail(err, "shrink gate_up");
+    }
     if ((err = mark_stage(3, s)) != cudaSuccess) return cuda_fail(err, "stage event");
     err = launch_gemm(kGateUp, gu, z.max_blocks * ((I + 127) / 128), s);
     if (err != cudaSuccess) return cuda_fail(err, "gate_up");
     if ((err = mark_stage(4, s)) != cudaSuccess) return cuda_fail(err, "stage event");
-    if (lora && (err = launch_gemm(kShrink, sh2, z.max_lt, s)) != cudaSuccess) return cuda_fail(err, "shrink down");
+    if (lora) {
+        err = rows_shrink ? launch_shrink_rows(sr2, z.max_lt, s) : launch_gemm(kShrink, sh2, z.max_lt, s);
+        if (err != cudaSuccess) return cuda_fail(err, "shrink down");
+    }
     if ((err = mark_stage(5, s)) != cudaSuccess) return cuda_fail(err, "stage event");
     err = launch_gemm(kDown, dn, z.max_blocks * ((H + 255) / 256), s);
     if (err != cudaSuccess) return cuda_fail(err, "down");

@@ -19,8 +19,9 @@
 //           other adapters zero, columns past the rank zero) in bf16.
 //
 // Roles (192 threads): warp 0 issues TMA loads into a ring of smem stages
-// (A tile 128 x 64 bf16, B tile N x 64 bf16, both K-major with 128-byte
-// swizzle); warp 1 allocates TMEM and one lane issues tcgen05.mma (M = 128,
+// (A tile 128 x 64 bf16: one 128-row box for a full block, 32-row boxes
+// covering only the real rows of a partial one; B tile N x 64 bf16; both
+// K-major with 128-byte swizzle); warp 1 allocates TMEM and one lane issues tcgen05.mma (M = 128,
 // K = 16 per instruction, fp32 accumulate) and tcgen05.commit; warps 2..5
 // drain the double-buffered TMEM accumulator with tcgen05.ld while the next
 // tile's MMAs run.  Tiles are strided over a grid of at most one CTA per SM.
@@ -121,9 +122,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         *abort_flag = 0;
         fence_barrier_init();
         prefetch_tensormap(&p.tm_a);
+        prefetch_tensormap(&p.tm_a_full);
         prefetch_tensormap(&p.tm_b);
         if (MODE != kShrink && p.has_lora) {
             prefetch_tensormap(&p.tm_t);
+            prefetch_tensormap(&p.tm_t_full);
             prefetch_tensormap(&p.tm_lb);
         }
     }
@@ -134,6 +137,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
+    // Everything above overlapped the previous kernel.  With a shrink as the
+    // previous kernel (pdl_early) only its shrink tiles are needed, and only
+    // by the expand stages: the producer waits for it there, while the base
+    // product (whose inputs were complete before the shrink started) runs.
+    if (!p.pdl_early) griddep_wait();
 
     const int nblocks = *p.n_pad / kBlockM;
     int ncb = 1;
@@ -157,9 +165,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         if (lane == 0) {
             long it = 0;
             bool ok = true;
+            bool waited = false;
             for (long tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
                 const TileCoord tc = decode_tile<MODE>(p, tile, ncb);
                 const int row0 = tc.b * kBlockM;
+                // only the block's real rows are loaded; the MMA rows past
+                // them hold stale data and feed only discarded output rows
+                const int nbox = (p.blk_rows[tc.b] + kRowBox - 1) / kRowBox;
+                const bool full_block = nbox * kRowBox == kBlockM;
+                const uint32_t a_bytes = static_cast<uint32_t>(nbox) * kRowBox * kBlockK * 2;
                 for (int kb = 0; kb < nk; ++kb, ++it) {
                     const int s = static_cast<int>(it % kStages);
                     const uint32_t ph = static_cast<uint32_t>(it / kStages) & 1u;
@@ -171,23 +185,29 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     uint8_t* sb = sa + kATileBytes;
                     const int k0 = kb * kBlockK;
                     if (MODE == kGateUp) {
-                        mbar_arrive_expect_tx(&full[s], kATileBytes + 2 * 128 * kBlockK * 2);
-                        tma_load_2d(sa, &p.tm_a, &full[s], k0, row0);
+                        mbar_arrive_expect_tx(&full[s], a_bytes + 2 * 128 * kBlockK * 2);
                         tma_load_4d(sb, &p.tm_b, &full[s], k0, tc.cb * 128, 0, tc.e);
                         tma_load_4d(sb + 128 * kBlockK * 2, &p.tm_b, &full[s], k0, tc.cb * 128, 1, tc.e);
                     } else if (MODE == kDown) {
-                        mbar_arrive_expect_tx(&full[s], kATileBytes + 256 * kBlockK * 2);
-                        tma_load_2d(sa, &p.tm_a, &full[s], k0, row0);
+                        mbar_arrive_expect_tx(&full[s], a_bytes + 256 * kBlockK * 2);
                         tma_load_3d(sb, &p.tm_b, &full[s], k0, tc.cb * 256, tc.e);
                     } else {
-                        mbar_arrive_expect_tx(&full[s], kATileBytes + rp * kBlockK * 2);
-                        tma_load_2d(sa, &p.tm_a, &full[s], k0, row0);
+                        mbar_arrive_expect_tx(&full[s], a_bytes + rp * kBlockK * 2);
                         tma_load_3d(sb, &p.tm_b, &full[s], k0, 0, tc.l * p.E_tot + tc.e);
                     }
+                    if (full_block)
+                        tma_load_2d(sa, &p.tm_a_full, &full[s], k0, row0);
+                    else
+                        for (int i = 0; i < nbox; ++i)
+                            tma_load_2d(sa + i * kRowBox * kBlockK * 2, &p.tm_a, &full[s], k0, row0 + i * kRowBox);
                 }
                 if (!ok || !expand) continue;
                 const int nad = p.blk_nad[tc.b];
                 const int lt0 = p.blk_lt_start[tc.b];
+                if (p.pdl_early && nad > 0 && !waited) {
+                    griddep_wait();  // the shrink tiles are complete from here on
+                    waited = true;
+                }
                 for (int i = 0; i < nad; ++i, ++it) {
                     const int l = p.blk_lora[static_cast<long>(tc.b) * p.cap + i];
                     const int s = static_cast<int>(it % kStages);
@@ -200,15 +220,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     uint8_t* sb = sa + kATileBytes;
                     const int le = l * p.E_tot + tc.e;
                     if (MODE == kGateUp) {
-                        mbar_arrive_expect_tx(&full[s], kATileBytes + 2 * 128 * kBlockK * 2);
-                        tma_load_2d(sa, &p.tm_t, &full[s], 0, (lt0 + i) * kBlockM);
+                        mbar_arrive_expect_tx(&full[s], a_bytes + 2 * 128 * kBlockK * 2);
                         tma_load_4d(sb, &p.tm_lb, &full[s], 0, tc.cb * 128, 0, le);
                         tma_load_4d(sb + 128 * kBlockK * 2, &p.tm_lb, &full[s], 0, tc.cb * 128, 1, le);
                     } else {
-                        mbar_arrive_expect_tx(&full[s], kATileBytes + 256 * kBlockK * 2);
-                        tma_load_2d(sa, &p.tm_t, &full[s], 0, (lt0 + i) * kBlockM);
+                        mbar_arrive_expect_tx(&full[s], a_bytes + 256 * kBlockK * 2);
                         tma_load_3d(sb, &p.tm_lb, &full[s], 0, tc.cb * 256, le);
                     }
+                    if (full_block)
+                        tma_load_2d(sa, &p.tm_t_full, &full[s], 0, (lt0 + i) * kBlockM);
+                    else
+                        for (int j = 0; j < nbox; ++j)
+                            tma_load_2d(sa + j * kRowBox * kBlockK * 2, &p.tm_t, &full[s], 0,
+                                        (lt0 + i) * kBlockM + j * kRowBox);
                 }
             }
             if (!ok) {
@@ -367,6 +391,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         tc_fence_after();
         tmem_dealloc(tmem_base, C::kTmemCols);
     }
+    // the grid never completes before the one it follows, so whatever runs
+    // after it may rely on both
+    if (p.pdl_early) griddep_wait();
 }
 
 template <int MODE>
@@ -383,8 +410,7 @@ cudaError_t launch_mode(const GemmParams& p, long max_tiles, cudaStream_t s) {
     }
     long grid = device_sm_count();
     if (grid > max_tiles) grid = max_tiles;
-    gemm_kernel<MODE><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(gemm_kernel<MODE>, dim3(static_cast<unsigned>(grid)), dim3(kThreads), smem, s, p);
 }
 
 }  // namespace

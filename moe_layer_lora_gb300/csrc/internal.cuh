@@ -5,6 +5,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "mlora.h"
 
 namespace mlora {
@@ -12,6 +14,7 @@ namespace mlora {
 constexpr int kBlockM = MLORA_FORWARD_BLOCK_M;  // token rows per GEMM tile (MMA M)
 constexpr int kBlockK = 64;                     // bf16 elements per 128-byte swizzle row
 constexpr int kLoraTileCols = 64;               // shrink result row, padded to one swizzle row
+constexpr int kRowBox = 32;                     // token rows per TMA box of an A operand
 
 // Per-forward buffers carved out of the caller's workspace.
 struct Workspace {
@@ -20,6 +23,7 @@ struct Workspace {
     int32_t* lt_total;     // number of (block, adapter) shrink tiles
     int32_t* sorted_ids;   // [max_padded]
     int32_t* expert_ids;   // [max_blocks]
+    int32_t* blk_rows;     // [max_blocks] real (non-padding) rows of each block
     int32_t* lora_of;      // [max_padded] adapter of each sorted position (-1: none / pad)
     int32_t* blk_nad;      // [max_blocks] distinct adapters in the block
     int32_t* blk_lt_start; // [max_blocks] first shrink tile of the block
@@ -48,8 +52,10 @@ Workspace carve_workspace(const Sizes& z, void* base);  // base == nullptr: sizi
 
 long align_max_padded(long S, int E_tot, int block_m);
 
-// Extra outputs of align used only inside the forward.
+// Extra outputs of align used only inside the forward.  blk_rows is always
+// written when set; the adapter fields only when token_lora_idx is set.
 struct AlignExtra {
+    int32_t* blk_rows;
     const int32_t* token_lora_idx;
     int L;
     int K_total;
@@ -80,12 +86,15 @@ cudaError_t launch_combine(const void* y_slot, const int32_t* topk_ids, const fl
 enum GemmMode : int { kGateUp = 0, kDown = 1, kShrink = 2 };
 
 struct alignas(64) GemmParams {
-    CUtensorMap tm_a;   // token rows [rows, K], box {64, 128}
+    CUtensorMap tm_a;   // token rows [rows, K], box {64, kRowBox}
     CUtensorMap tm_b;   // weight rows (w13 / w2 / A13 / A2 view)
-    CUtensorMap tm_t;   // LoRA shrink tiles [tiles*128, 64], box {64, 128}
+    CUtensorMap tm_t;   // LoRA shrink tiles [tiles*128, 64], box {64, kRowBox}
     CUtensorMap tm_lb;  // LoRA expand weights (B13 / B2 view)
+    CUtensorMap tm_a_full;  // tm_a with box {64, 128}: one box per full block
+    CUtensorMap tm_t_full;  // tm_t with box {64, 128}
     const int32_t* n_pad;
     const int32_t* expert_ids;
+    const int32_t* blk_rows;
     const int32_t* sorted_ids;
     const int32_t* lora_of;
     const int32_t* blk_nad;
@@ -103,11 +112,51 @@ struct alignas(64) GemmParams {
     int rank;
     int S;          // sentinel slot value M*K'
     int has_lora;
+    int pdl_early;  // the preceding kernel is a shrink: wait for it only before the expand stages
     float scaling;
 };
 
 cudaError_t launch_gemm(GemmMode mode, const GemmParams& p, long max_tiles, cudaStream_t s);
 
+// CUDA-core shrink for small batches (few rows per (block, adapter) tile):
+// T[t] = s * X[rows of block b with adapter l] A_{l,e}^T, masked, bf16.
+struct ShrinkParams {
+    const void* X;  // [rows, K] bf16, sorted order
+    const void* A;  // [L*E_tot, rank, K] bf16
+    int K;
+    int rank;
+    int E_tot;
+    float scaling;
+    const int32_t* lt_block;
+    const int32_t* lt_lora;
+    const int32_t* lt_total;
+    const int32_t* expert_ids;
+    const int32_t* lora_of;
+    const int32_t* blk_rows;
+    void* T;  // [tiles*128, 64] bf16
+};
+cudaError_t launch_shrink_rows(const ShrinkParams& p, long max_tiles, cudaStream_t s);
+// M*K'*rank up to which the CUDA-core shrink is used (it then runs beside
+// the GEMM that consumes it); larger shrinks run on the tensor cores
+constexpr long kShrinkRowsMaxWork = 4096L * 16;
+
 int device_sm_count();
+
+// Launch with programmatic stream serialisation (see griddep_wait in ptx.cuh).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 }  // namespace mlora

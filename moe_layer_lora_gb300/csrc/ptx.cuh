@@ -186,6 +186,19 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// ------------------------------------------------ programmatic dependent launch --
+// Every kernel of the layer is launched with programmatic stream
+// serialisation, so it may start while the previous kernel in the stream is
+// still running.  griddep_wait() blocks until that grid has completed and
+// its writes are visible (it returns at once without such a dependency);
+// griddep_launch_dependents() lets the next kernel start launching.  A
+// kernel triggers only after its own wait, so when a kernel starts, every
+// kernel two or more places before it in the stream has completed.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------- misc --
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);

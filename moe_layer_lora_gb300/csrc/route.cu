@@ -13,6 +13,7 @@
 #include <math.h>
 
 #include "internal.cuh"
+#include "ptx.cuh"
 
 namespace mlora {
 namespace {
@@ -26,6 +27,8 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ lo
                                                     int M, int E, int top_k, int scoring, int renormalize,
                                                     int n_shared, float inv_rsf, int32_t* __restrict__ ids,
                                                     float* __restrict__ w) {
+    griddep_wait();
+    griddep_launch_dependents();
     const int token = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (token >= M) return;  // whole warp leaves together
@@ -132,10 +135,9 @@ cudaError_t launch_route(const float* logits, const float* bias, int M, int E, i
     const dim3 block(256);
     const dim3 grid((M + 7) / 8);
     const int vpl = (E + 31) / 32;
-#define MLORA_ROUTE_CASE(V)                                                                                    \
-    route_kernel<V><<<grid, block, 0, s>>>(logits, bias, M, E, top_k, scoring, renormalize, n_shared, inv_rsf, \
-                                           ids, w);                                                            \
-    break;
+#define MLORA_ROUTE_CASE(V)                                                                                 \
+    return launch_pdl(route_kernel<V>, grid, block, 0, s, logits, bias, M, E, top_k, scoring, renormalize, n_shared, \
+                      inv_rsf, ids, w);
     switch (vpl <= 1 ? 1 : vpl <= 2 ? 2 : vpl <= 4 ? 4 : vpl <= 8 ? 8 : vpl <= 16 ? 16 : 32) {
         case 1: MLORA_ROUTE_CASE(1)
         case 2: MLORA_ROUTE_CASE(2)
@@ -145,7 +147,6 @@ cudaError_t launch_route(const float* logits, const float* bias, int M, int E, i
         default: MLORA_ROUTE_CASE(32)
     }
 #undef MLORA_ROUTE_CASE
-    return cudaGetLastError();
 }
 
 }  // namespace mlora

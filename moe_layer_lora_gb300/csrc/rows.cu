@@ -18,6 +18,8 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
                                                           const int32_t* __restrict__ sorted,
                                                           const int32_t* __restrict__ n_pad, int S, int K_total,
                                                           uint4* __restrict__ x_perm) {
+    griddep_wait();
+    griddep_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int warps = blockDim.x >> 5;
     const int np = *n_pad;
@@ -44,6 +46,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ 
                                                       const int32_t* __restrict__ topk_ids,
                                                       const float* __restrict__ topk_w, int M, int H8, int K_total,
                                                       int E_tot, float out_scale, uint4* __restrict__ y) {
+    griddep_wait();
+    griddep_launch_dependents();
     const long total = static_cast<long>(M) * H8;
     for (long idx = blockIdx.x * static_cast<long>(blockDim.x) + threadIdx.x; idx < total;
          idx += static_cast<long>(gridDim.x) * blockDim.x) {
@@ -78,10 +82,9 @@ cudaError_t launch_gather_rows(const void* x, int H, const int32_t* sorted, cons
     long blocks = (max_padded + warps_per_block - 1) / warps_per_block;
     const long cap = 8L * device_sm_count();
     if (blocks > cap) blocks = cap;
-    gather_rows_kernel<<<static_cast<unsigned>(blocks), 32 * warps_per_block, 0, s>>>(
-        static_cast<const uint4*>(x), H / 8, sorted, n_pad, static_cast<int>(S), K_total,
-        static_cast<uint4*>(x_perm));
-    return cudaGetLastError();
+    return launch_pdl(gather_rows_kernel, dim3(static_cast<unsigned>(blocks)), dim3(32 * warps_per_block), 0, s,
+                      static_cast<const uint4*>(x), H / 8, sorted, n_pad, static_cast<int>(S), K_total,
+                      static_cast<uint4*>(x_perm));
 }
 
 cudaError_t launch_combine(const void* y_slot, const int32_t* topk_ids, const float* topk_w, int M, int H,
@@ -91,10 +94,9 @@ cudaError_t launch_combine(const void* y_slot, const int32_t* topk_ids, const fl
     long blocks = (total + 255) / 256;
     const long cap = 16L * device_sm_count();
     if (blocks > cap) blocks = cap;
-    combine_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(static_cast<const uint4*>(y_slot), topk_ids,
-                                                                 topk_w, M, H / 8, K_total, E_tot, out_scale,
-                                                                 static_cast<uint4*>(y));
-    return cudaGetLastError();
+    return launch_pdl(combine_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s,
+                      static_cast<const uint4*>(y_slot), topk_ids, topk_w, M, H / 8, K_total, E_tot, out_scale,
+                      static_cast<uint4*>(y));
 }
 
 }  // namespace mlora

@@ -95,6 +95,9 @@ def test_stress_sampled_and_early_exit():
          scoring=wl.SCORE_SIGMOID_BIAS, L=4, r=16, seed=106),               # shared slots with adapters
     dict(M=16, H=256, I=128, E=8, top_k=2, L=0, r=0, lora_mode="none", seed=107),  # no adapters
     dict(M=24, H=384, I=136, E=8, top_k=2, renormalize=0, L=4, r=32, seed=108),
+    # more than 4096 slots: the tensor-core shrink on ragged K and rank
+    dict(M=1100, H=136, I=72, E=5, top_k=4, L=3, r=24, seed=109),
+    dict(M=1030, H=64, I=200, E=6, top_k=4, L=9, r=8, seed=110),
 ])
 def test_edges(over):
     _layer(wl.spec("tiny", **over), label=str(over))

@@ -123,12 +123,13 @@ def algorithmic(s: wl.Spec, ids: np.ndarray, idx) -> dict:
         n_pairs = a_slots = 0
     b = 2  # bf16
     st = {
-        "gate_up": dict(bytes=n_exp * 2 * I * H * b + n_pairs * 2 * I * r * b + S * (H + I) * b,
-                        flops=2.0 * S * H * 2 * I + 2.0 * a_slots * 2 * I * r),
-        "down": dict(bytes=n_exp * H * I * b + n_pairs * H * r * b + S * (I + H) * b,
-                     flops=2.0 * S * I * H + 2.0 * a_slots * H * r),
-        "shrink_gate_up": dict(bytes=n_pairs * r * H * b + a_slots * H * b, flops=2.0 * a_slots * r * H),
-        "shrink_down": dict(bytes=n_pairs * r * I * b + a_slots * I * b, flops=2.0 * a_slots * r * I),
+        # the gate_up and down kernels include their adapter shrink
+        "gate_up": dict(bytes=n_exp * 2 * I * H * b + n_pairs * (2 * I + H) * r * b + S * (H + I) * b,
+                        flops=2.0 * S * H * 2 * I + 2.0 * a_slots * (2 * I + H) * r),
+        "down": dict(bytes=n_exp * H * I * b + n_pairs * (H + I) * r * b + S * (I + H) * b,
+                     flops=2.0 * S * I * H + 2.0 * a_slots * (H + I) * r),
+        "shrink_gate_up": dict(bytes=0, flops=0.0),
+        "shrink_down": dict(bytes=0, flops=0.0),
         "gather": dict(bytes=S * H * b * 2, flops=0.0),
         "combine": dict(bytes=S * H * b + M * H * b, flops=2.0 * S * H),
         "align": dict(bytes=S * 4 * 3, flops=0.0),

@@ -199,9 +199,11 @@ mlora_status mlora_moe_read_status(const void* workspace, uint32_t* host_status,
  * cudaEvent_t handles (passed as void*) that every later mlora_moe_forward
  * on this thread records on its stream at the stage boundaries:
  *   [0] before align, [1] after align, [2] after the row gather,
- *   [3] after the gate_up shrink, [4] after the gate_up GEMM,
- *   [5] after the down shrink, [6] after the down GEMM, [7] after combine.
- * Stages that do not run record adjacent events.  The events are recorded
+ *   [3] = [2], [4] after the gate_up GEMM (its LoRA shrink included),
+ *   [5] = [4], [6] after the down GEMM (its LoRA shrink included),
+ *   [7] after combine.
+ * (Events [3] and [5] mark where a separate shrink pass would sit; the
+ * shrink runs inside the GEMM kernels, so those stages are empty.)  The events are recorded
  * with cudaEventRecordExternal, so they also become event nodes when the
  * forward is captured into a CUDA graph.  events == NULL (or count == 0)
  * switches the hook off.  The caller owns the events and keeps them alive

@@ -15,8 +15,8 @@
 // Inside the forward the same pass also records the real (non-padding) row
 // count of every block and, with adapters, per sorted position the token's
 // adapter and per block of kBlockM positions the ascending list of distinct
-// adapters, numbered globally into "shrink tiles" (block, adapter): one
-// masked LoRA tile per pair.
+// adapters; each (block, adapter) pair gets a masked LoRA tile, and the
+// adapters of a block are cut into shrink group tiles of up to gsize.
 #include "internal.cuh"
 #include "ptx.cuh"
 
@@ -185,24 +185,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncthreads();
 
-    // 6. number the (block, adapter) tiles
-    int running = 0;
+    // 6. number the blocks' LoRA tiles (one per (block, adapter)) and the
+    //    shrink group tiles (up to gsize adapters of one block each)
+    int run_lt = 0, run_gt = 0;
     for (int cb = 0; cb < nblocks; cb += kThreads) {
         const int b = cb + tid;
         const int v = b < nblocks ? ex.blk_nad[b] : 0;
-        int chunk_total;
-        const int excl = block_exclusive_scan(v, scratch, &chunk_total);
+        const int ng = (v + ex.gsize - 1) / ex.gsize;
+        int lt_chunk, gt_chunk;
+        const int lt_excl = block_exclusive_scan(v, scratch, &lt_chunk);
+        const int gt_excl = block_exclusive_scan(ng, scratch, &gt_chunk);
         if (b < nblocks) {
-            const int t0 = running + excl;
-            ex.blk_lt_start[b] = t0;
-            for (int i = 0; i < v; ++i) {
-                ex.lt_block[t0 + i] = b;
-                ex.lt_lora[t0 + i] = ex.blk_lora[static_cast<long>(b) * ex.cap + i];
+            ex.blk_lt_start[b] = run_lt + lt_excl;
+            for (int j = 0; j < ng; ++j) {
+                ex.gt_block[run_gt + gt_excl + j] = b;
+                ex.gt_first[run_gt + gt_excl + j] = j * ex.gsize;
             }
         }
-        running += chunk_total;
+        run_lt += lt_chunk;
+        run_gt += gt_chunk;
     }
-    if (tid == 0) *ex.lt_total = running;
+    if (tid == 0) *ex.gt_total = run_gt;
 }
 
 }  // namespace

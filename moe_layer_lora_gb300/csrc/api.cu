@@ -4,13 +4,14 @@
 //
 // Forward, all on the caller's stream, no host synchronisation, no
 // allocation (capturable in a CUDA graph):
-//   memset(status) -> align (+ per-block adapter lists) -> gather x rows
-//   -> [shrink gate_up] -> gate_up GEMM (+ expand, SwiGLU)
-//   -> [shrink down]    -> down GEMM (+ expand) -> weighted combine
-// The bracketed shrink launches are skipped when the call carries no
-// adapters; when adapters are given but no token uses one, the shrink grid
-// finds zero tiles on the device and the GEMMs skip the expand chunks, so
-// the layer exits early without a host round trip ("Amazon SageMaker 및
+//   memset(status, counters) -> align (+ per-block adapter lists)
+//   -> gather x rows -> gate_up GEMM (shrink tiles, then base tiles with the
+//   expand and SwiGLU) -> down GEMM (shrink tiles, base tiles with the
+//   expand) -> weighted combine
+// Without adapters the GEMMs run only base tiles; when adapters are given
+// but no token uses one, align finds no shrink tiles on the device and the
+// GEMMs skip the expand chunks, so the layer exits early without a host
+// round trip ("Amazon SageMaker 및
 // Amazon Bedrock에서 vLLM을 활용한 MoE 모델 Multi-LoRA 서빙 최적화", section
 // "섹션별 상세" paragraph 2).
 #include <cuda.h>
@@ -118,6 +119,7 @@ Sizes make_sizes(int M, int H, int I, int E_tot, int K_total, int L, int rank) {
     z.max_blocks = z.max_padded / kBlockM;
     z.cap = z.lora ? std::min(L, kBlockM) : 0;
     z.max_lt = z.max_blocks * z.cap;
+    z.gsize = z.lora ? 256 / ((rank + 15) / 16 * 16) : 1;
     return z;
 }
 
@@ -129,10 +131,16 @@ Workspace carve_workspace(const Sizes& z, void* base) {
         off += round256(bytes);
         return base ? static_cast<char*>(base) + o : nullptr;
     };
+    // cleared by every forward: the header and the per-block shrink counters
     char* header = take(256);
     w.status = reinterpret_cast<uint32_t*>(header);
     w.n_pad = reinterpret_cast<int32_t*>(header ? header + 4 : nullptr);
-    w.lt_total = reinterpret_cast<int32_t*>(header ? header + 8 : nullptr);
+    w.gt_total = reinterpret_cast<int32_t*>(header ? header + 8 : nullptr);
+    if (z.lora) {
+        w.done13 = reinterpret_cast<int32_t*>(take(4 * z.max_blocks));
+        w.done2 = reinterpret_cast<int32_t*>(take(4 * z.max_blocks));
+    }
+    w.zeroed_bytes = off;
     w.sorted_ids = reinterpret_cast<int32_t*>(take(4 * z.max_padded));
     w.expert_ids = reinterpret_cast<int32_t*>(take(4 * z.max_blocks));
     w.blk_rows = reinterpret_cast<int32_t*>(take(4 * z.max_blocks));
@@ -141,8 +149,8 @@ Workspace carve_workspace(const Sizes& z, void* base) {
         w.blk_nad = reinterpret_cast<int32_t*>(take(4 * z.max_blocks));
         w.blk_lt_start = reinterpret_cast<int32_t*>(take(4 * z.max_blocks));
         w.blk_lora = reinterpret_cast<int32_t*>(take(4 * z.max_blocks * z.cap));
-        w.lt_block = reinterpret_cast<int32_t*>(take(4 * z.max_lt));
-        w.lt_lora = reinterpret_cast<int32_t*>(take(4 * z.max_lt));
+        w.gt_block = reinterpret_cast<int32_t*>(take(4 * z.max_lt));
+        w.gt_first = reinterpret_cast<int32_t*>(take(4 * z.max_lt));
     }
     w.x_perm = take(2 * static_cast<size_t>(z.max_padded) * z.H);
     w.act = take(2 * static_cast<size_t>(z.max_padded) * z.I);
@@ -249,7 +257,7 @@ mlora_status mlora_moe_forward(const void* x, const void* w13, const void* w2, c
     if (workspace_bytes < ws.bytes) return MLORA_ERR_WORKSPACE;
 
     // ---- tensor maps (dims innermost first) ----
-    GemmParams gu{}, dn{}, sh13{}, sh2{};
+    GemmParams gu{}, dn{};
     const cuuint64_t H_ = H, I_ = I, E_ = E_tot, MP = z.max_padded;
     bool ok = true;
     {
@@ -275,15 +283,13 @@ mlora_status mlora_moe_forward(const void* x, const void* w13, const void* w2, c
             ok &= make_map(&gu.tm_t_full, ws.lora_t, 2, dt, st_, bxf);
             dn.tm_t = gu.tm_t;
             dn.tm_t_full = gu.tm_t_full;
+            // shrink weights: rank rows past the rank read as zero
             const cuuint64_t dA13[3] = {H_, R, LE}, sA13[2] = {H_ * 2, R * H_ * 2};
             const cuuint32_t bA[3] = {64, rp, 1};
-            sh13.tm_a = gu.tm_a;
-            sh13.tm_a_full = gu.tm_a_full;
-            ok &= make_map(&sh13.tm_b, A13, 3, dA13, sA13, bA);
+            ok &= make_map(&gu.tm_sa, A13, 3, dA13, sA13, bA);
             const cuuint64_t dA2[3] = {I_, R, LE}, sA2[2] = {I_ * 2, R * I_ * 2};
-            sh2.tm_a = dn.tm_a;
-            sh2.tm_a_full = dn.tm_a_full;
-            ok &= make_map(&sh2.tm_b, A2, 3, dA2, sA2, bA);
+            ok &= make_map(&dn.tm_sa, A2, 3, dA2, sA2, bA);
+            // expand weights: columns past the rank read as zero
             const cuuint64_t dB13[4] = {R, I_, 2, LE}, sB13[3] = {R * 2, I_ * R * 2, 2 * I_ * R * 2};
             ok &= make_map(&gu.tm_lb, B13, 4, dB13, sB13, b13);
             const cuuint64_t dB2[3] = {R, H_, LE}, sB2[2] = {R * 2, H_ * R * 2};
@@ -292,48 +298,40 @@ mlora_status mlora_moe_forward(const void* x, const void* w13, const void* w2, c
     }
     if (!ok) return cuda_fail(cudaErrorInvalidValue, "tensor map encoding");
 
-    auto fill_common = [&](GemmParams& p) {
-        p.n_pad = ws.n_pad;
-        p.expert_ids = ws.expert_ids;
-        p.blk_rows = ws.blk_rows;
-        p.sorted_ids = ws.sorted_ids;
-        p.lora_of = ws.lora_of;
-        p.blk_nad = ws.blk_nad;
-        p.blk_lora = ws.blk_lora;
-        p.blk_lt_start = ws.blk_lt_start;
-        p.lt_block = ws.lt_block;
-        p.lt_lora = ws.lt_lora;
-        p.lt_total = ws.lt_total;
-        p.status = ws.status;
-        p.E_tot = E_tot;
-        p.cap = z.cap;
-        p.rank = r_eff;
-        p.S = static_cast<int>(z.S);
-        p.has_lora = lora ? 1 : 0;
-        p.scaling = scaling;
-    };
-    fill_common(gu);
-    fill_common(dn);
-    fill_common(sh13);
-    fill_common(sh2);
-    gu.pdl_early = lora ? 1 : 0;
-    dn.pdl_early = lora ? 1 : 0;
+    for (GemmParams* p : {&gu, &dn}) {
+        p->n_pad = ws.n_pad;
+        p->expert_ids = ws.expert_ids;
+        p->blk_rows = ws.blk_rows;
+        p->sorted_ids = ws.sorted_ids;
+        p->lora_of = ws.lora_of;
+        p->blk_nad = ws.blk_nad;
+        p->blk_lora = ws.blk_lora;
+        p->blk_lt_start = ws.blk_lt_start;
+        p->gt_block = ws.gt_block;
+        p->gt_first = ws.gt_first;
+        p->gt_total = ws.gt_total;
+        p->lora_t = ws.lora_t;
+        p->status = ws.status;
+        p->E_tot = E_tot;
+        p->cap = z.cap;
+        p->gsize = z.gsize;
+        p->rank = r_eff;
+        p->S = static_cast<int>(z.S);
+        p->has_lora = lora ? 1 : 0;
+        p->scaling = scaling;
+    }
+    gu.done = ws.done13;
     gu.out = ws.act;
     gu.K = H;
     gu.n_out = I;
+    dn.done = ws.done2;
     dn.out = ws.y_slot;
     dn.K = I;
     dn.n_out = H;
-    sh13.out = ws.lora_t;
-    sh13.K = H;
-    sh13.n_out = r_eff;
-    sh2.out = ws.lora_t;
-    sh2.K = I;
-    sh2.n_out = r_eff;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t err = cudaMemsetAsync(ws.status, 0, 16, s);
-    if (err != cudaSuccess) return cuda_fail(err, "status reset");
+    cudaError_t err = cudaMemsetAsync(workspace, 0, ws.zeroed_bytes, s);
+    if (err != cudaSuccess) return cuda_fail(err, "workspace reset");
     if ((err = mark_stage(0, s)) != cudaSuccess) return cuda_fail(err, "stage event");
     AlignExtra ex{};
     ex.blk_rows = ws.blk_rows;
@@ -346,9 +344,10 @@ mlora_status mlora_moe_forward(const void* x, const void* w13, const void* w2, c
         ex.blk_nad = ws.blk_nad;
         ex.blk_lora = ws.blk_lora;
         ex.blk_lt_start = ws.blk_lt_start;
-        ex.lt_block = ws.lt_block;
-        ex.lt_lora = ws.lt_lora;
-        ex.lt_total = ws.lt_total;
+        ex.gsize = z.gsize;
+        ex.gt_block = ws.gt_block;
+        ex.gt_first = ws.gt_first;
+        ex.gt_total = ws.gt_total;
     }
     err = launch_align(topk_ids, z.S, E_tot, kBlockM, z.max_padded, ws.sorted_ids, ws.expert_ids, ws.n_pad,
                        ws.status, &ex, s);
@@ -356,43 +355,14 @@ mlora_status mlora_moe_forward(const void* x, const void* w13, const void* w2, c
     if ((err = mark_stage(1, s)) != cudaSuccess) return cuda_fail(err, "stage event");
     err = launch_gather_rows(x, H, ws.sorted_ids, ws.n_pad, z.S, K_total, z.max_padded, ws.x_perm, s);
     if (err != cudaSuccess) return cuda_fail(err, "gather");
-    if ((err = mark_stage(2, s)) != cudaSuccess) return cuda_fail(err, "stage event");
-    // the shrink: CUDA cores (beside the consuming GEMM) while it is small,
-    // tensor cores beyond
-    const bool rows_shrink = z.S * r_eff <= kShrinkRowsMaxWork;
-    ShrinkParams sr13{}, sr2{};
-    if (lora) {
-        for (ShrinkParams* sp : {&sr13, &sr2}) {
-            sp->rank = r_eff;
-            sp->E_tot = E_tot;
-            sp->scaling = scaling;
-            sp->lt_block = ws.lt_block;
-            sp->lt_lora = ws.lt_lora;
-            sp->lt_total = ws.lt_total;
-            sp->expert_ids = ws.expert_ids;
-            sp->lora_of = ws.lora_of;
-            sp->blk_rows = ws.blk_rows;
-            sp->T = ws.lora_t;
-        }
-        sr13.X = ws.x_perm;
-        sr13.A = A13;
-        sr13.K = H;
-        sr2.X = ws.act;
-        sr2.A = A2;
-        sr2.K = I;
-        err = rows_shrink ? launch_shrink_rows(sr13, z.max_lt, s) : launch_gemm(kShrink, sh13, z.max_lt, s);
-        if (err != cudaSuccess) return cuda_fail(err, "shrink gate_up");
-    }
-    if ((err = mark_stage(3, s)) != cudaSuccess) return cuda_fail(err, "stage event");
-    err = launch_gemm(kGateUp, gu, z.max_blocks * ((I + 127) / 128), s);
+    // the shrinks run inside the GEMM kernels: stages 3 and 5 stay empty
+    if ((err = mark_stage(2, s)) != cudaSuccess || (err = mark_stage(3, s)) != cudaSuccess)
+        return cuda_fail(err, "stage event");
+    err = launch_gemm(kGateUp, gu, z.max_lt + z.max_blocks * ((I + 127) / 128), s);
     if (err != cudaSuccess) return cuda_fail(err, "gate_up");
-    if ((err = mark_stage(4, s)) != cudaSuccess) return cuda_fail(err, "stage event");
-    if (lora) {
-        err = rows_shrink ? launch_shrink_rows(sr2, z.max_lt, s) : launch_gemm(kShrink, sh2, z.max_lt, s);
-        if (err != cudaSuccess) return cuda_fail(err, "shrink down");
-    }
-    if ((err = mark_stage(5, s)) != cudaSuccess) return cuda_fail(err, "stage event");
-    err = launch_gemm(kDown, dn, z.max_blocks * ((H + 255) / 256), s);
+    if ((err = mark_stage(4, s)) != cudaSuccess || (err = mark_stage(5, s)) != cudaSuccess)
+        return cuda_fail(err, "stage event");
+    err = launch_gemm(kDown, dn, z.max_lt + z.max_blocks * ((H + 255) / 256), s);
     if (err != cudaSuccess) return cuda_fail(err, "down");
     if ((err = mark_stage(6, s)) != cudaSuccess) return cuda_fail(err, "stage event");
     err = launch_combine(ws.y_slot, topk_ids, topk_w, M, H, K_total, E_tot, out_scale, y, s);

@@ -1,31 +1,42 @@
-// gemm.cu -- the grouped expert GEMMs on the 5th-generation tensor cores.
+// gemm.cu -- the grouped expert GEMMs on the 5th-generation tensor cores,
+// with the per-token LoRA shrink and expand folded into the same kernel.
 //
-// One persistent, warp-specialised kernel template serves three products
-// over blocks of kBlockM = 128 sorted slots (all slots of a block share one
-// expert e, from align):
+// One persistent, warp-specialised kernel per projection works through two
+// kinds of tiles over blocks of kBlockM = 128 sorted slots (all slots of a
+// block share one expert e, from align):
 //
-//  kGateUp: h = X W13_e^T over a 128-column slab j0.. of the gate rows and
-//           the same slab of the up rows (one MMA with N = 256: B rows 0..127
-//           gate, 128..255 up), then, per adapter l present in the block,
-//           h += T_l B13_{l,e}^T as extra K-chunks into the same TMEM
-//           accumulator (the LoRA expand folded into the projection,
-//           "Amazon SageMaker 및 Amazon Bedrock에서 vLLM을 활용한 MoE 모델
-//           Multi-LoRA 서빙 최적화", section "섹션별 상세" paragraphs 1 and 3);
-//           epilogue: act = silu(gate) * up -> bf16.
-//  kDown:   d = act W2_e^T over 256 output columns, + T2_l B2_{l,e}^T chunks;
-//           epilogue: bf16 row of the slot's expert output.
-//  kShrink: t = X A_{l,e}^T for one (block, adapter) pair, N = rank rounded
-//           up to 16; epilogue: the masked, scaled shrink tile T_l (rows of
-//           other adapters zero, columns past the rank zero) in bf16.
+//  shrink tiles (first in every CTA's sequence, only with adapters):
+//      T_l = s * X A_{l,e}^T for up to `gsize` adapters l of one block at
+//      once -- the adapters' rank rows are stacked along N (N = g * rank
+//      rounded up to 16) -- written as one masked bf16 tile per (block,
+//      adapter): rows of other adapters zero, columns past the rank zero.
+//      When a block's shrink tiles are all written, a per-block counter is
+//      bumped.
+//  base tiles:
+//      kGateUp: h = X W13_e^T over a 128-column slab j0.. of the gate rows
+//               and the same slab of the up rows (one MMA with N = 256: B
+//               rows 0..127 gate, 128..255 up); epilogue act = silu(g) * u.
+//      kDown:   d = act W2_e^T over 256 output columns; epilogue the slot's
+//               expert output in bf16.
+//      With adapters, after the K loop every adapter l present in the block
+//      adds T_l B_{l,e}^T as extra K-chunks into the same TMEM accumulator:
+//      the expand folded into the projection ("Amazon SageMaker 및 Amazon
+//      Bedrock에서 vLLM을 활용한 MoE 모델 Multi-LoRA 서빙 최적화", section
+//      "섹션별 상세" paragraphs 1-3).  The producer waits for the block's
+//      shrink counter only before those chunks, so the base product of the
+//      first tiles streams while other CTAs still run shrink tiles -- the
+//      overlap of shrink and expand the pages get from PDL, inside one grid.
 //
 // Roles (192 threads): warp 0 issues TMA loads into a ring of smem stages
 // (A tile 128 x 64 bf16: one 128-row box for a full block, 32-row boxes
-// covering only the real rows of a partial one; B tile N x 64 bf16; both
-// K-major with 128-byte swizzle); warp 1 allocates TMEM and one lane issues tcgen05.mma (M = 128,
-// K = 16 per instruction, fp32 accumulate) and tcgen05.commit; warps 2..5
-// drain the double-buffered TMEM accumulator with tcgen05.ld while the next
-// tile's MMAs run.  Tiles are strided over a grid of at most one CTA per SM.
-// Every mbarrier wait is bounded (ptx.cuh).
+// covering only the real rows of a partial one; B tile 256 x 64 bf16; both
+// K-major with 128-byte swizzle); warp 1 allocates TMEM and one lane issues
+// tcgen05.mma (M = 128, K = 16 per instruction, fp32 accumulate) and
+// tcgen05.commit; warps 2..5 drain the double-buffered TMEM accumulator with
+// tcgen05.ld while the next tile's MMAs run.  Tiles are strided over a grid
+// of at most one CTA per SM.  Every wait is bounded (~2 s, ptx.cuh): a
+// timeout records MLORA_DEV_TIMEOUT, drains the copies in flight, frees
+// TMEM and returns.
 #include "internal.cuh"
 #include "ptx.cuh"
 
@@ -33,32 +44,13 @@ namespace mlora {
 namespace {
 
 constexpr int kThreads = 192;
-constexpr int kATileBytes = kBlockM * kBlockK * 2;  // 16 KiB
-
-template <int MODE>
-struct Cfg {
-    static constexpr int kStages = 4;
-    static constexpr int kBRows = 256;
-    static constexpr int kAccCols = 256;
-    static constexpr int kTmemCols = 512;
-};
-template <>
-struct Cfg<kShrink> {
-    static constexpr int kStages = 6;
-    static constexpr int kBRows = 64;
-    static constexpr int kAccCols = 64;
-    static constexpr int kTmemCols = 128;
-};
-
-template <int MODE>
-constexpr int stage_bytes() {
-    return kATileBytes + Cfg<MODE>::kBRows * kBlockK * 2;
-}
-
-template <int MODE>
-constexpr int smem_bytes() {
-    return Cfg<MODE>::kStages * stage_bytes<MODE>() + 1024 /* alignment slack */ + 256 /* barriers */;
-}
+constexpr int kStages = 4;
+constexpr int kBRows = 256;
+constexpr int kATileBytes = kBlockM * kBlockK * 2;                // 16 KiB
+constexpr int kStageBytes = kATileBytes + kBRows * kBlockK * 2;  // 48 KiB
+constexpr int kAccCols = 256;
+constexpr int kTmemCols = 512;
+constexpr int kSmemBytes = kStages * kStageBytes + 1024 /* alignment slack */ + 256 /* barriers */;
 
 // Bounded wait used only while unwinding after an abort: ignores the abort
 // flag so that copies already in flight land before the CTA exits.
@@ -67,37 +59,61 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
     mbar_wait(bar, parity, &zero, nullptr, kWaitCycles / 8);
 }
 
-struct TileCoord {
+// Bounded wait until *flag >= target (acquire), then order this thread's
+// later TMA (async-proxy) reads after it.
+__device__ bool wait_counter(const int32_t* flag, int target, volatile int* abort_flag, uint32_t* status) {
+    const long long t0 = clock64();
+    for (uint32_t it = 0;; ++it) {
+        int v;
+        asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+        if (v >= target) {
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            return true;
+        }
+        if ((it & 63u) == 63u) {
+            if (*abort_flag) return false;
+            if (clock64() - t0 > kWaitCycles) {
+                *abort_flag = 1;
+                atomicOr(status, MLORA_DEV_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+struct Tile {
+    bool shrink;
     int b;   // block of kBlockM sorted positions
-    int cb;  // column slab
+    int cb;  // column slab (base tiles)
     int e;   // expert
-    int l;   // adapter (shrink only)
+    int i0;  // first adapter of the group in the block's list (shrink tiles)
+    int g;   // adapters in the group (shrink tiles)
 };
 
-template <int MODE>
-__device__ __forceinline__ TileCoord decode_tile(const GemmParams& p, long tile, int ncb) {
-    TileCoord c;
-    if (MODE == kShrink) {
-        c.b = p.lt_block[tile];
-        c.l = p.lt_lora[tile];
-        c.cb = 0;
+__device__ __forceinline__ Tile decode_tile(const GemmParams& p, long tile, int ns, int ncb) {
+    Tile t;
+    if (tile < ns) {
+        t.shrink = true;
+        t.b = p.gt_block[tile];
+        t.i0 = p.gt_first[tile];
+        t.g = min(p.gsize, p.blk_nad[t.b] - t.i0);
+        t.cb = 0;
     } else {
-        c.b = static_cast<int>(tile / ncb);
-        c.cb = static_cast<int>(tile - static_cast<long>(c.b) * ncb);
-        c.l = -1;
+        const long u = tile - ns;
+        t.shrink = false;
+        t.b = static_cast<int>(u / ncb);
+        t.cb = static_cast<int>(u - static_cast<long>(t.b) * ncb);
+        t.i0 = 0;
+        t.g = 0;
     }
-    c.e = p.expert_ids[c.b];
-    return c;
+    t.e = p.expert_ids[t.b];
+    return t;
 }
 
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + __expf(-z)); }
 
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
-    using C = Cfg<MODE>;
-    constexpr int kStages = C::kStages;
-    constexpr int kStageBytes = stage_bytes<MODE>();
-
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
@@ -105,7 +121,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     uint64_t* tfull = empty + kStages;
     uint64_t* tempty = tfull + 2;
     uint64_t* drain = tempty + 2;
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* pub = drain + 1;  // the 128 epilogue threads finished writing a shrink tile
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(pub + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -119,61 +136,51 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             mbar_init(&tempty[a], 128);
         }
         mbar_init(drain, 1);
+        mbar_init(pub, 128);
         *abort_flag = 0;
         fence_barrier_init();
         prefetch_tensormap(&p.tm_a);
         prefetch_tensormap(&p.tm_a_full);
         prefetch_tensormap(&p.tm_b);
-        if (MODE != kShrink && p.has_lora) {
+        if (p.has_lora) {
+            prefetch_tensormap(&p.tm_sa);
             prefetch_tensormap(&p.tm_t);
             prefetch_tensormap(&p.tm_t_full);
             prefetch_tensormap(&p.tm_lb);
         }
     }
     if (warp == 1) {
-        tmem_alloc(tmem_holder, C::kTmemCols);
+        tmem_alloc(tmem_holder, kTmemCols);
         tc_fence_before();
     }
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
-    // Everything above overlapped the previous kernel.  With a shrink as the
-    // previous kernel (pdl_early) only its shrink tiles are needed, and only
-    // by the expand stages: the producer waits for it there, while the base
-    // product (whose inputs were complete before the shrink started) runs.
-    if (!p.pdl_early) griddep_wait();
+    // everything above overlapped the previous kernel in the stream
+    griddep_wait();
 
     const int nblocks = *p.n_pad / kBlockM;
-    int ncb = 1;
-    long ntiles;
-    if (MODE == kGateUp) {
-        ncb = (p.n_out + 127) / 128;
-        ntiles = static_cast<long>(nblocks) * ncb;
-    } else if (MODE == kDown) {
-        ncb = (p.n_out + 255) / 256;
-        ntiles = static_cast<long>(nblocks) * ncb;
-    } else {
-        ntiles = *p.lt_total;
-    }
+    const int ncb = MODE == kGateUp ? (p.n_out + 127) / 128 : (p.n_out + 255) / 256;
+    const int ns = p.has_lora ? *p.gt_total : 0;
+    const long ntiles = ns + static_cast<long>(nblocks) * ncb;
     const int nk = (p.K + kBlockK - 1) / kBlockK;
-    const int rp = (p.rank + 15) / 16 * 16;       // shrink N
-    const int lora_ksteps = (p.rank + 15) / 16;   // expand K-steps of 16
-    const bool expand = MODE != kShrink && p.has_lora;
+    const int rp = (p.rank + 15) / 16 * 16;     // rank padded to the MMA's N granule
+    const int lora_ksteps = (p.rank + 15) / 16;  // expand K-steps of 16
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
             long it = 0;
             bool ok = true;
-            bool waited = false;
             for (long tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-                const TileCoord tc = decode_tile<MODE>(p, tile, ncb);
+                const Tile tc = decode_tile(p, tile, ns, ncb);
                 const int row0 = tc.b * kBlockM;
                 // only the block's real rows are loaded; the MMA rows past
                 // them hold stale data and feed only discarded output rows
                 const int nbox = (p.blk_rows[tc.b] + kRowBox - 1) / kRowBox;
                 const bool full_block = nbox * kRowBox == kBlockM;
                 const uint32_t a_bytes = static_cast<uint32_t>(nbox) * kRowBox * kBlockK * 2;
+                const int32_t* lora_list = p.blk_lora + static_cast<long>(tc.b) * p.cap;
                 for (int kb = 0; kb < nk; ++kb, ++it) {
                     const int s = static_cast<int>(it % kStages);
                     const uint32_t ph = static_cast<uint32_t>(it / kStages) & 1u;
@@ -184,16 +191,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     uint8_t* sa = smem + s * kStageBytes;
                     uint8_t* sb = sa + kATileBytes;
                     const int k0 = kb * kBlockK;
-                    if (MODE == kGateUp) {
+                    if (tc.shrink) {
+                        mbar_arrive_expect_tx(&full[s], a_bytes + tc.g * rp * kBlockK * 2);
+                        for (int i = 0; i < tc.g; ++i)
+                            tma_load_3d(sb + i * rp * kBlockK * 2, &p.tm_sa, &full[s], k0, 0,
+                                        lora_list[tc.i0 + i] * p.E_tot + tc.e);
+                    } else if (MODE == kGateUp) {
                         mbar_arrive_expect_tx(&full[s], a_bytes + 2 * 128 * kBlockK * 2);
                         tma_load_4d(sb, &p.tm_b, &full[s], k0, tc.cb * 128, 0, tc.e);
                         tma_load_4d(sb + 128 * kBlockK * 2, &p.tm_b, &full[s], k0, tc.cb * 128, 1, tc.e);
-                    } else if (MODE == kDown) {
+                    } else {
                         mbar_arrive_expect_tx(&full[s], a_bytes + 256 * kBlockK * 2);
                         tma_load_3d(sb, &p.tm_b, &full[s], k0, tc.cb * 256, tc.e);
-                    } else {
-                        mbar_arrive_expect_tx(&full[s], a_bytes + rp * kBlockK * 2);
-                        tma_load_3d(sb, &p.tm_b, &full[s], k0, 0, tc.l * p.E_tot + tc.e);
                     }
                     if (full_block)
                         tma_load_2d(sa, &p.tm_a_full, &full[s], k0, row0);
@@ -201,15 +210,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                         for (int i = 0; i < nbox; ++i)
                             tma_load_2d(sa + i * kRowBox * kBlockK * 2, &p.tm_a, &full[s], k0, row0 + i * kRowBox);
                 }
-                if (!ok || !expand) continue;
+                if (!ok || tc.shrink || !p.has_lora) continue;
                 const int nad = p.blk_nad[tc.b];
-                const int lt0 = p.blk_lt_start[tc.b];
-                if (p.pdl_early && nad > 0 && !waited) {
-                    griddep_wait();  // the shrink tiles are complete from here on
-                    waited = true;
+                if (nad == 0) continue;
+                // the expand needs every shrink tile of this block
+                if (!wait_counter(p.done + tc.b, (nad + p.gsize - 1) / p.gsize, abort_flag, p.status)) {
+                    ok = false;
+                    break;
                 }
+                const int lt0 = p.blk_lt_start[tc.b];
                 for (int i = 0; i < nad; ++i, ++it) {
-                    const int l = p.blk_lora[static_cast<long>(tc.b) * p.cap + i];
                     const int s = static_cast<int>(it % kStages);
                     const uint32_t ph = static_cast<uint32_t>(it / kStages) & 1u;
                     if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.status)) {
@@ -218,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     }
                     uint8_t* sa = smem + s * kStageBytes;
                     uint8_t* sb = sa + kATileBytes;
-                    const int le = l * p.E_tot + tc.e;
+                    const int le = lora_list[i] * p.E_tot + tc.e;
                     if (MODE == kGateUp) {
                         mbar_arrive_expect_tx(&full[s], a_bytes + 2 * 128 * kBlockK * 2);
                         tma_load_4d(sb, &p.tm_lb, &full[s], 0, tc.cb * 128, 0, le);
@@ -243,19 +253,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            const uint32_t idesc = umma_idesc_bf16(128, MODE == kShrink ? rp : 256);
+            const uint32_t idesc_base = umma_idesc_bf16(128, 256);
             long it = 0;
             int lt = 0;
             bool ok = true;
             for (long tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++lt) {
-                const TileCoord tc = decode_tile<MODE>(p, tile, ncb);
+                const Tile tc = decode_tile(p, tile, ns, ncb);
                 const int acc = lt & 1;
                 if (!mbar_wait(&tempty[acc], (static_cast<uint32_t>(lt >> 1) & 1u) ^ 1u, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d = tmem_base + static_cast<uint32_t>(acc * C::kAccCols);
+                const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kAccCols);
+                const uint32_t idesc = tc.shrink ? umma_idesc_bf16(128, tc.g * rp) : idesc_base;
                 for (int kb = 0; kb < nk; ++kb, ++it) {
                     const int s = static_cast<int>(it % kStages);
                     if (!mbar_wait(&full[s], static_cast<uint32_t>(it / kStages) & 1u, abort_flag, p.status)) {
@@ -272,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     umma_commit(&empty[s]);
                 }
                 if (!ok) break;
-                if (expand) {
+                if (!tc.shrink && p.has_lora) {
                     const int nad = p.blk_nad[tc.b];
                     for (int i = 0; i < nad; ++i, ++it) {
                         const int s = static_cast<int>(it % kStages);
@@ -300,15 +311,58 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         const int q = warp & 3;  // TMEM lane quarter this warp may access
         const int row = q * 32 + lane;
         int lt = 0;
+        uint32_t npub = 0;
         for (long tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++lt) {
-            const TileCoord tc = decode_tile<MODE>(p, tile, ncb);
+            const Tile tc = decode_tile(p, tile, ns, ncb);
             const int acc = lt & 1;
             if (!mbar_wait(&tfull[acc], static_cast<uint32_t>(lt >> 1) & 1u, abort_flag, p.status)) break;
             tc_fence_after();
-            const uint32_t tb = tmem_base + static_cast<uint32_t>(acc * C::kAccCols) +
+            const uint32_t tb = tmem_base + static_cast<uint32_t>(acc * kAccCols) +
                                 (static_cast<uint32_t>(q * 32) << 16);
             const int prow = tc.b * kBlockM + row;
-            if (MODE == kGateUp) {
+            if (tc.shrink) {
+                const int my_l = row < p.blk_rows[tc.b] ? p.lora_of[prow] : -1;
+                const int32_t* lora_list = p.blk_lora + static_cast<long>(tc.b) * p.cap;
+                const int lt0 = p.blk_lt_start[tc.b] + tc.i0;
+                for (int i = 0; i < tc.g; ++i) {
+                    const bool mine = my_l == lora_list[tc.i0 + i];
+                    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.lora_t) +
+                                         (static_cast<size_t>(lt0 + i) * kBlockM + row) * kLoraTileCols;
+                    for (int c = 0; c < kLoraTileCols; c += 16) {
+                        float v[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) v[j] = 0.f;
+                        if (c < rp) tmem_ld16(tb + i * rp + c, v);
+                        float o[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) o[j] = (mine && c + j < p.rank) ? p.scaling * v[j] : 0.f;
+                        uint4 w0, w1;
+                        w0.x = pack_bf16x2(o[0], o[1]);
+                        w0.y = pack_bf16x2(o[2], o[3]);
+                        w0.z = pack_bf16x2(o[4], o[5]);
+                        w0.w = pack_bf16x2(o[6], o[7]);
+                        w1.x = pack_bf16x2(o[8], o[9]);
+                        w1.y = pack_bf16x2(o[10], o[11]);
+                        w1.z = pack_bf16x2(o[12], o[13]);
+                        w1.w = pack_bf16x2(o[14], o[15]);
+                        reinterpret_cast<uint4*>(dst + c)[0] = w0;
+                        reinterpret_cast<uint4*>(dst + c)[1] = w1;
+                    }
+                }
+                // publish: the block's consumers read these tiles with TMA.
+                // Every thread fences its writes and arrives; one thread
+                // waits (bounded) for all 128 and bumps the block's counter.
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+                __threadfence();
+                mbar_arrive(pub);
+                if (warp == 2 && lane == 0) {
+                    if (mbar_wait(pub, npub & 1u, abort_flag, p.status)) {
+                        __threadfence();
+                        atomicAdd(p.done + tc.b, 1);
+                    }
+                }
+                ++npub;
+            } else if (MODE == kGateUp) {
                 const bool real = p.sorted_ids[prow] < p.S;
                 const int j0 = tc.cb * 128;
                 __nv_bfloat16* act = static_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(prow) * p.n_out;
@@ -332,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                         }
                     }
                 }
-            } else if (MODE == kDown) {
+            } else {
                 const int f = p.sorted_ids[prow];
                 const bool real = f < p.S;
                 const int o0 = tc.cb * 256;
@@ -356,30 +410,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                         }
                     }
                 }
-            } else {
-                const bool mine = p.lora_of[prow] == tc.l;
-                __nv_bfloat16* dst =
-                    static_cast<__nv_bfloat16*>(p.out) + (static_cast<size_t>(tile) * kBlockM + row) * kLoraTileCols;
-                for (int c = 0; c < kLoraTileCols; c += 16) {
-                    float v[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) v[i] = 0.f;
-                    if (c < rp) tmem_ld16(tb + c, v);
-                    float o[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) o[i] = (mine && c + i < p.rank) ? p.scaling * v[i] : 0.f;
-                    uint4 w0, w1;
-                    w0.x = pack_bf16x2(o[0], o[1]);
-                    w0.y = pack_bf16x2(o[2], o[3]);
-                    w0.z = pack_bf16x2(o[4], o[5]);
-                    w0.w = pack_bf16x2(o[6], o[7]);
-                    w1.x = pack_bf16x2(o[8], o[9]);
-                    w1.y = pack_bf16x2(o[10], o[11]);
-                    w1.z = pack_bf16x2(o[12], o[13]);
-                    w1.w = pack_bf16x2(o[14], o[15]);
-                    reinterpret_cast<uint4*>(dst + c)[0] = w0;
-                    reinterpret_cast<uint4*>(dst + c)[1] = w1;
-                }
             }
             tc_fence_before();
             mbar_arrive(&tempty[acc]);
@@ -389,39 +419,31 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, C::kTmemCols);
+        tmem_dealloc(tmem_base, kTmemCols);
     }
-    // the grid never completes before the one it follows, so whatever runs
-    // after it may rely on both
-    if (p.pdl_early) griddep_wait();
 }
 
 template <int MODE>
 cudaError_t launch_mode(const GemmParams& p, long max_tiles, cudaStream_t s) {
-    constexpr int smem = smem_bytes<MODE>();
     static unsigned long long attr_done = 0;  // one bit per device
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev < 64 && !((attr_done >> dev) & 1ull)) {
-        err = cudaFuncSetAttribute(gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        err = cudaFuncSetAttribute(gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (err != cudaSuccess) return err;
         attr_done |= 1ull << dev;
     }
     long grid = device_sm_count();
     if (grid > max_tiles) grid = max_tiles;
-    return launch_pdl(gemm_kernel<MODE>, dim3(static_cast<unsigned>(grid)), dim3(kThreads), smem, s, p);
+    return launch_pdl(gemm_kernel<MODE>, dim3(static_cast<unsigned>(grid)), dim3(kThreads), kSmemBytes, s, p);
 }
 
 }  // namespace
 
 cudaError_t launch_gemm(GemmMode mode, const GemmParams& p, long max_tiles, cudaStream_t s) {
     if (max_tiles <= 0) return cudaSuccess;
-    switch (mode) {
-        case kGateUp: return launch_mode<kGateUp>(p, max_tiles, s);
-        case kDown: return launch_mode<kDown>(p, max_tiles, s);
-        default: return launch_mode<kShrink>(p, max_tiles, s);
-    }
+    return mode == kGateUp ? launch_mode<kGateUp>(p, max_tiles, s) : launch_mode<kDown>(p, max_tiles, s);
 }
 
 }  // namespace mlora

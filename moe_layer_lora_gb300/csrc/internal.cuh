@@ -20,19 +20,22 @@ constexpr int kRowBox = 32;                     // token rows per TMA box of an 
 struct Workspace {
     uint32_t* status;      // [0] device status word
     int32_t* n_pad;        // padded slot total written by align
-    int32_t* lt_total;     // number of (block, adapter) shrink tiles
+    int32_t* gt_total;     // number of shrink group tiles
+    int32_t* done13;       // [max_blocks] shrink tiles finished per block, gate_up projection
+    int32_t* done2;        // [max_blocks] the same for the down projection
+    size_t zeroed_bytes;   // leading bytes cleared by every forward (header and counters)
     int32_t* sorted_ids;   // [max_padded]
     int32_t* expert_ids;   // [max_blocks]
     int32_t* blk_rows;     // [max_blocks] real (non-padding) rows of each block
     int32_t* lora_of;      // [max_padded] adapter of each sorted position (-1: none / pad)
     int32_t* blk_nad;      // [max_blocks] distinct adapters in the block
-    int32_t* blk_lt_start; // [max_blocks] first shrink tile of the block
+    int32_t* blk_lt_start; // [max_blocks] first LoRA tile of the block
     int32_t* blk_lora;     // [max_blocks * cap] the block's adapters, ascending
-    int32_t* lt_block;     // [max_lt] block of each shrink tile
-    int32_t* lt_lora;      // [max_lt] adapter of each shrink tile
+    int32_t* gt_block;     // [max_lt] block of each shrink group tile
+    int32_t* gt_first;     // [max_lt] first adapter (index into the block's list) of each group
     void* x_perm;          // [max_padded, H] bf16: x rows gathered in sorted order
     void* act;             // [max_padded, I] bf16: SwiGLU output in sorted order
-    void* lora_t;          // [max_lt * 128, 64] bf16: s * shrink, one masked tile per (block, adapter)
+    void* lora_t;          // [max_lt * 128, 64] bf16: s * shrink, one masked LoRA tile per (block, adapter)
     void* y_slot;          // [M*K', H] bf16: each slot's expert output
     size_t bytes;
 };
@@ -44,6 +47,7 @@ struct Sizes {
     long max_padded;  // with block_m = kBlockM
     long max_blocks;
     int cap;          // adapters per block list: min(L, kBlockM)
+    int gsize;        // adapters per shrink group tile: 256 / rank rounded up to 16
     long max_lt;
 };
 
@@ -64,9 +68,10 @@ struct AlignExtra {
     int32_t* blk_nad;
     int32_t* blk_lora;
     int32_t* blk_lt_start;
-    int32_t* lt_block;
-    int32_t* lt_lora;
-    int32_t* lt_total;
+    int gsize;
+    int32_t* gt_block;
+    int32_t* gt_first;
+    int32_t* gt_total;
 };
 
 cudaError_t launch_route(const float* logits, const float* bias, int M, int E, int top_k, int scoring,
@@ -83,11 +88,12 @@ cudaError_t launch_combine(const void* y_slot, const int32_t* topk_ids, const fl
                            int K_total, int E_tot, float out_scale, void* y, cudaStream_t s);
 
 // ------------------------------------------------------------ grouped GEMM --
-enum GemmMode : int { kGateUp = 0, kDown = 1, kShrink = 2 };
+enum GemmMode : int { kGateUp = 0, kDown = 1 };
 
 struct alignas(64) GemmParams {
     CUtensorMap tm_a;   // token rows [rows, K], box {64, kRowBox}
-    CUtensorMap tm_b;   // weight rows (w13 / w2 / A13 / A2 view)
+    CUtensorMap tm_b;   // weight rows (w13 / w2 view)
+    CUtensorMap tm_sa;  // LoRA shrink weights (A13 / A2 view), box {64, rank rounded up to 16, 1}
     CUtensorMap tm_t;   // LoRA shrink tiles [tiles*128, 64], box {64, kRowBox}
     CUtensorMap tm_lb;  // LoRA expand weights (B13 / B2 view)
     CUtensorMap tm_a_full;  // tm_a with box {64, 128}: one box per full block
@@ -100,45 +106,26 @@ struct alignas(64) GemmParams {
     const int32_t* blk_nad;
     const int32_t* blk_lora;
     const int32_t* blk_lt_start;
-    const int32_t* lt_block;
-    const int32_t* lt_lora;
-    const int32_t* lt_total;
+    const int32_t* gt_block;
+    const int32_t* gt_first;
+    const int32_t* gt_total;
+    int32_t* done;  // per-block count of finished shrink tiles (zero at launch)
+    void* lora_t;   // masked LoRA tiles: written by the shrink tiles, read by the expand
     void* out;
     uint32_t* status;
     int K;          // reduction length
-    int n_out;      // valid output columns (I for gate_up, H for down, rank for shrink)
+    int n_out;      // valid output columns (I for gate_up, H for down)
     int E_tot;
     int cap;
+    int gsize;
     int rank;
     int S;          // sentinel slot value M*K'
     int has_lora;
-    int pdl_early;  // the preceding kernel is a shrink: wait for it only before the expand stages
     float scaling;
 };
 
 cudaError_t launch_gemm(GemmMode mode, const GemmParams& p, long max_tiles, cudaStream_t s);
 
-// CUDA-core shrink for small batches (few rows per (block, adapter) tile):
-// T[t] = s * X[rows of block b with adapter l] A_{l,e}^T, masked, bf16.
-struct ShrinkParams {
-    const void* X;  // [rows, K] bf16, sorted order
-    const void* A;  // [L*E_tot, rank, K] bf16
-    int K;
-    int rank;
-    int E_tot;
-    float scaling;
-    const int32_t* lt_block;
-    const int32_t* lt_lora;
-    const int32_t* lt_total;
-    const int32_t* expert_ids;
-    const int32_t* lora_of;
-    const int32_t* blk_rows;
-    void* T;  // [tiles*128, 64] bf16
-};
-cudaError_t launch_shrink_rows(const ShrinkParams& p, long max_tiles, cudaStream_t s);
-// M*K'*rank up to which the CUDA-core shrink is used (it then runs beside
-// the GEMM that consumes it); larger shrinks run on the tensor cores
-constexpr long kShrinkRowsMaxWork = 4096L * 16;
 
 int device_sm_count();
 

@@ -10,7 +10,8 @@
 // padded counts, then a stable scatter in chunks of 1024 slots.  Within a
 // chunk a slot's rank is (slots of its expert in earlier warps) + (earlier
 // lanes of its warp with the same expert, from __match_any_sync); the
-// per-warp per-expert counts live in a small shared table.
+// per-warp per-expert counts live in a small shared table that one warp per
+// expert turns into exclusive prefixes with a shuffle scan.
 //
 // Inside the forward the same pass also records the real (non-padding) row
 // count of every block and, with adapters, per sorted position the token's
@@ -75,14 +76,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = tid; i < kWarps * E_tot; i += kThreads) wcnt[i] = 0;
     __syncthreads();
 
-    // 1. histogram
-    for (int f = tid; f < S; f += kThreads) {
-        const int e = ids[f];
-        if (static_cast<unsigned>(e) < static_cast<unsigned>(E_tot)) {
-            atomicAdd(&cnt[e], 1);
-        } else if (status) {
-            atomicOr(status, MLORA_DEV_BAD_EXPERT_ID);
-        }
+    // 1. histogram, one shared atomic per distinct expert of a warp
+    const unsigned lt_mask = (1u << lane) - 1u;
+    for (int f0 = 0; f0 < S; f0 += kThreads) {
+        const int f = f0 + tid;
+        const int e = f < S ? ids[f] : -1;
+        const bool valid = static_cast<unsigned>(e) < static_cast<unsigned>(E_tot);
+        if (f < S && !valid && status) atomicOr(status, MLORA_DEV_BAD_EXPERT_ID);
+        const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : -1);
+        if (valid && (peers & lt_mask) == 0) atomicAdd(&cnt[e], __popc(peers));
     }
     __syncthreads();
 
@@ -115,11 +117,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 
-    // 4. stable scatter, 1024 slots per pass
-    const unsigned lt_mask = (1u << lane) - 1u;
+    // 4. stable scatter, 1024 slots per pass.  Within a pass a slot's rank
+    //    among the slots of its expert is (its expert's slots in earlier
+    //    warps) + (earlier lanes of its warp with the same expert); the first
+    //    term comes from a per-expert scan over the warps' counts, done one
+    //    expert column per warp.
+    // the next pass's expert and adapter ids are loaded during this one
+    int e_next = tid < S ? ids[tid] : -1;
+    int l_next = (kWithLora && tid < S) ? ex.token_lora_idx[tid / ex.K_total] : -1;
     for (int base = 0; base < S; base += kThreads) {
         const int f = base + tid;
-        const int e = f < S ? ids[f] : -1;
+        const int e = e_next;
+        const int l_in = l_next;
+        const bool more = f + kThreads < S;
+        e_next = more ? ids[f + kThreads] : -1;
+        if (kWithLora) l_next = more ? ex.token_lora_idx[(f + kThreads) / ex.K_total] : -1;
         const bool valid = static_cast<unsigned>(e) < static_cast<unsigned>(E_tot);
         const int key = valid ? e : -1;
         const unsigned peers = __match_any_sync(0xffffffffu, key);
@@ -128,18 +140,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool leader = (peers & lt_mask) == 0;
         if (valid && leader) wcnt[warp * E_tot + e] = static_cast<uint16_t>(n_same);
         __syncthreads();
-        int pos = 0;
-        if (valid && leader) {
-            int pre = 0;
-            for (int w2 = 0; w2 < warp; ++w2) pre += wcnt[w2 * E_tot + e];
-            pos = cursor[e] + pre;
+        for (int ex_col = warp; ex_col < E_tot; ex_col += kWarps) {
+            const int c_w = wcnt[lane * E_tot + ex_col];
+            int inc = c_w;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int nb = __shfl_up_sync(0xffffffffu, inc, off);
+                if (lane >= off) inc += nb;
+            }
+            if (c_w) wcnt[lane * E_tot + ex_col] = static_cast<uint16_t>(inc - c_w);
         }
+        __syncthreads();
+        int pos = 0;
+        if (valid && leader) pos = cursor[e] + wcnt[warp * E_tot + e];
         pos = __shfl_sync(0xffffffffu, pos, __ffs(peers) - 1);
         if (valid) {
             const int p = pos + rank;
             sorted[p] = f;
             if (kWithLora) {
-                int l = ex.token_lora_idx[f / ex.K_total];
+                int l = l_in;
                 if (l < -1 || l >= ex.L) {
                     if (status) atomicOr(status, MLORA_DEV_BAD_LORA_IDX);
                     l = -1;

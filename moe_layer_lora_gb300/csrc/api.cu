@@ -119,7 +119,10 @@ Sizes make_sizes(int M, int H, int I, int E_tot, int K_total, int L, int rank) {
     z.max_blocks = z.max_padded / kBlockM;
     z.cap = z.lora ? std::min(L, kBlockM) : 0;
     z.max_lt = z.max_blocks * z.cap;
-    z.gsize = z.lora ? 256 / ((rank + 15) / 16 * 16) : 1;
+    // N tile of the GEMMs (256: measured faster than 64 even for a single
+    // token, since the weight bytes in flight per SM set the bandwidth)
+    z.bn = 256;
+    z.gsize = z.lora ? z.bn / ((rank + 15) / 16 * 16) : 1;
     return z;
 }
 
@@ -270,10 +273,10 @@ mlora_status mlora_moe_forward(const void* x, const void* w13, const void* w2, c
         ok &= make_map(&dn.tm_a, ws.act, 2, da, sa, bx);
         ok &= make_map(&dn.tm_a_full, ws.act, 2, da, sa, bxf);
         const cuuint64_t d13[4] = {H_, I_, 2, E_}, s13[3] = {H_ * 2, I_ * H_ * 2, 2 * I_ * H_ * 2};
-        const cuuint32_t b13[4] = {64, 128, 1, 1};
+        const cuuint32_t b13[4] = {64, static_cast<cuuint32_t>(z.bn / 2), 1, 1};
         ok &= make_map(&gu.tm_b, w13, 4, d13, s13, b13);
         const cuuint64_t d2[3] = {I_, H_, E_}, s2[2] = {I_ * 2, H_ * I_ * 2};
-        const cuuint32_t b2[3] = {64, 256, 1};
+        const cuuint32_t b2[3] = {64, static_cast<cuuint32_t>(z.bn), 1};
         ok &= make_map(&dn.tm_b, w2, 3, d2, s2, b2);
         if (lora) {
             const cuuint64_t R = rank, LE = static_cast<cuuint64_t>(L) * E_tot;
@@ -358,11 +361,11 @@ mlora_status mlora_moe_forward(const void* x, const void* w13, const void* w2, c
     // the shrinks run inside the GEMM kernels: stages 3 and 5 stay empty
     if ((err = mark_stage(2, s)) != cudaSuccess || (err = mark_stage(3, s)) != cudaSuccess)
         return cuda_fail(err, "stage event");
-    err = launch_gemm(kGateUp, gu, z.max_lt + z.max_blocks * ((I + 127) / 128), s);
+    err = launch_gemm(kGateUp, z.bn, gu, z.max_lt + z.max_blocks * ((I + z.bn / 2 - 1) / (z.bn / 2)), s);
     if (err != cudaSuccess) return cuda_fail(err, "gate_up");
     if ((err = mark_stage(4, s)) != cudaSuccess || (err = mark_stage(5, s)) != cudaSuccess)
         return cuda_fail(err, "stage event");
-    err = launch_gemm(kDown, dn, z.max_lt + z.max_blocks * ((H + 255) / 256), s);
+    err = launch_gemm(kDown, z.bn, dn, z.max_lt + z.max_blocks * ((H + z.bn - 1) / z.bn), s);
     if (err != cudaSuccess) return cuda_fail(err, "down");
     if ((err = mark_stage(6, s)) != cudaSuccess) return cuda_fail(err, "stage event");
     err = launch_combine(ws.y_slot, topk_ids, topk_w, M, H, K_total, E_tot, out_scale, y, s);

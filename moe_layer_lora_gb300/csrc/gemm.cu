@@ -13,11 +13,12 @@
 //      When a block's shrink tiles are all written, a per-block counter is
 //      bumped.
 //  base tiles:
-//      kGateUp: h = X W13_e^T over a 128-column slab j0.. of the gate rows
-//               and the same slab of the up rows (one MMA with N = 256: B
-//               rows 0..127 gate, 128..255 up); epilogue act = silu(g) * u.
-//      kDown:   d = act W2_e^T over 256 output columns; epilogue the slot's
+//      kGateUp: h = X W13_e^T over a BN/2-column slab j0.. of the gate rows
+//               and the same slab of the up rows (one MMA with N = BN: B
+//               rows [0, BN/2) gate, [BN/2, BN) up); epilogue act = silu(g) * u.
+//      kDown:   d = act W2_e^T over BN output columns; epilogue the slot's
 //               expert output in bf16.
+//      BN = 256.
 //      With adapters, after the K loop every adapter l present in the block
 //      adds T_l B_{l,e}^T as extra K-chunks into the same TMEM accumulator:
 //      the expand folded into the projection ("Amazon SageMaker 및 Amazon
@@ -29,7 +30,7 @@
 //
 // Roles (192 threads): warp 0 issues TMA loads into a ring of smem stages
 // (A tile 128 x 64 bf16: one 128-row box for a full block, 32-row boxes
-// covering only the real rows of a partial one; B tile 256 x 64 bf16; both
+// covering only the real rows of a partial one; B tile BN x 64 bf16; both
 // K-major with 128-byte swizzle); warp 1 allocates TMEM and one lane issues
 // tcgen05.mma (M = 128, K = 16 per instruction, fp32 accumulate) and
 // tcgen05.commit; warps 2..5 drain the double-buffered TMEM accumulator with
@@ -44,13 +45,18 @@ namespace mlora {
 namespace {
 
 constexpr int kThreads = 192;
-constexpr int kStages = 4;
-constexpr int kBRows = 256;
-constexpr int kATileBytes = kBlockM * kBlockK * 2;                // 16 KiB
-constexpr int kStageBytes = kATileBytes + kBRows * kBlockK * 2;  // 48 KiB
-constexpr int kAccCols = 256;
-constexpr int kTmemCols = 512;
-constexpr int kSmemBytes = kStages * kStageBytes + 1024 /* alignment slack */ + 256 /* barriers */;
+constexpr int kATileBytes = kBlockM * kBlockK * 2;  // 16 KiB
+
+// Per-N-tile shape: BN weight rows per tile (MMA N), a ~192 KiB ring of
+// stages, a double-buffered BN-column fp32 accumulator in TMEM.
+template <int BN>
+struct Shape {
+    static constexpr int kStageBytes = kATileBytes + BN * kBlockK * 2;
+    static constexpr int kStages = BN == 256 ? 4 : 8;
+    static constexpr int kAccCols = BN;
+    static constexpr int kTmemCols = BN == 256 ? 512 : 128;
+    static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /* alignment slack */ + 256 /* barriers */;
+};
 
 // Bounded wait used only while unwinding after an abort: ignores the abort
 // flag so that copies already in flight land before the CTA exits.
@@ -112,8 +118,14 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, long tile, int 
 
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + __expf(-z)); }
 
-template <int MODE>
+template <int MODE, int BN>
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
+    using Sh = Shape<BN>;
+    constexpr int kStages = Sh::kStages;
+    constexpr int kStageBytes = Sh::kStageBytes;
+    constexpr int kAccCols = Sh::kAccCols;
+    constexpr int kTmemCols = Sh::kTmemCols;
+    constexpr int kHalf = BN / 2;  // gate (and up) rows of a gate_up tile
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
@@ -160,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     griddep_wait();
 
     const int nblocks = *p.n_pad / kBlockM;
-    const int ncb = MODE == kGateUp ? (p.n_out + 127) / 128 : (p.n_out + 255) / 256;
+    const int ncb = MODE == kGateUp ? (p.n_out + kHalf - 1) / kHalf : (p.n_out + BN - 1) / BN;
     const int ns = p.has_lora ? *p.gt_total : 0;
     const long ntiles = ns + static_cast<long>(nblocks) * ncb;
     const int nk = (p.K + kBlockK - 1) / kBlockK;
@@ -197,12 +209,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                             tma_load_3d(sb + i * rp * kBlockK * 2, &p.tm_sa, &full[s], k0, 0,
                                         lora_list[tc.i0 + i] * p.E_tot + tc.e);
                     } else if (MODE == kGateUp) {
-                        mbar_arrive_expect_tx(&full[s], a_bytes + 2 * 128 * kBlockK * 2);
-                        tma_load_4d(sb, &p.tm_b, &full[s], k0, tc.cb * 128, 0, tc.e);
-                        tma_load_4d(sb + 128 * kBlockK * 2, &p.tm_b, &full[s], k0, tc.cb * 128, 1, tc.e);
+                        mbar_arrive_expect_tx(&full[s], a_bytes + BN * kBlockK * 2);
+                        tma_load_4d(sb, &p.tm_b, &full[s], k0, tc.cb * kHalf, 0, tc.e);
+                        tma_load_4d(sb + kHalf * kBlockK * 2, &p.tm_b, &full[s], k0, tc.cb * kHalf, 1, tc.e);
                     } else {
-                        mbar_arrive_expect_tx(&full[s], a_bytes + 256 * kBlockK * 2);
-                        tma_load_3d(sb, &p.tm_b, &full[s], k0, tc.cb * 256, tc.e);
+                        mbar_arrive_expect_tx(&full[s], a_bytes + BN * kBlockK * 2);
+                        tma_load_3d(sb, &p.tm_b, &full[s], k0, tc.cb * BN, tc.e);
                     }
                     if (full_block)
                         tma_load_2d(sa, &p.tm_a_full, &full[s], k0, row0);
@@ -230,12 +242,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     uint8_t* sb = sa + kATileBytes;
                     const int le = lora_list[i] * p.E_tot + tc.e;
                     if (MODE == kGateUp) {
-                        mbar_arrive_expect_tx(&full[s], a_bytes + 2 * 128 * kBlockK * 2);
-                        tma_load_4d(sb, &p.tm_lb, &full[s], 0, tc.cb * 128, 0, le);
-                        tma_load_4d(sb + 128 * kBlockK * 2, &p.tm_lb, &full[s], 0, tc.cb * 128, 1, le);
+                        mbar_arrive_expect_tx(&full[s], a_bytes + BN * kBlockK * 2);
+                        tma_load_4d(sb, &p.tm_lb, &full[s], 0, tc.cb * kHalf, 0, le);
+                        tma_load_4d(sb + kHalf * kBlockK * 2, &p.tm_lb, &full[s], 0, tc.cb * kHalf, 1, le);
                     } else {
-                        mbar_arrive_expect_tx(&full[s], a_bytes + 256 * kBlockK * 2);
-                        tma_load_3d(sb, &p.tm_lb, &full[s], 0, tc.cb * 256, le);
+                        mbar_arrive_expect_tx(&full[s], a_bytes + BN * kBlockK * 2);
+                        tma_load_3d(sb, &p.tm_lb, &full[s], 0, tc.cb * BN, le);
                     }
                     if (full_block)
                         tma_load_2d(sa, &p.tm_t_full, &full[s], 0, (lt0 + i) * kBlockM);
@@ -253,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            const uint32_t idesc_base = umma_idesc_bf16(128, 256);
+            const uint32_t idesc_base = umma_idesc_bf16(128, BN);
             long it = 0;
             int lt = 0;
             bool ok = true;
@@ -364,13 +376,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 ++npub;
             } else if (MODE == kGateUp) {
                 const bool real = p.sorted_ids[prow] < p.S;
-                const int j0 = tc.cb * 128;
+                const int j0 = tc.cb * kHalf;
                 __nv_bfloat16* act = static_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(prow) * p.n_out;
-                for (int c = 0; c < 128; c += 32) {
+                for (int c = 0; c < kHalf; c += 32) {
                     if (j0 + c >= p.n_out) break;
                     float g[32], u[32];
                     tmem_ld32(tb + c, g);
-                    tmem_ld32(tb + 128 + c, u);
+                    tmem_ld32(tb + kHalf + c, u);
                     if (real) {
 #pragma unroll
                         for (int v = 0; v < 4; ++v) {
@@ -389,9 +401,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             } else {
                 const int f = p.sorted_ids[prow];
                 const bool real = f < p.S;
-                const int o0 = tc.cb * 256;
+                const int o0 = tc.cb * BN;
                 __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(real ? f : 0) * p.n_out;
-                for (int c = 0; c < 256; c += 32) {
+                for (int c = 0; c < BN; c += 32) {
                     if (o0 + c >= p.n_out) break;
                     float v[32];
                     tmem_ld32(tb + c, v);
@@ -423,27 +435,29 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     }
 }
 
-template <int MODE>
+template <int MODE, int BN>
 cudaError_t launch_mode(const GemmParams& p, long max_tiles, cudaStream_t s) {
+    constexpr int smem = Shape<BN>::kSmemBytes;
     static unsigned long long attr_done = 0;  // one bit per device
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev < 64 && !((attr_done >> dev) & 1ull)) {
-        err = cudaFuncSetAttribute(gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        err = cudaFuncSetAttribute(gemm_kernel<MODE, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (err != cudaSuccess) return err;
         attr_done |= 1ull << dev;
     }
     long grid = device_sm_count();
     if (grid > max_tiles) grid = max_tiles;
-    return launch_pdl(gemm_kernel<MODE>, dim3(static_cast<unsigned>(grid)), dim3(kThreads), kSmemBytes, s, p);
+    return launch_pdl(gemm_kernel<MODE, BN>, dim3(static_cast<unsigned>(grid)), dim3(kThreads), smem, s, p);
 }
 
 }  // namespace
 
-cudaError_t launch_gemm(GemmMode mode, const GemmParams& p, long max_tiles, cudaStream_t s) {
+cudaError_t launch_gemm(GemmMode mode, int bn, const GemmParams& p, long max_tiles, cudaStream_t s) {
     if (max_tiles <= 0) return cudaSuccess;
-    return mode == kGateUp ? launch_mode<kGateUp>(p, max_tiles, s) : launch_mode<kDown>(p, max_tiles, s);
+    if (bn != 256) return cudaErrorInvalidValue;
+    return mode == kGateUp ? launch_mode<kGateUp, 256>(p, max_tiles, s) : launch_mode<kDown, 256>(p, max_tiles, s);
 }
 
 }  // namespace mlora

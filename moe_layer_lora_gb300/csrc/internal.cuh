@@ -47,7 +47,8 @@ struct Sizes {
     long max_padded;  // with block_m = kBlockM
     long max_blocks;
     int cap;          // adapters per block list: min(L, kBlockM)
-    int gsize;        // adapters per shrink group tile: 256 / rank rounded up to 16
+    int bn;           // weight rows per GEMM tile (MMA N)
+    int gsize;        // adapters per shrink group tile: bn / rank rounded up to 16
     long max_lt;
 };
 
@@ -124,7 +125,8 @@ struct alignas(64) GemmParams {
     float scaling;
 };
 
-cudaError_t launch_gemm(GemmMode mode, const GemmParams& p, long max_tiles, cudaStream_t s);
+// bn: weight rows per tile (MMA N); 256.
+cudaError_t launch_gemm(GemmMode mode, int bn, const GemmParams& p, long max_tiles, cudaStream_t s);
 
 
 int device_sm_count();

@@ -124,13 +124,9 @@ def algorithmic(s: wl.Spec, ids: np.ndarray, idx) -> dict:
         n_pairs = a_slots = 0
     b = 2  # bf16
     st = {
-        # the gate_up and down kernels include their adapter shrink
-        "gate_up": dict(bytes=n_exp * 2 * I * H * b + n_pairs * (2 * I + H) * r * b + S * (H + I) * b,
-                        flops=2.0 * S * H * 2 * I + 2.0 * a_slots * (2 * I + H) * r),
-        "down": dict(bytes=n_exp * H * I * b + n_pairs * (H + I) * r * b + S * (I + H) * b,
-                     flops=2.0 * S * I * H + 2.0 * a_slots * (H + I) * r),
-        "shrink_gate_up": dict(bytes=0, flops=0.0),
-        "shrink_down": dict(bytes=0, flops=0.0),
+        # the experts kernel: both projections, their adapter shrink and expand
+        "experts": dict(bytes=n_exp * 3 * I * H * b + n_pairs * r * (2 * H + 3 * I) * b + S * (2 * H + 2 * I) * b,
+                        flops=2.0 * S * 3 * H * I + 2.0 * a_slots * r * (2 * H + 3 * I)),
         "gather": dict(bytes=S * H * b * 2, flops=0.0),
         "combine": dict(bytes=S * H * b + M * H * b, flops=2.0 * S * H),
         "align": dict(bytes=S * 4 * 3, flops=0.0),
@@ -217,8 +213,7 @@ class ClockSampler:
 
 
 STAGE_SOURCES = {
-    "gate_up": ("gemm.cu", "ptx.cuh", "internal.cuh"),
-    "down": ("gemm.cu", "ptx.cuh", "internal.cuh"),
+    "experts": ("gemm.cu", "ptx.cuh", "internal.cuh"),
 }
 
 
@@ -378,7 +373,7 @@ def run_gpu(args, s: wl.Spec, rank: int, world: int, local_rank: int):
                     stage_ms[n].append(ev[i].elapsed_time(ev[i + 1]))
         torch.cuda.synchronize(device)
         barrier(world)
-        launches_per_step = 1 + 5 + (2 if s.has_lora else 0)  # route, align, gather, gate_up, down, combine, shrinks
+        launches_per_step = 5  # route, align, gather, experts, combine
 
         # end to end through the public API with host buffers: H2D of the
         # step's inputs from pinned memory, the layer, D2H of the output

@@ -199,18 +199,15 @@ mlora_status mlora_moe_read_status(const void* workspace, uint32_t* host_status,
  * cudaEvent_t handles (passed as void*) that every later mlora_moe_forward
  * on this thread records on its stream at the stage boundaries:
  *   [0] before align, [1] after align, [2] after the row gather,
- *   [3] = [2], [4] after the gate_up GEMM (its LoRA shrink included),
- *   [5] = [4], [6] after the down GEMM (its LoRA shrink included),
- *   [7] after combine.
- * (Events [3] and [5] mark where a separate shrink pass would sit; the
- * shrink runs inside the GEMM kernels, so those stages are empty.)  The events are recorded
- * with cudaEventRecordExternal, so they also become event nodes when the
- * forward is captured into a CUDA graph.  events == NULL (or count == 0)
- * switches the hook off.  The caller owns the events and keeps them alive
- * while the hook is set.  Returns MLORA_ERR_INVALID_ARG when
- * 0 < count < MLORA_STAGE_EVENTS.
+ *   [3] after the experts kernel (both projections with their LoRA shrink
+ *       and expand, and SwiGLU), [4] after the combine.
+ * The events are recorded with cudaEventRecordExternal while the stream is
+ * being captured, so they become event nodes of a CUDA graph.
+ * events == NULL (or count == 0) switches the hook off.  The caller owns
+ * the events and keeps them alive while the hook is set.  Returns
+ * MLORA_ERR_INVALID_ARG when 0 < count < MLORA_STAGE_EVENTS.
  */
-#define MLORA_STAGE_EVENTS 8
+#define MLORA_STAGE_EVENTS 5
 mlora_status mlora_set_stage_events(void* const* events, int count);
 
 /* Static, human-readable name of a status code. */

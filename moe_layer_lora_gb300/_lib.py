@@ -203,8 +203,8 @@ def mlora_moe_read_status(workspace: torch.Tensor, stream=None) -> int:
     return int(out.value)
 
 
-STAGE_EVENTS = 8
-STAGE_NAMES = ("align", "gather", "shrink_gate_up", "gate_up", "shrink_down", "down", "combine")
+STAGE_EVENTS = 5
+STAGE_NAMES = ("align", "gather", "experts", "combine")
 
 
 def mlora_set_stage_events(events) -> None:

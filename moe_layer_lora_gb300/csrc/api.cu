@@ -5,13 +5,12 @@
 // Forward, all on the caller's stream, no host synchronisation, no
 // allocation (capturable in a CUDA graph):
 //   memset(status, counters) -> align (+ per-block adapter lists)
-//   -> gather x rows -> gate_up GEMM (shrink tiles, then base tiles with the
-//   expand and SwiGLU) -> down GEMM (shrink tiles, base tiles with the
-//   expand) -> weighted combine
-// Without adapters the GEMMs run only base tiles; when adapters are given
-// but no token uses one, align finds no shrink tiles on the device and the
-// GEMMs skip the expand chunks, so the layer exits early without a host
-// round trip ("Amazon SageMaker 및
+//   -> gather x rows -> experts kernel (gate_up shrink, gate_up + expand +
+//   SwiGLU, down shrink, down + expand, one persistent grid) -> combine
+// Without adapters the experts kernel runs only base tiles; when adapters
+// are given but no token uses one, align finds no shrink tiles on the
+// device and the expand chunks are skipped, so the layer exits early
+// without a host round trip ("Amazon SageMaker 및
 // Amazon Bedrock에서 vLLM을 활용한 MoE 모델 Multi-LoRA 서빙 최적화", section
 // "섹션별 상세" paragraph 2).
 #include <cuda.h>
@@ -119,10 +118,7 @@ Sizes make_sizes(int M, int H, int I, int E_tot, int K_total, int L, int rank) {
     z.max_blocks = z.max_padded / kBlockM;
     z.cap = z.lora ? std::min(L, kBlockM) : 0;
     z.max_lt = z.max_blocks * z.cap;
-    // N tile of the GEMMs (256: measured faster than 64 even for a single
-    // token, since the weight bytes in flight per SM set the bandwidth)
-    z.bn = 256;
-    z.gsize = z.lora ? z.bn / ((rank + 15) / 16 * 16) : 1;
+    z.gsize = z.lora ? 256 / ((rank + 15) / 16 * 16) : 1;
     return z;
 }
 
@@ -139,6 +135,7 @@ Workspace carve_workspace(const Sizes& z, void* base) {
     w.status = reinterpret_cast<uint32_t*>(header);
     w.n_pad = reinterpret_cast<int32_t*>(header ? header + 4 : nullptr);
     w.gt_total = reinterpret_cast<int32_t*>(header ? header + 8 : nullptr);
+    w.act_done = reinterpret_cast<int32_t*>(take(4 * z.max_blocks));
     if (z.lora) {
         w.done13 = reinterpret_cast<int32_t*>(take(4 * z.max_blocks));
         w.done2 = reinterpret_cast<int32_t*>(take(4 * z.max_blocks));
@@ -157,7 +154,10 @@ Workspace carve_workspace(const Sizes& z, void* base) {
     }
     w.x_perm = take(2 * static_cast<size_t>(z.max_padded) * z.H);
     w.act = take(2 * static_cast<size_t>(z.max_padded) * z.I);
-    if (z.lora) w.lora_t = take(2 * static_cast<size_t>(z.max_lt) * kBlockM * kLoraTileCols);
+    if (z.lora) {
+        w.lora_t13 = take(2 * static_cast<size_t>(z.max_lt) * kBlockM * kLoraTileCols);
+        w.lora_t2 = take(2 * static_cast<size_t>(z.max_lt) * kBlockM * kLoraTileCols);
+    }
     w.y_slot = take(2 * static_cast<size_t>(z.S) * z.H);
     w.bytes = off;
     return w;
@@ -260,77 +260,81 @@ mlora_status mlora_moe_forward(const void* x, const void* w13, const void* w2, c
     if (workspace_bytes < ws.bytes) return MLORA_ERR_WORKSPACE;
 
     // ---- tensor maps (dims innermost first) ----
-    GemmParams gu{}, dn{};
+    GemmParams gp{};
+    GemmSide& up = gp.side[0];
+    GemmSide& dn = gp.side[1];
     const cuuint64_t H_ = H, I_ = I, E_ = E_tot, MP = z.max_padded;
     bool ok = true;
     {
-        const cuuint64_t dx[2] = {H_, MP}, sx[1] = {H_ * 2};
         const cuuint32_t bx[2] = {64, kRowBox};
         const cuuint32_t bxf[2] = {64, 128};
-        ok &= make_map(&gu.tm_a, ws.x_perm, 2, dx, sx, bx);
-        ok &= make_map(&gu.tm_a_full, ws.x_perm, 2, dx, sx, bxf);
+        const cuuint64_t dx[2] = {H_, MP}, sx[1] = {H_ * 2};
+        ok &= make_map(&up.tm_a, ws.x_perm, 2, dx, sx, bx);
+        ok &= make_map(&up.tm_a_full, ws.x_perm, 2, dx, sx, bxf);
         const cuuint64_t da[2] = {I_, MP}, sa[1] = {I_ * 2};
         ok &= make_map(&dn.tm_a, ws.act, 2, da, sa, bx);
         ok &= make_map(&dn.tm_a_full, ws.act, 2, da, sa, bxf);
         const cuuint64_t d13[4] = {H_, I_, 2, E_}, s13[3] = {H_ * 2, I_ * H_ * 2, 2 * I_ * H_ * 2};
-        const cuuint32_t b13[4] = {64, static_cast<cuuint32_t>(z.bn / 2), 1, 1};
-        ok &= make_map(&gu.tm_b, w13, 4, d13, s13, b13);
+        const cuuint32_t b13[4] = {64, 128, 1, 1};
+        ok &= make_map(&up.tm_b, w13, 4, d13, s13, b13);
         const cuuint64_t d2[3] = {I_, H_, E_}, s2[2] = {I_ * 2, H_ * I_ * 2};
-        const cuuint32_t b2[3] = {64, static_cast<cuuint32_t>(z.bn), 1};
+        const cuuint32_t b2[3] = {64, 256, 1};
         ok &= make_map(&dn.tm_b, w2, 3, d2, s2, b2);
         if (lora) {
             const cuuint64_t R = rank, LE = static_cast<cuuint64_t>(L) * E_tot;
             const cuuint32_t rp = static_cast<cuuint32_t>((rank + 15) / 16 * 16);
             const cuuint64_t dt[2] = {64, static_cast<cuuint64_t>(z.max_lt) * kBlockM}, st_[1] = {128};
-            ok &= make_map(&gu.tm_t, ws.lora_t, 2, dt, st_, bx);
-            ok &= make_map(&gu.tm_t_full, ws.lora_t, 2, dt, st_, bxf);
-            dn.tm_t = gu.tm_t;
-            dn.tm_t_full = gu.tm_t_full;
+            ok &= make_map(&up.tm_t, ws.lora_t13, 2, dt, st_, bx);
+            ok &= make_map(&up.tm_t_full, ws.lora_t13, 2, dt, st_, bxf);
+            ok &= make_map(&dn.tm_t, ws.lora_t2, 2, dt, st_, bx);
+            ok &= make_map(&dn.tm_t_full, ws.lora_t2, 2, dt, st_, bxf);
             // shrink weights: rank rows past the rank read as zero
             const cuuint64_t dA13[3] = {H_, R, LE}, sA13[2] = {H_ * 2, R * H_ * 2};
             const cuuint32_t bA[3] = {64, rp, 1};
-            ok &= make_map(&gu.tm_sa, A13, 3, dA13, sA13, bA);
+            ok &= make_map(&up.tm_sa, A13, 3, dA13, sA13, bA);
             const cuuint64_t dA2[3] = {I_, R, LE}, sA2[2] = {I_ * 2, R * I_ * 2};
             ok &= make_map(&dn.tm_sa, A2, 3, dA2, sA2, bA);
             // expand weights: columns past the rank read as zero
             const cuuint64_t dB13[4] = {R, I_, 2, LE}, sB13[3] = {R * 2, I_ * R * 2, 2 * I_ * R * 2};
-            ok &= make_map(&gu.tm_lb, B13, 4, dB13, sB13, b13);
+            ok &= make_map(&up.tm_lb, B13, 4, dB13, sB13, b13);
             const cuuint64_t dB2[3] = {R, H_, LE}, sB2[2] = {R * 2, H_ * R * 2};
             ok &= make_map(&dn.tm_lb, B2, 3, dB2, sB2, b2);
         }
     }
     if (!ok) return cuda_fail(cudaErrorInvalidValue, "tensor map encoding");
 
-    for (GemmParams* p : {&gu, &dn}) {
-        p->n_pad = ws.n_pad;
-        p->expert_ids = ws.expert_ids;
-        p->blk_rows = ws.blk_rows;
-        p->sorted_ids = ws.sorted_ids;
-        p->lora_of = ws.lora_of;
-        p->blk_nad = ws.blk_nad;
-        p->blk_lora = ws.blk_lora;
-        p->blk_lt_start = ws.blk_lt_start;
-        p->gt_block = ws.gt_block;
-        p->gt_first = ws.gt_first;
-        p->gt_total = ws.gt_total;
-        p->lora_t = ws.lora_t;
-        p->status = ws.status;
-        p->E_tot = E_tot;
-        p->cap = z.cap;
-        p->gsize = z.gsize;
-        p->rank = r_eff;
-        p->S = static_cast<int>(z.S);
-        p->has_lora = lora ? 1 : 0;
-        p->scaling = scaling;
-    }
-    gu.done = ws.done13;
-    gu.out = ws.act;
-    gu.K = H;
-    gu.n_out = I;
+    up.lora_t = ws.lora_t13;
+    up.done = ws.done13;
+    up.out = ws.act;
+    up.K = H;
+    up.n_out = I;
+    up.ncb = (I + 127) / 128;
+    dn.lora_t = ws.lora_t2;
     dn.done = ws.done2;
     dn.out = ws.y_slot;
     dn.K = I;
     dn.n_out = H;
+    dn.ncb = (H + 255) / 256;
+    gp.n_pad = ws.n_pad;
+    gp.expert_ids = ws.expert_ids;
+    gp.blk_rows = ws.blk_rows;
+    gp.sorted_ids = ws.sorted_ids;
+    gp.lora_of = ws.lora_of;
+    gp.blk_nad = ws.blk_nad;
+    gp.blk_lora = ws.blk_lora;
+    gp.blk_lt_start = ws.blk_lt_start;
+    gp.gt_block = ws.gt_block;
+    gp.gt_first = ws.gt_first;
+    gp.gt_total = ws.gt_total;
+    gp.act_done = ws.act_done;
+    gp.status = ws.status;
+    gp.E_tot = E_tot;
+    gp.cap = z.cap;
+    gp.gsize = z.gsize;
+    gp.rank = r_eff;
+    gp.S = static_cast<int>(z.S);
+    gp.has_lora = lora ? 1 : 0;
+    gp.scaling = scaling;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t err = cudaMemsetAsync(workspace, 0, ws.zeroed_bytes, s);
@@ -358,19 +362,14 @@ mlora_status mlora_moe_forward(const void* x, const void* w13, const void* w2, c
     if ((err = mark_stage(1, s)) != cudaSuccess) return cuda_fail(err, "stage event");
     err = launch_gather_rows(x, H, ws.sorted_ids, ws.n_pad, z.S, K_total, z.max_padded, ws.x_perm, s);
     if (err != cudaSuccess) return cuda_fail(err, "gather");
-    // the shrinks run inside the GEMM kernels: stages 3 and 5 stay empty
-    if ((err = mark_stage(2, s)) != cudaSuccess || (err = mark_stage(3, s)) != cudaSuccess)
-        return cuda_fail(err, "stage event");
-    err = launch_gemm(kGateUp, z.bn, gu, z.max_lt + z.max_blocks * ((I + z.bn / 2 - 1) / (z.bn / 2)), s);
-    if (err != cudaSuccess) return cuda_fail(err, "gate_up");
-    if ((err = mark_stage(4, s)) != cudaSuccess || (err = mark_stage(5, s)) != cudaSuccess)
-        return cuda_fail(err, "stage event");
-    err = launch_gemm(kDown, z.bn, dn, z.max_lt + z.max_blocks * ((H + z.bn - 1) / z.bn), s);
-    if (err != cudaSuccess) return cuda_fail(err, "down");
-    if ((err = mark_stage(6, s)) != cudaSuccess) return cuda_fail(err, "stage event");
+    if ((err = mark_stage(2, s)) != cudaSuccess) return cuda_fail(err, "stage event");
+    const long max_tiles = 2 * z.max_lt + z.max_blocks * (up.ncb + dn.ncb);
+    err = launch_experts(gp, max_tiles, s);
+    if (err != cudaSuccess) return cuda_fail(err, "experts");
+    if ((err = mark_stage(3, s)) != cudaSuccess) return cuda_fail(err, "stage event");
     err = launch_combine(ws.y_slot, topk_ids, topk_w, M, H, K_total, E_tot, out_scale, y, s);
     if (err != cudaSuccess) return cuda_fail(err, "combine");
-    if ((err = mark_stage(7, s)) != cudaSuccess) return cuda_fail(err, "stage event");
+    if ((err = mark_stage(4, s)) != cudaSuccess) return cuda_fail(err, "stage event");
     return MLORA_OK;
 }
 

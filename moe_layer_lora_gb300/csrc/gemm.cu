@@ -1,43 +1,46 @@
-// gemm.cu -- the grouped expert GEMMs on the 5th-generation tensor cores,
-// with the per-token LoRA shrink and expand folded into the same kernel.
+// gemm.cu -- the expert MLP of the layer on the 5th-generation tensor cores:
+// both grouped GEMMs, their per-token LoRA shrink and expand, and SwiGLU,
+// in one persistent kernel.
 //
-// One persistent, warp-specialised kernel per projection works through two
-// kinds of tiles over blocks of kBlockM = 128 sorted slots (all slots of a
-// block share one expert e, from align):
+// The kernel works through four phases of tiles over blocks of kBlockM =
+// 128 sorted slots (all slots of a block share one expert e, from align);
+// every CTA takes tiles c, c + grid, ... of the concatenated sequence:
 //
-//  shrink tiles (first in every CTA's sequence, only with adapters):
-//      T_l = s * X A_{l,e}^T for up to `gsize` adapters l of one block at
-//      once -- the adapters' rank rows are stacked along N (N = g * rank
-//      rounded up to 16) -- written as one masked bf16 tile per (block,
-//      adapter): rows of other adapters zero, columns past the rank zero.
-//      When a block's shrink tiles are all written, a per-block counter is
-//      bumped.
-//  base tiles:
-//      kGateUp: h = X W13_e^T over a BN/2-column slab j0.. of the gate rows
-//               and the same slab of the up rows (one MMA with N = BN: B
-//               rows [0, BN/2) gate, [BN/2, BN) up); epilogue act = silu(g) * u.
-//      kDown:   d = act W2_e^T over BN output columns; epilogue the slot's
-//               expert output in bf16.
-//      BN = 256.
-//      With adapters, after the K loop every adapter l present in the block
-//      adds T_l B_{l,e}^T as extra K-chunks into the same TMEM accumulator:
-//      the expand folded into the projection ("Amazon SageMaker 및 Amazon
-//      Bedrock에서 vLLM을 활용한 MoE 모델 Multi-LoRA 서빙 최적화", section
-//      "섹션별 상세" paragraphs 1-3).  The producer waits for the block's
-//      shrink counter only before those chunks, so the base product of the
-//      first tiles streams while other CTAs still run shrink tiles -- the
-//      overlap of shrink and expand the pages get from PDL, inside one grid.
+//  1. gate_up shrink tiles (with adapters): T13_l = s * X A13_{l,e}^T for
+//     up to `gsize` adapters l of one block at once -- their rank rows
+//     stacked along N (N = g * rank rounded up to 16) -- written as one
+//     masked bf16 tile per (block, adapter) (rows of other adapters and
+//     columns past the rank zero); then the block's shrink counter is
+//     bumped.
+//  2. gate_up tiles: h = X W13_e^T over a 128-column slab of the gate rows
+//     and the same slab of the up rows (one MMA with N = 256: B rows 0..127
+//     gate, 128..255 up); with adapters, after the K loop, every adapter l
+//     of the block adds T13_l B13_{l,e}^T as extra K-chunks into the same
+//     TMEM accumulator -- the expand folded into the projection ("Amazon
+//     SageMaker 및 Amazon Bedrock에서 vLLM을 활용한 MoE 모델 Multi-LoRA 서빙
+//     최적화", section "섹션별 상세" paragraphs 1-3); epilogue act =
+//     silu(g) * u in bf16, then the block's act counter is bumped.
+//  3. down shrink tiles: T2_l = s * act A2_{l,e}^T, as in phase 1.
+//  4. down tiles: d = act W2_e^T over 256 output columns + the T2 expand;
+//     epilogue the slot's expert output in bf16.
+//
+// A tile depends only on tiles of earlier phases of the same block, and
+// every CTA finishes its earlier-phase tiles first, so the producer waits
+// on the block's counters (act before a down-side tile starts, the shrink
+// counter before the expand stages) and the phases overlap across CTAs:
+// the gate_up base product streams while other CTAs run shrink tiles, and
+// the down GEMM fills the gate_up tail.  (The pages overlap the shrink and
+// expand kernels with PDL; here they share one grid.)
 //
 // Roles (192 threads): warp 0 issues TMA loads into a ring of smem stages
 // (A tile 128 x 64 bf16: one 128-row box for a full block, 32-row boxes
-// covering only the real rows of a partial one; B tile BN x 64 bf16; both
+// covering only the real rows of a partial one; B tile 256 x 64 bf16; both
 // K-major with 128-byte swizzle); warp 1 allocates TMEM and one lane issues
 // tcgen05.mma (M = 128, K = 16 per instruction, fp32 accumulate) and
 // tcgen05.commit; warps 2..5 drain the double-buffered TMEM accumulator with
-// tcgen05.ld while the next tile's MMAs run.  Tiles are strided over a grid
-// of at most one CTA per SM.  Every wait is bounded (~2 s, ptx.cuh): a
-// timeout records MLORA_DEV_TIMEOUT, drains the copies in flight, frees
-// TMEM and returns.
+// tcgen05.ld while the next tile's MMAs run.  Grid: at most one CTA per SM.
+// Every wait is bounded (~2 s, ptx.cuh): a timeout records
+// MLORA_DEV_TIMEOUT, drains the copies in flight, frees TMEM and returns.
 #include "internal.cuh"
 #include "ptx.cuh"
 
@@ -45,18 +48,16 @@ namespace mlora {
 namespace {
 
 constexpr int kThreads = 192;
-constexpr int kATileBytes = kBlockM * kBlockK * 2;  // 16 KiB
+constexpr int kBN = 256;                                         // weight rows per tile (MMA N)
+constexpr int kHalf = kBN / 2;                                   // gate (and up) rows of a gate_up tile
+constexpr int kStages = 4;
+constexpr int kATileBytes = kBlockM * kBlockK * 2;               // 16 KiB
+constexpr int kStageBytes = kATileBytes + kBN * kBlockK * 2;     // 48 KiB
+constexpr int kAccCols = kBN;
+constexpr int kTmemCols = 2 * kBN;
+constexpr int kSmemBytes = kStages * kStageBytes + 1024 /* alignment slack */ + 256 /* barriers */;
 
-// Per-N-tile shape: BN weight rows per tile (MMA N), a ~192 KiB ring of
-// stages, a double-buffered BN-column fp32 accumulator in TMEM.
-template <int BN>
-struct Shape {
-    static constexpr int kStageBytes = kATileBytes + BN * kBlockK * 2;
-    static constexpr int kStages = BN == 256 ? 4 : 8;
-    static constexpr int kAccCols = BN;
-    static constexpr int kTmemCols = BN == 256 ? 512 : 128;
-    static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /* alignment slack */ + 256 /* barriers */;
-};
+enum TileKind : int { kShrinkUp = 0, kGateUp = 1, kShrinkDown = 2, kDown = 3 };
 
 // Bounded wait used only while unwinding after an abort: ignores the abort
 // flag so that copies already in flight land before the CTA exits.
@@ -88,44 +89,60 @@ __device__ bool wait_counter(const int32_t* flag, int target, volatile int* abor
 }
 
 struct Tile {
+    int kind;
+    int side;  // 0: gate_up projection, 1: down projection
     bool shrink;
-    int b;   // block of kBlockM sorted positions
-    int cb;  // column slab (base tiles)
-    int e;   // expert
-    int i0;  // first adapter of the group in the block's list (shrink tiles)
-    int g;   // adapters in the group (shrink tiles)
+    int b;     // block of kBlockM sorted positions
+    int cb;    // column slab (base tiles)
+    int e;     // expert
+    int i0;    // first adapter of the group in the block's list (shrink tiles)
+    int g;     // adapters in the group (shrink tiles)
 };
 
-__device__ __forceinline__ Tile decode_tile(const GemmParams& p, long tile, int ns, int ncb) {
+// Phase boundaries of the tile sequence.
+struct Phases {
+    long s1, g, s2, d;  // ends of phases 1..4
+};
+
+__device__ __forceinline__ Tile decode_tile(const GemmParams& p, long tile, const Phases& ph, int ns, int nblocks) {
     Tile t;
-    if (tile < ns) {
-        t.shrink = true;
-        t.b = p.gt_block[tile];
-        t.i0 = p.gt_first[tile];
+    long u;
+    if (tile < ph.s1) {
+        t.kind = kShrinkUp;
+        u = tile;
+    } else if (tile < ph.g) {
+        t.kind = kGateUp;
+        u = tile - ph.s1;
+    } else if (tile < ph.s2) {
+        t.kind = kShrinkDown;
+        u = tile - ph.g;
+    } else {
+        t.kind = kDown;
+        u = tile - ph.s2;
+    }
+    t.side = t.kind >= kShrinkDown ? 1 : 0;
+    t.shrink = t.kind == kShrinkUp || t.kind == kShrinkDown;
+    if (t.shrink) {
+        t.b = p.gt_block[u];
+        t.i0 = p.gt_first[u];
         t.g = min(p.gsize, p.blk_nad[t.b] - t.i0);
         t.cb = 0;
     } else {
-        const long u = tile - ns;
-        t.shrink = false;
+        const int ncb = p.side[t.side].ncb;
         t.b = static_cast<int>(u / ncb);
         t.cb = static_cast<int>(u - static_cast<long>(t.b) * ncb);
         t.i0 = 0;
         t.g = 0;
     }
     t.e = p.expert_ids[t.b];
+    (void)ns;
+    (void)nblocks;
     return t;
 }
 
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + __expf(-z)); }
 
-template <int MODE, int BN>
-__global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
-    using Sh = Shape<BN>;
-    constexpr int kStages = Sh::kStages;
-    constexpr int kStageBytes = Sh::kStageBytes;
-    constexpr int kAccCols = Sh::kAccCols;
-    constexpr int kTmemCols = Sh::kTmemCols;
-    constexpr int kHalf = BN / 2;  // gate (and up) rows of a gate_up tile
+__global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_constant__ GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
@@ -133,7 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     uint64_t* tfull = empty + kStages;
     uint64_t* tempty = tfull + 2;
     uint64_t* drain = tempty + 2;
-    uint64_t* pub = drain + 1;  // the 128 epilogue threads finished writing a shrink tile
+    uint64_t* pub = drain + 1;  // the 128 epilogue threads finished writing a published tile
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(pub + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
@@ -151,14 +168,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         mbar_init(pub, 128);
         *abort_flag = 0;
         fence_barrier_init();
-        prefetch_tensormap(&p.tm_a);
-        prefetch_tensormap(&p.tm_a_full);
-        prefetch_tensormap(&p.tm_b);
-        if (p.has_lora) {
-            prefetch_tensormap(&p.tm_sa);
-            prefetch_tensormap(&p.tm_t);
-            prefetch_tensormap(&p.tm_t_full);
-            prefetch_tensormap(&p.tm_lb);
+        for (int sd = 0; sd < 2; ++sd) {
+            prefetch_tensormap(&p.side[sd].tm_a);
+            prefetch_tensormap(&p.side[sd].tm_a_full);
+            prefetch_tensormap(&p.side[sd].tm_b);
+            if (p.has_lora) {
+                prefetch_tensormap(&p.side[sd].tm_sa);
+                prefetch_tensormap(&p.side[sd].tm_lb);
+                prefetch_tensormap(&p.side[sd].tm_t);
+                prefetch_tensormap(&p.side[sd].tm_t_full);
+            }
         }
     }
     if (warp == 1) {
@@ -172,10 +191,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     griddep_wait();
 
     const int nblocks = *p.n_pad / kBlockM;
-    const int ncb = MODE == kGateUp ? (p.n_out + kHalf - 1) / kHalf : (p.n_out + BN - 1) / BN;
     const int ns = p.has_lora ? *p.gt_total : 0;
-    const long ntiles = ns + static_cast<long>(nblocks) * ncb;
-    const int nk = (p.K + kBlockK - 1) / kBlockK;
+    Phases ph;
+    ph.s1 = ns;
+    ph.g = ph.s1 + static_cast<long>(nblocks) * p.side[0].ncb;
+    ph.s2 = ph.g + ns;
+    ph.d = ph.s2 + static_cast<long>(nblocks) * p.side[1].ncb;
+    const long ntiles = ph.d;
     const int rp = (p.rank + 15) / 16 * 16;     // rank padded to the MMA's N granule
     const int lora_ksteps = (p.rank + 15) / 16;  // expand K-steps of 16
 
@@ -185,18 +207,26 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             long it = 0;
             bool ok = true;
             for (long tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-                const Tile tc = decode_tile(p, tile, ns, ncb);
+                const Tile tc = decode_tile(p, tile, ph, ns, nblocks);
+                const GemmSide& sd = p.side[tc.side];
                 const int row0 = tc.b * kBlockM;
+                // the down side reads act rows, complete once the block's
+                // gate_up tiles all are
+                if (tc.side == 1 && !wait_counter(p.act_done + tc.b, p.side[0].ncb, abort_flag, p.status)) {
+                    ok = false;
+                    break;
+                }
                 // only the block's real rows are loaded; the MMA rows past
                 // them hold stale data and feed only discarded output rows
                 const int nbox = (p.blk_rows[tc.b] + kRowBox - 1) / kRowBox;
                 const bool full_block = nbox * kRowBox == kBlockM;
                 const uint32_t a_bytes = static_cast<uint32_t>(nbox) * kRowBox * kBlockK * 2;
                 const int32_t* lora_list = p.blk_lora + static_cast<long>(tc.b) * p.cap;
+                const int nk = (sd.K + kBlockK - 1) / kBlockK;
                 for (int kb = 0; kb < nk; ++kb, ++it) {
                     const int s = static_cast<int>(it % kStages);
-                    const uint32_t ph = static_cast<uint32_t>(it / kStages) & 1u;
-                    if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.status)) {
+                    const uint32_t phs = static_cast<uint32_t>(it / kStages) & 1u;
+                    if (!mbar_wait(&empty[s], phs ^ 1u, abort_flag, p.status)) {
                         ok = false;
                         break;
                     }
@@ -206,54 +236,53 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     if (tc.shrink) {
                         mbar_arrive_expect_tx(&full[s], a_bytes + tc.g * rp * kBlockK * 2);
                         for (int i = 0; i < tc.g; ++i)
-                            tma_load_3d(sb + i * rp * kBlockK * 2, &p.tm_sa, &full[s], k0, 0,
+                            tma_load_3d(sb + i * rp * kBlockK * 2, &sd.tm_sa, &full[s], k0, 0,
                                         lora_list[tc.i0 + i] * p.E_tot + tc.e);
-                    } else if (MODE == kGateUp) {
-                        mbar_arrive_expect_tx(&full[s], a_bytes + BN * kBlockK * 2);
-                        tma_load_4d(sb, &p.tm_b, &full[s], k0, tc.cb * kHalf, 0, tc.e);
-                        tma_load_4d(sb + kHalf * kBlockK * 2, &p.tm_b, &full[s], k0, tc.cb * kHalf, 1, tc.e);
+                    } else if (tc.kind == kGateUp) {
+                        mbar_arrive_expect_tx(&full[s], a_bytes + kBN * kBlockK * 2);
+                        tma_load_4d(sb, &sd.tm_b, &full[s], k0, tc.cb * kHalf, 0, tc.e);
+                        tma_load_4d(sb + kHalf * kBlockK * 2, &sd.tm_b, &full[s], k0, tc.cb * kHalf, 1, tc.e);
                     } else {
-                        mbar_arrive_expect_tx(&full[s], a_bytes + BN * kBlockK * 2);
-                        tma_load_3d(sb, &p.tm_b, &full[s], k0, tc.cb * BN, tc.e);
+                        mbar_arrive_expect_tx(&full[s], a_bytes + kBN * kBlockK * 2);
+                        tma_load_3d(sb, &sd.tm_b, &full[s], k0, tc.cb * kBN, tc.e);
                     }
                     if (full_block)
-                        tma_load_2d(sa, &p.tm_a_full, &full[s], k0, row0);
+                        tma_load_2d(sa, &sd.tm_a_full, &full[s], k0, row0);
                     else
                         for (int i = 0; i < nbox; ++i)
-                            tma_load_2d(sa + i * kRowBox * kBlockK * 2, &p.tm_a, &full[s], k0, row0 + i * kRowBox);
+                            tma_load_2d(sa + i * kRowBox * kBlockK * 2, &sd.tm_a, &full[s], k0, row0 + i * kRowBox);
                 }
                 if (!ok || tc.shrink || !p.has_lora) continue;
                 const int nad = p.blk_nad[tc.b];
                 if (nad == 0) continue;
-                // the expand needs every shrink tile of this block
-                if (!wait_counter(p.done + tc.b, (nad + p.gsize - 1) / p.gsize, abort_flag, p.status)) {
+                // the expand needs every shrink tile of this block and side
+                if (!wait_counter(sd.done + tc.b, (nad + p.gsize - 1) / p.gsize, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
                 const int lt0 = p.blk_lt_start[tc.b];
                 for (int i = 0; i < nad; ++i, ++it) {
                     const int s = static_cast<int>(it % kStages);
-                    const uint32_t ph = static_cast<uint32_t>(it / kStages) & 1u;
-                    if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.status)) {
+                    const uint32_t phs = static_cast<uint32_t>(it / kStages) & 1u;
+                    if (!mbar_wait(&empty[s], phs ^ 1u, abort_flag, p.status)) {
                         ok = false;
                         break;
                     }
                     uint8_t* sa = smem + s * kStageBytes;
                     uint8_t* sb = sa + kATileBytes;
                     const int le = lora_list[i] * p.E_tot + tc.e;
-                    if (MODE == kGateUp) {
-                        mbar_arrive_expect_tx(&full[s], a_bytes + BN * kBlockK * 2);
-                        tma_load_4d(sb, &p.tm_lb, &full[s], 0, tc.cb * kHalf, 0, le);
-                        tma_load_4d(sb + kHalf * kBlockK * 2, &p.tm_lb, &full[s], 0, tc.cb * kHalf, 1, le);
+                    mbar_arrive_expect_tx(&full[s], a_bytes + kBN * kBlockK * 2);
+                    if (tc.kind == kGateUp) {
+                        tma_load_4d(sb, &sd.tm_lb, &full[s], 0, tc.cb * kHalf, 0, le);
+                        tma_load_4d(sb + kHalf * kBlockK * 2, &sd.tm_lb, &full[s], 0, tc.cb * kHalf, 1, le);
                     } else {
-                        mbar_arrive_expect_tx(&full[s], a_bytes + BN * kBlockK * 2);
-                        tma_load_3d(sb, &p.tm_lb, &full[s], 0, tc.cb * BN, le);
+                        tma_load_3d(sb, &sd.tm_lb, &full[s], 0, tc.cb * kBN, le);
                     }
                     if (full_block)
-                        tma_load_2d(sa, &p.tm_t_full, &full[s], 0, (lt0 + i) * kBlockM);
+                        tma_load_2d(sa, &sd.tm_t_full, &full[s], 0, (lt0 + i) * kBlockM);
                     else
                         for (int j = 0; j < nbox; ++j)
-                            tma_load_2d(sa + j * kRowBox * kBlockK * 2, &p.tm_t, &full[s], 0,
+                            tma_load_2d(sa + j * kRowBox * kBlockK * 2, &sd.tm_t, &full[s], 0,
                                         (lt0 + i) * kBlockM + j * kRowBox);
                 }
             }
@@ -265,12 +294,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            const uint32_t idesc_base = umma_idesc_bf16(128, BN);
+            const uint32_t idesc_base = umma_idesc_bf16(128, kBN);
             long it = 0;
             int lt = 0;
             bool ok = true;
             for (long tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++lt) {
-                const Tile tc = decode_tile(p, tile, ns, ncb);
+                const Tile tc = decode_tile(p, tile, ph, ns, nblocks);
+                const int nk = (p.side[tc.side].K + kBlockK - 1) / kBlockK;
                 const int acc = lt & 1;
                 if (!mbar_wait(&tempty[acc], (static_cast<uint32_t>(lt >> 1) & 1u) ^ 1u, abort_flag, p.status)) {
                     ok = false;
@@ -325,20 +355,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         int lt = 0;
         uint32_t npub = 0;
         for (long tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++lt) {
-            const Tile tc = decode_tile(p, tile, ns, ncb);
+            const Tile tc = decode_tile(p, tile, ph, ns, nblocks);
+            const GemmSide& sd = p.side[tc.side];
             const int acc = lt & 1;
             if (!mbar_wait(&tfull[acc], static_cast<uint32_t>(lt >> 1) & 1u, abort_flag, p.status)) break;
             tc_fence_after();
             const uint32_t tb = tmem_base + static_cast<uint32_t>(acc * kAccCols) +
                                 (static_cast<uint32_t>(q * 32) << 16);
             const int prow = tc.b * kBlockM + row;
+            int32_t* publish = nullptr;  // counter to bump once all 128 threads wrote
             if (tc.shrink) {
                 const int my_l = row < p.blk_rows[tc.b] ? p.lora_of[prow] : -1;
                 const int32_t* lora_list = p.blk_lora + static_cast<long>(tc.b) * p.cap;
                 const int lt0 = p.blk_lt_start[tc.b] + tc.i0;
                 for (int i = 0; i < tc.g; ++i) {
                     const bool mine = my_l == lora_list[tc.i0 + i];
-                    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.lora_t) +
+                    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(sd.lora_t) +
                                          (static_cast<size_t>(lt0 + i) * kBlockM + row) * kLoraTileCols;
                     for (int c = 0; c < kLoraTileCols; c += 16) {
                         float v[16];
@@ -361,25 +393,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                         reinterpret_cast<uint4*>(dst + c)[1] = w1;
                     }
                 }
-                // publish: the block's consumers read these tiles with TMA.
-                // Every thread fences its writes and arrives; one thread
-                // waits (bounded) for all 128 and bumps the block's counter.
-                asm volatile("fence.proxy.async.global;" ::: "memory");
-                __threadfence();
-                mbar_arrive(pub);
-                if (warp == 2 && lane == 0) {
-                    if (mbar_wait(pub, npub & 1u, abort_flag, p.status)) {
-                        __threadfence();
-                        atomicAdd(p.done + tc.b, 1);
-                    }
-                }
-                ++npub;
-            } else if (MODE == kGateUp) {
+                publish = sd.done + tc.b;
+            } else if (tc.kind == kGateUp) {
                 const bool real = p.sorted_ids[prow] < p.S;
                 const int j0 = tc.cb * kHalf;
-                __nv_bfloat16* act = static_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(prow) * p.n_out;
+                __nv_bfloat16* act = static_cast<__nv_bfloat16*>(sd.out) + static_cast<size_t>(prow) * sd.n_out;
                 for (int c = 0; c < kHalf; c += 32) {
-                    if (j0 + c >= p.n_out) break;
+                    if (j0 + c >= sd.n_out) break;
                     float g[32], u[32];
                     tmem_ld32(tb + c, g);
                     tmem_ld32(tb + kHalf + c, u);
@@ -387,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 #pragma unroll
                         for (int v = 0; v < 4; ++v) {
                             const int col = j0 + c + 8 * v;
-                            if (col < p.n_out) {
+                            if (col < sd.n_out) {
                                 uint4 o;
                                 o.x = pack_bf16x2(silu(g[8 * v + 0]) * u[8 * v + 0], silu(g[8 * v + 1]) * u[8 * v + 1]);
                                 o.y = pack_bf16x2(silu(g[8 * v + 2]) * u[8 * v + 2], silu(g[8 * v + 3]) * u[8 * v + 3]);
@@ -398,20 +418,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                         }
                     }
                 }
+                publish = p.act_done + tc.b;
             } else {
                 const int f = p.sorted_ids[prow];
                 const bool real = f < p.S;
-                const int o0 = tc.cb * BN;
-                __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(real ? f : 0) * p.n_out;
-                for (int c = 0; c < BN; c += 32) {
-                    if (o0 + c >= p.n_out) break;
+                const int o0 = tc.cb * kBN;
+                __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(sd.out) + static_cast<size_t>(real ? f : 0) * sd.n_out;
+                for (int c = 0; c < kBN; c += 32) {
+                    if (o0 + c >= sd.n_out) break;
                     float v[32];
                     tmem_ld32(tb + c, v);
                     if (real) {
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
                             const int col = o0 + c + 8 * j;
-                            if (col < p.n_out) {
+                            if (col < sd.n_out) {
                                 uint4 o;
                                 o.x = pack_bf16x2(v[8 * j + 0], v[8 * j + 1]);
                                 o.y = pack_bf16x2(v[8 * j + 2], v[8 * j + 3]);
@@ -425,6 +446,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             }
             tc_fence_before();
             mbar_arrive(&tempty[acc]);
+            if (publish) {
+                // other CTAs read what this tile wrote with TMA: every thread
+                // fences its writes and arrives; one thread waits (bounded)
+                // for all 128 and bumps the block's counter
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+                __threadfence();
+                mbar_arrive(pub);
+                if (warp == 2 && lane == 0) {
+                    if (mbar_wait(pub, npub & 1u, abort_flag, p.status)) {
+                        __threadfence();
+                        atomicAdd(publish, 1);
+                    }
+                }
+                ++npub;
+            }
         }
     }
 
@@ -435,29 +471,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     }
 }
 
-template <int MODE, int BN>
-cudaError_t launch_mode(const GemmParams& p, long max_tiles, cudaStream_t s) {
-    constexpr int smem = Shape<BN>::kSmemBytes;
+}  // namespace
+
+cudaError_t launch_experts(const GemmParams& p, long max_tiles, cudaStream_t s) {
+    if (max_tiles <= 0) return cudaSuccess;
     static unsigned long long attr_done = 0;  // one bit per device
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev < 64 && !((attr_done >> dev) & 1ull)) {
-        err = cudaFuncSetAttribute(gemm_kernel<MODE, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        err = cudaFuncSetAttribute(experts_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (err != cudaSuccess) return err;
         attr_done |= 1ull << dev;
     }
     long grid = device_sm_count();
     if (grid > max_tiles) grid = max_tiles;
-    return launch_pdl(gemm_kernel<MODE, BN>, dim3(static_cast<unsigned>(grid)), dim3(kThreads), smem, s, p);
-}
-
-}  // namespace
-
-cudaError_t launch_gemm(GemmMode mode, int bn, const GemmParams& p, long max_tiles, cudaStream_t s) {
-    if (max_tiles <= 0) return cudaSuccess;
-    if (bn != 256) return cudaErrorInvalidValue;
-    return mode == kGateUp ? launch_mode<kGateUp, 256>(p, max_tiles, s) : launch_mode<kDown, 256>(p, max_tiles, s);
+    return launch_pdl(experts_kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads), kSmemBytes, s, p);
 }
 
 }  // namespace mlora

@@ -23,6 +23,7 @@ struct Workspace {
     int32_t* gt_total;     // number of shrink group tiles
     int32_t* done13;       // [max_blocks] shrink tiles finished per block, gate_up projection
     int32_t* done2;        // [max_blocks] the same for the down projection
+    int32_t* act_done;     // [max_blocks] gate_up tiles finished per block
     size_t zeroed_bytes;   // leading bytes cleared by every forward (header and counters)
     int32_t* sorted_ids;   // [max_padded]
     int32_t* expert_ids;   // [max_blocks]
@@ -35,7 +36,8 @@ struct Workspace {
     int32_t* gt_first;     // [max_lt] first adapter (index into the block's list) of each group
     void* x_perm;          // [max_padded, H] bf16: x rows gathered in sorted order
     void* act;             // [max_padded, I] bf16: SwiGLU output in sorted order
-    void* lora_t;          // [max_lt * 128, 64] bf16: s * shrink, one masked LoRA tile per (block, adapter)
+    void* lora_t13;        // [max_lt * 128, 64] bf16: s * x A13^T, one masked LoRA tile per (block, adapter)
+    void* lora_t2;         // [max_lt * 128, 64] bf16: s * act A2^T, the same for the down projection
     void* y_slot;          // [M*K', H] bf16: each slot's expert output
     size_t bytes;
 };
@@ -47,8 +49,7 @@ struct Sizes {
     long max_padded;  // with block_m = kBlockM
     long max_blocks;
     int cap;          // adapters per block list: min(L, kBlockM)
-    int bn;           // weight rows per GEMM tile (MMA N)
-    int gsize;        // adapters per shrink group tile: bn / rank rounded up to 16
+    int gsize;        // adapters per shrink group tile: 256 / rank rounded up to 16
     long max_lt;
 };
 
@@ -89,16 +90,25 @@ cudaError_t launch_combine(const void* y_slot, const int32_t* topk_ids, const fl
                            int K_total, int E_tot, float out_scale, void* y, cudaStream_t s);
 
 // ------------------------------------------------------------ grouped GEMM --
-enum GemmMode : int { kGateUp = 0, kDown = 1 };
+// One projection of the expert MLP: gate_up (side 0) or down (side 1).
+struct alignas(64) GemmSide {
+    CUtensorMap tm_a;       // token rows [rows, K] (x in sorted order / act), box {64, kRowBox}
+    CUtensorMap tm_a_full;  // the same with box {64, 128}: one box per full block
+    CUtensorMap tm_b;       // weight rows: w13 view {H, I, 2, E_tot} / w2 view {I, H, E_tot}
+    CUtensorMap tm_sa;      // LoRA shrink weights: A13 / A2 view {K, rank, L*E_tot}
+    CUtensorMap tm_lb;      // LoRA expand weights: B13 view {rank, I, 2, L*E_tot} / B2 view {rank, H, L*E_tot}
+    CUtensorMap tm_t;       // this side's LoRA tiles [tiles*128, 64], box {64, kRowBox}
+    CUtensorMap tm_t_full;  // box {64, 128}
+    void* lora_t;           // LoRA tiles: written by the shrink tiles, read by the expand stages
+    int32_t* done;          // per block: finished shrink tiles (zero at launch)
+    void* out;              // act [rows, I] / y_slot [M*K', H], bf16
+    int K;                  // reduction length: H / I
+    int n_out;              // output columns: I / H
+    int ncb;                // column slabs per block: ceil(I/128) / ceil(H/256)
+};
 
 struct alignas(64) GemmParams {
-    CUtensorMap tm_a;   // token rows [rows, K], box {64, kRowBox}
-    CUtensorMap tm_b;   // weight rows (w13 / w2 view)
-    CUtensorMap tm_sa;  // LoRA shrink weights (A13 / A2 view), box {64, rank rounded up to 16, 1}
-    CUtensorMap tm_t;   // LoRA shrink tiles [tiles*128, 64], box {64, kRowBox}
-    CUtensorMap tm_lb;  // LoRA expand weights (B13 / B2 view)
-    CUtensorMap tm_a_full;  // tm_a with box {64, 128}: one box per full block
-    CUtensorMap tm_t_full;  // tm_t with box {64, 128}
+    GemmSide side[2];
     const int32_t* n_pad;
     const int32_t* expert_ids;
     const int32_t* blk_rows;
@@ -110,24 +120,21 @@ struct alignas(64) GemmParams {
     const int32_t* gt_block;
     const int32_t* gt_first;
     const int32_t* gt_total;
-    int32_t* done;  // per-block count of finished shrink tiles (zero at launch)
-    void* lora_t;   // masked LoRA tiles: written by the shrink tiles, read by the expand
-    void* out;
+    int32_t* act_done;  // per block: finished gate_up tiles (zero at launch)
     uint32_t* status;
-    int K;          // reduction length
-    int n_out;      // valid output columns (I for gate_up, H for down)
     int E_tot;
     int cap;
     int gsize;
     int rank;
-    int S;          // sentinel slot value M*K'
+    int S;              // sentinel slot value M*K'
     int has_lora;
     float scaling;
 };
 
-// bn: weight rows per tile (MMA N); 256.
-cudaError_t launch_gemm(GemmMode mode, int bn, const GemmParams& p, long max_tiles, cudaStream_t s);
-
+// The expert MLP of all blocks in one persistent kernel: gate_up shrink
+// tiles, gate_up tiles (+ expand, SwiGLU), down shrink tiles, down tiles
+// (+ expand); see gemm.cu.
+cudaError_t launch_experts(const GemmParams& p, long max_tiles, cudaStream_t s);
 
 int device_sm_count();
 

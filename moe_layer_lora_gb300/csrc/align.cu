@@ -7,11 +7,18 @@
 // sentinel M*K' to a multiple of block_m, sentinel / -1 tails.
 //
 // One CTA of 1024 threads: shared-memory histogram, a block scan of the
-// padded counts, then a stable scatter in chunks of 1024 slots.  Within a
-// chunk a slot's rank is (slots of its expert in earlier warps) + (earlier
-// lanes of its warp with the same expert, from __match_any_sync); the
-// per-warp per-expert counts live in a small shared table that one warp per
-// expert turns into exclusive prefixes with a shuffle scan.
+// padded counts, then a stable scatter.  Two ways to make it stable:
+//  * passes of 1024 slots (one pass of slots, or many experts): within a
+//    pass a slot's rank is (slots of its expert in earlier warps) + (earlier
+//    lanes of its warp with the same expert, from __match_any_sync); the
+//    per-warp per-expert counts live in a small shared table that one warp
+//    per expert turns into exclusive prefixes with a shuffle scan;
+//  * runs (more slots, up to 96 experts): each thread owns one contiguous
+//    run of slots and counts it into its own column of a [E_tot][1024]
+//    table; a scan along each expert's row gives every thread its first
+//    position per expert, and the thread places its run in order.  When the
+//    padded list fits, it is built in shared memory and copied out in one
+//    coalesced sweep instead of scattered 4-byte stores.
 //
 // Inside the forward the same pass also records the real (non-padding) row
 // count of every block and, with adapters, per sorted position the token's
@@ -26,6 +33,15 @@ namespace {
 
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
+constexpr int kRunsMaxExperts = 96;      // per-thread count columns: 96 x 1024 x 2 B
+constexpr int kMaxSmem = 227 * 1024;
+
+// kinds of the slot pass
+enum : int {
+    kPasses = 0,     // passes of 1024 slots with warp-level ranks
+    kRuns = 1,       // one contiguous run of slots per thread, direct stores
+    kRunsStaged = 2, // runs, sorted ids and adapters staged in shared memory
+};
 
 // Exclusive block scan of one int per thread; returns the exclusive prefix
 // and writes the block total to *total.  Uses 33 ints of scratch.
@@ -57,34 +73,94 @@ __device__ int block_exclusive_scan(int v, int* scratch, int* total) {
     return excl;
 }
 
+// ids[f .. f+4) clipped to end (missing entries read as -1); one 16-byte
+// load when the run is aligned
+__device__ __forceinline__ void load_ids4(const int32_t* __restrict__ ids, int f, int end, bool vec_ok, int* e4) {
+    if (vec_ok && f + 4 <= end) {
+        const int4 v = __ldg(reinterpret_cast<const int4*>(ids + f));
+        e4[0] = v.x; e4[1] = v.y; e4[2] = v.z; e4[3] = v.w;
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) e4[j] = f + j < end ? ids[f + j] : -1;
+    }
+}
+
 template <bool kWithLora>
 __global__ void __launch_bounds__(kThreads, 1)
     align_kernel(const int32_t* __restrict__ ids, int S, int E_tot, int BM, int max_padded,
                  int32_t* __restrict__ sorted, int32_t* __restrict__ expert_ids, int32_t* __restrict__ n_pad_out,
-                 uint32_t* __restrict__ status, AlignExtra ex) {
+                 uint32_t* __restrict__ status, int runs, AlignExtra ex) {
     extern __shared__ int smem_i[];
     int* cnt = smem_i;                                            // [E_tot] slots per expert
     int* first = cnt + E_tot;                                     // [E_tot] padded start of each expert
     int* cursor = first + E_tot;                                  // [E_tot] next free position
     int* scratch = cursor + E_tot;                                // [40]
-    uint16_t* wcnt = reinterpret_cast<uint16_t*>(scratch + 40);   // [kWarps][E_tot]
+    // passes: [kWarps][E_tot] per-warp counts; runs: [E_tot][kThreads] per-thread counts
+    uint16_t* wcnt = reinterpret_cast<uint16_t*>(scratch + 40);
+    // staged runs: [max_padded] sorted slot ids, then [max_padded] adapters
+    const bool staged = runs == kRunsStaged;
+    uint16_t* st_sorted = wcnt + static_cast<size_t>(E_tot) * kThreads;
+    int16_t* st_lora = reinterpret_cast<int16_t*>(st_sorted + max_padded);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     griddep_wait();
     griddep_launch_dependents();
+    const unsigned lt_mask = (1u << lane) - 1u;
+    // runs: slots per thread, a multiple of 4 so that a run starts on a
+    // 16-byte boundary when ids does
+    const int run_len = ((S + kThreads - 1) / kThreads + 3) & ~3;
+    const bool vec_ok = (reinterpret_cast<uintptr_t>(ids) & 15) == 0;
+    const int run0 = min(S, tid * run_len), run1 = min(S, run0 + run_len);
 
     for (int e = tid; e < E_tot; e += kThreads) cnt[e] = 0;
-    for (int i = tid; i < kWarps * E_tot; i += kThreads) wcnt[i] = 0;
+    if (runs) {
+        for (int e = 0; e < E_tot; ++e) wcnt[e * kThreads + tid] = 0;
+    } else {
+        for (int i = tid; i < kWarps * E_tot; i += kThreads) wcnt[i] = 0;
+    }
     __syncthreads();
 
-    // 1. histogram, one shared atomic per distinct expert of a warp
-    const unsigned lt_mask = (1u << lane) - 1u;
-    for (int f0 = 0; f0 < S; f0 += kThreads) {
-        const int f = f0 + tid;
-        const int e = f < S ? ids[f] : -1;
-        const bool valid = static_cast<unsigned>(e) < static_cast<unsigned>(E_tot);
-        if (f < S && !valid && status) atomicOr(status, MLORA_DEV_BAD_EXPERT_ID);
-        const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : -1);
-        if (valid && (peers & lt_mask) == 0) atomicAdd(&cnt[e], __popc(peers));
+    // 1. histogram
+    if (runs) {
+        // each thread counts its own run of slots into its own column, then
+        // one warp per expert turns the row into exclusive prefixes (in slot
+        // order) and the expert's total
+        for (int f = run0; f < run1; f += 4) {
+            int e4[4];
+            load_ids4(ids, f, run1, vec_ok, e4);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (f + j >= run1) break;
+                if (static_cast<unsigned>(e4[j]) < static_cast<unsigned>(E_tot))
+                    ++wcnt[e4[j] * kThreads + tid];
+                else if (status)
+                    atomicOr(status, MLORA_DEV_BAD_EXPERT_ID);
+            }
+        }
+        __syncthreads();
+        for (int e = warp; e < E_tot; e += kWarps) {
+            uint16_t* row = wcnt + e * kThreads;
+            int base = 0;
+            for (int j = 0; j < kThreads; j += 32) {
+                const int c = row[j + lane];
+                int inc = c;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const int nb = __shfl_up_sync(0xffffffffu, inc, off);
+                    if (lane >= off) inc += nb;
+                }
+                row[j + lane] = static_cast<uint16_t>(base + inc - c);
+                base += __shfl_sync(0xffffffffu, inc, 31);
+            }
+            if (lane == 0) cnt[e] = base;
+        }
+    } else {
+        for (int f = tid; f < S; f += kThreads) {
+            const int e = ids[f];
+            if (static_cast<unsigned>(e) < static_cast<unsigned>(E_tot))
+                atomicAdd(&cnt[e], 1);
+            else if (status)
+                atomicOr(status, MLORA_DEV_BAD_EXPERT_ID);
+        }
     }
     __syncthreads();
 
@@ -112,20 +188,63 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n = cnt[e];
         const int pad_end = first[e] + (n + BM - 1) / BM * BM;
         for (int p = first[e] + n + lane; p < pad_end; p += 32) {
-            sorted[p] = S;
-            if (kWithLora) ex.lora_of[p] = -1;
+            if (staged) {
+                st_sorted[p] = static_cast<uint16_t>(S);
+                st_lora[p] = -1;
+            } else {
+                sorted[p] = S;
+                if (kWithLora) ex.lora_of[p] = -1;
+            }
         }
     }
 
-    // 4. stable scatter, 1024 slots per pass.  Within a pass a slot's rank
+    // 4a. runs: every thread places its own run in order
+    if (runs) {
+        for (int f0 = run0; f0 < run1; f0 += 4) {
+            int e4[4];
+            load_ids4(ids, f0, run1, vec_ok, e4);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int f = f0 + j, e = e4[j];
+                if (f >= run1) break;
+                if (static_cast<unsigned>(e) >= static_cast<unsigned>(E_tot)) continue;
+                const int p = first[e] + wcnt[e * kThreads + tid]++;
+                int l = -1;
+                if (kWithLora) {
+                    l = ex.token_lora_idx[f / ex.K_total];
+                    if (l < -1 || l >= ex.L) {
+                        if (status) atomicOr(status, MLORA_DEV_BAD_LORA_IDX);
+                        l = -1;
+                    }
+                }
+                if (staged) {
+                    st_sorted[p] = static_cast<uint16_t>(f);
+                    st_lora[p] = static_cast<int16_t>(l);
+                } else {
+                    sorted[p] = f;
+                    if (kWithLora) ex.lora_of[p] = l;
+                }
+            }
+        }
+        __syncthreads();
+        // staged: one coalesced copy of the sorted ids (and adapters) out
+        if (staged) {
+            for (int p = tid; p < total; p += kThreads) {
+                sorted[p] = st_sorted[p];
+                if (kWithLora) ex.lora_of[p] = st_lora[p];
+            }
+        }
+    }
+
+    // 4b. passes: stable scatter, 1024 slots per pass.  Within a pass a slot's rank
     //    among the slots of its expert is (its expert's slots in earlier
     //    warps) + (earlier lanes of its warp with the same expert); the first
     //    term comes from a per-expert scan over the warps' counts, done one
     //    expert column per warp.
     // the next pass's expert and adapter ids are loaded during this one
-    int e_next = tid < S ? ids[tid] : -1;
-    int l_next = (kWithLora && tid < S) ? ex.token_lora_idx[tid / ex.K_total] : -1;
-    for (int base = 0; base < S; base += kThreads) {
+    int e_next = (!runs && tid < S) ? ids[tid] : -1;
+    int l_next = (kWithLora && !runs && tid < S) ? ex.token_lora_idx[tid / ex.K_total] : -1;
+    for (int base = 0; !runs && base < S; base += kThreads) {
         const int f = base + tid;
         const int e = e_next;
         const int l_in = l_next;
@@ -185,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < kMaxPerLane; ++i) {
             const int r = lane + 32 * i;
-            mine[i] = r < BM ? ex.lora_of[b * BM + r] : -1;
+            mine[i] = r >= BM ? -1 : staged ? st_lora[b * BM + r] : ex.lora_of[b * BM + r];
         }
         int prev = -1, count = 0;
         for (;;) {
@@ -238,8 +357,19 @@ long align_max_padded(long S, int E_tot, int block_m) {
 cudaError_t launch_align(const int32_t* ids, long S, int E_tot, int block_m, long max_padded, int32_t* sorted,
                          int32_t* expert_ids, int32_t* n_pad, uint32_t* status, const AlignExtra* extra,
                          cudaStream_t s) {
-    const size_t smem = sizeof(int) * (3 * static_cast<size_t>(E_tot) + 40) +
-                        sizeof(uint16_t) * static_cast<size_t>(kWarps) * E_tot;
+    // several passes over the slots, or (more than one pass of slots, few
+    // experts) per-thread runs with one count column per thread
+    // experts) per-thread runs with one count column per thread, staged in
+    // shared memory when the padded list fits there too
+    int runs = S > kThreads && E_tot <= kRunsMaxExperts && S <= 65535 ? kRuns : kPasses;
+    size_t smem = sizeof(int) * (3 * static_cast<size_t>(E_tot) + 40) +
+                  sizeof(uint16_t) * static_cast<size_t>(runs ? kThreads : kWarps) * E_tot;
+    const size_t stage_bytes = (sizeof(uint16_t) + sizeof(int16_t)) * static_cast<size_t>(max_padded);
+    const bool small_l = !extra || extra->L <= 32767;
+    if (runs == kRuns && small_l && smem + stage_bytes <= static_cast<size_t>(kMaxSmem)) {
+        runs = kRunsStaged;
+        smem += stage_bytes;
+    }
     static unsigned long long attr_set[2] = {0ull, 0ull};  // one bit per device
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
@@ -250,23 +380,23 @@ cudaError_t launch_align(const int32_t* ids, long S, int E_tot, int block_m, lon
     if (extra) ex = *extra;
     if (with_lora) {
         if (!(attr_set[1] & bit)) {
-            err = cudaFuncSetAttribute(align_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
+            err = cudaFuncSetAttribute(align_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
             if (err != cudaSuccess) return err;
             attr_set[1] |= bit;
         }
         err = launch_pdl(align_kernel<true>, dim3(1), dim3(kThreads), smem, s, ids, static_cast<int>(S), E_tot, block_m,
                                                      static_cast<int>(max_padded), sorted, expert_ids, n_pad, status,
-                                                     ex);
+                                                     runs, ex);
         if (err != cudaSuccess) return err;
     } else {
         if (!(attr_set[0] & bit)) {
-            err = cudaFuncSetAttribute(align_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
+            err = cudaFuncSetAttribute(align_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
             if (err != cudaSuccess) return err;
             attr_set[0] |= bit;
         }
         err = launch_pdl(align_kernel<false>, dim3(1), dim3(kThreads), smem, s, ids, static_cast<int>(S), E_tot, block_m,
                                                       static_cast<int>(max_padded), sorted, expert_ids, n_pad, status,
-                                                      ex);
+                                                      runs, ex);
         if (err != cudaSuccess) return err;
     }
     return cudaGetLastError();

@@ -98,6 +98,7 @@ def test_stress_sampled_and_early_exit():
     # more than 4096 slots: the tensor-core shrink on ragged K and rank
     dict(M=1100, H=136, I=72, E=5, top_k=4, L=3, r=24, seed=109),
     dict(M=1030, H=64, I=200, E=6, top_k=4, L=9, r=8, seed=110),
+    dict(M=1100, H=64, I=64, E=96, top_k=4, L=3, r=8, seed=112),           # runs align, not staged
 ])
 def test_edges(over):
     _layer(wl.spec("tiny", **over), label=str(over))

@@ -99,9 +99,35 @@ def test_align_edges():
     # the largest expert count
     ids = rng.integers(0, 1024, size=(700, 4), dtype=np.int32)
     _align_case(ids, 1024, 8)
-    # more slots than one pass of the scatter, ragged tail
+    # more slots than one pass of the scatter, ragged tail (per-thread runs,
+    # staged in shared memory)
     ids = rng.integers(0, 5, size=(3001, 3), dtype=np.int32)
     _align_case(ids, 5, 64)
+    # runs whose padded list does not fit in shared memory (96 experts)
+    ids = rng.integers(0, 96, size=(4000, 8), dtype=np.int32)
+    _align_case(ids, 96, 16)
+    # several passes: one expert too many for runs, and more than 65535 slots
+    ids = rng.integers(0, 97, size=(1500, 3), dtype=np.int32)
+    _align_case(ids, 97, 32)
+    ids = rng.integers(0, 8, size=(16500, 4), dtype=np.int32)
+    _align_case(ids, 8, 128)
+
+
+def test_align_unaligned_ids():
+    # ids that start 4 bytes past a 16-byte boundary: the runs read them
+    # one by one
+    rng = np.random.default_rng(1)
+    ids_np = rng.integers(0, 6, size=(2001, 3), dtype=np.int32)
+    buf = torch.empty(ids_np.size + 1, dtype=torch.int32, device="cuda")
+    buf[1:] = torch.from_numpy(ids_np.reshape(-1)).cuda()
+    view = buf[1:].view(2001, 3)
+    assert view.data_ptr() % 16 == 4
+    s_ref, e_ref, n_ref = oracle.moe_align(ids_np, 6, 16)
+    s, e, n = ml.mlora_moe_align(view, 6, 16)
+    torch.cuda.synchronize()
+    assert int(n.item()) == n_ref
+    assert np.array_equal(s.cpu().numpy(), s_ref)
+    assert np.array_equal(e.cpu().numpy(), e_ref)
 
 
 def test_align_empty():

@@ -235,8 +235,8 @@ def profiled_traffic(stage: str, workload: str):
         text = open(path).read()
     except OSError:
         return None
-    m_hash = re.search(r"kernel source hash:\s*`?([0-9a-f]{16})", text)
-    m_val = re.search(r"dram bytes per launch:\s*`?([0-9.eE+]+)", text)
+    m_hash = re.search(r"kernel source hash:[\s|`]*([0-9a-f]{16})", text)
+    m_val = re.search(r"dram bytes per launch:[\s|`]*([0-9.eE+]+)", text)
     if not m_hash or not m_val or m_hash.group(1) != kernel_source_hash(stage):
         return None
     return float(m_val.group(1))
@@ -458,7 +458,7 @@ def main(argv=None):
             "data": "synthetic (seeded, random-init weights)", "config": cfg,
             "roofline": {"bound": bound, "kernel": dom, "achieved": achieved, "peak": peak, "unit": unit,
                          "frac": achieved / peak, "peak_source": peak_src,
-                         "traffic": profiled_traffic(dom, s.name),
+                         "traffic": profiled_traffic(dom, s.name) if args.M is None else None,
                          "kernel_ms": dom_ms},
             "layer": {"hbm_frac": layer_hbm_frac, "tensor_frac": layer_tc_frac,
                       "ms_per_step_with_stage_events": res["inst_ms"],

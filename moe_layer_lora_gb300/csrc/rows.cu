@@ -28,7 +28,16 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
         if (f >= S) continue;  // padding row: never stored downstream
         const uint4* src = x + static_cast<size_t>(f / K_total) * H8;
         uint4* dst = x_perm + static_cast<size_t>(p) * H8;
-        for (int i = lane; i < H8; i += 32) dst[i] = __ldg(src + i);
+        // four independent 16-byte loads in flight per lane
+        for (int i0 = lane; i0 < H8; i0 += 128) {
+            uint4 v[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (i0 + 32 * j < H8) v[j] = __ldg(src + i0 + 32 * j);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (i0 + 32 * j < H8) dst[i0 + 32 * j] = v[j];
+        }
     }
 }
 
@@ -54,15 +63,31 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ 
         const int m = static_cast<int>(idx / H8);
         const int c = static_cast<int>(idx - static_cast<long>(m) * H8);
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        for (int k = 0; k < K_total; ++k) {
-            const long f = static_cast<long>(m) * K_total + k;
-            const int e = __ldg(topk_ids + f);
-            if (static_cast<unsigned>(e) >= static_cast<unsigned>(E_tot)) continue;  // dropped slot
-            const float wk = __ldg(topk_w + f);
-            float v[8];
-            bf16x8_to_f32(__ldg(y_slot + f * H8 + c), v);
+        // slots in groups of four: their loads are issued together, the sum
+        // still runs over k in ascending order
+        for (int k0 = 0; k0 < K_total; k0 += 4) {
+            uint4 raw[4];
+            float wk[4];
+            bool live[4];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] = fmaf(wk, v[i], acc[i]);
+            for (int j = 0; j < 4; ++j) {
+                const long f = static_cast<long>(m) * K_total + k0 + j;
+                const int e = k0 + j < K_total ? __ldg(topk_ids + f) : -1;
+                live[j] = static_cast<unsigned>(e) < static_cast<unsigned>(E_tot);  // else a dropped slot
+                wk[j] = 0.f;
+                if (live[j]) {
+                    wk[j] = __ldg(topk_w + f);
+                    raw[j] = __ldcs(y_slot + f * H8 + c);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (!live[j]) continue;
+                float v[8];
+                bf16x8_to_f32(raw[j], v);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[i] = fmaf(wk[j], v[i], acc[i]);
+            }
         }
         uint4 o;
         o.x = pack_bf16x2(out_scale * acc[0], out_scale * acc[1]);

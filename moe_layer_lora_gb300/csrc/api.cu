@@ -135,6 +135,7 @@ Workspace carve_workspace(const Sizes& z, void* base) {
     w.status = reinterpret_cast<uint32_t*>(header);
     w.n_pad = reinterpret_cast<int32_t*>(header ? header + 4 : nullptr);
     w.gt_total = reinterpret_cast<int32_t*>(header ? header + 8 : nullptr);
+    w.tile_next = reinterpret_cast<int32_t*>(header ? header + 12 : nullptr);
     w.act_done = reinterpret_cast<int32_t*>(take(4 * z.max_blocks));
     if (z.lora) {
         w.done13 = reinterpret_cast<int32_t*>(take(4 * z.max_blocks));
@@ -327,6 +328,7 @@ mlora_status mlora_moe_forward(const void* x, const void* w13, const void* w2, c
     gp.gt_first = ws.gt_first;
     gp.gt_total = ws.gt_total;
     gp.act_done = ws.act_done;
+    gp.tile_next = ws.tile_next;
     gp.status = ws.status;
     gp.E_tot = E_tot;
     gp.cap = z.cap;

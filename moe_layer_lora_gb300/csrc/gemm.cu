@@ -3,8 +3,11 @@
 // in one persistent kernel.
 //
 // The kernel works through four phases of tiles over blocks of kBlockM =
-// 128 sorted slots (all slots of a block share one expert e, from align);
-// every CTA takes tiles c, c + grid, ... of the concatenated sequence:
+// 128 sorted slots (all slots of a block share one expert e, from align).
+// CTA c starts with tile c of the concatenated sequence; from then on, as
+// it starts a tile its producer claims the next unclaimed one from a
+// global counter, so tiles of unequal cost (shrink, gate_up, down, blocks
+// with many adapters) spread evenly over the SMs:
 //
 //  1. gate_up shrink tiles (with adapters): T13_l = s * X A13_{l,e}^T for
 //     up to `gsize` adapters l of one block at once -- their rank rows
@@ -24,10 +27,13 @@
 //  4. down tiles: d = act W2_e^T over 256 output columns + the T2 expand;
 //     epilogue the slot's expert output in bf16.
 //
-// A tile depends only on tiles of earlier phases of the same block, and
-// every CTA finishes its earlier-phase tiles first, so the producer waits
-// on the block's counters (act before a down-side tile starts, the shrink
-// counter before the expand stages) and the phases overlap across CTAs:
+// A tile depends only on tiles of earlier phases of the same block, i.e.
+// on tiles with smaller indices.  Tiles are claimed in index order, every
+// CTA is resident (grid <= SMs) and works through its claims in order, so
+// the unfinished tile with the smallest index always has its inputs ready:
+// the producer can wait on the block's counters (act before a down-side
+// tile starts, the shrink counter before the expand stages) without
+// deadlock, and the phases overlap across CTAs:
 // the gate_up base product streams while other CTAs run shrink tiles, and
 // the down GEMM fills the gate_up tail.  (The pages overlap the shrink and
 // expand kernels with PDL; here they share one grid.)
@@ -51,6 +57,7 @@ constexpr int kThreads = 192;
 constexpr int kBN = 256;                                         // weight rows per tile (MMA N)
 constexpr int kHalf = kBN / 2;                                   // gate (and up) rows of a gate_up tile
 constexpr int kStages = 4;
+constexpr int kTileRing = 4;                                     // claimed tiles handed from producer to consumers
 constexpr int kATileBytes = kBlockM * kBlockK * 2;               // 16 KiB
 constexpr int kStageBytes = kATileBytes + kBN * kBlockK * 2;     // 48 KiB
 constexpr int kAccCols = kBN;
@@ -140,6 +147,21 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, long tile, cons
     return t;
 }
 
+// K-chunks of 64 packed into one stage of a shrink tile.  A chunk is the A
+// rows actually loaded (a_bytes) followed by the group's adapter rows
+// (b_bytes); both are multiples of 2 KiB, so every chunk starts on a
+// 1 KiB swizzle atom.  The MMA reads 128 A rows from a chunk's start, so
+// that 16 KiB window must stay inside the stage as well.
+constexpr int kMaxShrinkChunks = 4;
+__device__ __forceinline__ int shrink_chunks(uint32_t a_bytes, uint32_t b_bytes) {
+    const uint32_t chunk = a_bytes + b_bytes;
+    int c = 1;
+    while (c < kMaxShrinkChunks && (c + 1) * chunk <= static_cast<uint32_t>(kStageBytes) &&
+           c * chunk + kATileBytes <= static_cast<uint32_t>(kStageBytes))
+        ++c;
+    return c;
+}
+
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + __expf(-z)); }
 
 __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_constant__ GemmParams p) {
@@ -151,7 +173,10 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
     uint64_t* tempty = tfull + 2;
     uint64_t* drain = tempty + 2;
     uint64_t* pub = drain + 1;  // the 128 epilogue threads finished writing a published tile
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(pub + 1);
+    uint64_t* tile_full = pub + 1;                 // [kTileRing] a claimed tile index is in the ring
+    uint64_t* tile_empty = tile_full + kTileRing;  // [kTileRing] the MMA lane and 4 epilogue warps read it
+    long long* tile_ring = reinterpret_cast<long long*>(tile_empty + kTileRing);
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(tile_ring + kTileRing);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -166,6 +191,10 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
         }
         mbar_init(drain, 1);
         mbar_init(pub, 128);
+        for (int r = 0; r < kTileRing; ++r) {
+            mbar_init(&tile_full[r], 1);
+            mbar_init(&tile_empty[r], 1 + 4);
+        }
         *abort_flag = 0;
         fence_barrier_init();
         for (int sd = 0; sd < 2; ++sd) {
@@ -206,7 +235,21 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
         if (lane == 0) {
             long it = 0;
             bool ok = true;
-            for (long tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+            long tile = blockIdx.x, next = 0;
+            for (int jt = 0; ok; ++jt, tile = next) {
+                // hand the tile (or the end mark) to the MMA lane and the
+                // epilogue, then claim the next one; its index is needed
+                // only once this tile's loads are issued
+                const int ts = jt % kTileRing;
+                if (!mbar_wait(&tile_empty[ts], (static_cast<uint32_t>(jt / kTileRing) & 1u) ^ 1u, abort_flag,
+                               p.status)) {
+                    ok = false;
+                    break;
+                }
+                tile_ring[ts] = tile < ntiles ? tile : -1;
+                mbar_arrive(&tile_full[ts]);
+                if (tile >= ntiles) break;
+                next = gridDim.x + static_cast<long>(atomicAdd(p.tile_next, 1));
                 const Tile tc = decode_tile(p, tile, ph, ns, nblocks);
                 const GemmSide& sd = p.side[tc.side];
                 const int row0 = tc.b * kBlockM;
@@ -223,6 +266,39 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
                 const uint32_t a_bytes = static_cast<uint32_t>(nbox) * kRowBox * kBlockK * 2;
                 const int32_t* lora_list = p.blk_lora + static_cast<long>(tc.b) * p.cap;
                 const int nk = (sd.K + kBlockK - 1) / kBlockK;
+                if (tc.shrink) {
+                    // several K-chunks per stage: the shrink's operands are
+                    // small, and a stage of one chunk leaves the copy
+                    // engine latency-bound
+                    const uint32_t b_bytes = static_cast<uint32_t>(tc.g) * rp * kBlockK * 2;
+                    const uint32_t chunk = a_bytes + b_bytes;
+                    const int cps = shrink_chunks(a_bytes, b_bytes);
+                    for (int kb0 = 0; kb0 < nk; kb0 += cps, ++it) {
+                        const int s = static_cast<int>(it % kStages);
+                        const uint32_t phs = static_cast<uint32_t>(it / kStages) & 1u;
+                        if (!mbar_wait(&empty[s], phs ^ 1u, abort_flag, p.status)) {
+                            ok = false;
+                            break;
+                        }
+                        const int nc = min(cps, nk - kb0);
+                        mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(nc) * chunk);
+                        for (int c = 0; c < nc; ++c) {
+                            uint8_t* ca = smem + s * kStageBytes + c * chunk;
+                            uint8_t* cb = ca + a_bytes;
+                            const int k0 = (kb0 + c) * kBlockK;
+                            for (int i = 0; i < tc.g; ++i)
+                                tma_load_3d(cb + i * rp * kBlockK * 2, &sd.tm_sa, &full[s], k0, 0,
+                                            lora_list[tc.i0 + i] * p.E_tot + tc.e);
+                            if (full_block)
+                                tma_load_2d(ca, &sd.tm_a_full, &full[s], k0, row0);
+                            else
+                                for (int i = 0; i < nbox; ++i)
+                                    tma_load_2d(ca + i * kRowBox * kBlockK * 2, &sd.tm_a, &full[s], k0,
+                                                row0 + i * kRowBox);
+                        }
+                    }
+                    continue;
+                }
                 for (int kb = 0; kb < nk; ++kb, ++it) {
                     const int s = static_cast<int>(it % kStages);
                     const uint32_t phs = static_cast<uint32_t>(it / kStages) & 1u;
@@ -233,12 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
                     uint8_t* sa = smem + s * kStageBytes;
                     uint8_t* sb = sa + kATileBytes;
                     const int k0 = kb * kBlockK;
-                    if (tc.shrink) {
-                        mbar_arrive_expect_tx(&full[s], a_bytes + tc.g * rp * kBlockK * 2);
-                        for (int i = 0; i < tc.g; ++i)
-                            tma_load_3d(sb + i * rp * kBlockK * 2, &sd.tm_sa, &full[s], k0, 0,
-                                        lora_list[tc.i0 + i] * p.E_tot + tc.e);
-                    } else if (tc.kind == kGateUp) {
+                    if (tc.kind == kGateUp) {
                         mbar_arrive_expect_tx(&full[s], a_bytes + kBN * kBlockK * 2);
                         tma_load_4d(sb, &sd.tm_b, &full[s], k0, tc.cb * kHalf, 0, tc.e);
                         tma_load_4d(sb + kHalf * kBlockK * 2, &sd.tm_b, &full[s], k0, tc.cb * kHalf, 1, tc.e);
@@ -252,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
                         for (int i = 0; i < nbox; ++i)
                             tma_load_2d(sa + i * kRowBox * kBlockK * 2, &sd.tm_a, &full[s], k0, row0 + i * kRowBox);
                 }
-                if (!ok || tc.shrink || !p.has_lora) continue;
+                if (!ok || !p.has_lora) continue;
                 const int nad = p.blk_nad[tc.b];
                 if (nad == 0) continue;
                 // the expand needs every shrink tile of this block and side
@@ -296,9 +367,13 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
         if (lane == 0) {
             const uint32_t idesc_base = umma_idesc_bf16(128, kBN);
             long it = 0;
-            int lt = 0;
             bool ok = true;
-            for (long tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++lt) {
+            for (int lt = 0; ok; ++lt) {
+                const int ts = lt % kTileRing;
+                if (!mbar_wait(&tile_full[ts], static_cast<uint32_t>(lt / kTileRing) & 1u, abort_flag, p.status)) break;
+                const long tile = tile_ring[ts];
+                mbar_arrive(&tile_empty[ts]);
+                if (tile < 0) break;
                 const Tile tc = decode_tile(p, tile, ph, ns, nblocks);
                 const int nk = (p.side[tc.side].K + kBlockK - 1) / kBlockK;
                 const int acc = lt & 1;
@@ -309,6 +384,35 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
                 tc_fence_after();
                 const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kAccCols);
                 const uint32_t idesc = tc.shrink ? umma_idesc_bf16(128, tc.g * rp) : idesc_base;
+                if (tc.shrink) {
+                    // the producer's packing: cps K-chunks of (A rows, adapter rows) per stage
+                    const int nbox = (p.blk_rows[tc.b] + kRowBox - 1) / kRowBox;
+                    const uint32_t a_bytes = nbox * kRowBox == kBlockM ? static_cast<uint32_t>(kATileBytes)
+                                                                       : static_cast<uint32_t>(nbox) * kRowBox * kBlockK * 2;
+                    const uint32_t chunk = a_bytes + static_cast<uint32_t>(tc.g) * rp * kBlockK * 2;
+                    const int cps = shrink_chunks(a_bytes, chunk - a_bytes);
+                    for (int kb0 = 0; kb0 < nk; kb0 += cps, ++it) {
+                        const int s = static_cast<int>(it % kStages);
+                        if (!mbar_wait(&full[s], static_cast<uint32_t>(it / kStages) & 1u, abort_flag, p.status)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const int nc = min(cps, nk - kb0);
+                        for (int c = 0; c < nc; ++c) {
+                            const uint32_t a_addr = smem_u32(smem + s * kStageBytes + c * chunk);
+                            const uint64_t ad = umma_desc_sw128(a_addr);
+                            const uint64_t bd = umma_desc_sw128(a_addr + a_bytes);
+#pragma unroll
+                            for (int k = 0; k < kBlockK / 16; ++k)
+                                umma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (kb0 | c | k) != 0 ? 1u : 0u);
+                        }
+                        umma_commit(&empty[s]);
+                    }
+                    if (!ok) break;
+                    umma_commit(&tfull[acc]);
+                    continue;
+                }
                 for (int kb = 0; kb < nk; ++kb, ++it) {
                     const int s = static_cast<int>(it % kStages);
                     if (!mbar_wait(&full[s], static_cast<uint32_t>(it / kStages) & 1u, abort_flag, p.status)) {
@@ -352,9 +456,14 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
         // --------------------------------------------------------- epilogue
         const int q = warp & 3;  // TMEM lane quarter this warp may access
         const int row = q * 32 + lane;
-        int lt = 0;
         uint32_t npub = 0;
-        for (long tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++lt) {
+        for (int lt = 0;; ++lt) {
+            const int ts = lt % kTileRing;
+            if (!mbar_wait(&tile_full[ts], static_cast<uint32_t>(lt / kTileRing) & 1u, abort_flag, p.status)) break;
+            const long tile = tile_ring[ts];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tile_empty[ts]);
+            if (tile < 0) break;
             const Tile tc = decode_tile(p, tile, ph, ns, nblocks);
             const GemmSide& sd = p.side[tc.side];
             const int acc = lt & 1;

@@ -23,6 +23,7 @@ struct Workspace {
     int32_t* gt_total;     // number of shrink group tiles
     int32_t* done13;       // [max_blocks] shrink tiles finished per block, gate_up projection
     int32_t* done2;        // [max_blocks] the same for the down projection
+    int32_t* tile_next;    // experts tiles claimed past the first round
     int32_t* act_done;     // [max_blocks] gate_up tiles finished per block
     size_t zeroed_bytes;   // leading bytes cleared by every forward (header and counters)
     int32_t* sorted_ids;   // [max_padded]
@@ -121,6 +122,7 @@ struct alignas(64) GemmParams {
     const int32_t* gt_first;
     const int32_t* gt_total;
     int32_t* act_done;  // per block: finished gate_up tiles (zero at launch)
+    int32_t* tile_next; // tiles claimed past the first round (zero at launch)
     uint32_t* status;
     int E_tot;
     int cap;

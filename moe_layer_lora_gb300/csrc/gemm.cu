@@ -162,7 +162,9 @@ __device__ __forceinline__ int shrink_chunks(uint32_t a_bytes, uint32_t b_bytes)
     return c;
 }
 
-__device__ __forceinline__ float silu(float z) { return z / (1.0f + __expf(-z)); }
+// silu(z) = z * sigmoid(z); the fast divide returns 0 once 1 + e^-z
+// overflows, the limit for very negative z
+__device__ __forceinline__ float silu(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
 __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_constant__ GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -557,10 +559,11 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
             mbar_arrive(&tempty[acc]);
             if (publish) {
                 // other CTAs read what this tile wrote with TMA: every thread
-                // fences its writes and arrives; one thread waits (bounded)
-                // for all 128 and bumps the block's counter
+                // orders its writes for the async proxy and arrives
+                // (release, CTA scope); one thread waits (bounded, acquire)
+                // for all 128, then a GPU-scope fence -- cumulative over the
+                // writes it has synchronised with -- and the counter bump
                 asm volatile("fence.proxy.async.global;" ::: "memory");
-                __threadfence();
                 mbar_arrive(pub);
                 if (warp == 2 && lane == 0) {
                     if (mbar_wait(pub, npub & 1u, abort_flag, p.status)) {

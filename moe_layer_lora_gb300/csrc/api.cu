@@ -118,7 +118,9 @@ Sizes make_sizes(int M, int H, int I, int E_tot, int K_total, int L, int rank) {
     z.max_blocks = z.max_padded / kBlockM;
     z.cap = z.lora ? std::min(L, kBlockM) : 0;
     z.max_lt = z.max_blocks * z.cap;
-    z.gsize = z.lora ? 256 / ((rank + 15) / 16 * 16) : 1;
+    // adapters per shrink group tile: up to 256 stacked rank rows (the MMA's
+    // N), at most 4 so that a block's shrink spreads over more SMs
+    z.gsize = z.lora ? std::min(4, 256 / ((rank + 15) / 16 * 16)) : 1;
     return z;
 }
 

@@ -385,7 +385,13 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
                 }
                 tc_fence_after();
                 const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kAccCols);
-                const uint32_t idesc = tc.shrink ? umma_idesc_bf16(128, tc.g * rp) : idesc_base;
+                // a down tile whose slab runs past H multiplies only the
+                // valid weight rows (rounded up to the MMA's N granule of 16)
+                const int dn_valid = p.side[1].n_out - tc.cb * kBN;
+                const uint32_t idesc = tc.shrink ? umma_idesc_bf16(128, tc.g * rp)
+                                       : (tc.kind == kDown && dn_valid < kBN)
+                                           ? umma_idesc_bf16(128, (dn_valid + 15) / 16 * 16)
+                                           : idesc_base;
                 if (tc.shrink) {
                     // the producer's packing: cps K-chunks of (A rows, adapter rows) per stage
                     const int nbox = (p.blk_rows[tc.b] + kRowBox - 1) / kRowBox;

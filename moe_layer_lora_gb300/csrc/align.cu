@@ -96,7 +96,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     int* cursor = first + E_tot;                                  // [E_tot] next free position
     int* scratch = cursor + E_tot;                                // [40]
     // passes: [kWarps][E_tot] per-warp counts; runs: [E_tot][kThreads] per-thread counts
-    uint16_t* wcnt = reinterpret_cast<uint16_t*>(scratch + 40);
+    // (16-byte aligned: the runs' row scan reads it as uint4)
+    uint16_t* wcnt = reinterpret_cast<uint16_t*>((reinterpret_cast<uintptr_t>(scratch + 40) + 15) & ~uintptr_t(15));
     // staged runs: [max_padded] sorted slot ids, then [max_padded] adapters
     const bool staged = runs == kRunsStaged;
     uint16_t* st_sorted = wcnt + static_cast<size_t>(E_tot) * kThreads;
@@ -137,21 +138,39 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncthreads();
+        // two levels: each lane sums its 32 consecutive columns (four
+        // 16-byte reads), one shuffle scan over the lanes, then each lane
+        // writes its columns' exclusive prefixes
         for (int e = warp; e < E_tot; e += kWarps) {
-            uint16_t* row = wcnt + e * kThreads;
-            int base = 0;
-            for (int j = 0; j < kThreads; j += 32) {
-                const int c = row[j + lane];
-                int inc = c;
+            uint4* row = reinterpret_cast<uint4*>(wcnt + e * kThreads) + lane * 4;
+            uint4 v[4];
+            int sum = 0;
 #pragma unroll
-                for (int off = 1; off < 32; off <<= 1) {
-                    const int nb = __shfl_up_sync(0xffffffffu, inc, off);
-                    if (lane >= off) inc += nb;
-                }
-                row[j + lane] = static_cast<uint16_t>(base + inc - c);
-                base += __shfl_sync(0xffffffffu, inc, 31);
+            for (int q = 0; q < 4; ++q) {
+                v[q] = row[q];
+                const uint32_t w[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+#pragma unroll
+                for (int h = 0; h < 4; ++h) sum += static_cast<int>(w[h] & 0xffffu) + static_cast<int>(w[h] >> 16);
             }
-            if (lane == 0) cnt[e] = base;
+            int inc = sum;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int nb = __shfl_up_sync(0xffffffffu, inc, off);
+                if (lane >= off) inc += nb;
+            }
+            int run = inc - sum;  // columns of earlier lanes
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint32_t w[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    const int lo = static_cast<int>(w[h] & 0xffffu), hi = static_cast<int>(w[h] >> 16);
+                    w[h] = static_cast<uint32_t>(run) | (static_cast<uint32_t>(run + lo) << 16);
+                    run += lo + hi;
+                }
+                row[q] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            if (lane == 31) cnt[e] = inc;
         }
     } else {
         for (int f = tid; f < S; f += kThreads) {
@@ -362,7 +381,7 @@ cudaError_t launch_align(const int32_t* ids, long S, int E_tot, int block_m, lon
     // experts) per-thread runs with one count column per thread, staged in
     // shared memory when the padded list fits there too
     int runs = S > kThreads && E_tot <= kRunsMaxExperts && S <= 65535 ? kRuns : kPasses;
-    size_t smem = sizeof(int) * (3 * static_cast<size_t>(E_tot) + 40) +
+    size_t smem = sizeof(int) * (3 * static_cast<size_t>(E_tot) + 40) + 16 /* alignment of the count table */ +
                   sizeof(uint16_t) * static_cast<size_t>(runs ? kThreads : kWarps) * E_tot;
     const size_t stage_bytes = (sizeof(uint16_t) + sizeof(int16_t)) * static_cast<size_t>(max_padded);
     const bool small_l = !extra || extra->L <= 32767;

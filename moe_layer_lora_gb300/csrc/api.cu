@@ -278,11 +278,13 @@ mlora_status mlora_moe_forward(const void* x, const void* w13, const void* w2, c
         ok &= make_map(&dn.tm_a, ws.act, 2, da, sa, bx);
         ok &= make_map(&dn.tm_a_full, ws.act, 2, da, sa, bxf);
         const cuuint64_t d13[4] = {H_, I_, 2, E_}, s13[3] = {H_ * 2, I_ * H_ * 2, 2 * I_ * H_ * 2};
-        const cuuint32_t b13[4] = {64, 128, 1, 1};
+        const cuuint32_t b13[4] = {64, 128, 1, 1}, b13n[4] = {64, 64, 1, 1};
         ok &= make_map(&up.tm_b, w13, 4, d13, s13, b13);
+        ok &= make_map(&up.tm_b_n, w13, 4, d13, s13, b13n);
         const cuuint64_t d2[3] = {I_, H_, E_}, s2[2] = {I_ * 2, H_ * I_ * 2};
-        const cuuint32_t b2[3] = {64, 256, 1};
+        const cuuint32_t b2[3] = {64, 256, 1}, b2n[3] = {64, 128, 1};
         ok &= make_map(&dn.tm_b, w2, 3, d2, s2, b2);
+        ok &= make_map(&dn.tm_b_n, w2, 3, d2, s2, b2n);
         if (lora) {
             const cuuint64_t R = rank, LE = static_cast<cuuint64_t>(L) * E_tot;
             const cuuint32_t rp = static_cast<cuuint32_t>((rank + 15) / 16 * 16);
@@ -300,8 +302,10 @@ mlora_status mlora_moe_forward(const void* x, const void* w13, const void* w2, c
             // expand weights: columns past the rank read as zero
             const cuuint64_t dB13[4] = {R, I_, 2, LE}, sB13[3] = {R * 2, I_ * R * 2, 2 * I_ * R * 2};
             ok &= make_map(&up.tm_lb, B13, 4, dB13, sB13, b13);
+            ok &= make_map(&up.tm_lb_n, B13, 4, dB13, sB13, b13n);
             const cuuint64_t dB2[3] = {R, H_, LE}, sB2[2] = {R * 2, H_ * R * 2};
             ok &= make_map(&dn.tm_lb, B2, 3, dB2, sB2, b2);
+            ok &= make_map(&dn.tm_lb_n, B2, 3, dB2, sB2, b2n);
         }
     }
     if (!ok) return cuda_fail(cudaErrorInvalidValue, "tensor map encoding");
@@ -367,7 +371,8 @@ mlora_status mlora_moe_forward(const void* x, const void* w13, const void* w2, c
     err = launch_gather_rows(x, H, ws.sorted_ids, ws.n_pad, z.S, K_total, z.max_padded, ws.x_perm, s);
     if (err != cudaSuccess) return cuda_fail(err, "gather");
     if ((err = mark_stage(2, s)) != cudaSuccess) return cuda_fail(err, "stage event");
-    const long max_tiles = 2 * z.max_lt + z.max_blocks * (up.ncb + dn.ncb);
+    // narrow tiles (half width) at most double the slab count
+    const long max_tiles = 2 * z.max_lt + z.max_blocks * (2L * up.ncb + 2L * dn.ncb);
     err = launch_experts(gp, max_tiles, s);
     if (err != cudaSuccess) return cuda_fail(err, "experts");
     if ((err = mark_stage(3, s)) != cudaSuccess) return cuda_fail(err, "stage event");

@@ -54,8 +54,7 @@ namespace mlora {
 namespace {
 
 constexpr int kThreads = 192;
-constexpr int kBN = 256;                                         // weight rows per tile (MMA N)
-constexpr int kHalf = kBN / 2;                                   // gate (and up) rows of a gate_up tile
+constexpr int kBN = 256;                                         // weight rows per wide tile (MMA N)
 constexpr int kStages = 4;
 constexpr int kTileRing = 4;                                     // claimed tiles handed from producer to consumers
 constexpr int kATileBytes = kBlockM * kBlockK * 2;               // 16 KiB
@@ -106,12 +105,27 @@ struct Tile {
     int g;     // adapters in the group (shrink tiles)
 };
 
+// Tile width of a launch.  Wide tiles take 256 weight rows (gate_up: 128
+// gate + 128 up); when the batch has fewer wide gate_up tiles than the grid
+// has CTAs (a handful of tokens), every tile is narrow (128 rows: 64 gate +
+// 64 up), which doubles the tiles of each phase so that all SMs stream
+// weights (measured: shared-expert layer with one token 86 -> 82 us; with
+// 32 or more tokens narrow tiles were slower).  Every CTA derives the same
+// choice from the padded slot count.
+struct Geom {
+    int bn;      // weight rows per tile (MMA N)
+    int half;    // gate (and up) rows of a gate_up tile
+    int ncb0;    // column slabs per block, gate_up
+    int ncb1;    // column slabs per block, down
+};
+
 // Phase boundaries of the tile sequence.
 struct Phases {
     long s1, g, s2, d;  // ends of phases 1..4
 };
 
-__device__ __forceinline__ Tile decode_tile(const GemmParams& p, long tile, const Phases& ph, int ns, int nblocks) {
+__device__ __forceinline__ Tile decode_tile(const GemmParams& p, const Geom& gm, long tile, const Phases& ph, int ns,
+                                            int nblocks) {
     Tile t;
     long u;
     if (tile < ph.s1) {
@@ -135,7 +149,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, long tile, cons
         t.g = min(p.gsize, p.blk_nad[t.b] - t.i0);
         t.cb = 0;
     } else {
-        const int ncb = p.side[t.side].ncb;
+        const int ncb = t.side ? gm.ncb1 : gm.ncb0;
         t.b = static_cast<int>(u / ncb);
         t.cb = static_cast<int>(u - static_cast<long>(t.b) * ncb);
         t.i0 = 0;
@@ -203,9 +217,11 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
             prefetch_tensormap(&p.side[sd].tm_a);
             prefetch_tensormap(&p.side[sd].tm_a_full);
             prefetch_tensormap(&p.side[sd].tm_b);
+            prefetch_tensormap(&p.side[sd].tm_b_n);
             if (p.has_lora) {
                 prefetch_tensormap(&p.side[sd].tm_sa);
                 prefetch_tensormap(&p.side[sd].tm_lb);
+                prefetch_tensormap(&p.side[sd].tm_lb_n);
                 prefetch_tensormap(&p.side[sd].tm_t);
                 prefetch_tensormap(&p.side[sd].tm_t_full);
             }
@@ -223,11 +239,19 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
 
     const int nblocks = *p.n_pad / kBlockM;
     const int ns = p.has_lora ? *p.gt_total : 0;
+    Geom gm;
+    {
+        const bool narrow = static_cast<long>(nblocks) * p.side[0].ncb < gridDim.x;
+        gm.bn = narrow ? kBN / 2 : kBN;
+        gm.half = gm.bn / 2;
+        gm.ncb0 = (p.side[0].n_out + gm.half - 1) / gm.half;
+        gm.ncb1 = (p.side[1].n_out + gm.bn - 1) / gm.bn;
+    }
     Phases ph;
     ph.s1 = ns;
-    ph.g = ph.s1 + static_cast<long>(nblocks) * p.side[0].ncb;
+    ph.g = ph.s1 + static_cast<long>(nblocks) * gm.ncb0;
     ph.s2 = ph.g + ns;
-    ph.d = ph.s2 + static_cast<long>(nblocks) * p.side[1].ncb;
+    ph.d = ph.s2 + static_cast<long>(nblocks) * gm.ncb1;
     const long ntiles = ph.d;
     const int rp = (p.rank + 15) / 16 * 16;     // rank padded to the MMA's N granule
     const int lora_ksteps = (p.rank + 15) / 16;  // expand K-steps of 16
@@ -252,12 +276,12 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
                 mbar_arrive(&tile_full[ts]);
                 if (tile >= ntiles) break;
                 next = gridDim.x + static_cast<long>(atomicAdd(p.tile_next, 1));
-                const Tile tc = decode_tile(p, tile, ph, ns, nblocks);
+                const Tile tc = decode_tile(p, gm, tile, ph, ns, nblocks);
                 const GemmSide& sd = p.side[tc.side];
                 const int row0 = tc.b * kBlockM;
                 // the down side reads act rows, complete once the block's
                 // gate_up tiles all are
-                if (tc.side == 1 && !wait_counter(p.act_done + tc.b, p.side[0].ncb, abort_flag, p.status)) {
+                if (tc.side == 1 && !wait_counter(p.act_done + tc.b, gm.ncb0, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
@@ -268,6 +292,8 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
                 const uint32_t a_bytes = static_cast<uint32_t>(nbox) * kRowBox * kBlockK * 2;
                 const int32_t* lora_list = p.blk_lora + static_cast<long>(tc.b) * p.cap;
                 const int nk = (sd.K + kBlockK - 1) / kBlockK;
+                const CUtensorMap* bmap = gm.bn == kBN ? &sd.tm_b : &sd.tm_b_n;
+                const CUtensorMap* lbmap = gm.bn == kBN ? &sd.tm_lb : &sd.tm_lb_n;
                 if (tc.shrink) {
                     // several K-chunks per stage: the shrink's operands are
                     // small, and a stage of one chunk leaves the copy
@@ -312,12 +338,12 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
                     uint8_t* sb = sa + kATileBytes;
                     const int k0 = kb * kBlockK;
                     if (tc.kind == kGateUp) {
-                        mbar_arrive_expect_tx(&full[s], a_bytes + kBN * kBlockK * 2);
-                        tma_load_4d(sb, &sd.tm_b, &full[s], k0, tc.cb * kHalf, 0, tc.e);
-                        tma_load_4d(sb + kHalf * kBlockK * 2, &sd.tm_b, &full[s], k0, tc.cb * kHalf, 1, tc.e);
+                        mbar_arrive_expect_tx(&full[s], a_bytes + gm.bn * kBlockK * 2);
+                        tma_load_4d(sb, bmap, &full[s], k0, tc.cb * gm.half, 0, tc.e);
+                        tma_load_4d(sb + gm.half * kBlockK * 2, bmap, &full[s], k0, tc.cb * gm.half, 1, tc.e);
                     } else {
-                        mbar_arrive_expect_tx(&full[s], a_bytes + kBN * kBlockK * 2);
-                        tma_load_3d(sb, &sd.tm_b, &full[s], k0, tc.cb * kBN, tc.e);
+                        mbar_arrive_expect_tx(&full[s], a_bytes + gm.bn * kBlockK * 2);
+                        tma_load_3d(sb, bmap, &full[s], k0, tc.cb * gm.bn, tc.e);
                     }
                     if (full_block)
                         tma_load_2d(sa, &sd.tm_a_full, &full[s], k0, row0);
@@ -344,12 +370,12 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
                     uint8_t* sa = smem + s * kStageBytes;
                     uint8_t* sb = sa + kATileBytes;
                     const int le = lora_list[i] * p.E_tot + tc.e;
-                    mbar_arrive_expect_tx(&full[s], a_bytes + kBN * kBlockK * 2);
+                    mbar_arrive_expect_tx(&full[s], a_bytes + gm.bn * kBlockK * 2);
                     if (tc.kind == kGateUp) {
-                        tma_load_4d(sb, &sd.tm_lb, &full[s], 0, tc.cb * kHalf, 0, le);
-                        tma_load_4d(sb + kHalf * kBlockK * 2, &sd.tm_lb, &full[s], 0, tc.cb * kHalf, 1, le);
+                        tma_load_4d(sb, lbmap, &full[s], 0, tc.cb * gm.half, 0, le);
+                        tma_load_4d(sb + gm.half * kBlockK * 2, lbmap, &full[s], 0, tc.cb * gm.half, 1, le);
                     } else {
-                        tma_load_3d(sb, &sd.tm_lb, &full[s], 0, tc.cb * kBN, le);
+                        tma_load_3d(sb, lbmap, &full[s], 0, tc.cb * gm.bn, le);
                     }
                     if (full_block)
                         tma_load_2d(sa, &sd.tm_t_full, &full[s], 0, (lt0 + i) * kBlockM);
@@ -367,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            const uint32_t idesc_base = umma_idesc_bf16(128, kBN);
+            const uint32_t idesc_base = umma_idesc_bf16(128, gm.bn);
             long it = 0;
             bool ok = true;
             for (int lt = 0; ok; ++lt) {
@@ -376,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
                 const long tile = tile_ring[ts];
                 mbar_arrive(&tile_empty[ts]);
                 if (tile < 0) break;
-                const Tile tc = decode_tile(p, tile, ph, ns, nblocks);
+                const Tile tc = decode_tile(p, gm, tile, ph, ns, nblocks);
                 const int nk = (p.side[tc.side].K + kBlockK - 1) / kBlockK;
                 const int acc = lt & 1;
                 if (!mbar_wait(&tempty[acc], (static_cast<uint32_t>(lt >> 1) & 1u) ^ 1u, abort_flag, p.status)) {
@@ -387,9 +413,9 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
                 const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kAccCols);
                 // a down tile whose slab runs past H multiplies only the
                 // valid weight rows (rounded up to the MMA's N granule of 16)
-                const int dn_valid = p.side[1].n_out - tc.cb * kBN;
+                const int dn_valid = p.side[1].n_out - tc.cb * gm.bn;
                 const uint32_t idesc = tc.shrink ? umma_idesc_bf16(128, tc.g * rp)
-                                       : (tc.kind == kDown && dn_valid < kBN)
+                                       : (tc.kind == kDown && dn_valid < gm.bn)
                                            ? umma_idesc_bf16(128, (dn_valid + 15) / 16 * 16)
                                            : idesc_base;
                 if (tc.shrink) {
@@ -472,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
             __syncwarp();
             if (lane == 0) mbar_arrive(&tile_empty[ts]);
             if (tile < 0) break;
-            const Tile tc = decode_tile(p, tile, ph, ns, nblocks);
+            const Tile tc = decode_tile(p, gm, tile, ph, ns, nblocks);
             const GemmSide& sd = p.side[tc.side];
             const int acc = lt & 1;
             if (!mbar_wait(&tfull[acc], static_cast<uint32_t>(lt >> 1) & 1u, abort_flag, p.status)) break;
@@ -513,13 +539,13 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
                 publish = sd.done + tc.b;
             } else if (tc.kind == kGateUp) {
                 const bool real = p.sorted_ids[prow] < p.S;
-                const int j0 = tc.cb * kHalf;
+                const int j0 = tc.cb * gm.half;
                 __nv_bfloat16* act = static_cast<__nv_bfloat16*>(sd.out) + static_cast<size_t>(prow) * sd.n_out;
-                for (int c = 0; c < kHalf; c += 32) {
+                for (int c = 0; c < gm.half; c += 32) {
                     if (j0 + c >= sd.n_out) break;
                     float g[32], u[32];
                     tmem_ld32(tb + c, g);
-                    tmem_ld32(tb + kHalf + c, u);
+                    tmem_ld32(tb + gm.half + c, u);
                     if (real) {
 #pragma unroll
                         for (int v = 0; v < 4; ++v) {
@@ -539,9 +565,9 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
             } else {
                 const int f = p.sorted_ids[prow];
                 const bool real = f < p.S;
-                const int o0 = tc.cb * kBN;
+                const int o0 = tc.cb * gm.bn;
                 __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(sd.out) + static_cast<size_t>(real ? f : 0) * sd.n_out;
-                for (int c = 0; c < kBN; c += 32) {
+                for (int c = 0; c < gm.bn; c += 32) {
                     if (o0 + c >= sd.n_out) break;
                     float v[32];
                     tmem_ld32(tb + c, v);

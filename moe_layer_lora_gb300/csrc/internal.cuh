@@ -92,12 +92,14 @@ cudaError_t launch_combine(const void* y_slot, const int32_t* topk_ids, const fl
 
 // ------------------------------------------------------------ grouped GEMM --
 // One projection of the expert MLP: gate_up (side 0) or down (side 1).
-struct alignas(64) GemmSide {
+struct alignas(128) GemmSide {
     CUtensorMap tm_a;       // token rows [rows, K] (x in sorted order / act), box {64, kRowBox}
     CUtensorMap tm_a_full;  // the same with box {64, 128}: one box per full block
     CUtensorMap tm_b;       // weight rows: w13 view {H, I, 2, E_tot} / w2 view {I, H, E_tot}
+    CUtensorMap tm_b_n;     // the same with half-height boxes (narrow tiles)
     CUtensorMap tm_sa;      // LoRA shrink weights: A13 / A2 view {K, rank, L*E_tot}
     CUtensorMap tm_lb;      // LoRA expand weights: B13 view {rank, I, 2, L*E_tot} / B2 view {rank, H, L*E_tot}
+    CUtensorMap tm_lb_n;    // the same with half-height boxes (narrow tiles)
     CUtensorMap tm_t;       // this side's LoRA tiles [tiles*128, 64], box {64, kRowBox}
     CUtensorMap tm_t_full;  // box {64, 128}
     void* lora_t;           // LoRA tiles: written by the shrink tiles, read by the expand stages
@@ -105,10 +107,10 @@ struct alignas(64) GemmSide {
     void* out;              // act [rows, I] / y_slot [M*K', H], bf16
     int K;                  // reduction length: H / I
     int n_out;              // output columns: I / H
-    int ncb;                // column slabs per block: ceil(I/128) / ceil(H/256)
+    int ncb;                // column slabs per block, wide tiles: ceil(I/128) / ceil(H/256)
 };
 
-struct alignas(64) GemmParams {
+struct alignas(128) GemmParams {
     GemmSide side[2];
     const int32_t* n_pad;
     const int32_t* expert_ids;

@@ -210,6 +210,18 @@ mlora_status mlora_moe_read_status(const void* workspace, uint32_t* host_status,
 #define MLORA_STAGE_EVENTS 5
 mlora_status mlora_set_stage_events(void* const* events, int count);
 
+/*
+ * Test hook for the bounded waits of the experts kernel.  For the calling
+ * host thread: wait_limit_cycles (> 0) replaces the ~2 s limit (in SM clock
+ * cycles) after which a pipeline wait gives up; 0 restores it.  stall != 0
+ * makes every CTA of later forwards first wait on a workspace flag that
+ * nothing sets, so that the wait runs out: the forward then reports
+ * MLORA_DEV_TIMEOUT in the device status word (mlora_moe_read_status), its
+ * output is invalid, and the context stays usable.  No GPU fault is raised.
+ * Returns MLORA_ERR_INVALID_ARG for a negative limit.
+ */
+mlora_status mlora_set_wait_test(long long wait_limit_cycles, int stall);
+
 /* Static, human-readable name of a status code. */
 const char* mlora_status_string(mlora_status status);
 

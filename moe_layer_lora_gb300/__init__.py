@@ -23,6 +23,7 @@ from ._lib import (  # noqa: F401
     mlora_moe_route,
     mlora_moe_workspace_size,
     mlora_set_stage_events,
+    mlora_set_wait_test,
     mlora_status_string,
     STAGE_EVENTS,
     STAGE_NAMES,

@@ -63,6 +63,8 @@ def load(path: str = LIB_PATH):
     lib.mlora_moe_read_status.restype = i
     lib.mlora_set_stage_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), i]
     lib.mlora_set_stage_events.restype = i
+    lib.mlora_set_wait_test.argtypes = [ctypes.c_longlong, i]
+    lib.mlora_set_wait_test.restype = i
     lib.mlora_status_string.argtypes = [i]
     lib.mlora_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -216,6 +218,13 @@ def mlora_set_stage_events(events) -> None:
         return
     handles = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
     _check("mlora_set_stage_events", load().mlora_set_stage_events(handles, len(events)))
+
+
+def mlora_set_wait_test(wait_limit_cycles: int, stall: bool) -> None:
+    """Test hook (see include/mlora.h): a shorter limit for the experts
+    kernel's waits and, with stall, a first wait on a flag nothing sets.
+    (0, False) restores the defaults."""
+    _check("mlora_set_wait_test", load().mlora_set_wait_test(int(wait_limit_cycles), 1 if stall else 0))
 
 
 def mlora_status_string(status: int) -> str:

@@ -66,6 +66,9 @@ mlora_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MLORA_OK : M
 
 thread_local cudaEvent_t g_stage_events[MLORA_STAGE_EVENTS];
 thread_local bool g_stage_events_on = false;
+// wait-limit test hook (mlora_set_wait_test)
+thread_local long long g_wait_limit = kWaitCycles;
+thread_local bool g_stall_test = false;
 
 // Inside stream capture the events become graph event-record nodes (the
 // external flag); outside capture they are recorded normally.
@@ -336,6 +339,10 @@ mlora_status mlora_moe_forward(const void* x, const void* w13, const void* w2, c
     gp.act_done = ws.act_done;
     gp.tile_next = ws.tile_next;
     gp.status = ws.status;
+    gp.wait_limit = g_wait_limit;
+    // the never-set flag: a header word that the reset clears and nothing writes
+    gp.stall_flag = g_stall_test ? reinterpret_cast<const int32_t*>(reinterpret_cast<const char*>(ws.status) + 24)
+                                 : nullptr;
     gp.E_tot = E_tot;
     gp.cap = z.cap;
     gp.gsize = z.gsize;
@@ -393,6 +400,13 @@ mlora_status mlora_set_stage_events(void* const* events, int count) {
         g_stage_events[i] = static_cast<cudaEvent_t>(events[i]);
     }
     g_stage_events_on = true;
+    return MLORA_OK;
+}
+
+mlora_status mlora_set_wait_test(long long wait_limit_cycles, int stall) {
+    if (wait_limit_cycles < 0) return MLORA_ERR_INVALID_ARG;
+    g_wait_limit = wait_limit_cycles == 0 ? kWaitCycles : wait_limit_cycles;
+    g_stall_test = stall != 0;
     return MLORA_OK;
 }
 

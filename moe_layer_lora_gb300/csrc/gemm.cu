@@ -45,8 +45,9 @@
 // tcgen05.mma (M = 128, K = 16 per instruction, fp32 accumulate) and
 // tcgen05.commit; warps 2..5 drain the double-buffered TMEM accumulator with
 // tcgen05.ld while the next tile's MMAs run.  Grid: at most one CTA per SM.
-// Every wait is bounded (~2 s, ptx.cuh): a timeout records
-// MLORA_DEV_TIMEOUT, drains the copies in flight, frees TMEM and returns.
+// Every wait is bounded (~2 s unless a test sets a shorter limit): a
+// timeout records MLORA_DEV_TIMEOUT, drains the copies in flight, frees
+// TMEM and returns.
 #include "internal.cuh"
 #include "ptx.cuh"
 
@@ -67,14 +68,15 @@ enum TileKind : int { kShrinkUp = 0, kGateUp = 1, kShrinkDown = 2, kDown = 3 };
 
 // Bounded wait used only while unwinding after an abort: ignores the abort
 // flag so that copies already in flight land before the CTA exits.
-__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, long long limit) {
     int zero = 0;
-    mbar_wait(bar, parity, &zero, nullptr, kWaitCycles / 8);
+    mbar_wait(bar, parity, &zero, nullptr, limit / 8 + 1000);
 }
 
 // Bounded wait until *flag >= target (acquire), then order this thread's
 // later TMA (async-proxy) reads after it.
-__device__ bool wait_counter(const int32_t* flag, int target, volatile int* abort_flag, uint32_t* status) {
+__device__ bool wait_counter(const int32_t* flag, int target, volatile int* abort_flag, uint32_t* status,
+                             long long limit) {
     const long long t0 = clock64();
     for (uint32_t it = 0;; ++it) {
         int v;
@@ -85,7 +87,7 @@ __device__ bool wait_counter(const int32_t* flag, int target, volatile int* abor
         }
         if ((it & 63u) == 63u) {
             if (*abort_flag) return false;
-            if (clock64() - t0 > kWaitCycles) {
+            if (clock64() - t0 > limit) {
                 *abort_flag = 1;
                 atomicOr(status, MLORA_DEV_TIMEOUT);
                 return false;
@@ -196,6 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long long lim = p.wait_limit;  // cycles a wait may take before the CTA gives up
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
@@ -262,13 +265,16 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
             long it = 0;
             bool ok = true;
             long tile = blockIdx.x, next = 0;
+            // test hook: a wait on a flag that nothing sets, which must end
+            // in a reported timeout and a clean exit
+            if (p.stall_flag && !wait_counter(p.stall_flag, 1, abort_flag, p.status, lim)) ok = false;
             for (int jt = 0; ok; ++jt, tile = next) {
                 // hand the tile (or the end mark) to the MMA lane and the
                 // epilogue, then claim the next one; its index is needed
                 // only once this tile's loads are issued
                 const int ts = jt % kTileRing;
                 if (!mbar_wait(&tile_empty[ts], (static_cast<uint32_t>(jt / kTileRing) & 1u) ^ 1u, abort_flag,
-                               p.status)) {
+                               p.status, lim)) {
                     ok = false;
                     break;
                 }
@@ -281,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
                 const int row0 = tc.b * kBlockM;
                 // the down side reads act rows, complete once the block's
                 // gate_up tiles all are
-                if (tc.side == 1 && !wait_counter(p.act_done + tc.b, gm.ncb0, abort_flag, p.status)) {
+                if (tc.side == 1 && !wait_counter(p.act_done + tc.b, gm.ncb0, abort_flag, p.status, lim)) {
                     ok = false;
                     break;
                 }
@@ -304,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
                     for (int kb0 = 0; kb0 < nk; kb0 += cps, ++it) {
                         const int s = static_cast<int>(it % kStages);
                         const uint32_t phs = static_cast<uint32_t>(it / kStages) & 1u;
-                        if (!mbar_wait(&empty[s], phs ^ 1u, abort_flag, p.status)) {
+                        if (!mbar_wait(&empty[s], phs ^ 1u, abort_flag, p.status, lim)) {
                             ok = false;
                             break;
                         }
@@ -330,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
                 for (int kb = 0; kb < nk; ++kb, ++it) {
                     const int s = static_cast<int>(it % kStages);
                     const uint32_t phs = static_cast<uint32_t>(it / kStages) & 1u;
-                    if (!mbar_wait(&empty[s], phs ^ 1u, abort_flag, p.status)) {
+                    if (!mbar_wait(&empty[s], phs ^ 1u, abort_flag, p.status, lim)) {
                         ok = false;
                         break;
                     }
@@ -355,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
                 const int nad = p.blk_nad[tc.b];
                 if (nad == 0) continue;
                 // the expand needs every shrink tile of this block and side
-                if (!wait_counter(sd.done + tc.b, (nad + p.gsize - 1) / p.gsize, abort_flag, p.status)) {
+                if (!wait_counter(sd.done + tc.b, (nad + p.gsize - 1) / p.gsize, abort_flag, p.status, lim)) {
                     ok = false;
                     break;
                 }
@@ -363,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
                 for (int i = 0; i < nad; ++i, ++it) {
                     const int s = static_cast<int>(it % kStages);
                     const uint32_t phs = static_cast<uint32_t>(it / kStages) & 1u;
-                    if (!mbar_wait(&empty[s], phs ^ 1u, abort_flag, p.status)) {
+                    if (!mbar_wait(&empty[s], phs ^ 1u, abort_flag, p.status, lim)) {
                         ok = false;
                         break;
                     }
@@ -387,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
             }
             if (!ok) {
                 for (long j = it > kStages ? it - kStages : 0; j < it; ++j)
-                    drain_wait(&full[j % kStages], static_cast<uint32_t>(j / kStages) & 1u);
+                    drain_wait(&full[j % kStages], static_cast<uint32_t>(j / kStages) & 1u, lim);
             }
         }
     } else if (warp == 1) {
@@ -398,14 +404,14 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
             bool ok = true;
             for (int lt = 0; ok; ++lt) {
                 const int ts = lt % kTileRing;
-                if (!mbar_wait(&tile_full[ts], static_cast<uint32_t>(lt / kTileRing) & 1u, abort_flag, p.status)) break;
+                if (!mbar_wait(&tile_full[ts], static_cast<uint32_t>(lt / kTileRing) & 1u, abort_flag, p.status, lim)) break;
                 const long tile = tile_ring[ts];
                 mbar_arrive(&tile_empty[ts]);
                 if (tile < 0) break;
                 const Tile tc = decode_tile(p, gm, tile, ph, ns, nblocks);
                 const int nk = (p.side[tc.side].K + kBlockK - 1) / kBlockK;
                 const int acc = lt & 1;
-                if (!mbar_wait(&tempty[acc], (static_cast<uint32_t>(lt >> 1) & 1u) ^ 1u, abort_flag, p.status)) {
+                if (!mbar_wait(&tempty[acc], (static_cast<uint32_t>(lt >> 1) & 1u) ^ 1u, abort_flag, p.status, lim)) {
                     ok = false;
                     break;
                 }
@@ -427,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
                     const int cps = shrink_chunks(a_bytes, chunk - a_bytes);
                     for (int kb0 = 0; kb0 < nk; kb0 += cps, ++it) {
                         const int s = static_cast<int>(it % kStages);
-                        if (!mbar_wait(&full[s], static_cast<uint32_t>(it / kStages) & 1u, abort_flag, p.status)) {
+                        if (!mbar_wait(&full[s], static_cast<uint32_t>(it / kStages) & 1u, abort_flag, p.status, lim)) {
                             ok = false;
                             break;
                         }
@@ -449,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
                 }
                 for (int kb = 0; kb < nk; ++kb, ++it) {
                     const int s = static_cast<int>(it % kStages);
-                    if (!mbar_wait(&full[s], static_cast<uint32_t>(it / kStages) & 1u, abort_flag, p.status)) {
+                    if (!mbar_wait(&full[s], static_cast<uint32_t>(it / kStages) & 1u, abort_flag, p.status, lim)) {
                         ok = false;
                         break;
                     }
@@ -467,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
                     const int nad = p.blk_nad[tc.b];
                     for (int i = 0; i < nad; ++i, ++it) {
                         const int s = static_cast<int>(it % kStages);
-                        if (!mbar_wait(&full[s], static_cast<uint32_t>(it / kStages) & 1u, abort_flag, p.status)) {
+                        if (!mbar_wait(&full[s], static_cast<uint32_t>(it / kStages) & 1u, abort_flag, p.status, lim)) {
                             ok = false;
                             break;
                         }
@@ -484,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
             }
             // every MMA issued above completes before TMEM is released
             umma_commit(drain);
-            drain_wait(drain, 0);
+            drain_wait(drain, 0, lim);
         }
     } else {
         // --------------------------------------------------------- epilogue
@@ -493,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
         uint32_t npub = 0;
         for (int lt = 0;; ++lt) {
             const int ts = lt % kTileRing;
-            if (!mbar_wait(&tile_full[ts], static_cast<uint32_t>(lt / kTileRing) & 1u, abort_flag, p.status)) break;
+            if (!mbar_wait(&tile_full[ts], static_cast<uint32_t>(lt / kTileRing) & 1u, abort_flag, p.status, lim)) break;
             const long tile = tile_ring[ts];
             __syncwarp();
             if (lane == 0) mbar_arrive(&tile_empty[ts]);
@@ -501,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
             const Tile tc = decode_tile(p, gm, tile, ph, ns, nblocks);
             const GemmSide& sd = p.side[tc.side];
             const int acc = lt & 1;
-            if (!mbar_wait(&tfull[acc], static_cast<uint32_t>(lt >> 1) & 1u, abort_flag, p.status)) break;
+            if (!mbar_wait(&tfull[acc], static_cast<uint32_t>(lt >> 1) & 1u, abort_flag, p.status, lim)) break;
             tc_fence_after();
             const uint32_t tb = tmem_base + static_cast<uint32_t>(acc * kAccCols) +
                                 (static_cast<uint32_t>(q * 32) << 16);
@@ -598,7 +604,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
                 asm volatile("fence.proxy.async.global;" ::: "memory");
                 mbar_arrive(pub);
                 if (warp == 2 && lane == 0) {
-                    if (mbar_wait(pub, npub & 1u, abort_flag, p.status)) {
+                    if (mbar_wait(pub, npub & 1u, abort_flag, p.status, lim)) {
                         __threadfence();
                         atomicAdd(publish, 1);
                     }

@@ -15,6 +15,7 @@ constexpr int kBlockM = MLORA_FORWARD_BLOCK_M;  // token rows per GEMM tile (MMA
 constexpr int kBlockK = 64;                     // bf16 elements per 128-byte swizzle row
 constexpr int kLoraTileCols = 64;               // shrink result row, padded to one swizzle row
 constexpr int kRowBox = 32;                     // token rows per TMA box of an A operand
+constexpr long long kWaitCycles = 4000000000LL;  // default spin limit of a device wait (~2 s at 2 GHz)
 
 // Per-forward buffers carved out of the caller's workspace.
 struct Workspace {
@@ -126,6 +127,8 @@ struct alignas(128) GemmParams {
     int32_t* act_done;  // per block: finished gate_up tiles (zero at launch)
     int32_t* tile_next; // tiles claimed past the first round (zero at launch)
     uint32_t* status;
+    long long wait_limit;        // clock cycles a wait may take before the CTA gives up
+    const int32_t* stall_flag;   // test hook: non-null = wait on this never-set flag first
     int E_tot;
     int cap;
     int gsize;

@@ -48,8 +48,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Spin limit in SM clock cycles (~2 s at 2 GHz).
-constexpr long long kWaitCycles = 4000000000LL;
 
 // Bounded wait.  Returns false on timeout or when another role of the CTA
 // has already aborted; the caller then unwinds.

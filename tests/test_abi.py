@@ -19,7 +19,8 @@ def lib():
 def test_exports_every_declared_symbol(lib):
     names = _lib.declared_functions()
     for core in ("mlora_moe_route", "mlora_moe_align", "mlora_moe_align_max_padded", "mlora_moe_workspace_size",
-                 "mlora_moe_forward", "mlora_moe_read_status", "mlora_set_stage_events", "mlora_status_string"):
+                 "mlora_moe_forward", "mlora_moe_read_status", "mlora_set_stage_events", "mlora_status_string",
+                 "mlora_set_wait_test"):
         assert core in names, core
     raw = ctypes.CDLL(_lib.LIB_PATH)
     for n in names:
@@ -30,6 +31,11 @@ def test_stage_event_hook_validation(lib):
     assert lib.mlora_set_stage_events(None, 0) == 0
     arr = (ctypes.c_void_p * 3)(None, None, None)
     assert lib.mlora_set_stage_events(arr, 3) == 1
+
+
+def test_wait_test_hook_validation(lib):
+    assert lib.mlora_set_wait_test(-1, 0) == 1
+    assert lib.mlora_set_wait_test(0, 0) == 0
 
 
 def test_status_strings(lib):

@@ -116,6 +116,30 @@ def test_empty_batch():
     assert y.shape == (0, s.H)
 
 
+def test_wait_timeout_is_reported_and_the_context_recovers():
+    """Every CTA first waits on a workspace flag that nothing sets, with a
+    ~1 ms limit: the kernel must give up, report MLORA_DEV_TIMEOUT in the
+    status word and exit cleanly; the next forward on the same workspace is
+    clean and matches the oracle."""
+    s = wl.spec("tiny")
+    inp = wl.make(s, device="cuda")
+    d = gu.DeviceInputs(inp)
+    ids, w = gu.gpu_route(d)
+    ws = torch.empty(ml.mlora_moe_workspace_size(s.M, s.H, s.I, s.E_tot, s.K_total, s.L, s.r), dtype=torch.uint8,
+                     device="cuda")
+    ml.mlora_set_wait_test(2_000_000, True)
+    try:
+        gu.gpu_forward(d, ids, w, workspace=ws)
+        st = ml.mlora_moe_read_status(ws)
+    finally:
+        ml.mlora_set_wait_test(0, False)
+    assert st & ml.DEV_TIMEOUT, st
+    y = gu.gpu_forward(d, ids, w, workspace=ws)
+    assert ml.mlora_moe_read_status(ws) == 0
+    ids_ref, w_ref = gu.oracle_route(inp)
+    gu.check_y(y, gu.oracle_forward(inp, ids_ref, w_ref), "after a timed-out forward")
+
+
 def test_bad_device_values_are_flagged():
     """Out-of-range adapter ids act as 'no adapter', out-of-range expert ids
     drop their slot; both set a bit of the device status word."""

@@ -203,3 +203,63 @@ def test_graph_capture_replay():
         inp.logits, inp.x, inp.token_lora_idx = new.logits, new.x, new.token_lora_idx
         ids_ref, w_ref = gu.oracle_route(inp)
         gu.check_y(y_graph, gu.oracle_forward(inp, ids_ref, w_ref), f"graph replay seed {seed}")
+
+
+def _graph_step(d: gu.DeviceInputs, ids, w, y, ws, stream):
+    s = d.spec
+    lora = s.has_lora
+    ml.mlora_moe_route(d.logits, d.bias, s.top_k, s.scoring, s.renormalize, s.n_shared, s.routed_scaling_factor,
+                       topk_ids=ids, topk_w=w, stream=stream)
+    ml.mlora_moe_forward(d.x, d.w13, d.w2, d.A13 if lora else None, d.B13 if lora else None,
+                         d.A2 if lora else None, d.B2 if lora else None, d.idx if lora else None, ids, w,
+                         s.scaling, s.n_shared, s.out_scale, y=y, workspace=ws, stream=stream)
+
+
+@pytest.mark.parametrize("name", ["decode", "prefill", "shared"])
+def test_benchmark_launch_configuration(name):
+    """The step as the benchmark times it: route + forward captured in a CUDA
+    graph on a side stream, replayed after an L2 flush, plain and with the
+    stage events recorded inside the graph.  Both replays equal an eager call
+    bit for bit; the output matches the oracle on sampled tokens."""
+    s = wl.spec(name)
+    inp = wl.make(s, device="cuda")
+    d = gu.DeviceInputs(inp)
+    L, r = (s.L, s.r) if s.has_lora else (0, 0)
+    ids = torch.empty((s.M, s.K_total), dtype=torch.int32, device="cuda")
+    w = torch.empty((s.M, s.K_total), dtype=torch.float32, device="cuda")
+    y = torch.empty((s.M, s.H), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(ml.mlora_moe_workspace_size(s.M, s.H, s.I, s.E_tot, s.K_total, L, r), dtype=torch.uint8,
+                     device="cuda")
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        _graph_step(d, ids, w, y, ws, stream)
+    stream.synchronize()
+    y_eager = y.clone()
+    graphs = []
+    events = [torch.cuda.Event(enable_timing=True) for _ in range(ml.STAGE_EVENTS)]
+    for e in events:  # torch creates the CUDA event on first record
+        e.record(stream)
+    for instrumented in (False, True):
+        g = torch.cuda.CUDAGraph()
+        if instrumented:
+            ml.mlora_set_stage_events(events)
+        try:
+            with torch.cuda.graph(g, stream=stream):
+                _graph_step(d, ids, w, y, ws, stream)
+        finally:
+            ml.mlora_set_stage_events(None)
+        graphs.append(g)
+    for g in graphs:
+        for _ in range(2):
+            y.zero_()
+            flush.fill_(1)
+            g.replay()
+            torch.cuda.synchronize()
+            assert torch.equal(y, y_eager)
+            assert ml.mlora_moe_read_status(ws) == 0
+    rows = None if s.M <= 128 else np.linspace(0, s.M - 1, 24).round().astype(np.int64)
+    ids_ref, w_ref = gu.oracle_route(inp)
+    y_ref = gu.oracle_forward(inp, ids_ref, w_ref, rows=rows)
+    yg = y if rows is None else y[torch.as_tensor(rows, device="cuda")]
+    gu.check_y(yg, y_ref, f"{name} graph replay")

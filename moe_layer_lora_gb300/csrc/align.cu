@@ -105,6 +105,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     griddep_wait();
     griddep_launch_dependents();
+    // the forward's status word, counts and per-block counters start at
+    // zero (this kernel is the forward's first)
+    for (int i = tid; i < ex.zero_words; i += kThreads) ex.zero[i] = 0u;
+    __syncthreads();
     const unsigned lt_mask = (1u << lane) - 1u;
     // runs: slots per thread, a multiple of 4 so that a run starts on a
     // 16-byte boundary when ids does

@@ -352,10 +352,13 @@ mlora_status mlora_moe_forward(const void* x, const void* w13, const void* w2, c
     gp.scaling = scaling;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t err = cudaMemsetAsync(workspace, 0, ws.zeroed_bytes, s);
-    if (err != cudaSuccess) return cuda_fail(err, "workspace reset");
+    cudaError_t err;
     if ((err = mark_stage(0, s)) != cudaSuccess) return cuda_fail(err, "stage event");
     AlignExtra ex{};
+    // the align kernel clears the header and the counters itself (no
+    // memset node between the caller's route and align)
+    ex.zero = ws.status;
+    ex.zero_words = static_cast<int>(ws.zeroed_bytes / 4);
     ex.blk_rows = ws.blk_rows;
     if (lora) {
         ex.token_lora_idx = token_lora_idx;

@@ -63,6 +63,8 @@ long align_max_padded(long S, int E_tot, int block_m);
 // Extra outputs of align used only inside the forward.  blk_rows is always
 // written when set; the adapter fields only when token_lora_idx is set.
 struct AlignExtra {
+    uint32_t* zero;  // words cleared first thing (the forward's header and counters)
+    int zero_words;
     int32_t* blk_rows;
     const int32_t* token_lora_idx;
     int L;

@@ -16,9 +16,10 @@
 //  * runs (more slots, up to 96 experts): each thread owns one contiguous
 //    run of slots and counts it into its own column of a [E_tot][1024]
 //    table; a scan along each expert's row gives every thread its first
-//    position per expert, and the thread places its run in order.  When the
-//    padded list fits, it is built in shared memory and copied out in one
-//    coalesced sweep instead of scattered 4-byte stores.
+//    position per expert, and the thread places its run in order.
+// Either way, when the padded list fits in shared memory (16-bit slot ids
+// and adapters) it is built there and copied out in one coalesced sweep
+// instead of scattered 4-byte stores.
 //
 // Inside the forward the same pass also records the real (non-padding) row
 // count of every block and, with adapters, per sorted position the token's
@@ -35,13 +36,6 @@ constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
 constexpr int kRunsMaxExperts = 96;      // per-thread count columns: 96 x 1024 x 2 B
 constexpr int kMaxSmem = 227 * 1024;
-
-// kinds of the slot pass
-enum : int {
-    kPasses = 0,     // passes of 1024 slots with warp-level ranks
-    kRuns = 1,       // one contiguous run of slots per thread, direct stores
-    kRunsStaged = 2, // runs, sorted ids and adapters staged in shared memory
-};
 
 // Exclusive block scan of one int per thread; returns the exclusive prefix
 // and writes the block total to *total.  Uses 33 ints of scratch.
@@ -89,22 +83,28 @@ template <bool kWithLora>
 __global__ void __launch_bounds__(kThreads, 1)
     align_kernel(const int32_t* __restrict__ ids, int S, int E_tot, int BM, int max_padded,
                  int32_t* __restrict__ sorted, int32_t* __restrict__ expert_ids, int32_t* __restrict__ n_pad_out,
-                 uint32_t* __restrict__ status, int runs, AlignExtra ex) {
+                 uint32_t* __restrict__ status, int runs, int staged, AlignExtra ex) {
     extern __shared__ int smem_i[];
     int* cnt = smem_i;                                            // [E_tot] slots per expert
     int* first = cnt + E_tot;                                     // [E_tot] padded start of each expert
     int* cursor = first + E_tot;                                  // [E_tot] next free position
     int* scratch = cursor + E_tot;                                // [40]
+    int* nad_s = scratch + 40;  // with adapters: [max_padded / BM] adapters per block
     // passes: [kWarps][E_tot] per-warp counts; runs: [E_tot][kThreads] per-thread counts
     // (16-byte aligned: the runs' row scan reads it as uint4)
-    uint16_t* wcnt = reinterpret_cast<uint16_t*>((reinterpret_cast<uintptr_t>(scratch + 40) + 15) & ~uintptr_t(15));
-    // staged runs: [max_padded] sorted slot ids, then [max_padded] adapters
-    const bool staged = runs == kRunsStaged;
-    uint16_t* st_sorted = wcnt + static_cast<size_t>(E_tot) * kThreads;
+    uint16_t* wcnt =
+        reinterpret_cast<uint16_t*>((reinterpret_cast<uintptr_t>(nad_s + (kWithLora ? max_padded / BM : 0)) + 15) &
+                                    ~uintptr_t(15));
+    // staged: [max_padded] sorted slot ids, then [max_padded] adapters
+    uint16_t* st_sorted = wcnt + static_cast<size_t>(E_tot) * (runs ? kThreads : kWarps);
     int16_t* st_lora = reinterpret_cast<int16_t*>(st_sorted + max_padded);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     griddep_wait();
     griddep_launch_dependents();
+    // passes: the first pass's expert and adapter ids, loaded now so that
+    // their latency hides behind the clearing below
+    int e_next = (!runs && tid < S) ? __ldg(ids + tid) : -1;
+    int l_next = (kWithLora && !runs && tid < S) ? __ldg(ex.token_lora_idx + tid / ex.K_total) : -1;
     // the forward's status word, counts and per-block counters start at
     // zero (this kernel is the forward's first)
     for (int i = tid; i < ex.zero_words; i += kThreads) ex.zero[i] = 0u;
@@ -178,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         for (int f = tid; f < S; f += kThreads) {
-            const int e = ids[f];
+            const int e = f == tid ? e_next : ids[f];
             if (static_cast<unsigned>(e) < static_cast<unsigned>(E_tot))
                 atomicAdd(&cnt[e], 1);
             else if (status)
@@ -250,13 +250,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncthreads();
-        // staged: one coalesced copy of the sorted ids (and adapters) out
-        if (staged) {
-            for (int p = tid; p < total; p += kThreads) {
-                sorted[p] = st_sorted[p];
-                if (kWithLora) ex.lora_of[p] = st_lora[p];
-            }
-        }
     }
 
     // 4b. passes: stable scatter, 1024 slots per pass.  Within a pass a slot's rank
@@ -265,8 +258,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     //    term comes from a per-expert scan over the warps' counts, done one
     //    expert column per warp.
     // the next pass's expert and adapter ids are loaded during this one
-    int e_next = (!runs && tid < S) ? ids[tid] : -1;
-    int l_next = (kWithLora && !runs && tid < S) ? ex.token_lora_idx[tid / ex.K_total] : -1;
     for (int base = 0; !runs && base < S; base += kThreads) {
         const int f = base + tid;
         const int e = e_next;
@@ -298,14 +289,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         pos = __shfl_sync(0xffffffffu, pos, __ffs(peers) - 1);
         if (valid) {
             const int p = pos + rank;
-            sorted[p] = f;
-            if (kWithLora) {
-                int l = l_in;
-                if (l < -1 || l >= ex.L) {
-                    if (status) atomicOr(status, MLORA_DEV_BAD_LORA_IDX);
-                    l = -1;
-                }
-                ex.lora_of[p] = l;
+            int l = l_in;
+            if (kWithLora && (l < -1 || l >= ex.L)) {
+                if (status) atomicOr(status, MLORA_DEV_BAD_LORA_IDX);
+                l = -1;
+            }
+            if (staged) {
+                st_sorted[p] = static_cast<uint16_t>(f);
+                st_lora[p] = static_cast<int16_t>(l);
+            } else {
+                sorted[p] = f;
+                if (kWithLora) ex.lora_of[p] = l;
             }
         }
         __syncthreads();
@@ -314,6 +308,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             wcnt[warp * E_tot + e] = 0;
         }
         __syncthreads();
+    }
+
+    // staged: one coalesced copy of the sorted ids (and adapters) out
+    if (staged) {
+        for (int p = tid; p < total; p += kThreads) {
+            sorted[p] = st_sorted[p];
+            if (kWithLora) ex.lora_of[p] = st_lora[p];
+        }
     }
 
     if (!kWithLora) return;
@@ -342,7 +344,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++count;
             prev = cand;
         }
-        if (lane == 0) ex.blk_nad[b] = count;
+        if (lane == 0) {
+            ex.blk_nad[b] = count;
+            nad_s[b] = count;
+        }
     }
     __syncthreads();
 
@@ -351,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int run_lt = 0, run_gt = 0;
     for (int cb = 0; cb < nblocks; cb += kThreads) {
         const int b = cb + tid;
-        const int v = b < nblocks ? ex.blk_nad[b] : 0;
+        const int v = b < nblocks ? nad_s[b] : 0;
         const int ng = (v + ex.gsize - 1) / ex.gsize;
         int lt_chunk, gt_chunk;
         const int lt_excl = block_exclusive_scan(v, scratch, &lt_chunk);
@@ -384,13 +389,17 @@ cudaError_t launch_align(const int32_t* ids, long S, int E_tot, int block_m, lon
     // experts) per-thread runs with one count column per thread
     // experts) per-thread runs with one count column per thread, staged in
     // shared memory when the padded list fits there too
-    int runs = S > kThreads && E_tot <= kRunsMaxExperts && S <= 65535 ? kRuns : kPasses;
-    size_t smem = sizeof(int) * (3 * static_cast<size_t>(E_tot) + 40) + 16 /* alignment of the count table */ +
+    const int runs = S > kThreads && E_tot <= kRunsMaxExperts && S <= 65535 ? 1 : 0;
+    const bool with_lora = extra && extra->token_lora_idx;
+    size_t smem = sizeof(int) * (3 * static_cast<size_t>(E_tot) + 40 +
+                                 (with_lora ? static_cast<size_t>(max_padded / block_m) : 0)) +
+                  16 /* alignment of the count table */ +
                   sizeof(uint16_t) * static_cast<size_t>(runs ? kThreads : kWarps) * E_tot;
     const size_t stage_bytes = (sizeof(uint16_t) + sizeof(int16_t)) * static_cast<size_t>(max_padded);
-    const bool small_l = !extra || extra->L <= 32767;
-    if (runs == kRuns && small_l && smem + stage_bytes <= static_cast<size_t>(kMaxSmem)) {
-        runs = kRunsStaged;
+    const bool small_ids = S <= 65535 && (!extra || extra->L <= 32767);
+    int staged = 0;
+    if (small_ids && smem + stage_bytes <= static_cast<size_t>(kMaxSmem)) {
+        staged = 1;
         smem += stage_bytes;
     }
     static unsigned long long attr_set[2] = {0ull, 0ull};  // one bit per device
@@ -398,7 +407,6 @@ cudaError_t launch_align(const int32_t* ids, long S, int E_tot, int block_m, lon
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
-    const bool with_lora = extra && extra->token_lora_idx;
     AlignExtra ex{};
     if (extra) ex = *extra;
     if (with_lora) {
@@ -409,7 +417,7 @@ cudaError_t launch_align(const int32_t* ids, long S, int E_tot, int block_m, lon
         }
         err = launch_pdl(align_kernel<true>, dim3(1), dim3(kThreads), smem, s, ids, static_cast<int>(S), E_tot, block_m,
                                                      static_cast<int>(max_padded), sorted, expert_ids, n_pad, status,
-                                                     runs, ex);
+                                                     runs, staged, ex);
         if (err != cudaSuccess) return err;
     } else {
         if (!(attr_set[0] & bit)) {
@@ -419,7 +427,7 @@ cudaError_t launch_align(const int32_t* ids, long S, int E_tot, int block_m, lon
         }
         err = launch_pdl(align_kernel<false>, dim3(1), dim3(kThreads), smem, s, ids, static_cast<int>(S), E_tot, block_m,
                                                       static_cast<int>(max_padded), sorted, expert_ids, n_pad, status,
-                                                      runs, ex);
+                                                      runs, staged, ex);
         if (err != cudaSuccess) return err;
     }
     return cudaGetLastError();

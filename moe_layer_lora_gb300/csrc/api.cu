@@ -4,7 +4,7 @@
 //
 // Forward, all on the caller's stream, no host synchronisation, no
 // allocation (capturable in a CUDA graph):
-//   memset(status, counters) -> align (+ per-block adapter lists)
+//   align (clears the status word and counters first; + per-block adapter lists)
 //   -> gather x rows -> experts kernel (gate_up shrink, gate_up + expand +
 //   SwiGLU, down shrink, down + expand, one persistent grid) -> combine
 // Without adapters the experts kernel runs only base tiles; when adapters

@@ -26,6 +26,8 @@
 // adapter and per block of kBlockM positions the ascending list of distinct
 // adapters; each (block, adapter) pair gets a masked LoRA tile, and the
 // adapters of a block are cut into shrink group tiles of up to gsize.
+#include <atomic>
+
 #include "internal.cuh"
 #include "ptx.cuh"
 
@@ -402,7 +404,7 @@ cudaError_t launch_align(const int32_t* ids, long S, int E_tot, int block_m, lon
         staged = 1;
         smem += stage_bytes;
     }
-    static unsigned long long attr_set[2] = {0ull, 0ull};  // one bit per device
+    static std::atomic<unsigned long long> attr_set[2];  // one bit per device (shared by host threads)
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
@@ -410,20 +412,20 @@ cudaError_t launch_align(const int32_t* ids, long S, int E_tot, int block_m, lon
     AlignExtra ex{};
     if (extra) ex = *extra;
     if (with_lora) {
-        if (!(attr_set[1] & bit)) {
+        if (!(attr_set[1].load(std::memory_order_relaxed) & bit) || !bit) {
             err = cudaFuncSetAttribute(align_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
             if (err != cudaSuccess) return err;
-            attr_set[1] |= bit;
+            attr_set[1].fetch_or(bit, std::memory_order_relaxed);
         }
         err = launch_pdl(align_kernel<true>, dim3(1), dim3(kThreads), smem, s, ids, static_cast<int>(S), E_tot, block_m,
                                                      static_cast<int>(max_padded), sorted, expert_ids, n_pad, status,
                                                      runs, staged, ex);
         if (err != cudaSuccess) return err;
     } else {
-        if (!(attr_set[0] & bit)) {
+        if (!(attr_set[0].load(std::memory_order_relaxed) & bit) || !bit) {
             err = cudaFuncSetAttribute(align_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
             if (err != cudaSuccess) return err;
-            attr_set[0] |= bit;
+            attr_set[0].fetch_or(bit, std::memory_order_relaxed);
         }
         err = launch_pdl(align_kernel<false>, dim3(1), dim3(kThreads), smem, s, ids, static_cast<int>(S), E_tot, block_m,
                                                       static_cast<int>(max_padded), sorted, expert_ids, n_pad, status,

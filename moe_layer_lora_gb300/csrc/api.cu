@@ -17,6 +17,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -96,13 +97,17 @@ mlora_status cuda_fail(cudaError_t e, const char* where) {
 }  // namespace
 
 int device_sm_count() {
-    static int counts[64] = {0};
+    // per-device cache, shared by host threads (idempotent relaxed writes)
+    static std::atomic<int> counts[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 1;
-    if (dev >= 0 && dev < 64 && counts[dev] > 0) return counts[dev];
+    if (dev >= 0 && dev < 64) {
+        const int c = counts[dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
+    }
     int n = 1;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
-    if (dev >= 0 && dev < 64) counts[dev] = n;
+    if (dev >= 0 && dev < 64) counts[dev].store(n, std::memory_order_relaxed);
     return n;
 }
 

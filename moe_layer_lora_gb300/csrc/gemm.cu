@@ -48,6 +48,8 @@
 // Every wait is bounded (~2 s unless a test sets a shorter limit): a
 // timeout records MLORA_DEV_TIMEOUT, drains the copies in flight, frees
 // TMEM and returns.
+#include <atomic>
+
 #include "internal.cuh"
 #include "ptx.cuh"
 
@@ -625,14 +627,15 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
 
 cudaError_t launch_experts(const GemmParams& p, long max_tiles, cudaStream_t s) {
     if (max_tiles <= 0) return cudaSuccess;
-    static unsigned long long attr_done = 0;  // one bit per device
+    static std::atomic<unsigned long long> attr_done{0};  // one bit per device (shared by host threads)
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
-    if (dev < 64 && !((attr_done >> dev) & 1ull)) {
+    const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
+    if (!(attr_done.load(std::memory_order_relaxed) & bit) || !bit) {
         err = cudaFuncSetAttribute(experts_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (err != cudaSuccess) return err;
-        attr_done |= 1ull << dev;
+        attr_done.fetch_or(bit, std::memory_order_relaxed);
     }
     long grid = device_sm_count();
     if (grid > max_tiles) grid = max_tiles;

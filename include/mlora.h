@@ -61,6 +61,7 @@ enum { MLORA_SCORE_SOFTMAX = 0, MLORA_SCORE_SIGMOID_BIAS = 1 };
 #define MLORA_DEV_TIMEOUT 1u        /* a pipeline wait gave up after ~2 s; outputs invalid */
 #define MLORA_DEV_BAD_EXPERT_ID 2u  /* a topk id was outside [0, E_tot); that slot was dropped */
 #define MLORA_DEV_BAD_LORA_IDX 4u   /* a token_lora_idx was outside [-1, L); treated as -1 */
+#define MLORA_DEV_BOUNDS 8u         /* bounds-checked debug build only: an index left its buffer; the access was skipped */
 
 #define MLORA_MAX_EXPERTS 1024 /* E (routing) and E_tot (align, forward) */
 #define MLORA_MAX_TOPK 64      /* K' = top_k + n_shared */

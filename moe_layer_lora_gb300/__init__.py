@@ -8,6 +8,7 @@ step and the seeded synthetic workload generator.
 from ._lib import (  # noqa: F401
     DEV_BAD_EXPERT_ID,
     DEV_BAD_LORA_IDX,
+    DEV_BOUNDS,
     DEV_TIMEOUT,
     FORWARD_BLOCK_M,
     SCORE_SIGMOID_BIAS,

@@ -17,6 +17,7 @@ import torch
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libmlora.so")
+LIB_CHECKED_PATH = os.path.join(HERE, "libmlora_checked.so")  # bounds-checked debug build
 HEADER = os.path.join(os.path.dirname(HERE), "include", "mlora.h")
 
 MLORA_OK = 0
@@ -27,6 +28,7 @@ SCORE_SIGMOID_BIAS = 1
 DEV_TIMEOUT = 1
 DEV_BAD_EXPERT_ID = 2
 DEV_BAD_LORA_IDX = 4
+DEV_BOUNDS = 8  # bounds-checked debug build only
 FORWARD_BLOCK_M = 128
 
 
@@ -37,6 +39,14 @@ class MloraError(RuntimeError):
 
 
 _lib = None
+
+
+def use_library(path: str = LIB_PATH):
+    """Switch the binding to another build of the library, e.g. the
+    bounds-checked debug build LIB_CHECKED_PATH; LIB_PATH is the default."""
+    global _lib
+    _lib = None
+    return load(path)
 
 
 def load(path: str = LIB_PATH):

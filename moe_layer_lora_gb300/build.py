@@ -1,7 +1,11 @@
 """Build libmlora.so in-tree: every .cu under csrc/ compiled for sm_103a in
 parallel, then linked into one shared library with the CUDA runtime linked
 statically (the library then loads on machines without a GPU driver, where
-only its host-side argument checks can run)."""
+only its host-side argument checks can run).
+
+build(checked=True) makes libmlora_checked.so, the bounds-checked debug
+build (-DMLORA_CHECK_BOUNDS): a computed index outside its buffer sets
+MLORA_DEV_BOUNDS in the device status word and the store is skipped."""
 from __future__ import annotations
 
 import concurrent.futures as cf
@@ -17,6 +21,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmlora.so")
+BUILD_CHECKED = os.path.join(HERE, "_build_checked")
+LIB_CHECKED = os.path.join(HERE, "libmlora_checked.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC,
@@ -37,14 +43,17 @@ def _stale(out: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(verbose: bool = False, extra_flags=()) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, extra_flags=(), checked: bool = False) -> str:
+    build_dir, lib = (BUILD_CHECKED, LIB_CHECKED) if checked else (BUILD, LIB)
+    if checked:
+        extra_flags = (*extra_flags, "-DMLORA_CHECK_BOUNDS")
+    os.makedirs(build_dir, exist_ok=True)
     sources = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     headers = glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h"))
     objs = []
     jobs = []
     for src in sources:
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src) + ".o")
         objs.append(obj)
         if _stale(obj, [src, *headers]):
             jobs.append([nvcc(), *ARCH, *NVCC_FLAGS, *extra_flags, "-c", src, "-o", obj])
@@ -60,9 +69,9 @@ def build(verbose: bool = False, extra_flags=()) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=max(1, min(len(jobs), os.cpu_count() or 4))) as ex:
         list(ex.map(run, jobs))
-    if jobs or _stale(LIB, objs):
-        run([nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", LIB, *objs])
-    return LIB
+    if jobs or _stale(lib, objs):
+        run([nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", lib, *objs])
+    return lib
 
 
 if __name__ == "__main__":

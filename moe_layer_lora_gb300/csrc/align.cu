@@ -199,6 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         first[tid] = start;
         cursor[tid] = start;
         for (int b = start / BM; b < (start + padded) / BM; ++b) {
+            if (!MLORA_IN_BOUNDS(b < max_padded / BM, status)) break;
             expert_ids[b] = tid;
             if (ex.blk_rows) ex.blk_rows[b] = min(BM, c - (b - start / BM) * BM);
         }
@@ -213,6 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n = cnt[e];
         const int pad_end = first[e] + (n + BM - 1) / BM * BM;
         for (int p = first[e] + n + lane; p < pad_end; p += 32) {
+            if (!MLORA_IN_BOUNDS(p < max_padded, status)) break;
             if (staged) {
                 st_sorted[p] = static_cast<uint16_t>(S);
                 st_lora[p] = -1;
@@ -234,6 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (f >= run1) break;
                 if (static_cast<unsigned>(e) >= static_cast<unsigned>(E_tot)) continue;
                 const int p = first[e] + wcnt[e * kThreads + tid]++;
+                if (!MLORA_IN_BOUNDS(p >= 0 && p < max_padded, status)) continue;
                 int l = -1;
                 if (kWithLora) {
                     l = ex.token_lora_idx[f / ex.K_total];
@@ -291,12 +294,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         pos = __shfl_sync(0xffffffffu, pos, __ffs(peers) - 1);
         if (valid) {
             const int p = pos + rank;
+            const bool in_range = MLORA_IN_BOUNDS(p >= 0 && p < max_padded, status);
             int l = l_in;
             if (kWithLora && (l < -1 || l >= ex.L)) {
                 if (status) atomicOr(status, MLORA_DEV_BAD_LORA_IDX);
                 l = -1;
             }
-            if (staged) {
+            if (!in_range) {
+            } else if (staged) {
                 st_sorted[p] = static_cast<uint16_t>(f);
                 st_lora[p] = static_cast<int16_t>(l);
             } else {
@@ -342,6 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) cand = min(cand, __shfl_xor_sync(0xffffffffu, cand, off));
             if (cand == 0x7fffffff) break;
+            if (!MLORA_IN_BOUNDS(count < ex.cap, status)) break;
             if (lane == 0) ex.blk_lora[static_cast<long>(b) * ex.cap + count] = cand;
             ++count;
             prev = cand;
@@ -366,6 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (b < nblocks) {
             ex.blk_lt_start[b] = run_lt + lt_excl;
             for (int j = 0; j < ng; ++j) {
+                if (!MLORA_IN_BOUNDS(run_gt + gt_excl + j < ex.lt_cap, status)) break;
                 ex.gt_block[run_gt + gt_excl + j] = b;
                 ex.gt_first[run_gt + gt_excl + j] = j * ex.gsize;
             }

@@ -342,6 +342,8 @@ mlora_status mlora_moe_forward(const void* x, const void* w13, const void* w2, c
     gp.gt_first = ws.gt_first;
     gp.gt_total = ws.gt_total;
     gp.act_done = ws.act_done;
+    gp.lt_cap = z.max_lt;
+    gp.pad_cap = z.max_padded;
     gp.tile_next = ws.tile_next;
     gp.status = ws.status;
     gp.wait_limit = g_wait_limit;
@@ -364,6 +366,7 @@ mlora_status mlora_moe_forward(const void* x, const void* w13, const void* w2, c
     // memset node between the caller's route and align)
     ex.zero = ws.status;
     ex.zero_words = static_cast<int>(ws.zeroed_bytes / 4);
+    ex.lt_cap = z.max_lt;
     ex.blk_rows = ws.blk_rows;
     if (lora) {
         ex.token_lora_idx = token_lora_idx;
@@ -383,7 +386,7 @@ mlora_status mlora_moe_forward(const void* x, const void* w13, const void* w2, c
                        ws.status, &ex, s);
     if (err != cudaSuccess) return cuda_fail(err, "align");
     if ((err = mark_stage(1, s)) != cudaSuccess) return cuda_fail(err, "stage event");
-    err = launch_gather_rows(x, H, ws.sorted_ids, ws.n_pad, z.S, K_total, z.max_padded, ws.x_perm, s);
+    err = launch_gather_rows(x, H, ws.sorted_ids, ws.n_pad, z.S, K_total, z.max_padded, ws.x_perm, ws.status, s);
     if (err != cudaSuccess) return cuda_fail(err, "gather");
     if ((err = mark_stage(2, s)) != cudaSuccess) return cuda_fail(err, "stage event");
     // narrow tiles (half width) at most double the slab count

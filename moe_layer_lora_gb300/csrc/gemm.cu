@@ -520,6 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
                 const int32_t* lora_list = p.blk_lora + static_cast<long>(tc.b) * p.cap;
                 const int lt0 = p.blk_lt_start[tc.b] + tc.i0;
                 for (int i = 0; i < tc.g; ++i) {
+                    if (!MLORA_IN_BOUNDS(lt0 + i < p.lt_cap, p.status)) break;
                     const bool mine = my_l == lora_list[tc.i0 + i];
                     __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(sd.lora_t) +
                                          (static_cast<size_t>(lt0 + i) * kBlockM + row) * kLoraTileCols;
@@ -546,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
                 }
                 publish = sd.done + tc.b;
             } else if (tc.kind == kGateUp) {
-                const bool real = p.sorted_ids[prow] < p.S;
+                const bool real = MLORA_IN_BOUNDS(prow < p.pad_cap, p.status) && p.sorted_ids[prow] < p.S;
                 const int j0 = tc.cb * gm.half;
                 __nv_bfloat16* act = static_cast<__nv_bfloat16*>(sd.out) + static_cast<size_t>(prow) * sd.n_out;
                 for (int c = 0; c < gm.half; c += 32) {
@@ -571,7 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
                 }
                 publish = p.act_done + tc.b;
             } else {
-                const int f = p.sorted_ids[prow];
+                const int f = MLORA_IN_BOUNDS(prow < p.pad_cap, p.status) ? p.sorted_ids[prow] : p.S;
                 const bool real = f < p.S;
                 const int o0 = tc.cb * gm.bn;
                 __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(sd.out) + static_cast<size_t>(real ? f : 0) * sd.n_out;

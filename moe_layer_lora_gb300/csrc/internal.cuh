@@ -17,6 +17,22 @@ constexpr int kLoraTileCols = 64;               // shrink result row, padded to 
 constexpr int kRowBox = 32;                     // token rows per TMA box of an A operand
 constexpr long long kWaitCycles = 4000000000LL;  // default spin limit of a device wait (~2 s at 2 GHz)
 
+// Bounds-checked debug build (compiled with -DMLORA_CHECK_BOUNDS): every
+// computed index into a workspace or output buffer is checked before the
+// store; a bad one sets MLORA_DEV_BOUNDS in the status word and the store
+// is skipped, so nothing faults.  The normal build compiles the checks away.
+#ifdef MLORA_CHECK_BOUNDS
+#define MLORA_IN_BOUNDS(cond, status) (::mlora::bounds_ok((cond), (status)))
+#else
+#define MLORA_IN_BOUNDS(cond, status) true
+#endif
+#ifdef __CUDACC__
+__device__ __forceinline__ bool bounds_ok(bool ok, uint32_t* status) {
+    if (!ok && status) atomicOr(status, MLORA_DEV_BOUNDS);
+    return ok;
+}
+#endif
+
 // Per-forward buffers carved out of the caller's workspace.
 struct Workspace {
     uint32_t* status;      // [0] device status word
@@ -64,6 +80,7 @@ long align_max_padded(long S, int E_tot, int block_m);
 // written when set; the adapter fields only when token_lora_idx is set.
 struct AlignExtra {
     uint32_t* zero;  // words cleared first thing (the forward's header and counters)
+    long lt_cap;     // capacity of the group-tile lists (bounds checks)
     int zero_words;
     int32_t* blk_rows;
     const int32_t* token_lora_idx;
@@ -88,7 +105,7 @@ cudaError_t launch_align(const int32_t* ids, long S, int E_tot, int block_m, lon
                          cudaStream_t s);
 
 cudaError_t launch_gather_rows(const void* x, int H, const int32_t* sorted, const int32_t* n_pad, long S,
-                               int K_total, long max_padded, void* x_perm, cudaStream_t s);
+                               int K_total, long max_padded, void* x_perm, uint32_t* status, cudaStream_t s);
 
 cudaError_t launch_combine(const void* y_slot, const int32_t* topk_ids, const float* topk_w, int M, int H,
                            int K_total, int E_tot, float out_scale, void* y, cudaStream_t s);
@@ -127,6 +144,8 @@ struct alignas(128) GemmParams {
     const int32_t* gt_first;
     const int32_t* gt_total;
     int32_t* act_done;  // per block: finished gate_up tiles (zero at launch)
+    long lt_cap;        // LoRA tiles the workspace holds (bounds checks)
+    long pad_cap;       // sorted positions the workspace holds (bounds checks)
     int32_t* tile_next; // tiles claimed past the first round (zero at launch)
     uint32_t* status;
     long long wait_limit;        // clock cycles a wait may take before the CTA gives up

@@ -17,13 +17,15 @@ namespace {
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ x, int H8,
                                                           const int32_t* __restrict__ sorted,
                                                           const int32_t* __restrict__ n_pad, int S, int K_total,
-                                                          uint4* __restrict__ x_perm) {
+                                                          uint4* __restrict__ x_perm, int max_padded,
+                                                          uint32_t* __restrict__ status) {
     griddep_wait();
     griddep_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int warps = blockDim.x >> 5;
     const int np = *n_pad;
     for (int p = blockIdx.x * warps + (threadIdx.x >> 5); p < np; p += gridDim.x * warps) {
+        if (!MLORA_IN_BOUNDS(p < max_padded, status)) break;
         const int f = sorted[p];
         if (f >= S) continue;  // padding row: never stored downstream
         const uint4* src = x + static_cast<size_t>(f / K_total) * H8;
@@ -101,7 +103,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ 
 }  // namespace
 
 cudaError_t launch_gather_rows(const void* x, int H, const int32_t* sorted, const int32_t* n_pad, long S,
-                               int K_total, long max_padded, void* x_perm, cudaStream_t s) {
+                               int K_total, long max_padded, void* x_perm, uint32_t* status, cudaStream_t s) {
     if (max_padded == 0) return cudaSuccess;
     const int warps_per_block = 8;
     long blocks = (max_padded + warps_per_block - 1) / warps_per_block;
@@ -109,7 +111,7 @@ cudaError_t launch_gather_rows(const void* x, int H, const int32_t* sorted, cons
     if (blocks > cap) blocks = cap;
     return launch_pdl(gather_rows_kernel, dim3(static_cast<unsigned>(blocks)), dim3(32 * warps_per_block), 0, s,
                       static_cast<const uint4*>(x), H / 8, sorted, n_pad, static_cast<int>(S), K_total,
-                      static_cast<uint4*>(x_perm));
+                      static_cast<uint4*>(x_perm), static_cast<int>(max_padded), status);
 }
 
 cudaError_t launch_combine(const void* y_slot, const int32_t* topk_ids, const float* topk_w, int M, int H,

@@ -1,0 +1,73 @@
+"""The bounds-checked debug build (libmlora_checked.so, -DMLORA_CHECK_BOUNDS).
+
+Every computed index into a workspace or output buffer is checked before the
+store; a bad one would set MLORA_DEV_BOUNDS in the device status word and
+skip the store instead of faulting.  These tests run the layer through that
+build on shapes that exercise every tile kind, the narrow and wide tiles,
+both align methods and ragged edges: the status word must stay clean and
+the outputs must still match the oracle.  (A stand-in for a memory checker,
+which this GPU pool does not offer.)"""
+import numpy as np
+import pytest
+import torch
+
+import moe_layer_lora_gb300 as ml
+from moe_layer_lora_gb300 import _lib
+from moe_layer_lora_gb300 import workloads as wl
+import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def checked_library():
+    _lib.use_library(_lib.LIB_CHECKED_PATH)
+    yield
+    _lib.use_library(_lib.LIB_PATH)
+
+
+def _run(spec, rows=None):
+    inp = wl.make(spec, device="cuda")
+    d = gu.DeviceInputs(inp)
+    ids, w = gu.gpu_route(d)
+    L, r = (spec.L, spec.r) if spec.has_lora else (0, 0)
+    ws = torch.empty(ml.mlora_moe_workspace_size(spec.M, spec.H, spec.I, spec.E_tot, spec.K_total, L, r),
+                     dtype=torch.uint8, device="cuda")
+    y = gu.gpu_forward(d, ids, w, workspace=ws)
+    torch.cuda.synchronize()
+    status = ml.mlora_moe_read_status(ws)
+    assert not status & ml.DEV_BOUNDS, f"{spec.name}: an index left its buffer (status {status:#x})"
+    assert status == 0
+    ids_ref, w_ref = gu.oracle_route(inp)
+    y_ref = gu.oracle_forward(inp, ids_ref, w_ref, rows=rows)
+    yg = y if rows is None else y[torch.as_tensor(rows, device="cuda")]
+    gu.check_y(yg, y_ref, f"{spec.name} (bounds-checked build)")
+
+
+def test_checked_build_is_loaded():
+    assert _lib.load()._name.endswith("libmlora_checked.so")
+
+
+@pytest.mark.parametrize("over", [
+    dict(),                                                                   # tiny: narrow tiles
+    dict(M=37, H=136, I=72, E=5, top_k=3, L=3, r=24, seed=101),               # ragged K, N, rank
+    dict(M=9, H=8, I=8, E=4, top_k=4, L=5, r=64, seed=104),                   # tiny H/I, top_k = E
+    dict(M=300, H=200, I=328, E=16, top_k=2, L=70, r=8, seed=105),            # L > 64 adapters
+    dict(M=1100, H=136, I=72, E=5, top_k=4, L=3, r=24, seed=109),             # per-thread runs in align
+    dict(M=1100, H=64, I=64, E=96, top_k=4, L=3, r=8, seed=112),              # runs, not staged
+])
+def test_small_layers(over):
+    _run(wl.spec("tiny", **over))
+
+
+def test_decode():
+    _run(wl.spec("decode"))
+
+
+def test_prefill_sampled():
+    s = wl.spec("prefill")
+    _run(s, rows=np.linspace(0, s.M - 1, 16).round().astype(np.int64))
+
+
+def test_shared_one_token():
+    _run(wl.spec("shared", M=1))

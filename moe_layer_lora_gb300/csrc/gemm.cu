@@ -26,6 +26,9 @@
 //  3. down shrink tiles: T2_l = s * act A2_{l,e}^T, as in phase 1.
 //  4. down tiles: d = act W2_e^T over 256 output columns + the T2 expand;
 //     epilogue the slot's expert output in bf16.
+// Batches with fewer wide gate_up tiles than SMs use narrow tiles instead
+// (64 gate + 64 up rows, 128 down columns, N = 128) so that every SM
+// streams weights.  Shrink tiles pack up to four 64-wide K-chunks per stage.
 //
 // A tile depends only on tiles of earlier phases of the same block, i.e.
 // on tiles with smaller indices.  Tiles are claimed in index order, every

@@ -150,21 +150,23 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, const Geom& gm,
     }
     t.side = t.kind >= kShrinkDown ? 1 : 0;
     t.shrink = t.kind == kShrinkUp || t.kind == kShrinkDown;
+    // blocks in descending order: the row gather writes x_perm in ascending
+    // order, so the last blocks' rows are the ones still in L2
     if (t.shrink) {
-        t.b = p.gt_block[u];
-        t.i0 = p.gt_first[u];
+        const long v = ns - 1 - u;
+        t.b = p.gt_block[v];
+        t.i0 = p.gt_first[v];
         t.g = min(p.gsize, p.blk_nad[t.b] - t.i0);
         t.cb = 0;
     } else {
         const int ncb = t.side ? gm.ncb1 : gm.ncb0;
-        t.b = static_cast<int>(u / ncb);
-        t.cb = static_cast<int>(u - static_cast<long>(t.b) * ncb);
+        const int bu = static_cast<int>(u / ncb);
+        t.cb = static_cast<int>(u - static_cast<long>(bu) * ncb);
+        t.b = nblocks - 1 - bu;
         t.i0 = 0;
         t.g = 0;
     }
     t.e = p.expert_ids[t.b];
-    (void)ns;
-    (void)nblocks;
     return t;
 }
 

@@ -263,3 +263,37 @@ def test_benchmark_launch_configuration(name):
     y_ref = gu.oracle_forward(inp, ids_ref, w_ref, rows=rows)
     yg = y if rows is None else y[torch.as_tensor(rows, device="cuda")]
     gu.check_y(yg, y_ref, f"{name} graph replay")
+
+
+def _random_specs(n: int, seed: int = 2024):
+    """Seeded random small layers: shapes (multiples of 8), expert counts,
+    top-k, shared slots, both scorings, renormalisation, ranks 8..64,
+    adapter counts and modes."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        E = int(rng.integers(1, 40))
+        n_shared = int(rng.integers(0, 3)) if E > 1 else 0
+        top_k = int(rng.integers(1, min(E, 8) + 1))
+        scoring = int(rng.integers(0, 2))
+        lora = bool(rng.random() < 0.75)
+        over = dict(
+            M=int(rng.integers(1, 300)),
+            H=8 * int(rng.integers(1, 48)),
+            I=8 * int(rng.integers(1, 48)),
+            E=E, top_k=top_k, n_shared=n_shared,
+            routed_scaling_factor=float(rng.choice([1.0, 2.5])) if n_shared else 1.0,
+            scoring=scoring, renormalize=int(rng.integers(0, 2)),
+            L=int(rng.integers(1, 12)) if lora else 0,
+            r=8 * int(rng.integers(1, 9)) if lora else 0,
+            lora_mode=str(rng.choice(["uniform", "zipf", "all_none"])) if lora else "none",
+            seed=500 + i,
+        )
+        out.append(over)
+    return out
+
+
+@pytest.mark.parametrize("over", _random_specs(24), ids=lambda o: f"M{o['M']}H{o['H']}I{o['I']}E{o['E']}k{o['top_k']}")
+def test_random_small_layers(over):
+    """Random small configurations against the oracle (every output)."""
+    _layer(wl.spec("tiny", **over), label=str(over))

@@ -134,3 +134,30 @@ def test_align_empty():
     s, e, n = ml.mlora_moe_align(torch.zeros((0, 4), dtype=torch.int32, device="cuda"), 8, 16)
     torch.cuda.synchronize()
     assert int(n.item()) == 0 and s.numel() == 0 and e.numel() == 0
+
+
+def _random_align_cases(n: int, seed: int = 77):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        E = int(rng.choice([1, 3, 8, 32, 96, 97, 129, 500, 1024]))
+        K = int(rng.integers(1, 9))
+        M = int(rng.choice([1, 7, 100, 255, 256, 257, 1000, 3000, 9000]))
+        BM = int(rng.choice([1, 16, 64, 128, 256]))
+        skew = bool(rng.random() < 0.5)
+        out.append((i, E, K, M, BM, skew))
+    return out
+
+
+@pytest.mark.parametrize("case", _random_align_cases(20), ids=lambda c: f"E{c[1]}K{c[2]}M{c[3]}BM{c[4]}")
+def test_align_random(case):
+    """Seeded random expert counts, slot counts (one pass, several passes,
+    per-thread runs), block sizes and skewed loads: bit-exact vs the oracle."""
+    i, E, K, M, BM, skew = case
+    rng = np.random.default_rng(1000 + i)
+    if skew:
+        p = rng.dirichlet(np.full(E, 0.3))
+        ids = rng.choice(E, size=(M, K), p=p).astype(np.int32)
+    else:
+        ids = rng.integers(0, E, size=(M, K), dtype=np.int32)
+    _align_case(ids, E, BM)

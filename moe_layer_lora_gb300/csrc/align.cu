@@ -20,7 +20,8 @@
 // Either way, when the padded list fits in shared memory (16-bit slot ids
 // and adapters) it is built there and copied out in one coalesced sweep
 // instead of scattered 4-byte stores.
-// From 8192 slots a thread-block cluster of 8 such CTAs shares the work:
+// From 2048 slots a thread-block cluster of up to 8 such CTAs (about 1024
+// slots each) shares the work:
 // each sorts one contiguous chunk of the slots, the chunks' per-expert
 // counts are exchanged through distributed shared memory (cluster barrier,
 // then mapa + ld.shared::cluster), and every CTA places its chunk after the
@@ -33,6 +34,7 @@
 // adapter and per block of kBlockM positions the ascending list of distinct
 // adapters; each (block, adapter) pair gets a masked LoRA tile, and the
 // adapters of a block are cut into shrink group tiles of up to gsize.
+#include <algorithm>
 #include <atomic>
 
 #include "internal.cuh"
@@ -45,7 +47,7 @@ constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
 constexpr int kRunsMaxExperts = 96;      // per-thread count columns: 96 x 1024 x 2 B
 constexpr int kMaxSmem = 227 * 1024;
-constexpr long kClusterMinSlots = 8192;  // from here a cluster of CTAs sorts the slots
+constexpr long kClusterMinSlots = 2 * 1024;  // from here a cluster of CTAs sorts the slots
 
 // Exclusive block scan of one int per thread; returns the exclusive prefix
 // and writes the block total to *total.  Uses 33 ints of scratch.
@@ -510,7 +512,9 @@ cudaError_t launch_align(const int32_t* ids, long S, int E_tot, int block_m, lon
             if (nclusters > 0) cluster_ok[v].fetch_or(bit, std::memory_order_relaxed);
             cluster_known[v].fetch_or(bit, std::memory_order_relaxed);
         }
-        if (cluster_ok[v].load(std::memory_order_relaxed) & bit) ncl = kCluster;
+        // about one pass of 1024 slots per CTA, at most kCluster CTAs
+        if (cluster_ok[v].load(std::memory_order_relaxed) & bit)
+            ncl = static_cast<int>(std::min<long>(kCluster, (S + kThreads - 1) / kThreads));
     }
     // several passes over the slots, or (more than one pass of slots per
     // CTA, few experts) per-thread runs with one count column per thread;

@@ -154,7 +154,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // their flags only at the end, after the cluster barriers)
     if (crank == 0)
         for (int i = tid; i < ex.zero_words; i += kThreads) ex.zero[i] = 0u;
-    if (tid == 0) *flags = 0;
+    if (tid == 0) {
+        *flags = 0;
+        scratch[38] = 0;  // most slots of one expert
+    }
     __syncthreads();
     const unsigned lt_mask = (1u << lane) - 1u;
     // runs: slots per thread, a multiple of 4 so that a run starts on a
@@ -259,6 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         first[tid] = start;
         cursor[tid] = start + cbase[tid];
     }
+    if (tid < E_tot && c > 0) atomicMax(&scratch[38], c);
     if (tid < E_tot && crank == 0) {
         for (int b = start / BM; b < (start + padded) / BM; ++b) {
             if (!MLORA_IN_BOUNDS(b < max_padded / BM, status)) break;
@@ -272,6 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int b = total / BM + tid; b < max_padded / BM; b += kThreads) expert_ids[b] = -1;
     }
     __syncthreads();
+    if (crank == 0 && tid == 0 && ex.max_rows) *ex.max_rows = min(scratch[38], BM);
 
     // 3. per-expert padding, one warp per expert
     for (int e = warp * ncl + crank; e < E_tot; e += kWarps * ncl) {

@@ -146,6 +146,7 @@ Workspace carve_workspace(const Sizes& z, void* base) {
     w.n_pad = reinterpret_cast<int32_t*>(header ? header + 4 : nullptr);
     w.gt_total = reinterpret_cast<int32_t*>(header ? header + 8 : nullptr);
     w.tile_next = reinterpret_cast<int32_t*>(header ? header + 12 : nullptr);
+    w.max_rows = reinterpret_cast<int32_t*>(header ? header + 28 : nullptr);  // (+24: the wait test's flag)
     w.act_done = reinterpret_cast<int32_t*>(take(4 * z.max_blocks));
     if (z.lora) {
         w.done13 = reinterpret_cast<int32_t*>(take(4 * z.max_blocks));
@@ -345,6 +346,7 @@ mlora_status mlora_moe_forward(const void* x, const void* w13, const void* w2, c
     gp.lt_cap = z.max_lt;
     gp.pad_cap = z.max_padded;
     gp.tile_next = ws.tile_next;
+    gp.max_rows = ws.max_rows;
     gp.status = ws.status;
     gp.wait_limit = g_wait_limit;
     // the never-set flag: a header word that the reset clears and nothing writes
@@ -367,6 +369,7 @@ mlora_status mlora_moe_forward(const void* x, const void* w13, const void* w2, c
     ex.zero = ws.status;
     ex.zero_words = static_cast<int>(ws.zeroed_bytes / 4);
     ex.lt_cap = z.max_lt;
+    ex.max_rows = ws.max_rows;
     ex.blk_rows = ws.blk_rows;
     if (lora) {
         ex.token_lora_idx = token_lora_idx;

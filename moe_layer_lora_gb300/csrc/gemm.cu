@@ -61,13 +61,26 @@ namespace {
 
 constexpr int kThreads = 192;
 constexpr int kBN = 256;                                         // weight rows per wide tile (MMA N)
+// The shared-memory ring: 4 stages of 48 KiB (A 16 KiB + B 32 KiB); when
+// no block has more than 32 real rows (decode-like batches) the A part of a
+// stage is one 32-row box, and 6 stages of 36 KiB hold 50 % more bytes in
+// flight.
 constexpr int kStages = 4;
+constexpr int kSmallStages = 6;
+constexpr int kMaxStages = kSmallStages;
 constexpr int kTileRing = 4;                                     // claimed tiles handed from producer to consumers
 constexpr int kATileBytes = kBlockM * kBlockK * 2;               // 16 KiB
 constexpr int kStageBytes = kATileBytes + kBN * kBlockK * 2;     // 48 KiB
+constexpr int kSmallATileBytes = kRowBox * kBlockK * 2;          // 4 KiB
+constexpr int kSmallStageBytes = kSmallATileBytes + kBN * kBlockK * 2;  // 36 KiB
+constexpr int kRingBytes = kSmallStages * kSmallStageBytes;      // 216 KiB >= kStages * kStageBytes
 constexpr int kAccCols = kBN;
 constexpr int kTmemCols = 2 * kBN;
-constexpr int kSmemBytes = kStages * kStageBytes + 1024 /* alignment slack */ + 256 /* barriers */;
+constexpr int kSmemBytes = kRingBytes + 1024 /* alignment slack */ + 256 /* barriers */;
+static_assert(kStages * kStageBytes <= kRingBytes && kSmallStages * kSmallStageBytes <= kRingBytes, "ring");
+// one CTA per SM: each CTA allocates all 512 TMEM columns, so two CTAs of
+// this kernel on one SM would wait on each other
+static_assert(2 * kSmemBytes > 228 * 1024, "the experts kernel must not fit twice on an SM");
 
 enum TileKind : int { kShrinkUp = 0, kGateUp = 1, kShrinkDown = 2, kDown = 3 };
 
@@ -176,12 +189,10 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, const Geom& gm,
 // 1 KiB swizzle atom.  The MMA reads 128 A rows from a chunk's start, so
 // that 16 KiB window must stay inside the stage as well.
 constexpr int kMaxShrinkChunks = 4;
-__device__ __forceinline__ int shrink_chunks(uint32_t a_bytes, uint32_t b_bytes) {
+__device__ __forceinline__ int shrink_chunks(uint32_t a_bytes, uint32_t b_bytes, uint32_t stage_bytes) {
     const uint32_t chunk = a_bytes + b_bytes;
     int c = 1;
-    while (c < kMaxShrinkChunks && (c + 1) * chunk <= static_cast<uint32_t>(kStageBytes) &&
-           c * chunk + kATileBytes <= static_cast<uint32_t>(kStageBytes))
-        ++c;
+    while (c < kMaxShrinkChunks && (c + 1) * chunk <= stage_bytes && c * chunk + kATileBytes <= stage_bytes) ++c;
     return c;
 }
 
@@ -189,64 +200,51 @@ __device__ __forceinline__ int shrink_chunks(uint32_t a_bytes, uint32_t b_bytes)
 // overflows, the limit for very negative z
 __device__ __forceinline__ float silu(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
-__global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_constant__ GemmParams p) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
-    uint64_t* empty = full + kStages;
-    uint64_t* tfull = empty + kStages;
-    uint64_t* tempty = tfull + 2;
-    uint64_t* drain = tempty + 2;
-    uint64_t* pub = drain + 1;  // the 128 epilogue threads finished writing a published tile
-    uint64_t* tile_full = pub + 1;                 // [kTileRing] a claimed tile index is in the ring
-    uint64_t* tile_empty = tile_full + kTileRing;  // [kTileRing] the MMA lane and 4 epilogue warps read it
-    long long* tile_ring = reinterpret_cast<long long*>(tile_empty + kTileRing);
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(tile_ring + kTileRing);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+// Barriers and small shared state after the stage ring.
+struct SmemLayout {
+    uint64_t* full;        // [kMaxStages] a stage's loads landed
+    uint64_t* empty;       // [kMaxStages] the MMAs reading a stage finished
+    uint64_t* tfull;       // [2] an accumulator is ready for the epilogue
+    uint64_t* tempty;      // [2] the epilogue drained an accumulator
+    uint64_t* drain;       // the last MMAs of the CTA finished
+    uint64_t* pub;         // the 128 epilogue threads finished writing a published tile
+    uint64_t* tile_full;   // [kTileRing] a claimed tile index is in the ring
+    uint64_t* tile_empty;  // [kTileRing] the MMA lane and 4 epilogue warps read it
+    long long* tile_ring;
+    uint32_t* tmem_holder;
+    volatile int* abort_flag;
+    __device__ __forceinline__ explicit SmemLayout(uint8_t* smem) {
+        full = reinterpret_cast<uint64_t*>(smem + kRingBytes);
+        empty = full + kMaxStages;
+        tfull = empty + kMaxStages;
+        tempty = tfull + 2;
+        drain = tempty + 2;
+        pub = drain + 1;
+        tile_full = pub + 1;
+        tile_empty = tile_full + kTileRing;
+        tile_ring = reinterpret_cast<long long*>(tile_empty + kTileRing);
+        tmem_holder = reinterpret_cast<uint32_t*>(tile_ring + kTileRing);
+        abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+    }
+};
 
+// The tile loop of one CTA: producer, MMA issuer and epilogue roles over a
+// ring of nst stages of stb bytes, the first ab of each holding A rows.
+template <int nst, uint32_t stb, uint32_t ab>
+__device__ __forceinline__ void experts_run(const GemmParams& p, uint8_t* smem, uint32_t tmem_base) {
+    const SmemLayout L(smem);
+    uint64_t* const full = L.full;
+    uint64_t* const empty = L.empty;
+    uint64_t* const tfull = L.tfull;
+    uint64_t* const tempty = L.tempty;
+    uint64_t* const drain = L.drain;
+    uint64_t* const pub = L.pub;
+    uint64_t* const tile_full = L.tile_full;
+    uint64_t* const tile_empty = L.tile_empty;
+    long long* const tile_ring = L.tile_ring;
+    volatile int* const abort_flag = L.abort_flag;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long long lim = p.wait_limit;  // cycles a wait may take before the CTA gives up
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
-        }
-        for (int a = 0; a < 2; ++a) {
-            mbar_init(&tfull[a], 1);
-            mbar_init(&tempty[a], 128);
-        }
-        mbar_init(drain, 1);
-        mbar_init(pub, 128);
-        for (int r = 0; r < kTileRing; ++r) {
-            mbar_init(&tile_full[r], 1);
-            mbar_init(&tile_empty[r], 1 + 4);
-        }
-        *abort_flag = 0;
-        fence_barrier_init();
-        for (int sd = 0; sd < 2; ++sd) {
-            prefetch_tensormap(&p.side[sd].tm_a);
-            prefetch_tensormap(&p.side[sd].tm_a_full);
-            prefetch_tensormap(&p.side[sd].tm_b);
-            prefetch_tensormap(&p.side[sd].tm_b_n);
-            if (p.has_lora) {
-                prefetch_tensormap(&p.side[sd].tm_sa);
-                prefetch_tensormap(&p.side[sd].tm_lb);
-                prefetch_tensormap(&p.side[sd].tm_lb_n);
-                prefetch_tensormap(&p.side[sd].tm_t);
-                prefetch_tensormap(&p.side[sd].tm_t_full);
-            }
-        }
-    }
-    if (warp == 1) {
-        tmem_alloc(tmem_holder, kTmemCols);
-        tc_fence_before();
-    }
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem_base = *tmem_holder;
-    // everything above overlapped the previous kernel in the stream
-    griddep_wait();
-
     const int nblocks = *p.n_pad / kBlockM;
     const int ns = p.has_lora ? *p.gt_total : 0;
     Geom gm;
@@ -269,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
-            long it = 0;
+            long it = 0;  // stages issued
             bool ok = true;
             long tile = blockIdx.x, next = 0;
             // test hook: a wait on a flag that nothing sets, which must end
@@ -313,10 +311,10 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
                     // engine latency-bound
                     const uint32_t b_bytes = static_cast<uint32_t>(tc.g) * rp * kBlockK * 2;
                     const uint32_t chunk = a_bytes + b_bytes;
-                    const int cps = shrink_chunks(a_bytes, b_bytes);
+                    const int cps = shrink_chunks(a_bytes, b_bytes, stb);
                     for (int kb0 = 0; kb0 < nk; kb0 += cps, ++it) {
-                        const int s = static_cast<int>(it % kStages);
-                        const uint32_t phs = static_cast<uint32_t>(it / kStages) & 1u;
+                        const int s = static_cast<int>(it % nst);
+                        const uint32_t phs = static_cast<uint32_t>(it / nst) & 1u;
                         if (!mbar_wait(&empty[s], phs ^ 1u, abort_flag, p.status, lim)) {
                             ok = false;
                             break;
@@ -324,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
                         const int nc = min(cps, nk - kb0);
                         mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(nc) * chunk);
                         for (int c = 0; c < nc; ++c) {
-                            uint8_t* ca = smem + s * kStageBytes + c * chunk;
+                            uint8_t* ca = smem + s * stb + c * chunk;
                             uint8_t* cb = ca + a_bytes;
                             const int k0 = (kb0 + c) * kBlockK;
                             for (int i = 0; i < tc.g; ++i)
@@ -341,14 +339,14 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
                     continue;
                 }
                 for (int kb = 0; kb < nk; ++kb, ++it) {
-                    const int s = static_cast<int>(it % kStages);
-                    const uint32_t phs = static_cast<uint32_t>(it / kStages) & 1u;
+                    const int s = static_cast<int>(it % nst);
+                    const uint32_t phs = static_cast<uint32_t>(it / nst) & 1u;
                     if (!mbar_wait(&empty[s], phs ^ 1u, abort_flag, p.status, lim)) {
                         ok = false;
                         break;
                     }
-                    uint8_t* sa = smem + s * kStageBytes;
-                    uint8_t* sb = sa + kATileBytes;
+                    uint8_t* sa = smem + s * stb;
+                    uint8_t* sb = sa + ab;
                     const int k0 = kb * kBlockK;
                     if (tc.kind == kGateUp) {
                         mbar_arrive_expect_tx(&full[s], a_bytes + gm.bn * kBlockK * 2);
@@ -374,14 +372,14 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
                 }
                 const int lt0 = p.blk_lt_start[tc.b];
                 for (int i = 0; i < nad; ++i, ++it) {
-                    const int s = static_cast<int>(it % kStages);
-                    const uint32_t phs = static_cast<uint32_t>(it / kStages) & 1u;
+                    const int s = static_cast<int>(it % nst);
+                    const uint32_t phs = static_cast<uint32_t>(it / nst) & 1u;
                     if (!mbar_wait(&empty[s], phs ^ 1u, abort_flag, p.status, lim)) {
                         ok = false;
                         break;
                     }
-                    uint8_t* sa = smem + s * kStageBytes;
-                    uint8_t* sb = sa + kATileBytes;
+                    uint8_t* sa = smem + s * stb;
+                    uint8_t* sb = sa + ab;
                     const int le = lora_list[i] * p.E_tot + tc.e;
                     mbar_arrive_expect_tx(&full[s], a_bytes + gm.bn * kBlockK * 2);
                     if (tc.kind == kGateUp) {
@@ -399,15 +397,16 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
                 }
             }
             if (!ok) {
-                for (long j = it > kStages ? it - kStages : 0; j < it; ++j)
-                    drain_wait(&full[j % kStages], static_cast<uint32_t>(j / kStages) & 1u, lim);
+                // the last min(it, nst) stages issued, walking back from the ring position
+                for (long j = it > nst ? it - nst : 0; j < it; ++j)
+                    drain_wait(&full[j % nst], static_cast<uint32_t>(j / nst) & 1u, lim);
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
         if (lane == 0) {
             const uint32_t idesc_base = umma_idesc_bf16(128, gm.bn);
-            long it = 0;
+            long it = 0;  // stages consumed
             bool ok = true;
             for (int lt = 0; ok; ++lt) {
                 const int ts = lt % kTileRing;
@@ -437,17 +436,17 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
                     const uint32_t a_bytes = nbox * kRowBox == kBlockM ? static_cast<uint32_t>(kATileBytes)
                                                                        : static_cast<uint32_t>(nbox) * kRowBox * kBlockK * 2;
                     const uint32_t chunk = a_bytes + static_cast<uint32_t>(tc.g) * rp * kBlockK * 2;
-                    const int cps = shrink_chunks(a_bytes, chunk - a_bytes);
+                    const int cps = shrink_chunks(a_bytes, chunk - a_bytes, stb);
                     for (int kb0 = 0; kb0 < nk; kb0 += cps, ++it) {
-                        const int s = static_cast<int>(it % kStages);
-                        if (!mbar_wait(&full[s], static_cast<uint32_t>(it / kStages) & 1u, abort_flag, p.status, lim)) {
+                        const int s = static_cast<int>(it % nst);
+                        if (!mbar_wait(&full[s], static_cast<uint32_t>(it / nst) & 1u, abort_flag, p.status, lim)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
                         const int nc = min(cps, nk - kb0);
                         for (int c = 0; c < nc; ++c) {
-                            const uint32_t a_addr = smem_u32(smem + s * kStageBytes + c * chunk);
+                            const uint32_t a_addr = smem_u32(smem + s * stb + c * chunk);
                             const uint64_t ad = umma_desc_sw128(a_addr);
                             const uint64_t bd = umma_desc_sw128(a_addr + a_bytes);
 #pragma unroll
@@ -461,15 +460,15 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
                     continue;
                 }
                 for (int kb = 0; kb < nk; ++kb, ++it) {
-                    const int s = static_cast<int>(it % kStages);
-                    if (!mbar_wait(&full[s], static_cast<uint32_t>(it / kStages) & 1u, abort_flag, p.status, lim)) {
+                    const int s = static_cast<int>(it % nst);
+                    if (!mbar_wait(&full[s], static_cast<uint32_t>(it / nst) & 1u, abort_flag, p.status, lim)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_addr = smem_u32(smem + s * kStageBytes);
+                    const uint32_t a_addr = smem_u32(smem + s * stb);
                     const uint64_t ad = umma_desc_sw128(a_addr);
-                    const uint64_t bd = umma_desc_sw128(a_addr + kATileBytes);
+                    const uint64_t bd = umma_desc_sw128(a_addr + ab);
 #pragma unroll
                     for (int k = 0; k < kBlockK / 16; ++k)
                         umma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
@@ -479,15 +478,15 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
                 if (!tc.shrink && p.has_lora) {
                     const int nad = p.blk_nad[tc.b];
                     for (int i = 0; i < nad; ++i, ++it) {
-                        const int s = static_cast<int>(it % kStages);
-                        if (!mbar_wait(&full[s], static_cast<uint32_t>(it / kStages) & 1u, abort_flag, p.status, lim)) {
+                        const int s = static_cast<int>(it % nst);
+                        if (!mbar_wait(&full[s], static_cast<uint32_t>(it / nst) & 1u, abort_flag, p.status, lim)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        const uint32_t a_addr = smem_u32(smem + s * kStageBytes);
+                        const uint32_t a_addr = smem_u32(smem + s * stb);
                         const uint64_t ad = umma_desc_sw128(a_addr);
-                        const uint64_t bd = umma_desc_sw128(a_addr + kATileBytes);
+                        const uint64_t bd = umma_desc_sw128(a_addr + ab);
                         for (int k = 0; k < lora_ksteps; ++k) umma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, 1u);
                         umma_commit(&empty[s]);
                     }
@@ -621,6 +620,72 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
             }
         }
     }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_constant__ GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const SmemLayout L(smem);
+    uint64_t* const full = L.full;
+    uint64_t* const empty = L.empty;
+    uint64_t* const tfull = L.tfull;
+    uint64_t* const tempty = L.tempty;
+    uint64_t* const drain = L.drain;
+    uint64_t* const pub = L.pub;
+    uint64_t* const tile_full = L.tile_full;
+    uint64_t* const tile_empty = L.tile_empty;
+    uint32_t* const tmem_holder = L.tmem_holder;
+    volatile int* const abort_flag = L.abort_flag;
+
+    const int warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kMaxStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&tfull[a], 1);
+            mbar_init(&tempty[a], 128);
+        }
+        mbar_init(drain, 1);
+        mbar_init(pub, 128);
+        for (int r = 0; r < kTileRing; ++r) {
+            mbar_init(&tile_full[r], 1);
+            mbar_init(&tile_empty[r], 1 + 4);
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+        for (int sd = 0; sd < 2; ++sd) {
+            prefetch_tensormap(&p.side[sd].tm_a);
+            prefetch_tensormap(&p.side[sd].tm_a_full);
+            prefetch_tensormap(&p.side[sd].tm_b);
+            prefetch_tensormap(&p.side[sd].tm_b_n);
+            if (p.has_lora) {
+                prefetch_tensormap(&p.side[sd].tm_sa);
+                prefetch_tensormap(&p.side[sd].tm_lb);
+                prefetch_tensormap(&p.side[sd].tm_lb_n);
+                prefetch_tensormap(&p.side[sd].tm_t);
+                prefetch_tensormap(&p.side[sd].tm_t_full);
+            }
+        }
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_holder, kTmemCols);
+        tc_fence_before();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+    // everything above overlapped the previous kernel in the stream
+    griddep_wait();
+
+    // ring geometry of this launch (the same in every CTA): when no expert
+    // has more than one 32-row box of slots, A stages shrink to 4 KiB and
+    // the ring holds 6 stages instead of 4
+    if (*p.max_rows <= kRowBox)
+        experts_run<kSmallStages, kSmallStageBytes, kSmallATileBytes>(p, smem, tmem_base);
+    else
+        experts_run<kStages, kStageBytes, kATileBytes>(p, smem, tmem_base);
 
     __syncthreads();
     if (warp == 1) {

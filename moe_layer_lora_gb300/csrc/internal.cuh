@@ -38,6 +38,7 @@ struct Workspace {
     uint32_t* status;      // [0] device status word
     int32_t* n_pad;        // padded slot total written by align
     int32_t* gt_total;     // number of shrink group tiles
+    int32_t* max_rows;     // most real rows in any block
     int32_t* done13;       // [max_blocks] shrink tiles finished per block, gate_up projection
     int32_t* done2;        // [max_blocks] the same for the down projection
     int32_t* tile_next;    // experts tiles claimed past the first round
@@ -80,6 +81,7 @@ long align_max_padded(long S, int E_tot, int block_m);
 // written when set; the adapter fields only when token_lora_idx is set.
 struct AlignExtra {
     uint32_t* zero;  // words cleared first thing (the forward's header and counters)
+    int32_t* max_rows;  // most real rows in any block (<= block_m), or null
     long lt_cap;     // capacity of the group-tile lists (bounds checks)
     int zero_words;
     int32_t* blk_rows;
@@ -147,6 +149,7 @@ struct alignas(128) GemmParams {
     long lt_cap;        // LoRA tiles the workspace holds (bounds checks)
     long pad_cap;       // sorted positions the workspace holds (bounds checks)
     int32_t* tile_next; // tiles claimed past the first round (zero at launch)
+    const int32_t* max_rows;  // most real rows in any block (written by align)
     uint32_t* status;
     long long wait_limit;        // clock cycles a wait may take before the CTA gives up
     const int32_t* stall_flag;   // test hook: non-null = wait on this never-set flag first

@@ -297,3 +297,37 @@ def _random_specs(n: int, seed: int = 2024):
 def test_random_small_layers(over):
     """Random small configurations against the oracle (every output)."""
     _layer(wl.spec("tiny", **over), label=str(over))
+
+
+def _hot_expert_ids(M, E, k, n_hot, seed):
+    """Hand-made routing in which expert 0 gets exactly n_hot slots and the
+    others share the rest evenly (fewer than n_hot each), with distinct
+    experts within every row; positive weights that sum to 1 per row."""
+    ids = np.empty((M, k), np.int32)
+    for t in range(M):
+        if t < n_hot:
+            ids[t, 0] = 0
+            ids[t, 1:] = 1 + (t * (k - 1) + np.arange(k - 1)) % (E - 1)
+        else:
+            ids[t] = 1 + (t * k + np.arange(k)) % (E - 1)
+    assert all(len(set(r)) == k for r in ids.tolist())
+    counts = np.bincount(ids.ravel(), minlength=E)
+    assert counts[0] == n_hot and counts[1:].max() < n_hot
+    w = np.random.default_rng(seed).uniform(0.1, 1.0, (M, k)).astype(np.float32)
+    return ids, (w / w.sum(1, keepdims=True)).astype(np.float32)
+
+
+@pytest.mark.parametrize("M,E,n_hot", [(40, 4, 32), (40, 4, 33), (1024, 128, 32), (1024, 128, 33)])
+def test_ring_geometry_boundary(M, E, n_hot):
+    """The experts kernel shrinks its A stages when no expert has more than
+    32 slots; the busiest expert at exactly 32 and at 33 slots, with a
+    one-CTA align (80 slots) and a cluster align (2048 slots)."""
+    s = wl.spec("tiny", M=M, H=64, I=72, E=E, top_k=2, L=3, r=16, seed=120 + n_hot)
+    inp = wl.make(s, device="cuda")
+    d = gu.DeviceInputs(inp)
+    ids, w = _hot_expert_ids(M, E, 2, n_hot, seed=7)
+    ws = torch.empty(ml.mlora_moe_workspace_size(s.M, s.H, s.I, s.E_tot, s.K_total, s.L, s.r), dtype=torch.uint8,
+                     device="cuda")
+    y = gu.gpu_forward(d, torch.from_numpy(ids).cuda(), torch.from_numpy(w).cuda(), workspace=ws)
+    assert ml.mlora_moe_read_status(ws) == 0
+    gu.check_y(y, gu.oracle_forward(inp, ids, w), f"busiest expert {n_hot} slots")

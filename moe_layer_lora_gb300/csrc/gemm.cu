@@ -228,396 +228,447 @@ struct SmemLayout {
     }
 };
 
-// The tile loop of one CTA: producer, MMA issuer and epilogue roles over a
-// ring of nst stages of stb bytes, the first ab of each holding A rows.
-template <int nst, uint32_t stb, uint32_t ab>
-__device__ __forceinline__ void experts_run(const GemmParams& p, uint8_t* smem, uint32_t tmem_base) {
-    const SmemLayout L(smem);
-    uint64_t* const full = L.full;
-    uint64_t* const empty = L.empty;
-    uint64_t* const tfull = L.tfull;
-    uint64_t* const tempty = L.tempty;
-    uint64_t* const drain = L.drain;
-    uint64_t* const pub = L.pub;
-    uint64_t* const tile_full = L.tile_full;
-    uint64_t* const tile_empty = L.tile_empty;
-    long long* const tile_ring = L.tile_ring;
-    volatile int* const abort_flag = L.abort_flag;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const long long lim = p.wait_limit;  // cycles a wait may take before the CTA gives up
-    const int nblocks = *p.n_pad / kBlockM;
-    const int ns = p.has_lora ? *p.gt_total : 0;
+// What every role of a CTA derives once per launch: the shared-memory
+// layout, the tile geometry and the phase boundaries of the tile list.
+struct Ctx {
+    const GemmParams* p;
+    uint8_t* smem;
+    SmemLayout L;
     Geom gm;
-    {
-        const bool narrow = static_cast<long>(nblocks) * p.side[0].ncb < gridDim.x;
+    Phases ph;
+    int nblocks;
+    int ns;           // shrink tiles per projection
+    int rp;           // rank padded to the MMA's N granule
+    int lora_ksteps;  // expand K-steps of 16
+    uint32_t tmem_base;
+    long long lim;    // cycles a wait may take before the CTA gives up
+    __device__ __forceinline__ Ctx(const GemmParams& prm, uint8_t* sm, uint32_t tmem)
+        : p(&prm), smem(sm), L(sm), tmem_base(tmem), lim(prm.wait_limit) {
+        nblocks = *prm.n_pad / kBlockM;
+        ns = prm.has_lora ? *prm.gt_total : 0;
+        const bool narrow = static_cast<long>(nblocks) * prm.side[0].ncb < gridDim.x;
         gm.bn = narrow ? kBN / 2 : kBN;
         gm.half = gm.bn / 2;
-        gm.ncb0 = (p.side[0].n_out + gm.half - 1) / gm.half;
-        gm.ncb1 = (p.side[1].n_out + gm.bn - 1) / gm.bn;
+        gm.ncb0 = (prm.side[0].n_out + gm.half - 1) / gm.half;
+        gm.ncb1 = (prm.side[1].n_out + gm.bn - 1) / gm.bn;
+        ph.s1 = ns;
+        ph.g = ph.s1 + static_cast<long>(nblocks) * gm.ncb0;
+        ph.s2 = ph.g + ns;
+        ph.d = ph.s2 + static_cast<long>(nblocks) * gm.ncb1;
+        rp = (prm.rank + 15) / 16 * 16;
+        lora_ksteps = (prm.rank + 15) / 16;
     }
-    Phases ph;
-    ph.s1 = ns;
-    ph.g = ph.s1 + static_cast<long>(nblocks) * gm.ncb0;
-    ph.s2 = ph.g + ns;
-    ph.d = ph.s2 + static_cast<long>(nblocks) * gm.ncb1;
-    const long ntiles = ph.d;
-    const int rp = (p.rank + 15) / 16 * 16;     // rank padded to the MMA's N granule
-    const int lora_ksteps = (p.rank + 15) / 16;  // expand K-steps of 16
+};
 
-    if (warp == 0) {
-        // ------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            long it = 0;  // stages issued
-            bool ok = true;
-            long tile = blockIdx.x, next = 0;
-            // test hook: a wait on a flag that nothing sets, which must end
-            // in a reported timeout and a clean exit
-            if (p.stall_flag && !wait_counter(p.stall_flag, 1, abort_flag, p.status, lim)) ok = false;
-            for (int jt = 0; ok; ++jt, tile = next) {
-                // hand the tile (or the end mark) to the MMA lane and the
-                // epilogue, then claim the next one; its index is needed
-                // only once this tile's loads are issued
-                const int ts = jt % kTileRing;
-                if (!mbar_wait(&tile_empty[ts], (static_cast<uint32_t>(jt / kTileRing) & 1u) ^ 1u, abort_flag,
-                               p.status, lim)) {
+// TMA producer (one thread): claims tiles, hands them on through the tile
+// ring and streams their operands into a ring of nst stages of stb bytes,
+// the first ab of each holding A rows.
+template <int nst, uint32_t stb, uint32_t ab>
+__device__ __forceinline__ void producer(const Ctx& c) {
+    const GemmParams& p = *c.p;
+    uint64_t* const full = c.L.full;
+    uint64_t* const empty = c.L.empty;
+    uint64_t* const tile_full = c.L.tile_full;
+    uint64_t* const tile_empty = c.L.tile_empty;
+    long long* const tile_ring = c.L.tile_ring;
+    volatile int* const abort_flag = c.L.abort_flag;
+    const long long lim = c.lim;
+    const int nblocks = c.nblocks;
+    const int ns = c.ns;
+    const Geom& gm = c.gm;
+    const Phases& ph = c.ph;
+    const long ntiles = c.ph.d;
+    const int rp = c.rp;
+    uint8_t* const smem = c.smem;
+    long it = 0;  // stages issued
+    bool ok = true;
+    long tile = blockIdx.x, next = 0;
+    // test hook: a wait on a flag that nothing sets, which must end
+    // in a reported timeout and a clean exit
+    if (p.stall_flag && !wait_counter(p.stall_flag, 1, abort_flag, p.status, lim)) ok = false;
+    for (int jt = 0; ok; ++jt, tile = next) {
+        // hand the tile (or the end mark) to the MMA lane and the
+        // epilogue, then claim the next one; its index is needed
+        // only once this tile's loads are issued
+        const int ts = jt % kTileRing;
+        if (!mbar_wait(&tile_empty[ts], (static_cast<uint32_t>(jt / kTileRing) & 1u) ^ 1u, abort_flag,
+                       p.status, lim)) {
+            ok = false;
+            break;
+        }
+        tile_ring[ts] = tile < ntiles ? tile : -1;
+        mbar_arrive(&tile_full[ts]);
+        if (tile >= ntiles) break;
+        next = gridDim.x + static_cast<long>(atomicAdd(p.tile_next, 1));
+        const Tile tc = decode_tile(p, gm, tile, ph, ns, nblocks);
+        const GemmSide& sd = p.side[tc.side];
+        const int row0 = tc.b * kBlockM;
+        // the down side reads act rows, complete once the block's
+        // gate_up tiles all are
+        if (tc.side == 1 && !wait_counter(p.act_done + tc.b, gm.ncb0, abort_flag, p.status, lim)) {
+            ok = false;
+            break;
+        }
+        // only the block's real rows are loaded; the MMA rows past
+        // them hold stale data and feed only discarded output rows
+        const int nbox = (p.blk_rows[tc.b] + kRowBox - 1) / kRowBox;
+        const bool full_block = nbox * kRowBox == kBlockM;
+        const uint32_t a_bytes = static_cast<uint32_t>(nbox) * kRowBox * kBlockK * 2;
+        const int32_t* lora_list = p.blk_lora + static_cast<long>(tc.b) * p.cap;
+        const int nk = (sd.K + kBlockK - 1) / kBlockK;
+        const CUtensorMap* bmap = gm.bn == kBN ? &sd.tm_b : &sd.tm_b_n;
+        const CUtensorMap* lbmap = gm.bn == kBN ? &sd.tm_lb : &sd.tm_lb_n;
+        if (tc.shrink) {
+            // several K-chunks per stage: the shrink's operands are
+            // small, and a stage of one chunk leaves the copy
+            // engine latency-bound
+            const uint32_t b_bytes = static_cast<uint32_t>(tc.g) * rp * kBlockK * 2;
+            const uint32_t chunk = a_bytes + b_bytes;
+            const int cps = shrink_chunks(a_bytes, b_bytes, stb);
+            for (int kb0 = 0; kb0 < nk; kb0 += cps, ++it) {
+                const int s = static_cast<int>(it % nst);
+                const uint32_t phs = static_cast<uint32_t>(it / nst) & 1u;
+                if (!mbar_wait(&empty[s], phs ^ 1u, abort_flag, p.status, lim)) {
                     ok = false;
                     break;
                 }
-                tile_ring[ts] = tile < ntiles ? tile : -1;
-                mbar_arrive(&tile_full[ts]);
-                if (tile >= ntiles) break;
-                next = gridDim.x + static_cast<long>(atomicAdd(p.tile_next, 1));
-                const Tile tc = decode_tile(p, gm, tile, ph, ns, nblocks);
-                const GemmSide& sd = p.side[tc.side];
-                const int row0 = tc.b * kBlockM;
-                // the down side reads act rows, complete once the block's
-                // gate_up tiles all are
-                if (tc.side == 1 && !wait_counter(p.act_done + tc.b, gm.ncb0, abort_flag, p.status, lim)) {
-                    ok = false;
-                    break;
-                }
-                // only the block's real rows are loaded; the MMA rows past
-                // them hold stale data and feed only discarded output rows
-                const int nbox = (p.blk_rows[tc.b] + kRowBox - 1) / kRowBox;
-                const bool full_block = nbox * kRowBox == kBlockM;
-                const uint32_t a_bytes = static_cast<uint32_t>(nbox) * kRowBox * kBlockK * 2;
-                const int32_t* lora_list = p.blk_lora + static_cast<long>(tc.b) * p.cap;
-                const int nk = (sd.K + kBlockK - 1) / kBlockK;
-                const CUtensorMap* bmap = gm.bn == kBN ? &sd.tm_b : &sd.tm_b_n;
-                const CUtensorMap* lbmap = gm.bn == kBN ? &sd.tm_lb : &sd.tm_lb_n;
-                if (tc.shrink) {
-                    // several K-chunks per stage: the shrink's operands are
-                    // small, and a stage of one chunk leaves the copy
-                    // engine latency-bound
-                    const uint32_t b_bytes = static_cast<uint32_t>(tc.g) * rp * kBlockK * 2;
-                    const uint32_t chunk = a_bytes + b_bytes;
-                    const int cps = shrink_chunks(a_bytes, b_bytes, stb);
-                    for (int kb0 = 0; kb0 < nk; kb0 += cps, ++it) {
-                        const int s = static_cast<int>(it % nst);
-                        const uint32_t phs = static_cast<uint32_t>(it / nst) & 1u;
-                        if (!mbar_wait(&empty[s], phs ^ 1u, abort_flag, p.status, lim)) {
-                            ok = false;
-                            break;
-                        }
-                        const int nc = min(cps, nk - kb0);
-                        mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(nc) * chunk);
-                        for (int c = 0; c < nc; ++c) {
-                            uint8_t* ca = smem + s * stb + c * chunk;
-                            uint8_t* cb = ca + a_bytes;
-                            const int k0 = (kb0 + c) * kBlockK;
-                            for (int i = 0; i < tc.g; ++i)
-                                tma_load_3d(cb + i * rp * kBlockK * 2, &sd.tm_sa, &full[s], k0, 0,
-                                            lora_list[tc.i0 + i] * p.E_tot + tc.e);
-                            if (full_block)
-                                tma_load_2d(ca, &sd.tm_a_full, &full[s], k0, row0);
-                            else
-                                for (int i = 0; i < nbox; ++i)
-                                    tma_load_2d(ca + i * kRowBox * kBlockK * 2, &sd.tm_a, &full[s], k0,
-                                                row0 + i * kRowBox);
-                        }
-                    }
-                    continue;
-                }
-                for (int kb = 0; kb < nk; ++kb, ++it) {
-                    const int s = static_cast<int>(it % nst);
-                    const uint32_t phs = static_cast<uint32_t>(it / nst) & 1u;
-                    if (!mbar_wait(&empty[s], phs ^ 1u, abort_flag, p.status, lim)) {
-                        ok = false;
-                        break;
-                    }
-                    uint8_t* sa = smem + s * stb;
-                    uint8_t* sb = sa + ab;
-                    const int k0 = kb * kBlockK;
-                    if (tc.kind == kGateUp) {
-                        mbar_arrive_expect_tx(&full[s], a_bytes + gm.bn * kBlockK * 2);
-                        tma_load_4d(sb, bmap, &full[s], k0, tc.cb * gm.half, 0, tc.e);
-                        tma_load_4d(sb + gm.half * kBlockK * 2, bmap, &full[s], k0, tc.cb * gm.half, 1, tc.e);
-                    } else {
-                        mbar_arrive_expect_tx(&full[s], a_bytes + gm.bn * kBlockK * 2);
-                        tma_load_3d(sb, bmap, &full[s], k0, tc.cb * gm.bn, tc.e);
-                    }
+                const int nc = min(cps, nk - kb0);
+                mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(nc) * chunk);
+                for (int c = 0; c < nc; ++c) {
+                    uint8_t* ca = smem + s * stb + c * chunk;
+                    uint8_t* cb = ca + a_bytes;
+                    const int k0 = (kb0 + c) * kBlockK;
+                    for (int i = 0; i < tc.g; ++i)
+                        tma_load_3d(cb + i * rp * kBlockK * 2, &sd.tm_sa, &full[s], k0, 0,
+                                    lora_list[tc.i0 + i] * p.E_tot + tc.e);
                     if (full_block)
-                        tma_load_2d(sa, &sd.tm_a_full, &full[s], k0, row0);
+                        tma_load_2d(ca, &sd.tm_a_full, &full[s], k0, row0);
                     else
                         for (int i = 0; i < nbox; ++i)
-                            tma_load_2d(sa + i * kRowBox * kBlockK * 2, &sd.tm_a, &full[s], k0, row0 + i * kRowBox);
-                }
-                if (!ok || !p.has_lora) continue;
-                const int nad = p.blk_nad[tc.b];
-                if (nad == 0) continue;
-                // the expand needs every shrink tile of this block and side
-                if (!wait_counter(sd.done + tc.b, (nad + p.gsize - 1) / p.gsize, abort_flag, p.status, lim)) {
-                    ok = false;
-                    break;
-                }
-                const int lt0 = p.blk_lt_start[tc.b];
-                for (int i = 0; i < nad; ++i, ++it) {
-                    const int s = static_cast<int>(it % nst);
-                    const uint32_t phs = static_cast<uint32_t>(it / nst) & 1u;
-                    if (!mbar_wait(&empty[s], phs ^ 1u, abort_flag, p.status, lim)) {
-                        ok = false;
-                        break;
-                    }
-                    uint8_t* sa = smem + s * stb;
-                    uint8_t* sb = sa + ab;
-                    const int le = lora_list[i] * p.E_tot + tc.e;
-                    mbar_arrive_expect_tx(&full[s], a_bytes + gm.bn * kBlockK * 2);
-                    if (tc.kind == kGateUp) {
-                        tma_load_4d(sb, lbmap, &full[s], 0, tc.cb * gm.half, 0, le);
-                        tma_load_4d(sb + gm.half * kBlockK * 2, lbmap, &full[s], 0, tc.cb * gm.half, 1, le);
-                    } else {
-                        tma_load_3d(sb, lbmap, &full[s], 0, tc.cb * gm.bn, le);
-                    }
-                    if (full_block)
-                        tma_load_2d(sa, &sd.tm_t_full, &full[s], 0, (lt0 + i) * kBlockM);
-                    else
-                        for (int j = 0; j < nbox; ++j)
-                            tma_load_2d(sa + j * kRowBox * kBlockK * 2, &sd.tm_t, &full[s], 0,
-                                        (lt0 + i) * kBlockM + j * kRowBox);
+                            tma_load_2d(ca + i * kRowBox * kBlockK * 2, &sd.tm_a, &full[s], k0,
+                                        row0 + i * kRowBox);
                 }
             }
-            if (!ok) {
-                // the last min(it, nst) stages issued, walking back from the ring position
-                for (long j = it > nst ? it - nst : 0; j < it; ++j)
-                    drain_wait(&full[j % nst], static_cast<uint32_t>(j / nst) & 1u, lim);
-            }
+            continue;
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            const uint32_t idesc_base = umma_idesc_bf16(128, gm.bn);
-            long it = 0;  // stages consumed
-            bool ok = true;
-            for (int lt = 0; ok; ++lt) {
-                const int ts = lt % kTileRing;
-                if (!mbar_wait(&tile_full[ts], static_cast<uint32_t>(lt / kTileRing) & 1u, abort_flag, p.status, lim)) break;
-                const long tile = tile_ring[ts];
-                mbar_arrive(&tile_empty[ts]);
-                if (tile < 0) break;
-                const Tile tc = decode_tile(p, gm, tile, ph, ns, nblocks);
-                const int nk = (p.side[tc.side].K + kBlockK - 1) / kBlockK;
-                const int acc = lt & 1;
-                if (!mbar_wait(&tempty[acc], (static_cast<uint32_t>(lt >> 1) & 1u) ^ 1u, abort_flag, p.status, lim)) {
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+            const int s = static_cast<int>(it % nst);
+            const uint32_t phs = static_cast<uint32_t>(it / nst) & 1u;
+            if (!mbar_wait(&empty[s], phs ^ 1u, abort_flag, p.status, lim)) {
+                ok = false;
+                break;
+            }
+            uint8_t* sa = smem + s * stb;
+            uint8_t* sb = sa + ab;
+            const int k0 = kb * kBlockK;
+            if (tc.kind == kGateUp) {
+                mbar_arrive_expect_tx(&full[s], a_bytes + gm.bn * kBlockK * 2);
+                tma_load_4d(sb, bmap, &full[s], k0, tc.cb * gm.half, 0, tc.e);
+                tma_load_4d(sb + gm.half * kBlockK * 2, bmap, &full[s], k0, tc.cb * gm.half, 1, tc.e);
+            } else {
+                mbar_arrive_expect_tx(&full[s], a_bytes + gm.bn * kBlockK * 2);
+                tma_load_3d(sb, bmap, &full[s], k0, tc.cb * gm.bn, tc.e);
+            }
+            if (full_block)
+                tma_load_2d(sa, &sd.tm_a_full, &full[s], k0, row0);
+            else
+                for (int i = 0; i < nbox; ++i)
+                    tma_load_2d(sa + i * kRowBox * kBlockK * 2, &sd.tm_a, &full[s], k0, row0 + i * kRowBox);
+        }
+        if (!ok || !p.has_lora) continue;
+        const int nad = p.blk_nad[tc.b];
+        if (nad == 0) continue;
+        // the expand needs every shrink tile of this block and side
+        if (!wait_counter(sd.done + tc.b, (nad + p.gsize - 1) / p.gsize, abort_flag, p.status, lim)) {
+            ok = false;
+            break;
+        }
+        const int lt0 = p.blk_lt_start[tc.b];
+        for (int i = 0; i < nad; ++i, ++it) {
+            const int s = static_cast<int>(it % nst);
+            const uint32_t phs = static_cast<uint32_t>(it / nst) & 1u;
+            if (!mbar_wait(&empty[s], phs ^ 1u, abort_flag, p.status, lim)) {
+                ok = false;
+                break;
+            }
+            uint8_t* sa = smem + s * stb;
+            uint8_t* sb = sa + ab;
+            const int le = lora_list[i] * p.E_tot + tc.e;
+            mbar_arrive_expect_tx(&full[s], a_bytes + gm.bn * kBlockK * 2);
+            if (tc.kind == kGateUp) {
+                tma_load_4d(sb, lbmap, &full[s], 0, tc.cb * gm.half, 0, le);
+                tma_load_4d(sb + gm.half * kBlockK * 2, lbmap, &full[s], 0, tc.cb * gm.half, 1, le);
+            } else {
+                tma_load_3d(sb, lbmap, &full[s], 0, tc.cb * gm.bn, le);
+            }
+            if (full_block)
+                tma_load_2d(sa, &sd.tm_t_full, &full[s], 0, (lt0 + i) * kBlockM);
+            else
+                for (int j = 0; j < nbox; ++j)
+                    tma_load_2d(sa + j * kRowBox * kBlockK * 2, &sd.tm_t, &full[s], 0,
+                                (lt0 + i) * kBlockM + j * kRowBox);
+        }
+    }
+    if (!ok) {
+        // the last min(it, nst) stages issued, walking back from the ring position
+        for (long j = it > nst ? it - nst : 0; j < it; ++j)
+            drain_wait(&full[j % nst], static_cast<uint32_t>(j / nst) & 1u, lim);
+    }
+}
+
+// MMA issuer (one thread), over the same ring geometry as the producer.
+template <int nst, uint32_t stb, uint32_t ab>
+__device__ __forceinline__ void mma_issuer(const Ctx& c) {
+    const GemmParams& p = *c.p;
+    uint64_t* const full = c.L.full;
+    uint64_t* const empty = c.L.empty;
+    uint64_t* const tfull = c.L.tfull;
+    uint64_t* const tempty = c.L.tempty;
+    uint64_t* const drain = c.L.drain;
+    uint64_t* const tile_full = c.L.tile_full;
+    uint64_t* const tile_empty = c.L.tile_empty;
+    long long* const tile_ring = c.L.tile_ring;
+    volatile int* const abort_flag = c.L.abort_flag;
+    const long long lim = c.lim;
+    const int nblocks = c.nblocks;
+    const int ns = c.ns;
+    const Geom& gm = c.gm;
+    const Phases& ph = c.ph;
+    const int rp = c.rp;
+    const int lora_ksteps = c.lora_ksteps;
+    uint8_t* const smem = c.smem;
+    const uint32_t tmem_base = c.tmem_base;
+    const uint32_t idesc_base = umma_idesc_bf16(128, gm.bn);
+    long it = 0;  // stages consumed
+    bool ok = true;
+    for (int lt = 0; ok; ++lt) {
+        const int ts = lt % kTileRing;
+        if (!mbar_wait(&tile_full[ts], static_cast<uint32_t>(lt / kTileRing) & 1u, abort_flag, p.status, lim)) break;
+        const long tile = tile_ring[ts];
+        mbar_arrive(&tile_empty[ts]);
+        if (tile < 0) break;
+        const Tile tc = decode_tile(p, gm, tile, ph, ns, nblocks);
+        const int nk = (p.side[tc.side].K + kBlockK - 1) / kBlockK;
+        const int acc = lt & 1;
+        if (!mbar_wait(&tempty[acc], (static_cast<uint32_t>(lt >> 1) & 1u) ^ 1u, abort_flag, p.status, lim)) {
+            ok = false;
+            break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kAccCols);
+        // a down tile whose slab runs past H multiplies only the
+        // valid weight rows (rounded up to the MMA's N granule of 16)
+        const int dn_valid = p.side[1].n_out - tc.cb * gm.bn;
+        const uint32_t idesc = tc.shrink ? umma_idesc_bf16(128, tc.g * rp)
+                               : (tc.kind == kDown && dn_valid < gm.bn)
+                                   ? umma_idesc_bf16(128, (dn_valid + 15) / 16 * 16)
+                                   : idesc_base;
+        if (tc.shrink) {
+            // the producer's packing: cps K-chunks of (A rows, adapter rows) per stage
+            const int nbox = (p.blk_rows[tc.b] + kRowBox - 1) / kRowBox;
+            const uint32_t a_bytes = nbox * kRowBox == kBlockM ? static_cast<uint32_t>(kATileBytes)
+                                                               : static_cast<uint32_t>(nbox) * kRowBox * kBlockK * 2;
+            const uint32_t chunk = a_bytes + static_cast<uint32_t>(tc.g) * rp * kBlockK * 2;
+            const int cps = shrink_chunks(a_bytes, chunk - a_bytes, stb);
+            for (int kb0 = 0; kb0 < nk; kb0 += cps, ++it) {
+                const int s = static_cast<int>(it % nst);
+                if (!mbar_wait(&full[s], static_cast<uint32_t>(it / nst) & 1u, abort_flag, p.status, lim)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kAccCols);
-                // a down tile whose slab runs past H multiplies only the
-                // valid weight rows (rounded up to the MMA's N granule of 16)
-                const int dn_valid = p.side[1].n_out - tc.cb * gm.bn;
-                const uint32_t idesc = tc.shrink ? umma_idesc_bf16(128, tc.g * rp)
-                                       : (tc.kind == kDown && dn_valid < gm.bn)
-                                           ? umma_idesc_bf16(128, (dn_valid + 15) / 16 * 16)
-                                           : idesc_base;
-                if (tc.shrink) {
-                    // the producer's packing: cps K-chunks of (A rows, adapter rows) per stage
-                    const int nbox = (p.blk_rows[tc.b] + kRowBox - 1) / kRowBox;
-                    const uint32_t a_bytes = nbox * kRowBox == kBlockM ? static_cast<uint32_t>(kATileBytes)
-                                                                       : static_cast<uint32_t>(nbox) * kRowBox * kBlockK * 2;
-                    const uint32_t chunk = a_bytes + static_cast<uint32_t>(tc.g) * rp * kBlockK * 2;
-                    const int cps = shrink_chunks(a_bytes, chunk - a_bytes, stb);
-                    for (int kb0 = 0; kb0 < nk; kb0 += cps, ++it) {
-                        const int s = static_cast<int>(it % nst);
-                        if (!mbar_wait(&full[s], static_cast<uint32_t>(it / nst) & 1u, abort_flag, p.status, lim)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const int nc = min(cps, nk - kb0);
-                        for (int c = 0; c < nc; ++c) {
-                            const uint32_t a_addr = smem_u32(smem + s * stb + c * chunk);
-                            const uint64_t ad = umma_desc_sw128(a_addr);
-                            const uint64_t bd = umma_desc_sw128(a_addr + a_bytes);
-#pragma unroll
-                            for (int k = 0; k < kBlockK / 16; ++k)
-                                umma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (kb0 | c | k) != 0 ? 1u : 0u);
-                        }
-                        umma_commit(&empty[s]);
-                    }
-                    if (!ok) break;
-                    umma_commit(&tfull[acc]);
-                    continue;
-                }
-                for (int kb = 0; kb < nk; ++kb, ++it) {
-                    const int s = static_cast<int>(it % nst);
-                    if (!mbar_wait(&full[s], static_cast<uint32_t>(it / nst) & 1u, abort_flag, p.status, lim)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t a_addr = smem_u32(smem + s * stb);
+                const int nc = min(cps, nk - kb0);
+                for (int c = 0; c < nc; ++c) {
+                    const uint32_t a_addr = smem_u32(smem + s * stb + c * chunk);
                     const uint64_t ad = umma_desc_sw128(a_addr);
-                    const uint64_t bd = umma_desc_sw128(a_addr + ab);
+                    const uint64_t bd = umma_desc_sw128(a_addr + a_bytes);
 #pragma unroll
                     for (int k = 0; k < kBlockK / 16; ++k)
-                        umma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
-                    umma_commit(&empty[s]);
+                        umma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (kb0 | c | k) != 0 ? 1u : 0u);
                 }
-                if (!ok) break;
-                if (!tc.shrink && p.has_lora) {
-                    const int nad = p.blk_nad[tc.b];
-                    for (int i = 0; i < nad; ++i, ++it) {
-                        const int s = static_cast<int>(it % nst);
-                        if (!mbar_wait(&full[s], static_cast<uint32_t>(it / nst) & 1u, abort_flag, p.status, lim)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t a_addr = smem_u32(smem + s * stb);
-                        const uint64_t ad = umma_desc_sw128(a_addr);
-                        const uint64_t bd = umma_desc_sw128(a_addr + ab);
-                        for (int k = 0; k < lora_ksteps; ++k) umma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, 1u);
-                        umma_commit(&empty[s]);
-                    }
-                    if (!ok) break;
-                }
-                umma_commit(&tfull[acc]);
+                umma_commit(&empty[s]);
             }
-            // every MMA issued above completes before TMEM is released
-            umma_commit(drain);
-            drain_wait(drain, 0, lim);
+            if (!ok) break;
+            umma_commit(&tfull[acc]);
+            continue;
         }
-    } else {
-        // --------------------------------------------------------- epilogue
-        const int q = warp & 3;  // TMEM lane quarter this warp may access
-        const int row = q * 32 + lane;
-        uint32_t npub = 0;
-        for (int lt = 0;; ++lt) {
-            const int ts = lt % kTileRing;
-            if (!mbar_wait(&tile_full[ts], static_cast<uint32_t>(lt / kTileRing) & 1u, abort_flag, p.status, lim)) break;
-            const long tile = tile_ring[ts];
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&tile_empty[ts]);
-            if (tile < 0) break;
-            const Tile tc = decode_tile(p, gm, tile, ph, ns, nblocks);
-            const GemmSide& sd = p.side[tc.side];
-            const int acc = lt & 1;
-            if (!mbar_wait(&tfull[acc], static_cast<uint32_t>(lt >> 1) & 1u, abort_flag, p.status, lim)) break;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+            const int s = static_cast<int>(it % nst);
+            if (!mbar_wait(&full[s], static_cast<uint32_t>(it / nst) & 1u, abort_flag, p.status, lim)) {
+                ok = false;
+                break;
+            }
             tc_fence_after();
-            const uint32_t tb = tmem_base + static_cast<uint32_t>(acc * kAccCols) +
-                                (static_cast<uint32_t>(q * 32) << 16);
-            const int prow = tc.b * kBlockM + row;
-            int32_t* publish = nullptr;  // counter to bump once all 128 threads wrote
-            if (tc.shrink) {
-                const int my_l = row < p.blk_rows[tc.b] ? p.lora_of[prow] : -1;
-                const int32_t* lora_list = p.blk_lora + static_cast<long>(tc.b) * p.cap;
-                const int lt0 = p.blk_lt_start[tc.b] + tc.i0;
-                for (int i = 0; i < tc.g; ++i) {
-                    if (!MLORA_IN_BOUNDS(lt0 + i < p.lt_cap, p.status)) break;
-                    const bool mine = my_l == lora_list[tc.i0 + i];
-                    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(sd.lora_t) +
-                                         (static_cast<size_t>(lt0 + i) * kBlockM + row) * kLoraTileCols;
-                    for (int c = 0; c < kLoraTileCols; c += 16) {
-                        float v[16];
+            const uint32_t a_addr = smem_u32(smem + s * stb);
+            const uint64_t ad = umma_desc_sw128(a_addr);
+            const uint64_t bd = umma_desc_sw128(a_addr + ab);
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) v[j] = 0.f;
-                        if (c < rp) tmem_ld16(tb + i * rp + c, v);
-                        float o[16];
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) o[j] = (mine && c + j < p.rank) ? p.scaling * v[j] : 0.f;
-                        uint4 w0, w1;
-                        w0.x = pack_bf16x2(o[0], o[1]);
-                        w0.y = pack_bf16x2(o[2], o[3]);
-                        w0.z = pack_bf16x2(o[4], o[5]);
-                        w0.w = pack_bf16x2(o[6], o[7]);
-                        w1.x = pack_bf16x2(o[8], o[9]);
-                        w1.y = pack_bf16x2(o[10], o[11]);
-                        w1.z = pack_bf16x2(o[12], o[13]);
-                        w1.w = pack_bf16x2(o[14], o[15]);
-                        reinterpret_cast<uint4*>(dst + c)[0] = w0;
-                        reinterpret_cast<uint4*>(dst + c)[1] = w1;
-                    }
+            for (int k = 0; k < kBlockK / 16; ++k)
+                umma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+            umma_commit(&empty[s]);
+        }
+        if (!ok) break;
+        if (!tc.shrink && p.has_lora) {
+            const int nad = p.blk_nad[tc.b];
+            for (int i = 0; i < nad; ++i, ++it) {
+                const int s = static_cast<int>(it % nst);
+                if (!mbar_wait(&full[s], static_cast<uint32_t>(it / nst) & 1u, abort_flag, p.status, lim)) {
+                    ok = false;
+                    break;
                 }
-                publish = sd.done + tc.b;
-            } else if (tc.kind == kGateUp) {
-                const bool real = MLORA_IN_BOUNDS(prow < p.pad_cap, p.status) && p.sorted_ids[prow] < p.S;
-                const int j0 = tc.cb * gm.half;
-                __nv_bfloat16* act = static_cast<__nv_bfloat16*>(sd.out) + static_cast<size_t>(prow) * sd.n_out;
-                for (int c = 0; c < gm.half; c += 32) {
-                    if (j0 + c >= sd.n_out) break;
-                    float g[32], u[32];
-                    tmem_ld32(tb + c, g);
-                    tmem_ld32(tb + gm.half + c, u);
-                    if (real) {
+                tc_fence_after();
+                const uint32_t a_addr = smem_u32(smem + s * stb);
+                const uint64_t ad = umma_desc_sw128(a_addr);
+                const uint64_t bd = umma_desc_sw128(a_addr + ab);
+                for (int k = 0; k < lora_ksteps; ++k) umma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, 1u);
+                umma_commit(&empty[s]);
+            }
+            if (!ok) break;
+        }
+        umma_commit(&tfull[acc]);
+    }
+    // every MMA issued above completes before TMEM is released
+    umma_commit(drain);
+    drain_wait(drain, 0, lim);
+}
+
+// Epilogue (warps 2-5): drains the TMEM accumulators, writes shrink tiles,
+// act rows or slot rows and publishes the per-block counters.
+__device__ __forceinline__ void epilogue(const Ctx& c) {
+    const GemmParams& p = *c.p;
+    uint64_t* const tfull = c.L.tfull;
+    uint64_t* const tempty = c.L.tempty;
+    uint64_t* const pub = c.L.pub;
+    uint64_t* const tile_full = c.L.tile_full;
+    uint64_t* const tile_empty = c.L.tile_empty;
+    long long* const tile_ring = c.L.tile_ring;
+    volatile int* const abort_flag = c.L.abort_flag;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const long long lim = c.lim;
+    const int nblocks = c.nblocks;
+    const int ns = c.ns;
+    const Geom& gm = c.gm;
+    const Phases& ph = c.ph;
+    const int rp = c.rp;
+    const uint32_t tmem_base = c.tmem_base;
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int row = q * 32 + lane;
+    uint32_t npub = 0;
+    for (int lt = 0;; ++lt) {
+        const int ts = lt % kTileRing;
+        if (!mbar_wait(&tile_full[ts], static_cast<uint32_t>(lt / kTileRing) & 1u, abort_flag, p.status, lim)) break;
+        const long tile = tile_ring[ts];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tile_empty[ts]);
+        if (tile < 0) break;
+        const Tile tc = decode_tile(p, gm, tile, ph, ns, nblocks);
+        const GemmSide& sd = p.side[tc.side];
+        const int acc = lt & 1;
+        if (!mbar_wait(&tfull[acc], static_cast<uint32_t>(lt >> 1) & 1u, abort_flag, p.status, lim)) break;
+        tc_fence_after();
+        const uint32_t tb = tmem_base + static_cast<uint32_t>(acc * kAccCols) +
+                            (static_cast<uint32_t>(q * 32) << 16);
+        const int prow = tc.b * kBlockM + row;
+        int32_t* publish = nullptr;  // counter to bump once all 128 threads wrote
+        if (tc.shrink) {
+            const int my_l = row < p.blk_rows[tc.b] ? p.lora_of[prow] : -1;
+            const int32_t* lora_list = p.blk_lora + static_cast<long>(tc.b) * p.cap;
+            const int lt0 = p.blk_lt_start[tc.b] + tc.i0;
+            for (int i = 0; i < tc.g; ++i) {
+                if (!MLORA_IN_BOUNDS(lt0 + i < p.lt_cap, p.status)) break;
+                const bool mine = my_l == lora_list[tc.i0 + i];
+                __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(sd.lora_t) +
+                                     (static_cast<size_t>(lt0 + i) * kBlockM + row) * kLoraTileCols;
+                for (int c = 0; c < kLoraTileCols; c += 16) {
+                    float v[16];
 #pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            const int col = j0 + c + 8 * v;
-                            if (col < sd.n_out) {
-                                uint4 o;
-                                o.x = pack_bf16x2(silu(g[8 * v + 0]) * u[8 * v + 0], silu(g[8 * v + 1]) * u[8 * v + 1]);
-                                o.y = pack_bf16x2(silu(g[8 * v + 2]) * u[8 * v + 2], silu(g[8 * v + 3]) * u[8 * v + 3]);
-                                o.z = pack_bf16x2(silu(g[8 * v + 4]) * u[8 * v + 4], silu(g[8 * v + 5]) * u[8 * v + 5]);
-                                o.w = pack_bf16x2(silu(g[8 * v + 6]) * u[8 * v + 6], silu(g[8 * v + 7]) * u[8 * v + 7]);
-                                *reinterpret_cast<uint4*>(act + col) = o;
-                            }
-                        }
-                    }
+                    for (int j = 0; j < 16; ++j) v[j] = 0.f;
+                    if (c < rp) tmem_ld16(tb + i * rp + c, v);
+                    float o[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) o[j] = (mine && c + j < p.rank) ? p.scaling * v[j] : 0.f;
+                    uint4 w0, w1;
+                    w0.x = pack_bf16x2(o[0], o[1]);
+                    w0.y = pack_bf16x2(o[2], o[3]);
+                    w0.z = pack_bf16x2(o[4], o[5]);
+                    w0.w = pack_bf16x2(o[6], o[7]);
+                    w1.x = pack_bf16x2(o[8], o[9]);
+                    w1.y = pack_bf16x2(o[10], o[11]);
+                    w1.z = pack_bf16x2(o[12], o[13]);
+                    w1.w = pack_bf16x2(o[14], o[15]);
+                    reinterpret_cast<uint4*>(dst + c)[0] = w0;
+                    reinterpret_cast<uint4*>(dst + c)[1] = w1;
                 }
-                publish = p.act_done + tc.b;
-            } else {
-                const int f = MLORA_IN_BOUNDS(prow < p.pad_cap, p.status) ? p.sorted_ids[prow] : p.S;
-                const bool real = f < p.S;
-                const int o0 = tc.cb * gm.bn;
-                __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(sd.out) + static_cast<size_t>(real ? f : 0) * sd.n_out;
-                for (int c = 0; c < gm.bn; c += 32) {
-                    if (o0 + c >= sd.n_out) break;
-                    float v[32];
-                    tmem_ld32(tb + c, v);
-                    if (real) {
+            }
+            publish = sd.done + tc.b;
+        } else if (tc.kind == kGateUp) {
+            const bool real = MLORA_IN_BOUNDS(prow < p.pad_cap, p.status) && p.sorted_ids[prow] < p.S;
+            const int j0 = tc.cb * gm.half;
+            __nv_bfloat16* act = static_cast<__nv_bfloat16*>(sd.out) + static_cast<size_t>(prow) * sd.n_out;
+            for (int c = 0; c < gm.half; c += 32) {
+                if (j0 + c >= sd.n_out) break;
+                float g[32], u[32];
+                tmem_ld32(tb + c, g);
+                tmem_ld32(tb + gm.half + c, u);
+                if (real) {
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const int col = o0 + c + 8 * j;
-                            if (col < sd.n_out) {
-                                uint4 o;
-                                o.x = pack_bf16x2(v[8 * j + 0], v[8 * j + 1]);
-                                o.y = pack_bf16x2(v[8 * j + 2], v[8 * j + 3]);
-                                o.z = pack_bf16x2(v[8 * j + 4], v[8 * j + 5]);
-                                o.w = pack_bf16x2(v[8 * j + 6], v[8 * j + 7]);
-                                *reinterpret_cast<uint4*>(dst + col) = o;
-                            }
+                    for (int v = 0; v < 4; ++v) {
+                        const int col = j0 + c + 8 * v;
+                        if (col < sd.n_out) {
+                            uint4 o;
+                            o.x = pack_bf16x2(silu(g[8 * v + 0]) * u[8 * v + 0], silu(g[8 * v + 1]) * u[8 * v + 1]);
+                            o.y = pack_bf16x2(silu(g[8 * v + 2]) * u[8 * v + 2], silu(g[8 * v + 3]) * u[8 * v + 3]);
+                            o.z = pack_bf16x2(silu(g[8 * v + 4]) * u[8 * v + 4], silu(g[8 * v + 5]) * u[8 * v + 5]);
+                            o.w = pack_bf16x2(silu(g[8 * v + 6]) * u[8 * v + 6], silu(g[8 * v + 7]) * u[8 * v + 7]);
+                            *reinterpret_cast<uint4*>(act + col) = o;
                         }
                     }
                 }
             }
-            tc_fence_before();
-            mbar_arrive(&tempty[acc]);
-            if (publish) {
-                // other CTAs read what this tile wrote with TMA: every thread
-                // orders its writes for the async proxy and arrives
-                // (release, CTA scope); one thread waits (bounded, acquire)
-                // for all 128, then a GPU-scope fence -- cumulative over the
-                // writes it has synchronised with -- and the counter bump
-                asm volatile("fence.proxy.async.global;" ::: "memory");
-                mbar_arrive(pub);
-                if (warp == 2 && lane == 0) {
-                    if (mbar_wait(pub, npub & 1u, abort_flag, p.status, lim)) {
-                        __threadfence();
-                        atomicAdd(publish, 1);
+            publish = p.act_done + tc.b;
+        } else {
+            const int f = MLORA_IN_BOUNDS(prow < p.pad_cap, p.status) ? p.sorted_ids[prow] : p.S;
+            const bool real = f < p.S;
+            const int o0 = tc.cb * gm.bn;
+            __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(sd.out) + static_cast<size_t>(real ? f : 0) * sd.n_out;
+            for (int c = 0; c < gm.bn; c += 32) {
+                if (o0 + c >= sd.n_out) break;
+                float v[32];
+                tmem_ld32(tb + c, v);
+                if (real) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int col = o0 + c + 8 * j;
+                        if (col < sd.n_out) {
+                            uint4 o;
+                            o.x = pack_bf16x2(v[8 * j + 0], v[8 * j + 1]);
+                            o.y = pack_bf16x2(v[8 * j + 2], v[8 * j + 3]);
+                            o.z = pack_bf16x2(v[8 * j + 4], v[8 * j + 5]);
+                            o.w = pack_bf16x2(v[8 * j + 6], v[8 * j + 7]);
+                            *reinterpret_cast<uint4*>(dst + col) = o;
+                        }
                     }
                 }
-                ++npub;
             }
+        }
+        tc_fence_before();
+        mbar_arrive(&tempty[acc]);
+        if (publish) {
+            // other CTAs read what this tile wrote with TMA: every thread
+            // orders its writes for the async proxy and arrives
+            // (release, CTA scope); one thread waits (bounded, acquire)
+            // for all 128, then a GPU-scope fence -- cumulative over the
+            // writes it has synchronised with -- and the counter bump
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            mbar_arrive(pub);
+            if (warp == 2 && lane == 0) {
+                if (mbar_wait(pub, npub & 1u, abort_flag, p.status, lim)) {
+                    __threadfence();
+                    atomicAdd(publish, 1);
+                }
+            }
+            ++npub;
         }
     }
 }
@@ -679,13 +730,29 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
     // everything above overlapped the previous kernel in the stream
     griddep_wait();
 
+    const Ctx c(p, smem, tmem_base);
     // ring geometry of this launch (the same in every CTA): when no expert
     // has more than one 32-row box of slots, A stages shrink to 4 KiB and
-    // the ring holds 6 stages instead of 4
-    if (*p.max_rows <= kRowBox)
-        experts_run<kSmallStages, kSmallStageBytes, kSmallATileBytes>(p, smem, tmem_base);
-    else
-        experts_run<kStages, kStageBytes, kATileBytes>(p, smem, tmem_base);
+    // the ring holds 6 stages instead of 4.  Only the two ring roles are
+    // compiled per geometry; the epilogue exists once.
+    const bool small_a = *p.max_rows <= kRowBox;
+    if (warp == 0) {
+        if ((threadIdx.x & 31) == 0) {
+            if (small_a)
+                producer<kSmallStages, kSmallStageBytes, kSmallATileBytes>(c);
+            else
+                producer<kStages, kStageBytes, kATileBytes>(c);
+        }
+    } else if (warp == 1) {
+        if ((threadIdx.x & 31) == 0) {
+            if (small_a)
+                mma_issuer<kSmallStages, kSmallStageBytes, kSmallATileBytes>(c);
+            else
+                mma_issuer<kStages, kStageBytes, kATileBytes>(c);
+        }
+    } else {
+        epilogue(c);
+    }
 
     __syncthreads();
     if (warp == 1) {

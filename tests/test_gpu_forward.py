@@ -331,3 +331,54 @@ def test_ring_geometry_boundary(M, E, n_hot):
     y = gu.gpu_forward(d, torch.from_numpy(ids).cuda(), torch.from_numpy(w).cuda(), workspace=ws)
     assert ml.mlora_moe_read_status(ws) == 0
     gu.check_y(y, gu.oracle_forward(inp, ids, w), f"busiest expert {n_hot} slots")
+
+
+def test_graph_replay_switches_tile_geometry():
+    """One captured forward, replayed on routings that move the kernel
+    between its tile widths (wide/narrow, chosen from the padded block
+    count) and ring geometries (chosen from the busiest expert), all decided
+    on the device at each replay; every replay equals an eager call and the
+    oracle."""
+    M, E, k = 1024, 128, 2
+    s = wl.spec("tiny", M=M, H=64, I=136, E=E, top_k=k, L=3, r=16, seed=131)
+    inp = wl.make(s, device="cuda")
+    d = gu.DeviceInputs(inp)
+
+    def spread_over(n_e):
+        ids = ((np.arange(M)[:, None] * k + np.arange(k)[None, :]) % n_e).astype(np.int32)
+        return ids, np.full((M, k), 1.0 / k, np.float32)
+
+    routings = {
+        "wide, 4 KiB A stages": _hot_expert_ids(M, E, k, 32, seed=1),   # 128 blocks x 2 slabs, max 32 slots
+        "wide, 16 KiB A stages": _hot_expert_ids(M, E, k, 33, seed=2),  # max 33 slots
+        "narrow, 16 KiB A stages": spread_over(40),                     # 40 blocks, ~52 slots each
+        "narrow, 4 KiB A stages": spread_over(64),                      # 64 blocks, 32 slots each
+    }
+    ids = torch.empty((M, k), dtype=torch.int32, device="cuda")
+    w = torch.empty((M, k), dtype=torch.float32, device="cuda")
+    y = torch.empty((M, s.H), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(ml.mlora_moe_workspace_size(M, s.H, s.I, s.E_tot, s.K_total, s.L, s.r), dtype=torch.uint8,
+                     device="cuda")
+    first_ids, first_w = routings["wide, 4 KiB A stages"]
+    ids.copy_(torch.from_numpy(first_ids))
+    w.copy_(torch.from_numpy(first_w))
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        ml.mlora_moe_forward(d.x, d.w13, d.w2, d.A13, d.B13, d.A2, d.B2, d.idx, ids, w, s.scaling, y=y,
+                             workspace=ws, stream=stream)
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        ml.mlora_moe_forward(d.x, d.w13, d.w2, d.A13, d.B13, d.A2, d.B2, d.idx, ids, w, s.scaling, y=y,
+                             workspace=ws, stream=stream)
+    for label, (ids_h, w_h) in routings.items():
+        ids.copy_(torch.from_numpy(ids_h))
+        w.copy_(torch.from_numpy(w_h))
+        g.replay()
+        torch.cuda.synchronize()
+        assert ml.mlora_moe_read_status(ws) == 0, label
+        y_graph = y.clone()
+        y_eager = ml.mlora_moe_forward(d.x, d.w13, d.w2, d.A13, d.B13, d.A2, d.B2, d.idx, ids, w, s.scaling)
+        torch.cuda.synchronize()
+        assert torch.equal(y_graph, y_eager), label
+        gu.check_y(y_graph, gu.oracle_forward(inp, ids_h, w_h), label)

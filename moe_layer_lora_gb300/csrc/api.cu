@@ -287,13 +287,18 @@ mlora_status mlora_moe_forward(const void* x, const void* w13, const void* w2, c
         ok &= make_map(&dn.tm_a, ws.act, 2, da, sa, bx);
         ok &= make_map(&dn.tm_a_full, ws.act, 2, da, sa, bxf);
         const cuuint64_t d13[4] = {H_, I_, 2, E_}, s13[3] = {H_ * 2, I_ * H_ * 2, 2 * I_ * H_ * 2};
-        const cuuint32_t b13[4] = {64, 128, 1, 1}, b13n[4] = {64, 64, 1, 1};
-        ok &= make_map(&up.tm_b, w13, 4, d13, s13, b13);
-        ok &= make_map(&up.tm_b_n, w13, 4, d13, s13, b13n);
+        // a gate_up tile of width n takes n/2 gate and n/2 up rows, a down tile n rows
+        cuuint32_t b13[kTileWidths][4], b2[kTileWidths][3];
+        for (int wc = 0; wc < kTileWidths; ++wc) {
+            const cuuint32_t n = static_cast<cuuint32_t>(tile_width(wc));
+            b13[wc][0] = 64, b13[wc][1] = n / 2, b13[wc][2] = 1, b13[wc][3] = 1;
+            b2[wc][0] = 64, b2[wc][1] = n, b2[wc][2] = 1;
+        }
         const cuuint64_t d2[3] = {I_, H_, E_}, s2[2] = {I_ * 2, H_ * I_ * 2};
-        const cuuint32_t b2[3] = {64, 256, 1}, b2n[3] = {64, 128, 1};
-        ok &= make_map(&dn.tm_b, w2, 3, d2, s2, b2);
-        ok &= make_map(&dn.tm_b_n, w2, 3, d2, s2, b2n);
+        for (int wc = 0; wc < kTileWidths; ++wc) {
+            ok &= make_map(&up.tm_b[wc], w13, 4, d13, s13, b13[wc]);
+            ok &= make_map(&dn.tm_b[wc], w2, 3, d2, s2, b2[wc]);
+        }
         if (lora) {
             const cuuint64_t R = rank, LE = static_cast<cuuint64_t>(L) * E_tot;
             const cuuint32_t rp = static_cast<cuuint32_t>((rank + 15) / 16 * 16);
@@ -310,11 +315,11 @@ mlora_status mlora_moe_forward(const void* x, const void* w13, const void* w2, c
             ok &= make_map(&dn.tm_sa, A2, 3, dA2, sA2, bA);
             // expand weights: columns past the rank read as zero
             const cuuint64_t dB13[4] = {R, I_, 2, LE}, sB13[3] = {R * 2, I_ * R * 2, 2 * I_ * R * 2};
-            ok &= make_map(&up.tm_lb, B13, 4, dB13, sB13, b13);
-            ok &= make_map(&up.tm_lb_n, B13, 4, dB13, sB13, b13n);
             const cuuint64_t dB2[3] = {R, H_, LE}, sB2[2] = {R * 2, H_ * R * 2};
-            ok &= make_map(&dn.tm_lb, B2, 3, dB2, sB2, b2);
-            ok &= make_map(&dn.tm_lb_n, B2, 3, dB2, sB2, b2n);
+            for (int wc = 0; wc < kTileWidths; ++wc) {
+                ok &= make_map(&up.tm_lb[wc], B13, 4, dB13, sB13, b13[wc]);
+                ok &= make_map(&dn.tm_lb[wc], B2, 3, dB2, sB2, b2[wc]);
+            }
         }
     }
     if (!ok) return cuda_fail(cudaErrorInvalidValue, "tensor map encoding");

@@ -26,9 +26,10 @@
 //  3. down shrink tiles: T2_l = s * act A2_{l,e}^T, as in phase 1.
 //  4. down tiles: d = act W2_e^T over 256 output columns + the T2 expand;
 //     epilogue the slot's expert output in bf16.
-// Batches with fewer wide gate_up tiles than SMs use narrow tiles instead
-// (64 gate + 64 up rows, 128 down columns, N = 128) so that every SM
-// streams weights.  Shrink tiles pack up to four 64-wide K-chunks per stage.
+// Batches with few blocks take tiles of 192 or 128 weight rows instead
+// (N = 192 or 128; gate_up tiles half gate, half up rows) so that the
+// tiles of each phase fill the grid's SMs.  Shrink tiles pack up to four
+// 64-wide K-chunks per stage.
 //
 // A tile depends only on tiles of earlier phases of the same block, i.e.
 // on tiles with smaller indices.  Tiles are claimed in index order, every
@@ -125,19 +126,41 @@ struct Tile {
     int g;     // adapters in the group (shrink tiles)
 };
 
-// Tile width of a launch.  Wide tiles take 256 weight rows (gate_up: 128
-// gate + 128 up); when the batch has fewer wide gate_up tiles than the grid
-// has CTAs (a handful of tokens), every tile is narrow (128 rows: 64 gate +
-// 64 up), which doubles the tiles of each phase so that all SMs stream
-// weights (measured: shared-expert layer with one token 86 -> 82 us; with
-// 32 or more tokens narrow tiles were slower).  Every CTA derives the same
-// choice from the padded slot count.
+// Tile width of a launch: 256 weight rows (gate_up: 128 gate + 128 up),
+// 192 or 128, the same for every tile of the launch.  Every CTA derives it
+// from the padded slot count (choose_width).
 struct Geom {
+    int wc;      // width class: tile_width(wc) weight rows per tile
     int bn;      // weight rows per tile (MMA N)
     int half;    // gate (and up) rows of a gate_up tile
     int ncb0;    // column slabs per block, gate_up
     int ncb1;    // column slabs per block, down
 };
+
+// The tile width of a launch with nblocks blocks on a grid of `grid` CTAs.
+// One SM streams weights at a rate of its own (~44 GB/s measured, about
+// the HBM rate divided by the SM count), so a phase whose tiles do not fill
+// whole waves of the grid leaves HBM idle.  With at most two waves of wide
+// gate_up tiles, the width that minimises (waves of gate_up tiles) x (bytes
+// per gate_up tile) + the same for down is taken, the wider on a tie;
+// larger batches keep wide tiles.
+__device__ __forceinline__ int choose_width(int nblocks, int I, int H, long grid) {
+    const long wide = static_cast<long>(nblocks) * ((I + 127) / 128);
+    if (wide > 2 * grid) return 0;
+    int best = 0;
+    long best_cost = -1;
+    for (int wc = 0; wc < kTileWidths; ++wc) {
+        const int n = tile_width(wc);
+        const long tg = static_cast<long>(nblocks) * ((I + n / 2 - 1) / (n / 2));
+        const long td = static_cast<long>(nblocks) * ((H + n - 1) / n);
+        const long cost = ((tg + grid - 1) / grid) * n * static_cast<long>(H) + ((td + grid - 1) / grid) * n * static_cast<long>(I);
+        if (best_cost < 0 || cost < best_cost) {
+            best = wc;
+            best_cost = cost;
+        }
+    }
+    return best;
+}
 
 // Phase boundaries of the tile sequence.
 struct Phases {
@@ -246,8 +269,8 @@ struct Ctx {
         : p(&prm), smem(sm), L(sm), tmem_base(tmem), lim(prm.wait_limit) {
         nblocks = *prm.n_pad / kBlockM;
         ns = prm.has_lora ? *prm.gt_total : 0;
-        const bool narrow = static_cast<long>(nblocks) * prm.side[0].ncb < gridDim.x;
-        gm.bn = narrow ? kBN / 2 : kBN;
+        gm.wc = choose_width(nblocks, prm.side[0].n_out, prm.side[1].n_out, gridDim.x);
+        gm.bn = tile_width(gm.wc);
         gm.half = gm.bn / 2;
         gm.ncb0 = (prm.side[0].n_out + gm.half - 1) / gm.half;
         gm.ncb1 = (prm.side[1].n_out + gm.bn - 1) / gm.bn;
@@ -282,24 +305,30 @@ __device__ __forceinline__ void producer(const Ctx& c) {
     uint8_t* const smem = c.smem;
     long it = 0;  // stages issued
     bool ok = true;
-    long tile = blockIdx.x, next = 0;
+    long tile = blockIdx.x, next = -1;
+    // the next tile is claimed a few stages before this one's base loads
+    // are all issued: late enough that the CTA is about to be free (a
+    // claim at the start of a tile hands work to CTAs that will be busy
+    // for a whole tile while others idle), early enough that the atomic's
+    // latency hides behind the last loads
+    auto claim = [&]() {
+        if (next < 0) next = gridDim.x + static_cast<long>(atomicAdd(p.tile_next, 1));
+    };
     // test hook: a wait on a flag that nothing sets, which must end
     // in a reported timeout and a clean exit
     if (p.stall_flag && !wait_counter(p.stall_flag, 1, abort_flag, p.status, lim)) ok = false;
-    for (int jt = 0; ok; ++jt, tile = next) {
-        // hand the tile (or the end mark) to the MMA lane and the
-        // epilogue, then claim the next one; its index is needed
-        // only once this tile's loads are issued
+    for (int jt = 0; ok; ++jt, tile = next, next = -1) {
+        // hand the tile (or the end mark) to the MMA lane and the epilogue
         const int ts = jt % kTileRing;
         if (!mbar_wait(&tile_empty[ts], (static_cast<uint32_t>(jt / kTileRing) & 1u) ^ 1u, abort_flag,
                        p.status, lim)) {
             ok = false;
             break;
         }
-        tile_ring[ts] = tile < ntiles ? tile : -1;
+        const bool have = tile >= 0 && tile < ntiles;
+        tile_ring[ts] = have ? tile : -1;
         mbar_arrive(&tile_full[ts]);
-        if (tile >= ntiles) break;
-        next = gridDim.x + static_cast<long>(atomicAdd(p.tile_next, 1));
+        if (!have) break;
         const Tile tc = decode_tile(p, gm, tile, ph, ns, nblocks);
         const GemmSide& sd = p.side[tc.side];
         const int row0 = tc.b * kBlockM;
@@ -316,8 +345,8 @@ __device__ __forceinline__ void producer(const Ctx& c) {
         const uint32_t a_bytes = static_cast<uint32_t>(nbox) * kRowBox * kBlockK * 2;
         const int32_t* lora_list = p.blk_lora + static_cast<long>(tc.b) * p.cap;
         const int nk = (sd.K + kBlockK - 1) / kBlockK;
-        const CUtensorMap* bmap = gm.bn == kBN ? &sd.tm_b : &sd.tm_b_n;
-        const CUtensorMap* lbmap = gm.bn == kBN ? &sd.tm_lb : &sd.tm_lb_n;
+        const CUtensorMap* bmap = &sd.tm_b[gm.wc];
+        const CUtensorMap* lbmap = &sd.tm_lb[gm.wc];
         if (tc.shrink) {
             // several K-chunks per stage: the shrink's operands are
             // small, and a stage of one chunk leaves the copy
@@ -333,6 +362,7 @@ __device__ __forceinline__ void producer(const Ctx& c) {
                     break;
                 }
                 const int nc = min(cps, nk - kb0);
+                if (kb0 + nc >= nk) claim();
                 mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(nc) * chunk);
                 for (int c = 0; c < nc; ++c) {
                     uint8_t* ca = smem + s * stb + c * chunk;
@@ -358,6 +388,7 @@ __device__ __forceinline__ void producer(const Ctx& c) {
                 ok = false;
                 break;
             }
+            if (kb + 3 >= nk) claim();
             uint8_t* sa = smem + s * stb;
             uint8_t* sb = sa + ab;
             const int k0 = kb * kBlockK;
@@ -709,12 +740,10 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
         for (int sd = 0; sd < 2; ++sd) {
             prefetch_tensormap(&p.side[sd].tm_a);
             prefetch_tensormap(&p.side[sd].tm_a_full);
-            prefetch_tensormap(&p.side[sd].tm_b);
-            prefetch_tensormap(&p.side[sd].tm_b_n);
+            for (int wc = 0; wc < kTileWidths; ++wc) prefetch_tensormap(&p.side[sd].tm_b[wc]);
             if (p.has_lora) {
                 prefetch_tensormap(&p.side[sd].tm_sa);
-                prefetch_tensormap(&p.side[sd].tm_lb);
-                prefetch_tensormap(&p.side[sd].tm_lb_n);
+                for (int wc = 0; wc < kTileWidths; ++wc) prefetch_tensormap(&p.side[sd].tm_lb[wc]);
                 prefetch_tensormap(&p.side[sd].tm_t);
                 prefetch_tensormap(&p.side[sd].tm_t_full);
             }

@@ -13,6 +13,8 @@ namespace mlora {
 
 constexpr int kBlockM = MLORA_FORWARD_BLOCK_M;  // token rows per GEMM tile (MMA M)
 constexpr int kBlockK = 64;                     // bf16 elements per 128-byte swizzle row
+constexpr int kTileWidths = 3;                   // weight rows per experts tile: 256, 192 or 128
+__host__ __device__ constexpr int tile_width(int wc) { return 256 - 64 * wc; }
 constexpr int kLoraTileCols = 64;               // shrink result row, padded to one swizzle row
 constexpr int kRowBox = 32;                     // token rows per TMA box of an A operand
 constexpr long long kWaitCycles = 4000000000LL;  // default spin limit of a device wait (~2 s at 2 GHz)
@@ -117,11 +119,13 @@ cudaError_t launch_combine(const void* y_slot, const int32_t* topk_ids, const fl
 struct alignas(128) GemmSide {
     CUtensorMap tm_a;       // token rows [rows, K] (x in sorted order / act), box {64, kRowBox}
     CUtensorMap tm_a_full;  // the same with box {64, 128}: one box per full block
-    CUtensorMap tm_b;       // weight rows: w13 view {H, I, 2, E_tot} / w2 view {I, H, E_tot}
-    CUtensorMap tm_b_n;     // the same with half-height boxes (narrow tiles)
+    // weight rows: w13 view {H, I, 2, E_tot} / w2 view {I, H, E_tot}, one
+    // map per tile width (256, 192, 128 weight rows; gate_up boxes take half)
+    CUtensorMap tm_b[kTileWidths];
     CUtensorMap tm_sa;      // LoRA shrink weights: A13 / A2 view {K, rank, L*E_tot}
-    CUtensorMap tm_lb;      // LoRA expand weights: B13 view {rank, I, 2, L*E_tot} / B2 view {rank, H, L*E_tot}
-    CUtensorMap tm_lb_n;    // the same with half-height boxes (narrow tiles)
+    // LoRA expand weights: B13 view {rank, I, 2, L*E_tot} / B2 view {rank, H, L*E_tot},
+    // one map per tile width
+    CUtensorMap tm_lb[kTileWidths];
     CUtensorMap tm_t;       // this side's LoRA tiles [tiles*128, 64], box {64, kRowBox}
     CUtensorMap tm_t_full;  // box {64, 128}
     void* lora_t;           // LoRA tiles: written by the shrink tiles, read by the expand stages

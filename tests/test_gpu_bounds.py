@@ -69,5 +69,9 @@ def test_prefill_sampled():
     _run(s, rows=np.linspace(0, s.M - 1, 16).round().astype(np.int64))
 
 
+def test_decode_two_tokens():
+    _run(wl.spec("decode", M=2))                                              # 192-row tiles with adapters
+
+
 def test_shared_one_token():
     _run(wl.spec("shared", M=1))

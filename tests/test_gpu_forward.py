@@ -39,6 +39,13 @@ def test_tiny():
     _layer(wl.spec("tiny"))
 
 
+@pytest.mark.parametrize("M", [1, 2, 5])
+def test_decode_few_tokens(M):
+    """Decode-shaped layers with a handful of tokens: the launches whose tile
+    width is 192 or 128 rows instead of 256, with adapters."""
+    _layer(wl.spec("decode", M=M), label=f"decode M={M}")
+
+
 def test_decode_full():
     _layer(wl.spec("decode"))
 

@@ -32,12 +32,14 @@
 // 64-wide K-chunks per stage.
 //
 // A tile depends only on tiles of earlier phases of the same block, i.e.
-// on tiles with smaller indices.  Tiles are claimed in index order, every
-// CTA is resident (grid <= SMs) and works through its claims in order, so
-// the unfinished tile with the smallest index always has its inputs ready:
-// the producer can wait on the block's counters (act before a down-side
-// tile starts, the shrink counter before the expand stages) without
-// deadlock, and the phases overlap across CTAs:
+// on tiles with smaller indices.  Every tile, a CTA's first included, is
+// claimed from one counter in index order by a CTA that is already running,
+// and a CTA works through its claims in order, so the unfinished claimed
+// tile with the smallest index always has its inputs ready -- however many
+// of the grid's CTAs are resident (other kernels may hold SMs): the
+// producer can wait on the block's counters (act before a down-side tile
+// starts, the shrink counter before the expand stages) without deadlock,
+// and the phases overlap across CTAs:
 // the gate_up base product streams while other CTAs run shrink tiles, and
 // the down GEMM fills the gate_up tail.  (The pages overlap the shrink and
 // expand kernels with PDL; here they share one grid.)
@@ -305,14 +307,16 @@ __device__ __forceinline__ void producer(const Ctx& c) {
     uint8_t* const smem = c.smem;
     long it = 0;  // stages issued
     bool ok = true;
-    long tile = blockIdx.x, next = -1;
+    // the first tile is claimed like every other: a CTA that another
+    // kernel keeps waiting for an SM holds no tile that others depend on
+    long tile = atomicAdd(p.tile_next, 1), next = -1;
     // the next tile is claimed a few stages before this one's base loads
     // are all issued: late enough that the CTA is about to be free (a
     // claim at the start of a tile hands work to CTAs that will be busy
     // for a whole tile while others idle), early enough that the atomic's
     // latency hides behind the last loads
     auto claim = [&]() {
-        if (next < 0) next = gridDim.x + static_cast<long>(atomicAdd(p.tile_next, 1));
+        if (next < 0) next = atomicAdd(p.tile_next, 1);
     };
     // test hook: a wait on a flag that nothing sets, which must end
     // in a reported timeout and a clean exit

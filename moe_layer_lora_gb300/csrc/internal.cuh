@@ -43,7 +43,7 @@ struct Workspace {
     int32_t* max_rows;     // most real rows in any block
     int32_t* done13;       // [max_blocks] shrink tiles finished per block, gate_up projection
     int32_t* done2;        // [max_blocks] the same for the down projection
-    int32_t* tile_next;    // experts tiles claimed past the first round
+    int32_t* tile_next;    // experts tiles claimed so far
     int32_t* act_done;     // [max_blocks] gate_up tiles finished per block
     size_t zeroed_bytes;   // leading bytes cleared by every forward (header and counters)
     int32_t* sorted_ids;   // [max_padded]
@@ -152,7 +152,7 @@ struct alignas(128) GemmParams {
     int32_t* act_done;  // per block: finished gate_up tiles (zero at launch)
     long lt_cap;        // LoRA tiles the workspace holds (bounds checks)
     long pad_cap;       // sorted positions the workspace holds (bounds checks)
-    int32_t* tile_next; // tiles claimed past the first round (zero at launch)
+    int32_t* tile_next; // tiles claimed so far (zero at launch)
     const int32_t* max_rows;  // most real rows in any block (written by align)
     uint32_t* status;
     long long wait_limit;        // clock cycles a wait may take before the CTA gives up

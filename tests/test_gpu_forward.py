@@ -389,3 +389,36 @@ def test_graph_replay_switches_tile_geometry():
         torch.cuda.synchronize()
         assert torch.equal(y_graph, y_eager), label
         gu.check_y(y_graph, gu.oracle_forward(inp, ids_h, w_h), label)
+
+
+def test_concurrent_forwards_on_two_streams():
+    """Two layers launched on two streams without synchronisation: their
+    persistent experts grids compete for the SMs, so each may start with only
+    part of its CTAs resident.  Every tile, a CTA's first included, is
+    claimed by a running CTA, so both finish with a clean status and the
+    same bytes as one at a time."""
+    specs = [wl.spec("decode", M=24, seed=140), wl.spec("decode", M=40, seed=141)]
+    layers = []
+    for s in specs:
+        inp = wl.make(s, device="cuda")
+        d = gu.DeviceInputs(inp)
+        ids, w = gu.gpu_route(d)
+        ws = torch.empty(ml.mlora_moe_workspace_size(s.M, s.H, s.I, s.E_tot, s.K_total, s.L, s.r),
+                         dtype=torch.uint8, device="cuda")
+        y_ref = gu.gpu_forward(d, ids, w, workspace=ws)
+        layers.append((d, ids, w, ws, y_ref))
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for _ in range(4):
+        outs = []
+        for (d, ids, w, ws, _), st in zip(layers, streams):
+            s = d.spec
+            y = torch.empty((s.M, s.H), dtype=torch.bfloat16, device="cuda")
+            with torch.cuda.stream(st):
+                ml.mlora_moe_forward(d.x, d.w13, d.w2, d.A13, d.B13, d.A2, d.B2, d.idx, ids, w, s.scaling, y=y,
+                                     workspace=ws, stream=st)
+            outs.append(y)
+        torch.cuda.synchronize()
+        for (d, ids, w, ws, y_ref), y in zip(layers, outs):
+            assert ml.mlora_moe_read_status(ws) == 0
+            assert torch.equal(y, y_ref)

@@ -290,6 +290,21 @@ def run_gpu(args, s: wl.Spec, rank: int, world: int, local_rank: int):
     d = {k: (None if v is None else v.to(device)) for k, v in dict(
         logits=inp.logits, bias=inp.bias, x=inp.x, w13=inp.w13, w2=inp.w2, A13=inp.A13, B13=inp.B13, A2=inp.A2,
         B2=inp.B2, idx=inp.token_lora_idx).items()}
+    # the per-step inputs (x, router logits, adapter ids) live in one device
+    # buffer with a pinned host twin, so the end-to-end step brings them over
+    # in one copy
+    parts = [("x", inp.x), ("logits", inp.logits)] + ([("idx", inp.token_lora_idx)] if s.has_lora else [])
+    offs, in_bytes = {}, 0
+    for name, t in parts:
+        offs[name] = in_bytes
+        in_bytes += (t.numel() * t.element_size() + 255) // 256 * 256
+    h_in = torch.empty(in_bytes, dtype=torch.uint8).pin_memory()
+    d_in = torch.empty(in_bytes, dtype=torch.uint8, device=device)
+    for name, t in parts:
+        nb = t.numel() * t.element_size()
+        h_in[offs[name]:offs[name] + nb].copy_(t.contiguous().reshape(-1).view(torch.uint8))
+        d[name] = d_in[offs[name]:offs[name] + nb].view(t.dtype).view(t.shape)
+    d_in.copy_(h_in)
     L, r = (s.L, s.r) if s.has_lora else (0, 0)
     ids = torch.empty((s.M, s.K_total), dtype=torch.int32, device=device)
     w = torch.empty((s.M, s.K_total), dtype=torch.float32, device=device)
@@ -376,21 +391,28 @@ def run_gpu(args, s: wl.Spec, rank: int, world: int, local_rank: int):
         launches_per_step = 5  # route, align, gather, experts, combine
 
         # end to end through the public API with host buffers: H2D of the
-        # step's inputs from pinned memory, the layer, D2H of the output
-        h_logits = inp.logits.pin_memory()
-        h_x = inp.x.pin_memory()
-        h_idx = inp.token_lora_idx.pin_memory() if s.has_lora else None
+        # step's inputs from pinned memory (one copy), the layer, D2H of the
+        # output, captured with the layer in one CUDA graph
         h_y = torch.empty((s.M, s.H), dtype=torch.bfloat16).pin_memory()
-        bi = h_logits.numel() * 4 + h_x.numel() * 2 + (h_idx.numel() * 4 if h_idx is not None else 0)
+        bi = in_bytes
         bo = h_y.numel() * 2
 
-        def e2e_step():
-            d["logits"].copy_(h_logits, non_blocking=True)
-            d["x"].copy_(h_x, non_blocking=True)
-            if h_idx is not None:
-                d["idx"].copy_(h_idx, non_blocking=True)
-            run()
+        def e2e_body():
+            d_in.copy_(h_in, non_blocking=True)
+            step()
             h_y.copy_(y, non_blocking=True)
+
+        e2e_graph = None
+        if not args.no_graph:
+            e2e_graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(e2e_graph, stream=stream):
+                e2e_body()
+
+        def e2e_step():
+            if e2e_graph is not None:
+                e2e_graph.replay()
+            else:
+                e2e_body()
             stream.synchronize()
 
         for _ in range(max(1, args.warmup)):

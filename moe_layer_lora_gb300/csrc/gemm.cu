@@ -289,7 +289,7 @@ struct Ctx {
 // ring and streams their operands into a ring of nst stages of stb bytes,
 // the first ab of each holding A rows.
 template <int nst, uint32_t stb, uint32_t ab>
-__device__ __forceinline__ void producer(const Ctx& c) {
+__device__ __forceinline__ void producer(const Ctx& c, long first_tile) {
     const GemmParams& p = *c.p;
     uint64_t* const full = c.L.full;
     uint64_t* const empty = c.L.empty;
@@ -307,9 +307,7 @@ __device__ __forceinline__ void producer(const Ctx& c) {
     uint8_t* const smem = c.smem;
     long it = 0;  // stages issued
     bool ok = true;
-    // the first tile is claimed like every other: a CTA that another
-    // kernel keeps waiting for an SM holds no tile that others depend on
-    long tile = atomicAdd(p.tile_next, 1), next = -1;
+    long tile = first_tile, next = -1;
     // the next tile is claimed a few stages before this one's base loads
     // are all issued: late enough that the CTA is about to be free (a
     // claim at the start of a tile hands work to CTAs that will be busy
@@ -763,6 +761,11 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
     // everything above overlapped the previous kernel in the stream
     griddep_wait();
 
+    // the producer's first tile is claimed like every other (a CTA that
+    // another kernel keeps waiting for an SM holds no tile that others
+    // depend on), before the loads below so that the latencies overlap
+    long first_tile = -1;
+    if (threadIdx.x == 0) first_tile = atomicAdd(p.tile_next, 1);
     const Ctx c(p, smem, tmem_base);
     // ring geometry of this launch (the same in every CTA): when no expert
     // has more than one 32-row box of slots, A stages shrink to 4 KiB and
@@ -772,9 +775,9 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
     if (warp == 0) {
         if ((threadIdx.x & 31) == 0) {
             if (small_a)
-                producer<kSmallStages, kSmallStageBytes, kSmallATileBytes>(c);
+                producer<kSmallStages, kSmallStageBytes, kSmallATileBytes>(c, first_tile);
             else
-                producer<kStages, kStageBytes, kATileBytes>(c);
+                producer<kStages, kStageBytes, kATileBytes>(c, first_tile);
         }
     } else if (warp == 1) {
         if ((threadIdx.x & 31) == 0) {

@@ -4,10 +4,10 @@
 //
 // The kernel works through four phases of tiles over blocks of kBlockM =
 // 128 sorted slots (all slots of a block share one expert e, from align).
-// CTA c starts with tile c of the concatenated sequence; from then on, as
-// it starts a tile its producer claims the next unclaimed one from a
-// global counter, so tiles of unequal cost (shrink, gate_up, down, blocks
-// with many adapters) spread evenly over the SMs:
+// Every CTA claims its tiles of the concatenated sequence from a global
+// counter -- the first as it starts, each next one a few stages before the
+// current tile's loads are all issued -- so tiles of unequal cost (shrink,
+// gate_up, down, blocks with many adapters) spread evenly over the SMs:
 //
 //  1. gate_up shrink tiles (with adapters): T13_l = s * X A13_{l,e}^T for
 //     up to `gsize` adapters l of one block at once -- their rank rows

@@ -73,5 +73,9 @@ def test_decode_two_tokens():
     _run(wl.spec("decode", M=2))                                              # 192-row tiles with adapters
 
 
+def test_mid_width_ragged():
+    _run(wl.spec("decode", M=8, H=2888, I=1448, E=8, top_k=2, L=4, r=16, seed=150))  # partial 192-row slabs
+
+
 def test_shared_one_token():
     _run(wl.spec("shared", M=1))

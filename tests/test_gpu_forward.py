@@ -39,6 +39,14 @@ def test_tiny():
     _layer(wl.spec("tiny"))
 
 
+def test_mid_width_tiles_ragged():
+    """Eight tokens over eight experts on a layer whose I and H are not
+    multiples of the 192-row tile (the width a launch of 7 or 8 blocks
+    takes here): the last gate_up slab holds 8 valid rows of each half and
+    the last down slab 8 (MMA N trimmed to 16), with adapters."""
+    _layer(wl.spec("decode", M=8, H=2888, I=1448, E=8, top_k=2, L=4, r=16, seed=150), label="192-row ragged")
+
+
 @pytest.mark.parametrize("M", [1, 2, 5])
 def test_decode_few_tokens(M):
     """Decode-shaped layers with a handful of tokens: the launches whose tile

@@ -430,3 +430,30 @@ def test_concurrent_forwards_on_two_streams():
         for (d, ids, w, ws, y_ref), y in zip(layers, outs):
             assert ml.mlora_moe_read_status(ws) == 0
             assert torch.equal(y, y_ref)
+
+
+def test_largest_batch():
+    """A prefill-shaped layer with 65536 tokens (262144 routed slots, 32 768
+    per CTA of the align cluster, ~2100 blocks): routing and the sorted,
+    padded permutation bit-exact against the oracle over the whole batch,
+    the layer output on sampled tokens."""
+    s = wl.spec("prefill", M=65536)
+    inp = wl.make(s, device="cuda")
+    d = gu.DeviceInputs(inp)
+    ids, w = gu.gpu_route(d)
+    ids_ref, w_ref = gu.oracle_route(inp)
+    gu.check_route(ids, w, ids_ref, w_ref)
+    s_ref, e_ref, n_ref = oracle.moe_align(ids_ref, s.E_tot, 128)
+    srt, eid, npad = ml.mlora_moe_align(ids, s.E_tot, 128)
+    torch.cuda.synchronize()
+    assert int(npad.item()) == n_ref
+    assert np.array_equal(srt.cpu().numpy(), s_ref)
+    assert np.array_equal(eid.cpu().numpy(), e_ref)
+    ws = torch.empty(ml.mlora_moe_workspace_size(s.M, s.H, s.I, s.E_tot, s.K_total, s.L, s.r), dtype=torch.uint8,
+                     device="cuda")
+    y = gu.gpu_forward(d, ids, w, workspace=ws)
+    torch.cuda.synchronize()
+    assert ml.mlora_moe_read_status(ws) == 0
+    rows = gu.sample_rows(s.M, 12, seed=9, must=(0, s.M - 1))
+    gu.check_y(y[torch.as_tensor(rows, device="cuda")], gu.oracle_forward(inp, ids_ref, w_ref, rows=rows),
+               "65536 tokens")

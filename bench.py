@@ -228,18 +228,28 @@ def kernel_source_hash(stage: str) -> str:
 
 
 def profiled_traffic(stage: str, workload: str):
-    """DRAM bytes per launch of `stage` from a committed ncu summary, when
-    that summary was taken on the current kernel sources (else None)."""
-    path = os.path.join(ROOT, "profiles", f"{stage}_{workload}.md")
-    try:
-        text = open(path).read()
-    except OSError:
-        return None
-    m_hash = re.search(r"kernel source hash:[\s|`]*([0-9a-f]{16})", text)
-    m_val = re.search(r"dram bytes per launch:[\s|`]*([0-9.eE+]+)", text)
-    if not m_hash or not m_val or m_hash.group(1) != kernel_source_hash(stage):
-        return None
-    return float(m_val.group(1))
+    """DRAM bytes per launch of `stage` on the named workload (its default
+    size) from a committed ncu summary, when that summary was taken on the
+    current kernel sources (else None).  A summary covers one workload
+    (profiles/<stage>_<workload>.md, "dram bytes per launch: `v`") or
+    several (any profiles/<stage>_*.md, "dram bytes per launch (<workload>): `v`")."""
+    pdir = os.path.join(ROOT, "profiles")
+    own = f"{stage}_{workload}.md"
+    names = [own] + sorted(n for n in os.listdir(pdir) if n.startswith(stage + "_") and n != own)
+    for name in names:
+        try:
+            text = open(os.path.join(pdir, name)).read()
+        except OSError:
+            continue
+        key = r"dram bytes per launch:" if name == own else r"dram bytes per launch \(" + re.escape(workload) + r"\):"
+        m_val = re.search(key + r"[\s|`]*([0-9.eE+]+)", text)
+        if not m_val:
+            continue
+        m_hash = re.search(r"kernel source hash:[\s|`]*([0-9a-f]{16})", text)
+        if not m_hash or m_hash.group(1) != kernel_source_hash(stage):
+            return None
+        return float(m_val.group(1))
+    return None
 
 
 # --------------------------------------------------------------- CPU oracle --

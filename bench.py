@@ -284,8 +284,17 @@ def cpu_baseline(inp, target_s: float):
         n2 = max(n, min(s.M, n2))
         if n2 > n:
             dt, n = oracle_sample(inp, ids, w, n2)
-    return {"value": n / dt, "unit": "tokens/s", "cores": min(cores, n), "kind": "oracle",
-            "sample": f"first {n} of the {s.M} tokens of the {s.name} batch, one fp64 layer pass ({dt:.1f} s)",
+    # a whole batch that takes well under the target is timed over several
+    # passes, so that the figure is not one short run
+    passes = 1
+    if dt < target_s / 3:
+        passes = int(min(50, max(1, target_s / max(dt, 1e-3) - 1)))
+        for _ in range(passes - 1):
+            dt_i, _ = oracle_sample(inp, ids, w, n)
+            dt += dt_i
+    return {"value": n * passes / dt, "unit": "tokens/s", "cores": min(cores, n), "kind": "oracle",
+            "sample": f"first {n} of the {s.M} tokens of the {s.name} batch, {passes} fp64 layer "
+                      f"pass{'es' if passes > 1 else ''} ({dt:.1f} s)",
             "seconds": dt}
 
 

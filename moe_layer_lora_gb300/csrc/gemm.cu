@@ -70,7 +70,7 @@ constexpr int kBN = 256;                                         // weight rows 
 // flight.
 constexpr int kStages = 4;
 constexpr int kSmallStages = 6;
-constexpr int kMaxStages = kSmallStages;
+constexpr int kMaxStages = kSmallStages > kStages ? kSmallStages : kStages;  // barrier arrays
 constexpr int kTileRing = 4;                                     // claimed tiles handed from producer to consumers
 constexpr int kATileBytes = kBlockM * kBlockK * 2;               // 16 KiB
 constexpr int kStageBytes = kATileBytes + kBN * kBlockK * 2;     // 48 KiB

@@ -457,3 +457,37 @@ def test_largest_batch():
     rows = gu.sample_rows(s.M, 12, seed=9, must=(0, s.M - 1))
     gu.check_y(y[torch.as_tensor(rows, device="cuda")], gu.oracle_forward(inp, ids_ref, w_ref, rows=rows),
                "65536 tokens")
+
+
+def _random_wide_specs(n: int, seed: int = 77):
+    """Seeded random layers over wider shapes than the small ones above: H and
+    I up to 4096 (slabs of every tile width, ragged last slabs), up to 128
+    experts, batches from one token to 600, with and without adapters."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        E = int(rng.integers(1, 129))
+        n_shared = int(rng.integers(0, 2)) if E > 1 else 0
+        top_k = int(rng.integers(1, min(E, 8) + 1))
+        lora = bool(rng.random() < 0.7)
+        out.append(dict(
+            M=int(rng.choice([1, 2, 3, 5, 8, 13, 32, 64, 100, 257, 600])),
+            H=8 * int(rng.integers(1, 513)), I=8 * int(rng.integers(1, 513)),
+            E=E, top_k=top_k, n_shared=n_shared,
+            routed_scaling_factor=float(rng.choice([1.0, 2.5])) if n_shared else 1.0,
+            scoring=int(rng.integers(0, 2)), renormalize=int(rng.integers(0, 2)),
+            L=int(rng.integers(1, 20)) if lora else 0, r=8 * int(rng.integers(1, 9)) if lora else 0,
+            lora_mode=str(rng.choice(["uniform", "zipf", "all_none"])) if lora else "none",
+            seed=9000 + i,
+        ))
+    return out
+
+
+@pytest.mark.parametrize("over", _random_wide_specs(40),
+                         ids=lambda o: f"M{o['M']}H{o['H']}I{o['I']}E{o['E']}k{o['top_k']}L{o['L']}")
+def test_random_wide_layers(over):
+    """Random wider layers against the oracle on sampled tokens (the first,
+    the last and six more)."""
+    s = wl.spec("tiny", **over)
+    rows = gu.sample_rows(s.M, 6, seed=over["seed"], must=(0, s.M - 1))
+    _layer(s, rows=rows, label=str(over))

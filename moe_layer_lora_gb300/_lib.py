@@ -106,24 +106,89 @@ def _check(fn: str, status: int):
         raise MloraError(fn, status)
 
 
-def _need(t: torch.Tensor, dtype, name: str):
-    if not t.is_cuda or t.dtype != dtype or not t.is_contiguous():
-        raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor")
+def _need_shape(t, dtype, name: str, shape=None):
+    """The library reads every tensor as a dense row-major array of the given
+    shape (its tensor maps are built from those sizes, not from the
+    allocation), so a mismatch is refused here, before any device work."""
+    if not isinstance(t, torch.Tensor):
+        raise ValueError(f"{name} must be a torch.Tensor")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def _need_place(t: torch.Tensor, name: str, device=None):
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA {t.dtype} tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, the layer's inputs on {device}")
+
+
+def _need(t, dtype, name: str, shape=None, device=None):
+    _need_shape(t, dtype, name, shape)
+    _need_place(t, name, device)
+
+
+def _layer_args(x, w13, w2, A13, B13, A2, B2, token_lora_idx, topk_ids, topk_w, y):
+    """Checks the layer's tensors against each other; returns
+    (M, H, I, E_tot, K', L, rank, lora)."""
+    if not isinstance(x, torch.Tensor) or x.dim() != 2 or not isinstance(w13, torch.Tensor) or w13.dim() != 3:
+        raise ValueError("x must be [M, H] and w13 [E_tot, 2I, H]")
+    M, H = x.shape
+    E_tot, twoI = w13.shape[0], w13.shape[1]
+    if twoI % 2:
+        raise ValueError(f"w13 must have an even row count 2I, got {twoI}")
+    I = twoI // 2
+    if not isinstance(topk_ids, torch.Tensor) or topk_ids.dim() != 2:
+        raise ValueError("topk_ids must be [M, K']")
+    KT = topk_ids.shape[1]
+    checks = [(x, torch.bfloat16, "x", (M, H)), (w13, torch.bfloat16, "w13", (E_tot, 2 * I, H)),
+              (w2, torch.bfloat16, "w2", (E_tot, H, I)), (topk_ids, torch.int32, "topk_ids", (M, KT)),
+              (topk_w, torch.float32, "topk_w", (M, KT))]
+    if y is not None:
+        checks.append((y, torch.bfloat16, "y", (M, H)))
+    lora = all(t is not None for t in (A13, B13, A2, B2, token_lora_idx))
+    L = r = 0
+    if lora:
+        if not isinstance(A13, torch.Tensor) or A13.dim() != 4:
+            raise ValueError("A13 must be [L, E_tot, rank, H]")
+        L, r = A13.shape[0], A13.shape[2]
+        checks += [(A13, torch.bfloat16, "A13", (L, E_tot, r, H)), (B13, torch.bfloat16, "B13", (L, E_tot, 2 * I, r)),
+                   (A2, torch.bfloat16, "A2", (L, E_tot, r, I)), (B2, torch.bfloat16, "B2", (L, E_tot, H, r)),
+                   (token_lora_idx, torch.int32, "token_lora_idx", (M,))]
+    # every shape and dtype first, then where the tensors live
+    for t, dtype, name, shape in checks:
+        _need_shape(t, dtype, name, shape)
+    for t, _, name, _ in checks:
+        _need_place(t, name, x.device)
+    return M, H, I, E_tot, KT, L, r, lora
 
 
 def mlora_moe_route(logits: torch.Tensor, bias: Optional[torch.Tensor], top_k: int, scoring: int,
                     renormalize: int = 1, n_shared: int = 0, routed_scaling_factor: float = 1.0,
                     topk_ids: Optional[torch.Tensor] = None, topk_w: Optional[torch.Tensor] = None,
                     stream=None):
-    _need(logits, torch.float32, "logits")
+    if not isinstance(logits, torch.Tensor) or logits.dim() != 2:
+        raise ValueError("logits must be [M, E]")
     M, E = logits.shape
     KT = top_k + n_shared
-    if topk_ids is None:
-        topk_ids = torch.empty((M, KT), dtype=torch.int32, device=logits.device)
-    if topk_w is None:
-        topk_w = torch.empty((M, KT), dtype=torch.float32, device=logits.device)
+    dev = logits.device
+    checks = [(logits, torch.float32, "logits", (M, E))]
+    if topk_ids is not None:
+        checks.append((topk_ids, torch.int32, "topk_ids", (M, KT)))
+    if topk_w is not None:
+        checks.append((topk_w, torch.float32, "topk_w", (M, KT)))
     if bias is not None:
-        _need(bias, torch.float32, "bias")
+        checks.append((bias, torch.float32, "bias", (E,)))
+    for t, dtype, name, shape in checks:
+        _need_shape(t, dtype, name, shape)
+    for t, _, name, _ in checks:
+        _need_place(t, name, dev)
+    if topk_ids is None:
+        topk_ids = torch.empty((M, KT), dtype=torch.int32, device=dev)
+    if topk_w is None:
+        topk_w = torch.empty((M, KT), dtype=torch.float32, device=dev)
     st = load().mlora_moe_route(_ptr(logits), _ptr(bias), M, E, top_k, scoring, renormalize, n_shared,
                                 float(routed_scaling_factor), _ptr(topk_ids), _ptr(topk_w), _stream(stream))
     _check("mlora_moe_route", st)
@@ -136,8 +201,10 @@ def mlora_moe_align_max_padded(M: int, K_total: int, E_tot: int, block_m: int) -
 
 def mlora_moe_align(topk_ids: torch.Tensor, E_tot: int, block_m: int, stream=None):
     """Returns (sorted_ids, expert_ids, num_post_padded[1]) as CUDA tensors."""
-    _need(topk_ids, torch.int32, "topk_ids")
+    if not isinstance(topk_ids, torch.Tensor) or topk_ids.dim() != 2:
+        raise ValueError("topk_ids must be [M, K']")
     M, KT = topk_ids.shape
+    _need(topk_ids, torch.int32, "topk_ids", (M, KT))
     mp = mlora_moe_align_max_padded(M, KT, E_tot, block_m)
     dev = topk_ids.device
     sorted_ids = torch.empty(mp, dtype=torch.int32, device=dev)
@@ -157,18 +224,13 @@ def mlora_moe_forward(x, w13, w2, A13, B13, A2, B2, token_lora_idx, topk_ids, to
                       n_shared: int = 0, out_scale: float = 1.0, y: Optional[torch.Tensor] = None,
                       workspace: Optional[torch.Tensor] = None, stream=None):
     """The fused MoE-LoRA layer; returns y [M, H] bf16 (see include/mlora.h)."""
-    _need(x, torch.bfloat16, "x")
-    M, H = x.shape
-    E_tot, twoI, _ = w13.shape
-    I = twoI // 2
-    KT = topk_ids.shape[1]
-    lora = all(t is not None for t in (A13, B13, A2, B2, token_lora_idx))
-    L, r = (A13.shape[0], A13.shape[2]) if lora else (0, 0)
+    M, H, I, E_tot, KT, L, r, lora = _layer_args(x, w13, w2, A13, B13, A2, B2, token_lora_idx, topk_ids, topk_w, y)
     if y is None:
         y = torch.empty((M, H), dtype=torch.bfloat16, device=x.device)
     need = mlora_moe_workspace_size(M, H, I, E_tot, KT, L, r)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=x.device)
+    _need(workspace, torch.uint8, "workspace", None, x.device)
     st = load().mlora_moe_forward(
         _ptr(x), _ptr(w13), _ptr(w2), _ptr(A13) if lora else None, _ptr(B13) if lora else None,
         _ptr(A2) if lora else None, _ptr(B2) if lora else None, _ptr(token_lora_idx) if lora else None,
@@ -193,16 +255,12 @@ def mlora_moe_forward_static(x, w13, w2, A13, B13, A2, B2, token_lora_idx, topk_
         P, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
         fn.argtypes = [P] * 10 + [i] * 7 + [f, i, f, P, P]
         fn.restype = i
-    _need(x, torch.bfloat16, "x")
-    M, H = x.shape
-    E_tot, twoI, _ = w13.shape
-    lora = all(t is not None for t in (A13, B13, A2, B2, token_lora_idx))
-    L, r = (A13.shape[0], A13.shape[2]) if lora else (0, 0)
+    M, H, I, E_tot, KT, L, r, lora = _layer_args(x, w13, w2, A13, B13, A2, B2, token_lora_idx, topk_ids, topk_w, y)
     if y is None:
         y = torch.empty((M, H), dtype=torch.bfloat16, device=x.device)
     st = fn(_ptr(x), _ptr(w13), _ptr(w2), _ptr(A13) if lora else None, _ptr(B13) if lora else None,
             _ptr(A2) if lora else None, _ptr(B2) if lora else None, _ptr(token_lora_idx) if lora else None,
-            _ptr(topk_ids), _ptr(topk_w), M, H, twoI // 2, E_tot, topk_ids.shape[1], L, r, float(scaling),
+            _ptr(topk_ids), _ptr(topk_w), M, H, I, E_tot, KT, L, r, float(scaling),
             int(n_shared), float(out_scale), _ptr(y), _stream(stream))
     _check("mlora_moe_forward_static", st)
     return y

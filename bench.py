@@ -56,6 +56,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU work of the oracle baseline")
     ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of replaying a graph")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the per-workload breakdown that follows the headline measurement")
     return ap.parse_args(argv)
 
 
@@ -254,208 +256,333 @@ def profiled_traffic(stage: str, workload: str):
 
 # --------------------------------------------------------------- CPU oracle --
 
-def oracle_sample(inp, ids, w, n_tokens: int):
+def oracle_sample(inp, n_tokens: int, hb=None):
+    """The oracle's route + forward of the first n_tokens tokens (the step
+    the GPU arm times, on a bounded sample); returns (seconds, tokens)."""
     import oracle
     s = inp.spec
     rows = np.arange(min(n_tokens, s.M))
-    b = wl.bits
+    hb = hb or host_bits(inp)
     lora = s.has_lora
     t0 = time.perf_counter()
-    oracle.moe_forward(b(inp.x)[rows], b(inp.w13), b(inp.w2), b(inp.A13) if lora else None,
-                       b(inp.B13) if lora else None, b(inp.A2) if lora else None, b(inp.B2) if lora else None,
-                       inp.token_lora_idx.numpy()[rows] if lora else None, ids[rows],
-                       w[rows].astype(np.float32), s.scaling, s.out_scale)
+    ids, w = oracle.moe_route(inp.logits.numpy()[rows], None if inp.bias is None else inp.bias.numpy(), s.top_k,
+                              s.scoring, s.renormalize, s.n_shared, s.routed_scaling_factor)
+    oracle.moe_forward(hb["x"][rows], hb["w13"], hb["w2"], hb["A13"], hb["B13"], hb["A2"], hb["B2"],
+                       inp.token_lora_idx.numpy()[rows] if lora else None, ids, w.astype(np.float32), s.scaling,
+                       s.out_scale)
     return time.perf_counter() - t0, len(rows)
 
 
+def host_bits(inp):
+    """Host bf16 bit arrays of the layer's tensors (copied once)."""
+    b = wl.bits
+    lora = inp.spec.has_lora
+    return {"x": b(inp.x), "w13": b(inp.w13), "w2": b(inp.w2), "A13": b(inp.A13) if lora else None,
+            "B13": b(inp.B13) if lora else None, "A2": b(inp.A2) if lora else None,
+            "B2": b(inp.B2) if lora else None}
+
+
 def cpu_baseline(inp, target_s: float):
-    """The oracle as it stands on the host cores, on a bounded token sample
-    sized to roughly target_s seconds of work."""
+    """The oracle as it stands on the host cores (route + forward), on a
+    bounded token sample sized to roughly target_s seconds of work."""
     import oracle
     s = inp.spec
     oracle.load()
-    ids, w = oracle.moe_route(inp.logits.numpy(), None if inp.bias is None else inp.bias.numpy(), s.top_k,
-                              s.scoring, s.renormalize, s.n_shared, s.routed_scaling_factor)
+    hb = host_bits(inp)
     cores = os.cpu_count() or 1
     n = min(s.M, cores)
-    dt, n = oracle_sample(inp, ids, w, n)
+    dt, n = oracle_sample(inp, n, hb)
     if dt < target_s / 3 and n < s.M:
         n2 = int(min(s.M, max(n, n * target_s / max(dt, 1e-3))) // max(1, min(cores, n)) * min(cores, n))
         n2 = max(n, min(s.M, n2))
         if n2 > n:
-            dt, n = oracle_sample(inp, ids, w, n2)
+            dt, n = oracle_sample(inp, n2, hb)
     # a whole batch that takes well under the target is timed over several
     # passes, so that the figure is not one short run
     passes = 1
     if dt < target_s / 3:
         passes = int(min(50, max(1, target_s / max(dt, 1e-3) - 1)))
         for _ in range(passes - 1):
-            dt_i, _ = oracle_sample(inp, ids, w, n)
+            dt_i, _ = oracle_sample(inp, n, hb)
             dt += dt_i
     return {"value": n * passes / dt, "unit": "tokens/s", "cores": min(cores, n), "kind": "oracle",
-            "sample": f"first {n} of the {s.M} tokens of the {s.name} batch, {passes} fp64 layer "
-                      f"pass{'es' if passes > 1 else ''} ({dt:.1f} s)",
+            "sample": f"route + forward of the first {n} of the {s.M} tokens of the {s.name} batch, {passes} "
+                      f"fp64 pass{'es' if passes > 1 else ''} ({dt:.1f} s)",
             "seconds": dt}
 
 
 # ---------------------------------------------------------------- GPU path --
 
-def run_gpu(args, s: wl.Spec, rank: int, world: int, local_rank: int):
-    import moe_layer_lora_gb300 as ml
+# The workloads timed after the headline (the default run reports all of
+# them): label -> (workload name, spec overrides).  "stress_all_none" is
+# the adapter-stress batch with every token's adapter id at -1, the early
+# exit of a layer whose adapters are given but unused.
+SWEEP = (
+    ("tiny", "tiny", {}),
+    ("decode", "decode", {}),
+    ("prefill", "prefill", {}),
+    ("shared_M1", "shared", {"M": 1}),
+    ("shared_M32", "shared", {"M": 32}),
+    ("shared_M128", "shared", {"M": 128}),
+    ("stress", "stress", {}),
+    ("stress_all_none", "stress", {"lora_mode": "all_none"}),
+)
 
-    device = torch.device("cuda", local_rank)
-    torch.cuda.set_device(device)
-    inp = wl.make(s, device=device)
-    d = {k: (None if v is None else v.to(device)) for k, v in dict(
-        logits=inp.logits, bias=inp.bias, x=inp.x, w13=inp.w13, w2=inp.w2, A13=inp.A13, B13=inp.B13, A2=inp.A2,
-        B2=inp.B2, idx=inp.token_lora_idx).items()}
-    # the per-step inputs (x, router logits, adapter ids) live in one device
-    # buffer with a pinned host twin, so the end-to-end step brings them over
-    # in one copy
-    parts = [("x", inp.x), ("logits", inp.logits)] + ([("idx", inp.token_lora_idx)] if s.has_lora else [])
-    offs, in_bytes = {}, 0
-    for name, t in parts:
-        offs[name] = in_bytes
-        in_bytes += (t.numel() * t.element_size() + 255) // 256 * 256
-    h_in = torch.empty(in_bytes, dtype=torch.uint8).pin_memory()
-    d_in = torch.empty(in_bytes, dtype=torch.uint8, device=device)
-    for name, t in parts:
-        nb = t.numel() * t.element_size()
-        h_in[offs[name]:offs[name] + nb].copy_(t.contiguous().reshape(-1).view(torch.uint8))
-        d[name] = d_in[offs[name]:offs[name] + nb].view(t.dtype).view(t.shape)
-    d_in.copy_(h_in)
-    L, r = (s.L, s.r) if s.has_lora else (0, 0)
-    ids = torch.empty((s.M, s.K_total), dtype=torch.int32, device=device)
-    w = torch.empty((s.M, s.K_total), dtype=torch.float32, device=device)
-    y = torch.empty((s.M, s.H), dtype=torch.bfloat16, device=device)
-    ws = torch.empty(ml.mlora_moe_workspace_size(s.M, s.H, s.I, s.E_tot, s.K_total, L, r), dtype=torch.uint8,
-                     device=device)
-    flush = L2Flush(device)
-    stream = torch.cuda.Stream(device=device)
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(ml.STAGE_EVENTS)]
-    for e in ev:
-        e.record(stream)  # creates the event handles
-    ml.mlora_set_stage_events(None)
-    step_start = torch.cuda.Event(enable_timing=True)
-    step_end = torch.cuda.Event(enable_timing=True)
 
-    def step():
+class LayerRun:
+    """One workload's layer on one device: its inputs resident in HBM, the
+    step (route + forward on a side stream), and CUDA graphs of the step --
+    a plain one and one with event nodes at the stage boundaries."""
+
+    def __init__(self, s: wl.Spec, device, use_graph: bool, packed: bool = False):
+        import moe_layer_lora_gb300 as ml
+        self.ml = ml
+        self.s = s
+        self.device = device
+        inp = wl.make(s, device=device)
+        self.inp = inp
+        d = {k: (None if v is None else v.to(device)) for k, v in dict(
+            logits=inp.logits, bias=inp.bias, x=inp.x, w13=inp.w13, w2=inp.w2, A13=inp.A13, B13=inp.B13,
+            A2=inp.A2, B2=inp.B2, idx=inp.token_lora_idx).items()}
+        self.in_bytes = 0
+        if packed:
+            # the per-step inputs (x, router logits, adapter ids) live in one
+            # device buffer with a pinned host twin, so the end-to-end step
+            # brings them over in one copy
+            parts = [("x", inp.x), ("logits", inp.logits)] + ([("idx", inp.token_lora_idx)] if s.has_lora else [])
+            offs = {}
+            for name, t in parts:
+                offs[name] = self.in_bytes
+                self.in_bytes += (t.numel() * t.element_size() + 255) // 256 * 256
+            self.h_in = torch.empty(self.in_bytes, dtype=torch.uint8).pin_memory()
+            self.d_in = torch.empty(self.in_bytes, dtype=torch.uint8, device=device)
+            for name, t in parts:
+                nb = t.numel() * t.element_size()
+                self.h_in[offs[name]:offs[name] + nb].copy_(t.contiguous().reshape(-1).view(torch.uint8))
+                d[name] = self.d_in[offs[name]:offs[name] + nb].view(t.dtype).view(t.shape)
+            self.d_in.copy_(self.h_in)
+        self.d = d
+        L, r = (s.L, s.r) if s.has_lora else (0, 0)
+        self.ids = torch.empty((s.M, s.K_total), dtype=torch.int32, device=device)
+        self.w = torch.empty((s.M, s.K_total), dtype=torch.float32, device=device)
+        self.y = torch.empty((s.M, s.H), dtype=torch.bfloat16, device=device)
+        self.ws = torch.empty(ml.mlora_moe_workspace_size(s.M, s.H, s.I, s.E_tot, s.K_total, L, r),
+                              dtype=torch.uint8, device=device)
+        self.stream = torch.cuda.Stream(device=device)
+        self.ev = [torch.cuda.Event(enable_timing=True) for _ in range(ml.STAGE_EVENTS)]
+        for e in self.ev:
+            e.record(self.stream)  # creates the event handles
+        ml.mlora_set_stage_events(None)
+        with torch.cuda.stream(self.stream):
+            self.step()
+            self.stream.synchronize()
+            status = ml.mlora_moe_read_status(self.ws, stream=self.stream)
+            if status != 0:
+                raise RuntimeError(f"{s.name}: device status {status:#x} after the first step")
+            self.plain = self.inst = None
+            if use_graph:
+                self.plain = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(self.plain, stream=self.stream):
+                    self.step()
+                ml.mlora_set_stage_events(self.ev)
+                try:
+                    self.inst = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(self.inst, stream=self.stream):
+                        self.step()
+                finally:
+                    ml.mlora_set_stage_events(None)
+
+    def step(self):
+        s, d, ml = self.s, self.d, self.ml
         ml.mlora_moe_route(d["logits"], d["bias"], s.top_k, s.scoring, s.renormalize, s.n_shared,
-                           s.routed_scaling_factor, topk_ids=ids, topk_w=w, stream=stream)
-        ml.mlora_moe_forward(d["x"], d["w13"], d["w2"], d["A13"], d["B13"], d["A2"], d["B2"], d["idx"], ids, w,
-                             s.scaling, s.n_shared, s.out_scale, y=y, workspace=ws, stream=stream)
+                           s.routed_scaling_factor, topk_ids=self.ids, topk_w=self.w, stream=self.stream)
+        ml.mlora_moe_forward(d["x"], d["w13"], d["w2"], d["A13"], d["B13"], d["A2"], d["B2"], d["idx"], self.ids,
+                             self.w, s.scaling, s.n_shared, s.out_scale, y=self.y, workspace=self.ws,
+                             stream=self.stream)
 
-    with torch.cuda.stream(stream):
-        step()
-        stream.synchronize()
-        status = ml.mlora_moe_read_status(ws, stream=stream)
-        if status != 0:
-            raise RuntimeError(f"device status {status:#x} after the first step")
-        # two graphs of the same step: a plain one for the headline time and
-        # one with event nodes at the stage boundaries for per-kernel times
-        plain = inst = None
-        if not args.no_graph:
-            plain = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(plain, stream=stream):
-                step()
-            ml.mlora_set_stage_events(ev)
-            inst = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(inst, stream=stream):
-                step()
-            ml.mlora_set_stage_events(None)
-        run = plain.replay if plain is not None else step
+    def run_plain(self):
+        if self.plain is not None:
+            self.plain.replay()
+        else:
+            self.step()
 
-        def run_inst():
-            if inst is not None:
-                inst.replay()
-            else:
-                ml.mlora_set_stage_events(ev)
-                step()
-                ml.mlora_set_stage_events(None)
+    def run_inst(self):
+        if self.inst is not None:
+            self.inst.replay()
+        else:
+            self.ml.mlora_set_stage_events(self.ev)
+            try:
+                self.step()
+            finally:
+                self.ml.mlora_set_stage_events(None)
 
-        for _ in range(args.warmup):
-            flush()
-            run()
-            flush()
-            run_inst()
-        stream.synchronize()
-        ids_host = ids.cpu().numpy()
-        alg = algorithmic(s, ids_host, inp.token_lora_idx.numpy() if s.has_lora else None)
+    def alg(self):
+        return algorithmic(self.s, self.ids.cpu().numpy(),
+                           self.inp.token_lora_idx.numpy() if self.s.has_lora else None)
 
-        barrier(world)
-        torch.cuda.synchronize(device)
-        step_ms, inst_ms, stage_ms = [], [], {n: [] for n in ml.STAGE_NAMES}
-        with ClockSampler(local_rank) as clocks:
-            for _ in range(args.steps):
+    def time(self, flush, steps: int, warmup: int, world: int = 1, clocks=None):
+        """W warm-up steps, then K timed steps of the plain graph and K of the
+        instrumented one, each after an L2 flush and bracketed by events on
+        the layer's stream."""
+        ml = self.ml
+        st0 = torch.cuda.Event(enable_timing=True)
+        st1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(self.stream):
+            for _ in range(warmup):
                 flush()
-                step_start.record(stream)
-                run()
-                step_end.record(stream)
-                stream.synchronize()
-                step_ms.append(step_start.elapsed_time(step_end))
-            torch.cuda.synchronize(device)
+                self.run_plain()
+                flush()
+                self.run_inst()
+            self.stream.synchronize()
             barrier(world)
-            # per-kernel times: as many steps of the instrumented graph
-            for _ in range(args.steps):
-                flush()
-                step_start.record(stream)
-                run_inst()
-                step_end.record(stream)
-                stream.synchronize()
-                inst_ms.append(step_start.elapsed_time(step_end))
-                for i, n in enumerate(ml.STAGE_NAMES):
-                    stage_ms[n].append(ev[i].elapsed_time(ev[i + 1]))
-        torch.cuda.synchronize(device)
-        barrier(world)
-        launches_per_step = 5  # route, align, gather, experts, combine
+            torch.cuda.synchronize(self.device)
+            step_ms, inst_ms, stage_ms = [], [], {n: [] for n in ml.STAGE_NAMES}
+            if clocks is not None:
+                clocks.__enter__()
+            try:
+                for _ in range(steps):
+                    flush()
+                    st0.record(self.stream)
+                    self.run_plain()
+                    st1.record(self.stream)
+                    self.stream.synchronize()
+                    step_ms.append(st0.elapsed_time(st1))
+                torch.cuda.synchronize(self.device)
+                barrier(world)
+                # per-kernel times: as many steps of the instrumented graph
+                for _ in range(steps):
+                    flush()
+                    st0.record(self.stream)
+                    self.run_inst()
+                    st1.record(self.stream)
+                    self.stream.synchronize()
+                    inst_ms.append(st0.elapsed_time(st1))
+                    for i, n in enumerate(ml.STAGE_NAMES):
+                        stage_ms[n].append(self.ev[i].elapsed_time(self.ev[i + 1]))
+            finally:
+                if clocks is not None:
+                    clocks.__exit__(None, None, None)
+            torch.cuda.synchronize(self.device)
+            barrier(world)
+            status = ml.mlora_moe_read_status(self.ws, stream=self.stream)
+            if status != 0:
+                raise RuntimeError(f"{self.s.name}: device status {status:#x} after the timed steps")
+        return dict(step_ms=step_ms, inst_ms=float(np.mean(inst_ms)),
+                    stage_avg={n: float(np.mean(v)) for n, v in stage_ms.items()})
 
-        # end to end through the public API with host buffers: H2D of the
-        # step's inputs from pinned memory (one copy), the layer, D2H of the
-        # output, captured with the layer in one CUDA graph
-        h_y = torch.empty((s.M, s.H), dtype=torch.bfloat16).pin_memory()
-        bi = in_bytes
-        bo = h_y.numel() * 2
+    def time_e2e(self, steps: int, warmup: int, world: int):
+        """The same step end to end with host buffers: every step copies its
+        inputs from pinned host memory (one H2D), runs the layer and reads y
+        back (one D2H), captured with the layer in one CUDA graph; host clock,
+        one stream synchronisation per step."""
+        h_y = torch.empty((self.s.M, self.s.H), dtype=torch.bfloat16).pin_memory()
 
-        def e2e_body():
-            d_in.copy_(h_in, non_blocking=True)
-            step()
-            h_y.copy_(y, non_blocking=True)
+        def body():
+            self.d_in.copy_(self.h_in, non_blocking=True)
+            self.step()
+            h_y.copy_(self.y, non_blocking=True)
 
-        e2e_graph = None
-        if not args.no_graph:
-            e2e_graph = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(e2e_graph, stream=stream):
-                e2e_body()
+        with torch.cuda.stream(self.stream):
+            g = None
+            if self.plain is not None:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=self.stream):
+                    body()
 
-        def e2e_step():
-            if e2e_graph is not None:
-                e2e_graph.replay()
-            else:
-                e2e_body()
-            stream.synchronize()
+            def e2e_step():
+                if g is not None:
+                    g.replay()
+                else:
+                    body()
+                self.stream.synchronize()
 
-        for _ in range(max(1, args.warmup)):
-            e2e_step()
-        barrier(world)
-        t0 = time.perf_counter()
-        for _ in range(args.steps):
-            e2e_step()
-        e2e_s = time.perf_counter() - t0
-        status = ml.mlora_moe_read_status(ws, stream=stream)
-        if status != 0:
-            raise RuntimeError(f"device status {status:#x} after the timed steps")
+            for _ in range(max(1, warmup)):
+                e2e_step()
+            barrier(world)
+            t0 = time.perf_counter()
+            for _ in range(steps):
+                e2e_step()
+            e2e_s = time.perf_counter() - t0
+            status = self.ml.mlora_moe_read_status(self.ws, stream=self.stream)
+            if status != 0:
+                raise RuntimeError(f"device status {status:#x} after the end-to-end steps")
+        return e2e_s, self.in_bytes, h_y.numel() * 2
 
-    total_ms, _, _ = aggregate(step_ms, s.M, world, device)
-    e2e_s = reduce_max(e2e_s, world, device)
-    stage_avg = {n: float(np.mean(v)) for n, v in stage_ms.items()}
-    return dict(inp=inp, alg=alg, total_ms=total_ms, step_ms=step_ms, inst_ms=float(np.mean(inst_ms)),
-                stage_avg=stage_avg, e2e_s=e2e_s, bi=bi,
-                bo=bo, clocks=clocks.summary(), launches=launches_per_step * args.steps)
+
+def roofline_fields(s: wl.Spec, alg: dict, kernel_ms: float, layer_ms: float, peaks: dict) -> dict:
+    """The experts kernel's and the whole layer's fraction of the roofline
+    that bounds the workload: bf16 tensor peak for prefill, HBM otherwise."""
+    st = alg["stages"]["experts"]
+    if s.name == "prefill":
+        kernel = st["flops"] / (kernel_ms / 1e3) / 1e12
+        layer = alg["layer_flops"] / (layer_ms / 1e3) / 1e12
+        return {"bound": "tensor", "unit": "TFLOP/s", "peak": peaks["bf16_tflops"], "experts_achieved": kernel,
+                "experts_frac": kernel / peaks["bf16_tflops"], "layer_frac": layer / peaks["bf16_tflops"]}
+    kernel = st["bytes"] / (kernel_ms / 1e3) / 1e9
+    layer = alg["layer_bytes"] / (layer_ms / 1e3) / 1e9
+    return {"bound": "hbm", "unit": "GB/s", "peak": peaks["hbm_gbs"], "experts_achieved": kernel,
+            "experts_frac": kernel / peaks["hbm_gbs"], "layer_frac": layer / peaks["hbm_gbs"]}
+
+
+def workload_entry(s: wl.Spec, t: dict, alg: dict, peaks: dict) -> dict:
+    ms = float(np.mean(t["step_ms"]))
+    kernel_ms = t["stage_avg"]["experts"]
+    e = {"workload": workload_config(s)["workload"], "M": s.M, "us_per_layer": ms * 1e3,
+         "tokens_per_s": s.M / (ms / 1e3), "experts_us": kernel_ms * 1e3,
+         "stage_us": {k: v * 1e3 for k, v in t["stage_avg"].items()},
+         "algorithmic_bytes": alg["layer_bytes"], "algorithmic_flops": alg["layer_flops"],
+         "experts_touched": alg["experts"], "adapter_pairs_touched": alg["pairs"]}
+    e.update(roofline_fields(s, alg, kernel_ms, ms, peaks))
+    return e
+
+
+def run_sweep(args, device, flush, peaks, skip_label=None, skip_entry=None):
+    """Every workload of SWEEP on this device, one at a time (inputs freed in
+    between), with the same timing as the headline."""
+    out = {}
+    sampler = ClockSampler(device.index or 0)
+    for label, name, over in SWEEP:
+        if label == skip_label and skip_entry is not None:
+            out[label] = skip_entry
+            continue
+        s = wl.spec(name, **over)
+        run = LayerRun(s, device, not args.no_graph)
+        t = run.time(flush, steps=args.steps, warmup=max(3, min(args.warmup, 5)))
+        out[label] = workload_entry(s, t, run.alg(), peaks)
+        del run
+        torch.cuda.empty_cache()
+    return out
+
+
+def sweep_label(s: wl.Spec, overrides: dict):
+    for label, name, over in SWEEP:
+        if name == s.name and over == overrides:
+            return label
+    return None
+
+
+def relaunch_replicas(args, argv) -> int:
+    """`--gpus N` without a launcher: start N ranks of this script under
+    torch.distributed.run on this node (one replica per GPU)."""
+    import socket
+    n_dev = torch.cuda.device_count()
+    if n_dev < args.gpus:
+        print(f"bench.py: --gpus {args.gpus} asks for more GPUs than this node has ({n_dev})", file=sys.stderr)
+        return 2
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={args.gpus}",
+           "--master-addr=127.0.0.1", f"--master-port={port}", os.path.abspath(__file__),
+           *(sys.argv[1:] if argv is None else argv)]
+    return subprocess.call(cmd)
 
 
 def main(argv=None):
     args = parse_args(argv)
     rank, world, local_rank = dist_env()
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ and args.impl == "mlora":
+        return relaunch_replicas(args, argv)
     overrides = {} if args.M is None else {"M": args.M}
     s = wl.spec(args.workload, **overrides)
     if args.impl == "reference":
@@ -464,29 +591,33 @@ def main(argv=None):
         import torch.distributed as dist
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
-    res = run_gpu(args, s, rank, world, local_rank)
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    peaks, peak_src = load_peaks()
+    flush = L2Flush(device)
+    run = LayerRun(s, device, not args.no_graph, packed=True)
+    clocks = ClockSampler(local_rank)
+    t = run.time(flush, args.steps, args.warmup, world, clocks=clocks)
+    e2e_s, bi, bo = run.time_e2e(args.steps, args.warmup, world)
+    alg = run.alg()
+    total_ms, _, _ = aggregate(t["step_ms"], s.M, world, device)
+    e2e_s = reduce_max(e2e_s, world, device)
+    inp = run.inp
+    headline_entry = workload_entry(s, t, alg, peaks)
+    del run
+    torch.cuda.empty_cache()
+    workloads = None
+    if not args.no_workloads and world == 1 and args.M is None:
+        workloads = run_sweep(args, device, flush, peaks, sweep_label(s, overrides), headline_entry)
     if rank == 0:
-        peaks, peak_src = load_peaks()
-        alg = res["alg"]
-        ms_per_step = res["total_ms"] / args.steps
+        ms_per_step = total_ms / args.steps
         tokens = s.M * world
         value = tokens / (ms_per_step / 1e3)
-        # dominant kernel and its roofline
-        dom = max(res["stage_avg"], key=lambda n: res["stage_avg"][n])
-        dom_ms = res["stage_avg"][dom]
-        st = alg["stages"].get(dom, {"bytes": 0, "flops": 0})
-        bound = "tensor" if s.name == "prefill" else "hbm"
-        if bound == "hbm":
-            achieved = st["bytes"] / (dom_ms / 1e3) / 1e9
-            peak, unit = peaks["hbm_gbs"], "GB/s"
-        else:
-            achieved = st["flops"] / (dom_ms / 1e3) / 1e12
-            peak, unit = peaks["bf16_tflops"], "TFLOP/s"
-        layer_hbm_frac = alg["layer_bytes"] / (ms_per_step / 1e3) / 1e9 / peaks["hbm_gbs"]
-        layer_tc_frac = alg["layer_flops"] / (ms_per_step / 1e3) / 1e12 / peaks["bf16_tflops"]
+        dom_ms = t["stage_avg"]["experts"]
+        rf = roofline_fields(s, alg, dom_ms, ms_per_step, peaks)
         cpu = None
         if not args.no_cpu_baseline and world == 1:
-            cpu = cpu_baseline(res["inp"], args.cpu_seconds)
+            cpu = cpu_baseline(inp, args.cpu_seconds)
             cpu.pop("seconds", None)
         cfg = workload_config(s)
         cfg.update({"parallelism": f"replicas x{world}" if world > 1 else "single GPU",
@@ -497,20 +628,21 @@ def main(argv=None):
             "warmup": args.warmup, "ms_per_step": ms_per_step, "us_per_layer": ms_per_step * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded, random-init weights)", "config": cfg,
-            "roofline": {"bound": bound, "kernel": dom, "achieved": achieved, "peak": peak, "unit": unit,
-                         "frac": achieved / peak, "peak_source": peak_src,
-                         "traffic": profiled_traffic(dom, s.name) if args.M is None else None,
+            "roofline": {"bound": rf["bound"], "kernel": "experts", "achieved": rf["experts_achieved"],
+                         "peak": rf["peak"], "unit": rf["unit"], "frac": rf["experts_frac"],
+                         "peak_source": peak_src,
+                         "traffic": profiled_traffic("experts", s.name) if args.M is None else None,
                          "kernel_ms": dom_ms},
-            "layer": {"hbm_frac": layer_hbm_frac, "tensor_frac": layer_tc_frac,
-                      "ms_per_step_with_stage_events": res["inst_ms"],
+            "layer": {"frac": rf["layer_frac"], "ms_per_step_with_stage_events": t["inst_ms"],
                       "algorithmic_bytes": alg["layer_bytes"], "algorithmic_flops": alg["layer_flops"],
                       "experts_touched": alg["experts"], "adapter_pairs_touched": alg["pairs"],
-                      "stage_us": {k: v * 1e3 for k, v in res["stage_avg"].items()}},
+                      "stage_us": {k: v * 1e3 for k, v in t["stage_avg"].items()}},
+            "workloads": workloads,
             "cpu_baseline": cpu,
-            "e2e": {"value": tokens * args.steps / res["e2e_s"], "unit": "tokens/s",
-                    "h2d_bytes_per_step": res["bi"], "d2h_bytes_per_step": res["bo"]},
-            "gpu_launches": res["launches"],
-            "clocks": res["clocks"],
+            "e2e": {"value": tokens * args.steps / e2e_s, "unit": "tokens/s",
+                    "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo},
+            "gpu_launches": 5 * args.steps,  # route, align, gather, experts, combine per step
+            "clocks": clocks.summary(),
         }
         print(json.dumps(out), flush=True)
     if world > 1:
@@ -521,30 +653,32 @@ def main(argv=None):
 
 
 def main_reference(args, s: wl.Spec, rank: int, world: int):
-    """The oracle timed on the host cores as the reference arm."""
+    """The oracle timed on the host cores as the reference arm: each step is
+    the route + forward of a bounded token sample of the batch; the per-step
+    time is scaled to the whole batch."""
     if rank != 0:
         return 0
     import oracle
     inp = wl.make(s)
     oracle.load()
-    ids, w = oracle.moe_route(inp.logits.numpy(), None if inp.bias is None else inp.bias.numpy(), s.top_k,
-                              s.scoring, s.renormalize, s.n_shared, s.routed_scaling_factor)
+    hb = host_bits(inp)
     cores = os.cpu_count() or 1
     n = min(s.M, cores)
     for _ in range(args.warmup):
-        oracle_sample(inp, ids, w, n)
+        oracle_sample(inp, n, hb)
     total, tokens = 0.0, 0
     for _ in range(args.steps):
-        dt, k = oracle_sample(inp, ids, w, n)
+        dt, k = oracle_sample(inp, n, hb)
         total += dt
         tokens += k
     value = tokens / total
     cfg = workload_config(s)
-    cfg.update({"parallelism": "host cores", "global_batch": s.M})
-    cpu = {"value": value, "unit": "tokens/s", "cores": min(cores, n), "kind": "oracle",
-           "sample": f"first {n} of the {s.M} tokens of the {s.name} batch per step"}
+    sample = (f"route + forward of the first {n} of the {s.M} tokens of the {s.name} batch per step; "
+              f"ms_per_step is that time scaled to the whole {s.M}-token batch")
+    cfg.update({"parallelism": "host cores", "global_batch": s.M, "sample": sample})
+    cpu = {"value": value, "unit": "tokens/s", "cores": min(cores, n), "kind": "oracle", "sample": sample}
     out = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-           "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": s.M / value * 1e3,
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
            "data": "synthetic (seeded, random-init weights)", "config": cfg, "cpu_baseline": cpu,
            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}

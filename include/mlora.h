@@ -22,10 +22,13 @@
  *  - Tensor pointers are DEVICE pointers owned by the caller: contiguous,
  *    row-major, 16-byte aligned.  The library never allocates or frees
  *    device memory and never synchronises the stream, except
- *    mlora_moe_read_status, which waits for the stream by design.
+ *    mlora_moe_read_status(_static), which waits for the stream by design.
  *  - `stream` is a cudaStream_t passed as void*; NULL is the legacy default
  *    stream.  All work is enqueued on it, so every call can be captured into
- *    a CUDA graph (mlora_moe_read_status excepted).
+ *    a CUDA graph (mlora_moe_read_status(_static) excepted).
+ *  - The work runs on the current device (cudaGetDevice).  Outside stream
+ *    capture, a tensor pointer that is device memory of another GPU is
+ *    refused with MLORA_ERR_INVALID_ARG before anything is enqueued.
  *  - bf16 tensors are passed as void*.
  *  - Arguments are validated on the host before anything is enqueued; a
  *    failed check returns a non-zero status and enqueues nothing.  Values
@@ -85,7 +88,10 @@ enum { MLORA_SCORE_SOFTMAX = 0, MLORA_SCORE_SIGMOID_BIAS = 1 };
  *    1 / routed_scaling_factor.
  * Constraints: 0 <= M, 1 <= top_k <= E <= MLORA_MAX_EXPERTS, 0 <= n_shared,
  * K' <= MLORA_MAX_TOPK, routed_scaling_factor > 0 when n_shared > 0.
- * Logits must be finite.
+ * Logits should be finite.  A NaN key (NaN logit, or NaN bias) ranks below
+ * every number, ties among NaN keys going to the lower id, so the ids stay
+ * in [0, E) whatever the input; the weights of a token with NaN logits are
+ * NaN.
  */
 mlora_status mlora_moe_route(const float* logits, const float* bias, int M, int E, int top_k, int scoring,
                              int renormalize, int n_shared, float routed_scaling_factor, int32_t* topk_ids,
@@ -172,15 +178,17 @@ mlora_status mlora_moe_forward(const void* x, const void* w13, const void* w2, c
  *    MLORA_ERR_WORKSPACE and enqueue nothing (64 MiB holds, e.g., the
  *    M=64, H=I=2880, E=32, top_k=4, L=8, rank=16 layer).
  *  - The first call on a device looks up the array's device address
- *    (once per device, with that device current); make that first call
- *    before any stream capture on the device.
+ *    (once per device and CUDA context, with that device current); make
+ *    that first call before any stream capture on the device.  After
+ *    cudaDeviceReset the device's context is a new one and the next call
+ *    looks the address up again, so it too should precede any capture.
  *  - Every call shares the one array and it keeps the last call's
  *    contents.  The call clears what must start at zero (its status word)
  *    itself; everything else is written before it is read.  Calls whose
  *    work overlaps on the GPU (different streams, or concurrent host
  *    threads) race on the array: serialise them.
- *  - mlora_moe_read_status on the array is not offered; the device status
- *    bits are only readable through mlora_moe_forward's workspace.
+ *  - The device status bits of the last call on the current device are
+ *    read with mlora_moe_read_status_static.
  */
 #define MLORA_STATIC_WORKSPACE_BYTES (64u << 20)
 mlora_status mlora_moe_forward_static(const void* x, const void* w13, const void* w2, const void* A13,
@@ -194,6 +202,18 @@ mlora_status mlora_moe_forward_static(const void* x, const void* w13, const void
  * (MLORA_DEV_* bits, 0 = clean) to *host_status after waiting for `stream`.
  */
 mlora_status mlora_moe_read_status(const void* workspace, uint32_t* host_status, void* stream);
+
+/*
+ * mlora_moe_read_status for mlora_moe_forward_static: copies the device
+ * status word (MLORA_DEV_* bits, 0 = clean) of the last static forward on
+ * the current device to *host_status after waiting for `stream`.  Like the
+ * static forward itself it has no counterpart on the pages; it lets callers
+ * without a workspace see a wait timeout or a bad expert or adapter id.
+ * It allocates nothing.  The word belongs to whichever static call ran
+ * last on the device: read it on the stream that call used, before another
+ * static call is enqueued.
+ */
+mlora_status mlora_moe_read_status_static(uint32_t* host_status, void* stream);
 
 /*
  * Measurement hook.  Sets, for the calling host thread, MLORA_STAGE_EVENTS

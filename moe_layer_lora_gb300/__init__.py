@@ -21,6 +21,7 @@ from ._lib import (  # noqa: F401
     mlora_moe_forward,
     mlora_moe_forward_static,
     mlora_moe_read_status,
+    mlora_moe_read_status_static,
     mlora_moe_route,
     mlora_moe_workspace_size,
     mlora_set_stage_events,

@@ -77,6 +77,10 @@ def load(path: str = LIB_PATH):
     lib.mlora_set_wait_test.restype = i
     lib.mlora_status_string.argtypes = [i]
     lib.mlora_status_string.restype = ctypes.c_char_p
+    lib.mlora_moe_forward_static.argtypes = [P] * 10 + [i] * 7 + [f, i, f, P, P]
+    lib.mlora_moe_forward_static.restype = i
+    lib.mlora_moe_read_status_static.argtypes = [ctypes.POINTER(ctypes.c_uint32), P]
+    lib.mlora_moe_read_status_static.restype = i
     _lib = lib
     return lib
 
@@ -95,9 +99,15 @@ def _ptr(t: Optional[torch.Tensor]):
     return ctypes.c_void_p(t.data_ptr())
 
 
-def _stream(stream) -> ctypes.c_void_p:
+def _stream(stream, device=None) -> ctypes.c_void_p:
+    """The stream handle to enqueue on: `stream`, else the current stream of
+    `device`.  A stream of another device than the tensors' is refused (the
+    library launches on the current device, which the callers below set to
+    the tensors' device)."""
     if stream is None:
-        stream = torch.cuda.current_stream()
+        stream = torch.cuda.current_stream(device)
+    elif device is not None and stream.device != torch.device(device):
+        raise ValueError(f"stream is on {stream.device}, the tensors on {device}")
     return ctypes.c_void_p(stream.cuda_stream)
 
 
@@ -148,7 +158,11 @@ def _layer_args(x, w13, w2, A13, B13, A2, B2, token_lora_idx, topk_ids, topk_w, 
               (topk_w, torch.float32, "topk_w", (M, KT))]
     if y is not None:
         checks.append((y, torch.bfloat16, "y", (M, H)))
-    lora = all(t is not None for t in (A13, B13, A2, B2, token_lora_idx))
+    given = [t is not None for t in (A13, B13, A2, B2, token_lora_idx)]
+    if any(given) and not all(given):
+        raise ValueError("A13, B13, A2, B2 and token_lora_idx are given together (adapters) or all None "
+                         "(no adapters)")
+    lora = all(given)
     L = r = 0
     if lora:
         if not isinstance(A13, torch.Tensor) or A13.dim() != 4:
@@ -189,8 +203,10 @@ def mlora_moe_route(logits: torch.Tensor, bias: Optional[torch.Tensor], top_k: i
         topk_ids = torch.empty((M, KT), dtype=torch.int32, device=dev)
     if topk_w is None:
         topk_w = torch.empty((M, KT), dtype=torch.float32, device=dev)
-    st = load().mlora_moe_route(_ptr(logits), _ptr(bias), M, E, top_k, scoring, renormalize, n_shared,
-                                float(routed_scaling_factor), _ptr(topk_ids), _ptr(topk_w), _stream(stream))
+    with torch.cuda.device(dev):
+        st = load().mlora_moe_route(_ptr(logits), _ptr(bias), M, E, top_k, scoring, renormalize, n_shared,
+                                    float(routed_scaling_factor), _ptr(topk_ids), _ptr(topk_w),
+                                    _stream(stream, dev))
     _check("mlora_moe_route", st)
     return topk_ids, topk_w
 
@@ -210,8 +226,9 @@ def mlora_moe_align(topk_ids: torch.Tensor, E_tot: int, block_m: int, stream=Non
     sorted_ids = torch.empty(mp, dtype=torch.int32, device=dev)
     expert_ids = torch.empty(mp // block_m, dtype=torch.int32, device=dev)
     npp = torch.empty(1, dtype=torch.int32, device=dev)
-    st = load().mlora_moe_align(_ptr(topk_ids), M, KT, E_tot, block_m, _ptr(sorted_ids), _ptr(expert_ids),
-                                _ptr(npp), _stream(stream))
+    with torch.cuda.device(dev):
+        st = load().mlora_moe_align(_ptr(topk_ids), M, KT, E_tot, block_m, _ptr(sorted_ids), _ptr(expert_ids),
+                                    _ptr(npp), _stream(stream, dev))
     _check("mlora_moe_align", st)
     return sorted_ids, expert_ids, npp
 
@@ -231,11 +248,12 @@ def mlora_moe_forward(x, w13, w2, A13, B13, A2, B2, token_lora_idx, topk_ids, to
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=x.device)
     _need(workspace, torch.uint8, "workspace", None, x.device)
-    st = load().mlora_moe_forward(
-        _ptr(x), _ptr(w13), _ptr(w2), _ptr(A13) if lora else None, _ptr(B13) if lora else None,
-        _ptr(A2) if lora else None, _ptr(B2) if lora else None, _ptr(token_lora_idx) if lora else None,
-        _ptr(topk_ids), _ptr(topk_w), M, H, I, E_tot, KT, L, r, float(scaling), int(n_shared),
-        float(out_scale), _ptr(y), _ptr(workspace), workspace.numel(), _stream(stream))
+    with torch.cuda.device(x.device):
+        st = load().mlora_moe_forward(
+            _ptr(x), _ptr(w13), _ptr(w2), _ptr(A13) if lora else None, _ptr(B13) if lora else None,
+            _ptr(A2) if lora else None, _ptr(B2) if lora else None, _ptr(token_lora_idx) if lora else None,
+            _ptr(topk_ids), _ptr(topk_w), M, H, I, E_tot, KT, L, r, float(scaling), int(n_shared),
+            float(out_scale), _ptr(y), _ptr(workspace), workspace.numel(), _stream(stream, x.device))
     _check("mlora_moe_forward", st)
     return y
 
@@ -249,26 +267,34 @@ def mlora_moe_forward_static(x, w13, w2, A13, B13, A2, B2, token_lora_idx, topk_
     """The layer with the library's fixed scratch array instead of a
     workspace: for callers that cannot allocate device memory where they
     run it.  Only y is allocated here (by torch) when not passed in."""
-    lib = load()
-    fn = lib.mlora_moe_forward_static
-    if fn.argtypes is None:
-        P, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
-        fn.argtypes = [P] * 10 + [i] * 7 + [f, i, f, P, P]
-        fn.restype = i
     M, H, I, E_tot, KT, L, r, lora = _layer_args(x, w13, w2, A13, B13, A2, B2, token_lora_idx, topk_ids, topk_w, y)
     if y is None:
         y = torch.empty((M, H), dtype=torch.bfloat16, device=x.device)
-    st = fn(_ptr(x), _ptr(w13), _ptr(w2), _ptr(A13) if lora else None, _ptr(B13) if lora else None,
+    with torch.cuda.device(x.device):
+        st = load().mlora_moe_forward_static(
+            _ptr(x), _ptr(w13), _ptr(w2), _ptr(A13) if lora else None, _ptr(B13) if lora else None,
             _ptr(A2) if lora else None, _ptr(B2) if lora else None, _ptr(token_lora_idx) if lora else None,
-            _ptr(topk_ids), _ptr(topk_w), M, H, I, E_tot, KT, L, r, float(scaling),
-            int(n_shared), float(out_scale), _ptr(y), _stream(stream))
+            _ptr(topk_ids), _ptr(topk_w), M, H, I, E_tot, KT, L, r, float(scaling), int(n_shared),
+            float(out_scale), _ptr(y), _stream(stream, x.device))
     _check("mlora_moe_forward_static", st)
     return y
 
 
+def mlora_moe_read_status_static(device=None, stream=None) -> int:
+    """Device status word of the last mlora_moe_forward_static on `device`
+    (default: the current device); waits for the stream."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    out = ctypes.c_uint32(0)
+    with torch.cuda.device(dev):
+        st = load().mlora_moe_read_status_static(ctypes.byref(out), _stream(stream, dev))
+    _check("mlora_moe_read_status_static", st)
+    return int(out.value)
+
+
 def mlora_moe_read_status(workspace: torch.Tensor, stream=None) -> int:
     out = ctypes.c_uint32(0)
-    st = load().mlora_moe_read_status(_ptr(workspace), ctypes.byref(out), _stream(stream))
+    with torch.cuda.device(workspace.device):
+        st = load().mlora_moe_read_status(_ptr(workspace), ctypes.byref(out), _stream(stream, workspace.device))
     _check("mlora_moe_read_status", st)
     return int(out.value)
 

@@ -21,6 +21,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <initializer_list>
 #include <mutex>
 
 #include "internal.cuh"
@@ -92,6 +93,32 @@ mlora_status cuda_fail(cudaError_t e, const char* where) {
     }();
     if (verbose) fprintf(stderr, "libmlora: %s: %s\n", where, cudaGetErrorString(e));
     return MLORA_ERR_CUDA;
+}
+
+// Outside stream capture: does any of the pointers name device memory of
+// a GPU other than the current one?  The kernels run on the current device,
+// and their tensor maps and loads would then reach another GPU's memory.
+// (During capture the check is skipped: the capture's own eager calls, made
+// before it, ran it.)  Host, managed and unregistered pointers pass.
+bool foreign_device_memory(cudaStream_t s, std::initializer_list<const void*> ptrs) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    if (cs != cudaStreamCaptureStatusNone) return false;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    for (const void* p : ptrs) {
+        if (!p) continue;
+        cudaPointerAttributes a{};
+        if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+            (void)cudaGetLastError();
+            continue;
+        }
+        if (a.type == cudaMemoryTypeDevice && a.device != dev) return true;
+    }
+    return false;
 }
 
 }  // namespace
@@ -203,6 +230,8 @@ mlora_status mlora_moe_route(const float* logits, const float* bias, int M, int 
     if (n_shared > 0 && !(routed_scaling_factor > 0.0f)) return MLORA_ERR_INVALID_ARG;
     if (M == 0) return MLORA_OK;
     if (!logits || !topk_ids || !topk_w) return MLORA_ERR_INVALID_ARG;
+    if (foreign_device_memory(static_cast<cudaStream_t>(stream), {logits, bias, topk_ids, topk_w}))
+        return MLORA_ERR_INVALID_ARG;
     const float inv_rsf = n_shared > 0 ? 1.0f / routed_scaling_factor : 0.0f;
     return cuda_status(launch_route(logits, scoring == MLORA_SCORE_SIGMOID_BIAS ? bias : nullptr, M, E, top_k,
                                     scoring, renormalize, n_shared, inv_rsf, topk_ids, topk_w,
@@ -222,6 +251,8 @@ mlora_status mlora_moe_align(const int32_t* topk_ids, int M, int K_total, int E_
     const long S = static_cast<long>(M) * K_total;
     if (S + static_cast<long>(E_tot) * block_m >= 0x7fffffffL) return MLORA_ERR_SHAPE;
     if (!num_post_padded || (S > 0 && (!topk_ids || !sorted_ids || !expert_ids))) return MLORA_ERR_INVALID_ARG;
+    if (foreign_device_memory(static_cast<cudaStream_t>(stream), {topk_ids, sorted_ids, expert_ids, num_post_padded}))
+        return MLORA_ERR_INVALID_ARG;
     const long mp = align_max_padded(S, E_tot, block_m);
     return cuda_status(launch_align(topk_ids, S, E_tot, block_m, mp, sorted_ids, expert_ids, num_post_padded,
                                     nullptr, nullptr, static_cast<cudaStream_t>(stream)));
@@ -266,6 +297,9 @@ mlora_status mlora_moe_forward(const void* x, const void* w13, const void* w2, c
             if (!aligned16(ptr)) return MLORA_ERR_INVALID_ARG;
         if (reinterpret_cast<uintptr_t>(token_lora_idx) & 3u) return MLORA_ERR_INVALID_ARG;
     }
+    if (foreign_device_memory(static_cast<cudaStream_t>(stream), {x, w13, w2, topk_ids, topk_w, y, workspace,
+                                                                  lora ? A13 : nullptr, lora ? token_lora_idx : nullptr}))
+        return MLORA_ERR_INVALID_ARG;
     const Sizes z = make_sizes(M, H, I, E_tot, K_total, L_eff, r_eff);
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return MLORA_ERR_WORKSPACE;
     const Workspace ws = carve_workspace(z, workspace);

@@ -10,6 +10,9 @@
 //
 // Each lane holds experts lane, lane+32, ... in registers (coalesced row
 // read); every selection step is one butterfly arg-max over the warp.
+// Non-finite input never yields an id outside [0, E): a NaN key ranks
+// last (ties among them to the lower id); the weights of such a token are
+// then NaN as well.
 #include <math.h>
 
 #include "internal.cuh"
@@ -40,8 +43,11 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ lo
         const int e = lane + 32 * v;
         if (e < E) {
             raw[v] = l[e];
-            key[v] = scoring == MLORA_SCORE_SOFTMAX ? raw[v]
-                                                    : 1.0f / (1.0f + expf(-raw[v])) + (bias ? bias[e] : 0.0f);
+            const float k = scoring == MLORA_SCORE_SOFTMAX ? raw[v]
+                                                           : 1.0f / (1.0f + expf(-raw[v])) + (bias ? bias[e] : 0.0f);
+            // a NaN key ranks below every number (and equal NaN keys go to
+            // the lower id), so every selected id is a real expert
+            key[v] = isnan(k) ? -INFINITY : k;
         } else {
             raw[v] = -INFINITY;
             key[v] = -INFINITY;

@@ -81,6 +81,26 @@ def oracle_forward(inp: wl.Inputs, ids, w, rows=None, lora=True, idx=None):
                               w[sel].astype(np.float32), s.scaling, s.out_scale)
 
 
+def assert_unambiguous(inp: wl.Inputs):
+    """Sigmoid+bias routing takes its integer decision on an fp32 key,
+    sigmoid(l) + b, on both sides with each side's own expf.  The seeded
+    inputs must keep every key that decides the order (the first top_k + 1
+    of a token) more than 8 ulp from its neighbour, so that a 1-2 ulp expf
+    difference cannot change the ids; a closer pair is an ambiguous input,
+    reported as such rather than as an id mismatch."""
+    s = inp.spec
+    if s.scoring != wl.SCORE_SIGMOID_BIAS or s.M == 0:
+        return
+    l = inp.logits.numpy().astype(np.float32)
+    b = np.zeros(s.E, np.float32) if inp.bias is None else inp.bias.numpy().astype(np.float32)
+    key = (np.float32(1) / (np.float32(1) + np.exp(-l))) + b[None, :]
+    srt = -np.sort(-key, axis=1)[:, : s.top_k + 1]
+    gaps = srt[:, :-1] - srt[:, 1:]
+    ulp = np.spacing(np.abs(srt[:, :-1])).astype(np.float64)
+    close = np.argwhere(~(gaps > 8 * ulp))
+    assert close.size == 0, f"ambiguous input: sigmoid+bias keys within 8 ulp at (token, rank) {close[:4].tolist()}"
+
+
 def check_route(ids_gpu, w_gpu, ids_ref, w_ref):
     ids_g = ids_gpu.cpu().numpy()
     assert np.array_equal(ids_g, ids_ref), f"route ids differ at {np.argwhere(ids_g != ids_ref)[:8]}"

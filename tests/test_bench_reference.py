@@ -25,3 +25,29 @@ def test_reference_arm_json_line():
     assert j["cpu_baseline"]["value"] == j["value"]
     assert j["e2e"] == {"value": j["value"], "unit": j["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
     assert j["config"]["workload"].startswith("tiny")
+
+
+def test_reference_arm_per_step_time_is_the_whole_batch():
+    """ms_per_step of the reference arm is the time of the whole batch (the
+    timed token sample scaled up), consistent with its tokens/s."""
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload", "tiny",
+                          "--steps", "1", "--warmup", "0"], capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    j = json.loads([l for l in out.stdout.splitlines() if l.startswith("{")][0])
+    M = j["config"]["M"]
+    assert abs(j["ms_per_step"] - M / j["value"] * 1e3) < 1e-6 * j["ms_per_step"]
+    assert "sample" in j["config"]
+
+
+def test_gpus_flag_without_launcher_checks_the_device_count():
+    """`--gpus N` with no launcher relaunches itself as N ranks; on a node
+    with fewer GPUs it says so and exits non-zero instead."""
+    import torch
+    if torch.cuda.device_count() >= 2:
+        import pytest
+        pytest.skip("needs a node with fewer than 2 GPUs")
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK")}
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2", "--steps", "1"],
+                         capture_output=True, text=True, timeout=300, cwd=ROOT, env=env)
+    assert out.returncode == 2
+    assert "more GPUs than this node has" in out.stderr

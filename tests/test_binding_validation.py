@@ -81,3 +81,25 @@ def test_route_refuses_mismatched_tensors():
 def test_align_refuses_wrong_ids():
     with pytest.raises(ValueError, match="topk_ids"):
         ml.mlora_moe_align(torch.zeros(M, K, dtype=torch.int64), E, 16)
+
+
+@pytest.mark.parametrize("missing", ["A13", "B13", "A2", "B2", "token_lora_idx"])
+def test_forward_refuses_a_partial_adapter_set(missing):
+    """Four of the five adapter tensors would otherwise run the layer
+    silently without adapters: all five or none."""
+    with pytest.raises(ValueError, match="all None"):
+        _forward(_layer(**{missing: None}))
+
+
+def test_stream_of_another_device_is_refused():
+    """The library launches on the current device, which the binding sets
+    to the tensors' device; a stream of another device is refused."""
+    from moe_layer_lora_gb300 import _lib
+
+    class FakeStream:
+        device = torch.device("cuda", 1)
+        cuda_stream = 0
+
+    with pytest.raises(ValueError, match="stream is on cuda:1"):
+        _lib._stream(FakeStream(), torch.device("cuda", 0))
+    assert _lib._stream(FakeStream(), torch.device("cuda", 1)).value is None

@@ -28,6 +28,7 @@ def checked_library():
 
 def _run(spec, rows=None):
     inp = wl.make(spec, device="cuda")
+    gu.assert_unambiguous(inp)
     d = gu.DeviceInputs(inp)
     ids, w = gu.gpu_route(d)
     L, r = (spec.L, spec.r) if spec.has_lora else (0, 0)

@@ -17,27 +17,12 @@ def _route_case(spec):
     d_logits = gu.dev(inp.logits)
     d_bias = gu.dev(inp.bias)
     ids_ref, w_ref = gu.oracle_route(inp)
-    if spec.scoring == wl.SCORE_SIGMOID_BIAS:
-        _assert_unambiguous(inp, ids_ref)
+    gu.assert_unambiguous(inp)
     ids, w = ml.mlora_moe_route(d_logits, d_bias, spec.top_k, spec.scoring, spec.renormalize, spec.n_shared,
                                 spec.routed_scaling_factor)
     torch.cuda.synchronize()
     gu.check_route(ids, w, ids_ref, w_ref)
     return ids_ref
-
-
-def _assert_unambiguous(inp, ids_ref):
-    """The integer decision is taken in fp32 on both sides with each side's
-    own expf; the seeded inputs must keep every key that decides the order
-    more than 8 ulp from its neighbour so that a 1-2 ulp expf difference
-    cannot change the result."""
-    s = inp.spec
-    l = inp.logits.numpy().astype(np.float32)
-    key = (np.float32(1) / (np.float32(1) + np.exp(-l))) + inp.bias.numpy()[None, :]
-    srt = -np.sort(-key, axis=1)[:, : s.top_k + 1]
-    gaps = srt[:, :-1] - srt[:, 1:]
-    ulp = np.spacing(np.abs(srt[:, :-1])).astype(np.float64)
-    assert (gaps > 8 * ulp).all(), "seeded input has a near-tie in the sigmoid+bias keys"
 
 
 @pytest.mark.parametrize("name", wl.WORKLOADS)
@@ -161,3 +146,23 @@ def test_align_random(case):
     else:
         ids = rng.integers(0, E, size=(M, K), dtype=np.int32)
     _align_case(ids, E, BM)
+
+
+@pytest.mark.parametrize("scoring", [wl.SCORE_SOFTMAX, wl.SCORE_SIGMOID_BIAS])
+def test_route_nan_keys_rank_last(scoring):
+    """A NaN key ranks below every number (ties among NaN keys to the lower
+    id), so ids stay in range: a row of NaN logits takes experts 0..k-1, and
+    a row with some NaN logits takes the top-k of its finite ones."""
+    E, k = 40, 4
+    logits = torch.randn(4, E, generator=torch.Generator().manual_seed(3), dtype=torch.float32)
+    logits[0] = float("nan")
+    logits[1, :5] = float("nan")
+    bias = (torch.randn(E, generator=torch.Generator().manual_seed(4)) * 0.5).float() if scoring else None
+    ids, _ = ml.mlora_moe_route(logits.cuda(), None if bias is None else bias.cuda(), k, scoring)
+    ids = ids.cpu().numpy()
+    assert ((ids >= 0) & (ids < E)).all()
+    assert ids[0].tolist() == [0, 1, 2, 3]
+    part_ids, _ = oracle.moe_route(logits[1:2, 5:].numpy(), None if bias is None else bias[5:].numpy(), k, scoring, 1)
+    assert ids[1].tolist() == (part_ids[0] + 5).tolist()
+    full_ids, _ = oracle.moe_route(logits[2:].numpy(), None if bias is None else bias.numpy(), k, scoring, 1)
+    assert np.array_equal(ids[2:], full_ids)

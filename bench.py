@@ -130,7 +130,7 @@ def algorithmic(s: wl.Spec, ids: np.ndarray, idx) -> dict:
         "experts": dict(bytes=n_exp * 3 * I * H * b + n_pairs * r * (2 * H + 3 * I) * b + S * (2 * H + 2 * I) * b,
                         flops=2.0 * S * 3 * H * I + 2.0 * a_slots * r * (2 * H + 3 * I)),
         "gather": dict(bytes=S * H * b * 2, flops=0.0),
-        "combine": dict(bytes=S * H * b + M * H * b, flops=2.0 * S * H),
+        "combine": dict(bytes=S * H * 4 + M * H * b, flops=2.0 * S * H),
         "align": dict(bytes=S * 4 * 3, flops=0.0),
     }
     layer_bytes = (n_exp * 3 * I * H * b + n_pairs * r * (2 * H + 3 * I) * b + 2 * M * H * b

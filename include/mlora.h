@@ -152,8 +152,9 @@ size_t mlora_moe_workspace_size(int M, int H, int I, int E_tot, int K_total, int
  * rank in {8, 16, ..., 64}; E_tot <= MLORA_MAX_EXPERTS; K' <= MLORA_MAX_TOPK;
  * workspace_bytes >= mlora_moe_workspace_size(...).
  * Intermediates: the adapter shrink result is kept as bf16 (s * x A^T), the
- * SwiGLU output as bf16, each slot's expert output as bf16, all
- * accumulation in fp32; y is rounded to bf16 (nearest even).
+ * SwiGLU output as bf16 (both feed the tensor cores), each slot's expert
+ * output as fp32, all accumulation in fp32; y is rounded to bf16 (nearest
+ * even).
  */
 mlora_status mlora_moe_forward(const void* x, const void* w13, const void* w2, const void* A13, const void* B13,
                                const void* A2, const void* B2, const int32_t* token_lora_idx,

@@ -478,6 +478,10 @@ long align_max_padded(long S, int E_tot, int block_m) {
 cudaError_t launch_align(const int32_t* ids, long S, int E_tot, int block_m, long max_padded, int32_t* sorted,
                          int32_t* expert_ids, int32_t* n_pad, uint32_t* status, const AlignExtra* extra,
                          cudaStream_t s) {
+    // small batches take the latency-lean kernel (same outputs, bit for bit)
+    if (align_small_fits(S, E_tot, block_m, max_padded, extra, false))
+        return launch_align_small(ids, S, E_tot, block_m, max_padded, sorted, expert_ids, n_pad, status, extra,
+                                  nullptr, s);
     const bool with_lora = extra && extra->token_lora_idx;
     void (*kernel)(const int32_t*, int, int, int, int, int32_t*, int32_t*, int32_t*, uint32_t*, int, int, int,
                    AlignExtra) = with_lora ? align_kernel<true> : align_kernel<false>;

@@ -1,0 +1,385 @@
+// align_small.cu -- sort and pad the routed slots by expert (align) for
+// batches of at most kSmallMaxSlots slots, and inside the forward the row
+// gather in the same launch.
+//
+// "[vllm] vLLM ROCm 환경에서 Shared-Expert Fusion을 통한 MoE 추론 성능 최적화",
+// section "코드 분석" item 2: the sort runs over E_tot = w13.shape[0]
+// experts, shared ones included.  The output contract is the one of
+// align.cu, bit for bit: experts ascending, each expert's slots f = m*K'+k
+// ascending, each list padded with the sentinel M*K' to a multiple of
+// block_m, sentinel / -1 tails; with adapters the same per-position adapter,
+// per-block adapter lists and shrink group numbering.
+//
+// Small batches are latency-bound: the large-batch kernel spends most of
+// its time in CTA-wide barriers.  Here 512 threads take at most 4 slots
+// each; warp w owns one contiguous run of slots and ranks them in rounds of
+// 32 (a slot's rank within its expert in the warp = the expert's slots in
+// the warp's earlier rounds + the earlier lanes of its round with the same
+// expert, from __match_any_sync), with no CTA barrier until every warp is
+// done; one pass over the per-warp counts then gives each warp's first
+// position per expert.  About eight barriers in all.
+//
+// The grid has several CTAs when the forward asks for the row gather: each
+// CTA computes the same (cheap) sort, CTA 0 alone writes the sort's outputs,
+// and every CTA copies the x rows of its share of the slots into their
+// sorted positions -- one launch and one dependency instead of two.
+#include <algorithm>
+#include <atomic>
+
+#include "internal.cuh"
+#include "ptx.cuh"
+
+namespace mlora {
+namespace {
+
+constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;
+constexpr int kRounds = kSmallMaxSlots / kThreads;  // slots per thread
+constexpr int kMaxSmem = 227 * 1024;
+constexpr int kScratch = 64;  // ints: scan scratch [0, 17), flags [48], largest count [49], gather list length [50]
+static_assert(kRounds * kThreads == kSmallMaxSlots, "slots per thread");
+
+// Exclusive scan of one int per thread over the CTA; the CTA total goes to
+// *total.  Three barriers (the last lets scratch be reused).
+__device__ int cta_exclusive_scan(int v, int* scratch, int* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int inc = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, inc, off);
+        if (lane >= off) inc += n;
+    }
+    if (lane == 31) scratch[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+        const int s = lane < kWarps ? scratch[lane] : 0;
+        int si = s;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, si, off);
+            if (lane >= off) si += n;
+        }
+        if (lane < kWarps) scratch[lane] = si - s;
+        if (lane == kWarps - 1) scratch[kWarps] = si;
+    }
+    __syncthreads();
+    const int excl = scratch[warp] + inc - v;
+    *total = scratch[kWarps];
+    __syncthreads();
+    return excl;
+}
+
+template <bool kWithLora, bool kGather>
+__global__ void __launch_bounds__(kThreads, 1)
+    align_small_kernel(const int32_t* __restrict__ ids, int S, int E_tot, int BM, int max_padded,
+                       int32_t* __restrict__ sorted, int32_t* __restrict__ expert_ids,
+                       int32_t* __restrict__ n_pad_out, uint32_t* __restrict__ status, AlignExtra ex,
+                       const uint4* __restrict__ x, int H8, int K_total, uint4* __restrict__ x_perm) {
+    extern __shared__ int smem_i[];
+    int* wcnt = smem_i;                  // [kWarps][E_tot] a warp's slots per expert, then its first offset
+    int* tot = wcnt + kWarps * E_tot;    // [E_tot] slots per expert
+    int* first = tot + E_tot;            // [E_tot] padded start of each expert
+    int* scratch = first + E_tot;        // [kScratch]
+    int* nad_s = scratch + kScratch;     // with adapters: [max_padded / BM] adapters per block
+    int* glist = nad_s + (kWithLora ? max_padded / BM : 0);  // gather: [2 * S] (position, token) of this CTA's rows
+    uint16_t* st_sorted = reinterpret_cast<uint16_t*>(glist + (kGather ? 2 * S : 0));  // [max_padded]
+    int16_t* st_lora = reinterpret_cast<int16_t*>(st_sorted + max_padded);            // with adapters: [max_padded]
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const bool writer = blockIdx.x == 0;  // CTA-uniform: the CTA that writes the sort's outputs
+    int* flags = scratch + 48;
+    griddep_wait();
+    griddep_launch_dependents();
+
+    // this warp's contiguous run of slots, in rounds of 32 (all loads issued
+    // first)
+    const int per_warp = ((S + kWarps - 1) / kWarps + 31) & ~31;
+    const int w0 = warp * per_warp;
+    int e_r[kRounds], l_r[kRounds], rank_r[kRounds];
+#pragma unroll
+    for (int r = 0; r < kRounds; ++r) {
+        const int f = w0 + r * 32 + lane;
+        const bool in = r * 32 < per_warp && f < S;
+        e_r[r] = in ? __ldg(ids + f) : -1;
+        l_r[r] = (kWithLora && in) ? __ldg(ex.token_lora_idx + f / ex.K_total) : -1;
+        rank_r[r] = 0;
+    }
+    for (int e = lane; e < E_tot; e += 32) wcnt[warp * E_tot + e] = 0;
+    if (tid == 0) {
+        *flags = 0;
+        scratch[49] = 0;
+        scratch[50] = 0;
+    }
+    // the forward's status word, counts and per-block counters start at zero
+    if (writer)
+        for (int i = tid; i < ex.zero_words; i += kThreads) ex.zero[i] = 0u;
+    __syncthreads();
+
+    // 1. ranks within the warp, round by round in slot order
+    const unsigned lt = (1u << lane) - 1u;
+#pragma unroll
+    for (int r = 0; r < kRounds; ++r) {
+        if (r * 32 >= per_warp) break;  // warp-uniform
+        const int f = w0 + r * 32 + lane;
+        const bool in = f < S;
+        const bool valid = in && static_cast<unsigned>(e_r[r]) < static_cast<unsigned>(E_tot);
+        if (in && !valid) atomicOr(flags, static_cast<int>(MLORA_DEV_BAD_EXPERT_ID));
+        const int key = valid ? e_r[r] : -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, key);
+        const int base = valid ? wcnt[warp * E_tot + key] : 0;
+        rank_r[r] = base + __popc(peers & lt);
+        __syncwarp();
+        if (valid && (peers & lt) == 0) wcnt[warp * E_tot + key] = base + __popc(peers);
+        __syncwarp();
+    }
+    __syncthreads();
+
+    // 2. per expert: each warp's first offset (exclusive over warps, in
+    //    place), the total and the padded size; thread t takes experts 2t
+    //    and 2t+1 (E_tot <= 1024), then one scan of the padded sizes
+    int c_e[2] = {0, 0}, pad_e[2] = {0, 0};
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const int e = 2 * tid + q;
+        if (e < E_tot) {
+            int run = 0;
+            for (int w = 0; w < kWarps; ++w) {
+                const int t = wcnt[w * E_tot + e];
+                wcnt[w * E_tot + e] = run;
+                run += t;
+            }
+            tot[e] = run;
+            c_e[q] = run;
+            pad_e[q] = (run + BM - 1) / BM * BM;
+            if (run > 0) atomicMax(&scratch[49], run);
+        }
+    }
+    int total;
+    const int start = cta_exclusive_scan(pad_e[0] + pad_e[1], scratch, &total);
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const int e = 2 * tid + q;
+        if (e >= E_tot) break;
+        const int s_e = start + (q ? pad_e[0] : 0);
+        first[e] = s_e;
+        if (writer) {
+            // the block -> expert map and the real rows of each block
+            for (int b = s_e / BM; b < (s_e + pad_e[q]) / BM; ++b) {
+                if (!MLORA_IN_BOUNDS(b < max_padded / BM, status)) break;
+                expert_ids[b] = e;
+                if (ex.blk_rows) ex.blk_rows[b] = min(BM, c_e[q] - (b - s_e / BM) * BM);
+            }
+        }
+    }
+    if (writer) {
+        if (tid == 0) {
+            *n_pad_out = total;
+            if (ex.max_rows) *ex.max_rows = min(scratch[49], BM);
+        }
+        for (int b = total / BM + tid; b < max_padded / BM; b += kThreads) expert_ids[b] = -1;
+    }
+    __syncthreads();
+
+    // 3. every slot's sorted position: the expert's start + the warp's
+    //    first offset + its rank in the warp
+#pragma unroll
+    for (int r = 0; r < kRounds; ++r) {
+        if (r * 32 >= per_warp) break;
+        const int f = w0 + r * 32 + lane;
+        const int e = e_r[r];
+        if (f >= S || static_cast<unsigned>(e) >= static_cast<unsigned>(E_tot)) continue;
+        const int pos = first[e] + wcnt[warp * E_tot + e] + rank_r[r];
+        if (!MLORA_IN_BOUNDS(pos >= 0 && pos < max_padded, status)) continue;
+        if (writer) {
+            st_sorted[pos] = static_cast<uint16_t>(f);
+            if (kWithLora) {
+                int l = l_r[r];
+                if (l < -1 || l >= ex.L) {
+                    atomicOr(flags, static_cast<int>(MLORA_DEV_BAD_LORA_IDX));
+                    l = -1;
+                }
+                st_lora[pos] = static_cast<int16_t>(l);
+            }
+        }
+        if (kGather && f % static_cast<int>(gridDim.x) == static_cast<int>(blockIdx.x)) {
+            const int i = atomicAdd(&scratch[50], 1);
+            glist[2 * i] = pos;
+            glist[2 * i + 1] = f / K_total;
+        }
+    }
+    // the padding of each expert's last block, one warp per expert
+    if (writer)
+        for (int e = warp; e < E_tot; e += kWarps) {
+            const int n = tot[e];
+            const int pad_end = first[e] + (n + BM - 1) / BM * BM;
+            for (int p = first[e] + n + lane; p < pad_end; p += 32) {
+                if (!MLORA_IN_BOUNDS(p < max_padded, status)) break;
+                st_sorted[p] = static_cast<uint16_t>(S);
+                if (kWithLora) st_lora[p] = -1;
+            }
+        }
+    __syncthreads();
+
+    // 4. this CTA's x rows into their sorted positions: one warp per row,
+    //    four 16-byte loads in flight per lane
+    if (kGather) {
+        const int n = scratch[50];
+        for (int i = warp; i < n; i += kWarps) {
+            const int pos = glist[2 * i];
+            const uint4* src = x + static_cast<size_t>(glist[2 * i + 1]) * H8;
+            uint4* dst = x_perm + static_cast<size_t>(pos) * H8;
+            for (int i0 = lane; i0 < H8; i0 += 128) {
+                uint4 v[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (i0 + 32 * j < H8) v[j] = __ldg(src + i0 + 32 * j);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (i0 + 32 * j < H8) dst[i0 + 32 * j] = v[j];
+            }
+        }
+    }
+    if (!writer) return;
+
+    // 5. the sorted ids (and adapters) out in one coalesced sweep, the
+    //    sentinel tail
+    for (int p = tid; p < total; p += kThreads) {
+        sorted[p] = st_sorted[p];
+        if (kWithLora) ex.lora_of[p] = st_lora[p];
+    }
+    for (int p = total + tid; p < max_padded; p += kThreads) sorted[p] = S;
+    if (!kWithLora) {
+        if (tid == 0 && *flags && status) atomicOr(status, static_cast<uint32_t>(*flags));
+        return;
+    }
+
+    // 6. distinct adapters of each block (ascending), one warp per block
+    constexpr int kMaxPerLane = MLORA_FORWARD_BLOCK_M / 32;
+    const int nblocks = total / BM;
+    for (int b = warp; b < nblocks; b += kWarps) {
+        int mine[kMaxPerLane];
+#pragma unroll
+        for (int i = 0; i < kMaxPerLane; ++i) {
+            const int r = lane + 32 * i;
+            mine[i] = r >= BM ? -1 : st_lora[b * BM + r];
+        }
+        int prev = -1, count = 0;
+        for (;;) {
+            int cand = 0x7fffffff;
+#pragma unroll
+            for (int i = 0; i < kMaxPerLane; ++i)
+                if (mine[i] > prev && mine[i] < cand) cand = mine[i];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) cand = min(cand, __shfl_xor_sync(0xffffffffu, cand, off));
+            if (cand == 0x7fffffff) break;
+            if (!MLORA_IN_BOUNDS(count < ex.cap, status)) break;
+            if (lane == 0) ex.blk_lora[static_cast<long>(b) * ex.cap + count] = cand;
+            ++count;
+            prev = cand;
+        }
+        if (lane == 0) {
+            ex.blk_nad[b] = count;
+            nad_s[b] = count;
+        }
+    }
+    __syncthreads();
+    if (tid == 0 && *flags && status) atomicOr(status, static_cast<uint32_t>(*flags));
+
+    // 7. number the blocks' LoRA tiles (one per (block, adapter)) and the
+    //    shrink group tiles (up to gsize adapters of one block each)
+    int run_lt = 0, run_gt = 0;
+    for (int cb = 0; cb < nblocks; cb += kThreads) {
+        const int b = cb + tid;
+        const int v = b < nblocks ? nad_s[b] : 0;
+        const int ng = (v + ex.gsize - 1) / ex.gsize;
+        int lt_chunk, gt_chunk;
+        const int lt_excl = cta_exclusive_scan(v, scratch, &lt_chunk);
+        const int gt_excl = cta_exclusive_scan(ng, scratch, &gt_chunk);
+        if (b < nblocks) {
+            ex.blk_lt_start[b] = run_lt + lt_excl;
+            for (int j = 0; j < ng; ++j) {
+                if (!MLORA_IN_BOUNDS(run_gt + gt_excl + j < ex.lt_cap, status)) break;
+                ex.gt_block[run_gt + gt_excl + j] = b;
+                ex.gt_first[run_gt + gt_excl + j] = j * ex.gsize;
+            }
+        }
+        run_lt += lt_chunk;
+        run_gt += gt_chunk;
+    }
+    if (tid == 0) *ex.gt_total = run_gt;
+}
+
+template <bool kWithLora, bool kGather>
+cudaError_t launch_variant(int variant, const cudaLaunchConfig_t& cfg, const int32_t* ids, int S, int E_tot, int BM,
+                           int max_padded, int32_t* sorted, int32_t* expert_ids, int32_t* n_pad, uint32_t* status,
+                           const AlignExtra& ex, const uint4* x, int H8, int K_total, uint4* x_perm) {
+    static std::atomic<unsigned long long> attr_set[4];  // one bit per device (shared by host threads)
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
+    if (!(attr_set[variant].load(std::memory_order_relaxed) & bit) || !bit) {
+        err = cudaFuncSetAttribute(align_small_kernel<kWithLora, kGather>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
+        if (err != cudaSuccess) return err;
+        attr_set[variant].fetch_or(bit, std::memory_order_relaxed);
+    }
+    return cudaLaunchKernelEx(&cfg, align_small_kernel<kWithLora, kGather>, ids, S, E_tot, BM, max_padded, sorted,
+                              expert_ids, n_pad, status, ex, x, H8, K_total, x_perm);
+}
+
+}  // namespace
+
+size_t align_small_smem(long S, int E_tot, int block_m, long max_padded, bool with_lora, bool gather) {
+    return sizeof(int) * (static_cast<size_t>(kWarps + 2) * E_tot + kScratch +
+                          (with_lora ? static_cast<size_t>(max_padded / block_m) : 0) +
+                          (gather ? 2 * static_cast<size_t>(S) : 0)) +
+           (sizeof(uint16_t) + (with_lora ? sizeof(int16_t) : 0)) * static_cast<size_t>(max_padded);
+}
+
+bool align_small_fits(long S, int E_tot, int block_m, long max_padded, const AlignExtra* extra, bool gather) {
+    const bool with_lora = extra && extra->token_lora_idx;
+    if (S < 1 || S > kSmallMaxSlots || E_tot > 2 * kThreads) return false;
+    if (with_lora && (extra->L > 32767 || block_m != MLORA_FORWARD_BLOCK_M)) return false;
+    return align_small_smem(S, E_tot, block_m, max_padded, with_lora, gather) <= static_cast<size_t>(kMaxSmem);
+}
+
+cudaError_t launch_align_small(const int32_t* ids, long S, int E_tot, int block_m, long max_padded, int32_t* sorted,
+                               int32_t* expert_ids, int32_t* n_pad, uint32_t* status, const AlignExtra* extra,
+                               const GatherArgs* gather, cudaStream_t s) {
+    const bool with_lora = extra && extra->token_lora_idx;
+    const bool g = gather != nullptr;
+    // with the gather: about two slots' rows per CTA, at most one CTA per SM
+    const int grid = g ? static_cast<int>(std::min<long>(device_sm_count(), (S + 1) / 2)) : 1;
+    AlignExtra ex{};
+    if (extra) ex = *extra;
+    const uint4* x = g ? static_cast<const uint4*>(gather->x) : nullptr;
+    uint4* x_perm = g ? static_cast<uint4*>(gather->x_perm) : nullptr;
+    const int H8 = g ? gather->H / 8 : 0;
+    const int K_total = g ? gather->K_total : 1;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = align_small_smem(S, E_tot, block_m, max_padded, with_lora, g);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const int Si = static_cast<int>(S), mpi = static_cast<int>(max_padded);
+    cudaError_t err;
+    if (with_lora)
+        err = g ? launch_variant<true, true>(3, cfg, ids, Si, E_tot, block_m, mpi, sorted, expert_ids, n_pad, status,
+                                             ex, x, H8, K_total, x_perm)
+                : launch_variant<true, false>(2, cfg, ids, Si, E_tot, block_m, mpi, sorted, expert_ids, n_pad,
+                                              status, ex, x, H8, K_total, x_perm);
+    else
+        err = g ? launch_variant<false, true>(1, cfg, ids, Si, E_tot, block_m, mpi, sorted, expert_ids, n_pad,
+                                              status, ex, x, H8, K_total, x_perm)
+                : launch_variant<false, false>(0, cfg, ids, Si, E_tot, block_m, mpi, sorted, expert_ids, n_pad,
+                                               status, ex, x, H8, K_total, x_perm);
+    if (err != cudaSuccess) return err;
+    return cudaGetLastError();
+}
+
+}  // namespace mlora

@@ -5,7 +5,8 @@
 // Forward, all on the caller's stream, no host synchronisation, no
 // allocation (capturable in a CUDA graph):
 //   align (clears the status word and counters first; + per-block adapter lists)
-//   -> gather x rows -> experts kernel (gate_up shrink, gate_up + expand +
+//   -> gather x rows (in the align launch for batches of up to
+//   kSmallMaxSlots slots) -> experts kernel (gate_up shrink, gate_up + expand +
 //   SwiGLU, down shrink, down + expand, one persistent grid) -> combine
 // Without adapters the experts kernel runs only base tiles; when adapters
 // are given but no token uses one, align finds no shrink tiles on the
@@ -197,7 +198,7 @@ Workspace carve_workspace(const Sizes& z, void* base) {
         w.lora_t13 = take(2 * static_cast<size_t>(z.max_lt) * kBlockM * kLoraTileCols);
         w.lora_t2 = take(2 * static_cast<size_t>(z.max_lt) * kBlockM * kLoraTileCols);
     }
-    w.y_slot = take(2 * static_cast<size_t>(z.S) * z.H);
+    w.y_slot = take(4 * static_cast<size_t>(z.S) * z.H);
     w.bytes = off;
     return w;
 }
@@ -424,12 +425,23 @@ mlora_status mlora_moe_forward(const void* x, const void* w13, const void* w2, c
         ex.gt_first = ws.gt_first;
         ex.gt_total = ws.gt_total;
     }
-    err = launch_align(topk_ids, z.S, E_tot, kBlockM, z.max_padded, ws.sorted_ids, ws.expert_ids, ws.n_pad,
-                       ws.status, &ex, s);
-    if (err != cudaSuccess) return cuda_fail(err, "align");
-    if ((err = mark_stage(1, s)) != cudaSuccess) return cuda_fail(err, "stage event");
-    err = launch_gather_rows(x, H, ws.sorted_ids, ws.n_pad, z.S, K_total, z.max_padded, ws.x_perm, ws.status, s);
-    if (err != cudaSuccess) return cuda_fail(err, "gather");
+    if (align_small_fits(z.S, E_tot, kBlockM, z.max_padded, &ex, true)) {
+        // small batches: align and the row gather in one launch (stage
+        // boundaries 1 and 2 coincide)
+        const GatherArgs ga{x, ws.x_perm, H, K_total};
+        err = launch_align_small(topk_ids, z.S, E_tot, kBlockM, z.max_padded, ws.sorted_ids, ws.expert_ids,
+                                 ws.n_pad, ws.status, &ex, &ga, s);
+        if (err != cudaSuccess) return cuda_fail(err, "align + gather");
+        if ((err = mark_stage(1, s)) != cudaSuccess) return cuda_fail(err, "stage event");
+    } else {
+        err = launch_align(topk_ids, z.S, E_tot, kBlockM, z.max_padded, ws.sorted_ids, ws.expert_ids, ws.n_pad,
+                           ws.status, &ex, s);
+        if (err != cudaSuccess) return cuda_fail(err, "align");
+        if ((err = mark_stage(1, s)) != cudaSuccess) return cuda_fail(err, "stage event");
+        err = launch_gather_rows(x, H, ws.sorted_ids, ws.n_pad, z.S, K_total, z.max_padded, ws.x_perm, ws.status,
+                                 s);
+        if (err != cudaSuccess) return cuda_fail(err, "gather");
+    }
     if ((err = mark_stage(2, s)) != cudaSuccess) return cuda_fail(err, "stage event");
     // narrow tiles (half width) at most double the slab count
     const long max_tiles = 2 * z.max_lt + z.max_blocks * (2L * up.ncb + 2L * dn.ncb);

@@ -25,7 +25,7 @@
 //     silu(g) * u in bf16, then the block's act counter is bumped.
 //  3. down shrink tiles: T2_l = s * act A2_{l,e}^T, as in phase 1.
 //  4. down tiles: d = act W2_e^T over 256 output columns + the T2 expand;
-//     epilogue the slot's expert output in bf16.
+//     epilogue the slot's expert output in fp32.
 // Batches with few blocks take tiles of 192 or 128 weight rows instead
 // (N = 192 or 128; gate_up tiles half gate, half up rows) so that the
 // tiles of each phase fill the grid's SMs.  Shrink tiles pack up to four
@@ -664,23 +664,19 @@ __device__ __forceinline__ void epilogue(const Ctx& c) {
             const int f = MLORA_IN_BOUNDS(prow < p.pad_cap, p.status) ? p.sorted_ids[prow] : p.S;
             const bool real = f < p.S;
             const int o0 = tc.cb * gm.bn;
-            __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(sd.out) + static_cast<size_t>(real ? f : 0) * sd.n_out;
+            // the slot's expert output stays fp32 until the combine
+            float* dst = static_cast<float*>(sd.out) + static_cast<size_t>(real ? f : 0) * sd.n_out;
             for (int c = 0; c < gm.bn; c += 32) {
                 if (o0 + c >= sd.n_out) break;
                 float v[32];
                 tmem_ld32(tb + c, v);
                 if (real) {
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int col = o0 + c + 8 * j;
-                        if (col < sd.n_out) {
-                            uint4 o;
-                            o.x = pack_bf16x2(v[8 * j + 0], v[8 * j + 1]);
-                            o.y = pack_bf16x2(v[8 * j + 2], v[8 * j + 3]);
-                            o.z = pack_bf16x2(v[8 * j + 4], v[8 * j + 5]);
-                            o.w = pack_bf16x2(v[8 * j + 6], v[8 * j + 7]);
-                            *reinterpret_cast<uint4*>(dst + col) = o;
-                        }
+                    for (int j = 0; j < 8; ++j) {
+                        const int col = o0 + c + 4 * j;
+                        if (col < sd.n_out)
+                            *reinterpret_cast<float4*>(dst + col) =
+                                make_float4(v[4 * j + 0], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
                     }
                 }
             }

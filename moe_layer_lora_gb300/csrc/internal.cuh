@@ -59,7 +59,7 @@ struct Workspace {
     void* act;             // [max_padded, I] bf16: SwiGLU output in sorted order
     void* lora_t13;        // [max_lt * 128, 64] bf16: s * x A13^T, one masked LoRA tile per (block, adapter)
     void* lora_t2;         // [max_lt * 128, 64] bf16: s * act A2^T, the same for the down projection
-    void* y_slot;          // [M*K', H] bf16: each slot's expert output
+    void* y_slot;          // [M*K', H] fp32: each slot's expert output
     size_t bytes;
 };
 
@@ -108,6 +108,21 @@ cudaError_t launch_align(const int32_t* ids, long S, int E_tot, int block_m, lon
                          int32_t* expert_ids, int32_t* n_pad, uint32_t* status, const AlignExtra* extra,
                          cudaStream_t s);
 
+// Small batches (align_small.cu): at most kSmallMaxSlots slots, one
+// latency-lean launch; with `gather` set the same launch also copies the x
+// rows into sorted order (the row gather of the forward).
+constexpr long kSmallMaxSlots = 2048;
+struct GatherArgs {
+    const void* x;  // [M, H] bf16
+    void* x_perm;   // [max_padded, H] bf16
+    int H;
+    int K_total;
+};
+bool align_small_fits(long S, int E_tot, int block_m, long max_padded, const AlignExtra* extra, bool gather);
+cudaError_t launch_align_small(const int32_t* ids, long S, int E_tot, int block_m, long max_padded, int32_t* sorted,
+                               int32_t* expert_ids, int32_t* n_pad, uint32_t* status, const AlignExtra* extra,
+                               const GatherArgs* gather, cudaStream_t s);
+
 cudaError_t launch_gather_rows(const void* x, int H, const int32_t* sorted, const int32_t* n_pad, long S,
                                int K_total, long max_padded, void* x_perm, uint32_t* status, cudaStream_t s);
 
@@ -130,7 +145,7 @@ struct alignas(128) GemmSide {
     CUtensorMap tm_t_full;  // box {64, 128}
     void* lora_t;           // LoRA tiles: written by the shrink tiles, read by the expand stages
     int32_t* done;          // per block: finished shrink tiles (zero at launch)
-    void* out;              // act [rows, I] / y_slot [M*K', H], bf16
+    void* out;              // act [rows, I] bf16 / y_slot [M*K', H] fp32
     int K;                  // reduction length: H / I
     int n_out;              // output columns: I / H
     int ncb;                // column slabs per block, wide tiles: ceil(I/128) / ceil(H/256)

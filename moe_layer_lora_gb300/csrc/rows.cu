@@ -1,8 +1,8 @@
 // rows.cu -- the two bandwidth-bound row kernels around the grouped GEMMs:
 //  * gather: x rows copied into sorted (expert-grouped) order so each GEMM
 //    tile reads 128 consecutive rows with one TMA box;
-//  * combine: y[m] = out_scale * sum_k topk_w[m,k] * y_slot[m*K'+k], the
-//    weighted top-k sum ("[vllm] vLLM ROCm 환경에서 Shared-Expert Fusion을 통한
+//  * combine: y[m] = out_scale * sum_k topk_w[m,k] * y_slot[m*K'+k] (fp32
+//    slot rows, fp32 sum, y rounded once to bf16), the weighted top-k sum ("[vllm] vLLM ROCm 환경에서 Shared-Expert Fusion을 통한
 //    MoE 추론 성능 최적화", section "코드 분석" item 1: the routing weights,
 //    shared slots included, weight each slot's expert output).
 // Both move 16-byte vectors; one warp owns one row.
@@ -43,17 +43,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
     }
 }
 
-__device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float (&f)[8]) {
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float2 t = __bfloat1622float2(h[i]);
-        f[2 * i] = t.x;
-        f[2 * i + 1] = t.y;
-    }
-}
-
-__global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ y_slot,
+__global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__ y_slot,
                                                       const int32_t* __restrict__ topk_ids,
                                                       const float* __restrict__ topk_w, int M, int H8, int K_total,
                                                       int E_tot, float out_scale, uint4* __restrict__ y) {
@@ -68,7 +58,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ 
         // slots in groups of four: their loads are issued together, the sum
         // still runs over k in ascending order
         for (int k0 = 0; k0 < K_total; k0 += 4) {
-            uint4 raw[4];
+            float4 raw[4][2];
             float wk[4];
             bool live[4];
 #pragma unroll
@@ -79,14 +69,16 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ 
                 wk[j] = 0.f;
                 if (live[j]) {
                     wk[j] = __ldg(topk_w + f);
-                    raw[j] = __ldcs(y_slot + f * H8 + c);
+                    const float4* src = y_slot + (f * H8 + c) * 2;
+                    raw[j][0] = __ldcs(src);
+                    raw[j][1] = __ldcs(src + 1);
                 }
             }
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 if (!live[j]) continue;
-                float v[8];
-                bf16x8_to_f32(raw[j], v);
+                const float v[8] = {raw[j][0].x, raw[j][0].y, raw[j][0].z, raw[j][0].w,
+                                    raw[j][1].x, raw[j][1].y, raw[j][1].z, raw[j][1].w};
 #pragma unroll
                 for (int i = 0; i < 8; ++i) acc[i] = fmaf(wk[j], v[i], acc[i]);
             }
@@ -122,7 +114,7 @@ cudaError_t launch_combine(const void* y_slot, const int32_t* topk_ids, const fl
     const long cap = 16L * device_sm_count();
     if (blocks > cap) blocks = cap;
     return launch_pdl(combine_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s,
-                      static_cast<const uint4*>(y_slot), topk_ids, topk_w, M, H / 8, K_total, E_tot, out_scale,
+                      static_cast<const float4*>(y_slot), topk_ids, topk_w, M, H / 8, K_total, E_tot, out_scale,
                       static_cast<uint4*>(y));
 }
 

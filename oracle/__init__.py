@@ -51,6 +51,12 @@ def load(path: str = _LIB_PATH):
     lib.oracle_moe_align.restype = i
     lib.oracle_moe_forward.argtypes = [P] * 10 + [i] * 7 + [f, f, P]
     lib.oracle_moe_forward.restype = i
+    lib.oracle_mx_quantize.argtypes = [P, ctypes.c_long, i, P, P]
+    lib.oracle_mx_quantize.restype = i
+    lib.oracle_mx_dequantize.argtypes = [P, P, ctypes.c_long, i, P]
+    lib.oracle_mx_dequantize.restype = i
+    lib.oracle_moe_forward_mx.argtypes = [P] * 12 + [i] * 7 + [f, f, P]
+    lib.oracle_moe_forward_mx.restype = i
     if path == _LIB_PATH:
         _lib = lib
     return lib
@@ -131,4 +137,59 @@ def moe_forward(x, w13, w2, A13, B13, A2, B2, token_lora_idx, topk_ids, topk_w,
                                 M, H, I, E_tot, KT, L, r, float(scaling), float(out_scale), _ptr(y))
     if rc != 0:
         raise ValueError(f"oracle_moe_forward rejected its arguments ({rc})")
+    return y
+
+
+def mx_quantize(w_bits, lib=None):
+    """MXFP8 (E4M3 elements, one E8M0 scale per 32 along the last axis) of a
+    bf16 bit array [..., K]: returns (codes uint8 [..., K], scales uint8
+    [..., K/32])."""
+    lib = lib or load()
+    w = _c(w_bits, np.uint16)
+    K = w.shape[-1]
+    rows = w.size // K
+    codes = np.zeros(w.shape, np.uint8)
+    scales = np.zeros(w.shape[:-1] + (K // 32,), np.uint8)
+    rc = lib.oracle_mx_quantize(_ptr(w), rows, K, _ptr(codes), _ptr(scales))
+    if rc != 0:
+        raise ValueError(f"oracle_mx_quantize rejected its arguments ({rc})")
+    return codes, scales
+
+
+def mx_dequantize(codes, scales, lib=None):
+    """The float64 values an MXFP8 array stands for."""
+    lib = lib or load()
+    codes = _c(codes, np.uint8)
+    scales = _c(scales, np.uint8)
+    K = codes.shape[-1]
+    out = np.zeros(codes.shape, np.float64)
+    rc = lib.oracle_mx_dequantize(_ptr(codes), _ptr(scales), codes.size // K, K, _ptr(out))
+    if rc != 0:
+        raise ValueError(f"oracle_mx_dequantize rejected its arguments ({rc})")
+    return out
+
+
+def moe_forward_mx(x, w13q, w13s, w2q, w2s, A13, B13, A2, B2, token_lora_idx, topk_ids, topk_w,
+                   scaling, out_scale=1.0, lib=None):
+    """fp64 layer output [M, H] with MXFP8 expert weights (codes and scales
+    as mx_quantize returns them); x and the LoRA tensors as bf16 bits."""
+    lib = lib or load()
+    x = _c(x, np.uint16)
+    w13q, w13s, w2q, w2s = (_c(t, np.uint8) for t in (w13q, w13s, w2q, w2s))
+    A13, B13, A2, B2 = (_c(t, np.uint16) for t in (A13, B13, A2, B2))
+    token_lora_idx = _c(token_lora_idx, np.int32)
+    topk_ids = _c(topk_ids, np.int32)
+    topk_w = _c(topk_w, np.float32)
+    M, H = x.shape
+    E_tot, twoI, H2 = w13q.shape
+    assert H2 == H and twoI % 2 == 0
+    I = twoI // 2
+    KT = topk_ids.shape[1]
+    L, r = (A13.shape[0], A13.shape[2]) if A13 is not None else (0, 0)
+    y = np.zeros((M, H), np.float64)
+    rc = lib.oracle_moe_forward_mx(_ptr(x), _ptr(w13q), _ptr(w13s), _ptr(w2q), _ptr(w2s), _ptr(A13), _ptr(B13),
+                                   _ptr(A2), _ptr(B2), _ptr(token_lora_idx), _ptr(topk_ids), _ptr(topk_w),
+                                   M, H, I, E_tot, KT, L, r, float(scaling), float(out_scale), _ptr(y))
+    if rc != 0:
+        raise ValueError(f"oracle_moe_forward_mx rejected its arguments ({rc})")
     return y

@@ -284,3 +284,232 @@ int oracle_moe_forward(const uint16_t* x, const uint16_t* w13, const uint16_t* w
     }
     return bad ? ORACLE_BAD_ARG : ORACLE_OK;
 }
+
+/* ------------------------------------------------------------------ MXFP8 --
+ * The layer with MXFP8 expert weights.  [P3] "코드 분석" item 2 names the
+ * experts implementation the fused layer runs on (an "mxfp8 native" MoE);
+ * the pages do not define the format, so it is taken from the OCP
+ * Microscaling (MX) Formats Specification v1.0, MXFP8 with E4M3 elements:
+ *  - a block is 32 consecutive elements along the reduction dimension (H for
+ *    the gate_up weights and for x, I for the down weights and for the
+ *    SwiGLU output); it shares one E8M0 scale 2^(s - 127), s in [0, 254];
+ *  - each element is FP8 E4M3: sign, 4 exponent bits (bias 7), 3 mantissa
+ *    bits, subnormals m * 2^-9, no infinity, largest finite 448;
+ *  - conversion of a block (the specification's section on converting a
+ *    vector to an MX format): the shared exponent is floor(log2(max |v|))
+ *    minus 8 (8 = the exponent of E4M3's largest normal), clamped to the
+ *    E8M0 range; each element is v / 2^shared rounded to the nearest E4M3
+ *    value, ties to even, and saturated to +-448.  A block of zeros gets the
+ *    smallest scale.
+ * Readings (not fixed by the pages): the expert weights and the activations
+ * that meet them (x for gate_up, the SwiGLU output for down) are MXFP8;
+ * the LoRA adapters stay bf16 and read the unquantized activations, as in
+ * the bf16 layer.  Everything else is fp64, as above.
+ */
+static double e4m3_value(uint8_t b) {
+    const int s = b >> 7, E = (b >> 3) & 15, m = b & 7;
+    double v;
+    if (E == 15 && m == 7) return NAN;
+    if (E == 0)
+        v = ldexp((double)m, -9);
+    else
+        v = ldexp(1.0 + m / 8.0, E - 7);
+    return s ? -v : v;
+}
+
+/* Nearest E4M3 value to v (ties to even), saturated to +-448; the sign of
+ * zero is kept. */
+static uint8_t e4m3_code(double v) {
+    const uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    const double a = fabs(v);
+    if (!(a < 448.0)) return sign | 0x7E;
+    int e;
+    if (a < ldexp(1.0, -6)) {
+        e = -6; /* subnormals share the smallest normal exponent's step */
+    } else {
+        frexp(a, &e);
+        e -= 1; /* a in [2^e, 2^(e+1)) */
+    }
+    const double step = ldexp(1.0, e - 3);
+    const double q = rint(a / step) * step; /* round to nearest, ties to even */
+    if (q == 0.0) return sign;
+    if (q < ldexp(1.0, -6)) return sign | (uint8_t)(q / ldexp(1.0, -9));
+    int E;
+    frexp(q, &E);
+    E -= 1;
+    const int m = (int)((q / ldexp(1.0, E) - 1.0) * 8.0);
+    return sign | (uint8_t)(((E + 7) << 3) | m);
+}
+
+/* One block of 32 values to E4M3 codes and its E8M0 scale byte. */
+static void mx_block(const double* v, uint8_t* codes, uint8_t* scale) {
+    double amax = 0.0;
+    for (int i = 0; i < 32; ++i)
+        if (fabs(v[i]) > amax) amax = fabs(v[i]);
+    int se = -127;
+    if (amax > 0.0) {
+        int e;
+        frexp(amax, &e);
+        se = (e - 1) - 8;
+        if (se < -127) se = -127;
+        if (se > 127) se = 127;
+    }
+    *scale = (uint8_t)(se + 127);
+    const double inv = ldexp(1.0, -se);
+    for (int i = 0; i < 32; ++i) codes[i] = e4m3_code(v[i] * inv);
+}
+
+/* MXFP8 of a bf16 matrix [rows, K] (K a multiple of 32): codes [rows, K],
+ * scales [rows, K/32]. */
+int oracle_mx_quantize(const uint16_t* w, long rows, int K, uint8_t* codes, uint8_t* scales) {
+    if (rows < 0 || K <= 0 || K % 32) return ORACLE_BAD_ARG;
+    double v[32];
+    for (long r = 0; r < rows; ++r)
+        for (int b = 0; b < K / 32; ++b) {
+            for (int i = 0; i < 32; ++i) v[i] = bf16_bits_to_double(w[r * K + b * 32 + i]);
+            mx_block(v, codes + r * K + b * 32, scales + r * (K / 32) + b);
+        }
+    return ORACLE_OK;
+}
+
+/* The values an MXFP8 matrix stands for: code value * 2^(scale - 127). */
+int oracle_mx_dequantize(const uint8_t* codes, const uint8_t* scales, long rows, int K, double* out) {
+    if (rows < 0 || K <= 0 || K % 32) return ORACLE_BAD_ARG;
+    for (long r = 0; r < rows; ++r)
+        for (int k = 0; k < K; ++k)
+            out[r * K + k] = e4m3_value(codes[r * K + k]) * ldexp(1.0, (int)scales[r * (K / 32) + k / 32] - 127);
+    return ORACLE_OK;
+}
+
+/* A vector quantized to MXFP8 and read back: n a multiple of 32. */
+static void mx_round_trip(const double* v, int n, double* out) {
+    uint8_t c[32], s;
+    for (int b = 0; b < n / 32; ++b) {
+        mx_block(v + b * 32, c, &s);
+        for (int i = 0; i < 32; ++i) out[b * 32 + i] = e4m3_value(c[i]) * ldexp(1.0, (int)s - 127);
+    }
+}
+
+/*
+ * One expert on one token with MXFP8 weights ([P1] "섹션별 상세" 1,
+ * "Diagram": the adapter on both projections; the adapter reads the
+ * unquantized activations).  xq: the token's x through MXFP8, xm: x itself.
+ * wv: a 256-entry table of E4M3 code values, sv: of E8M0 scales.
+ */
+static void expert_mx(const double* xq, const double* xm, const uint8_t* w13q, const uint8_t* w13s,
+                      const uint8_t* w2q, const uint8_t* w2s, const uint16_t* A13, const uint16_t* B13,
+                      const uint16_t* A2, const uint16_t* B2, int e, int l, int H, int I, int E_tot, int r,
+                      double scaling, const double* wv, const double* sv, double* scratch, double* d) {
+    double* h = scratch;            /* [2I] */
+    double* a = h + 2 * (size_t)I;  /* [I] */
+    double* aq = a + I;             /* [I] */
+    double* t = aq + I;             /* [r] */
+    double* t2 = t + r;             /* [r] */
+    const uint8_t* Q13 = w13q + (size_t)e * 2 * I * H;
+    const uint8_t* S13 = w13s + (size_t)e * 2 * I * (H / 32);
+    for (int j = 0; j < 2 * I; ++j) {
+        double s = 0.0;
+        for (int i = 0; i < H; ++i)
+            s += xq[i] * wv[Q13[(size_t)j * H + i]] * sv[S13[(size_t)j * (H / 32) + i / 32]];
+        h[j] = s;
+    }
+    if (l >= 0) {
+        const uint16_t* A = A13 + ((size_t)l * E_tot + e) * r * H;
+        const uint16_t* B = B13 + ((size_t)l * E_tot + e) * 2 * I * r;
+        for (int q = 0; q < r; ++q) {
+            double s = 0.0;
+            for (int i = 0; i < H; ++i) s += xm[i] * bf16_bits_to_double(A[(size_t)q * H + i]);
+            t[q] = s;
+        }
+        for (int j = 0; j < 2 * I; ++j) {
+            double s = 0.0;
+            for (int q = 0; q < r; ++q) s += t[q] * bf16_bits_to_double(B[(size_t)j * r + q]);
+            h[j] += scaling * s;
+        }
+    }
+    for (int j = 0; j < I; ++j) a[j] = silu(h[j]) * h[I + j];
+    mx_round_trip(a, I, aq);
+    const uint8_t* Q2 = w2q + (size_t)e * H * I;
+    const uint8_t* S2 = w2s + (size_t)e * H * (I / 32);
+    for (int o = 0; o < H; ++o) {
+        double s = 0.0;
+        for (int j = 0; j < I; ++j)
+            s += aq[j] * wv[Q2[(size_t)o * I + j]] * sv[S2[(size_t)o * (I / 32) + j / 32]];
+        d[o] = s;
+    }
+    if (l >= 0) {
+        const uint16_t* A = A2 + ((size_t)l * E_tot + e) * r * I;
+        const uint16_t* B = B2 + ((size_t)l * E_tot + e) * H * r;
+        for (int q = 0; q < r; ++q) {
+            double s = 0.0;
+            for (int j = 0; j < I; ++j) s += a[j] * bf16_bits_to_double(A[(size_t)q * I + j]);
+            t2[q] = s;
+        }
+        for (int o = 0; o < H; ++o) {
+            double s = 0.0;
+            for (int q = 0; q < r; ++q) s += t2[q] * bf16_bits_to_double(B[(size_t)o * r + q]);
+            d[o] += scaling * s;
+        }
+    }
+}
+
+/*
+ * The layer with MXFP8 expert weights: as oracle_moe_forward, with w13 given
+ * as codes [E_tot, 2I, H] and scales [E_tot, 2I, H/32], w2 as codes
+ * [E_tot, H, I] and scales [E_tot, H, I/32]; H and I multiples of 32.
+ */
+int oracle_moe_forward_mx(const uint16_t* x, const uint8_t* w13q, const uint8_t* w13s, const uint8_t* w2q,
+                          const uint8_t* w2s, const uint16_t* A13, const uint16_t* B13, const uint16_t* A2,
+                          const uint16_t* B2, const int32_t* token_lora_idx, const int32_t* topk_ids,
+                          const float* topk_w, int M, int H, int I, int E_tot, int K_total, int L, int r,
+                          float scaling, float out_scale, double* y) {
+    if (M < 0 || H <= 0 || I <= 0 || H % 32 || I % 32 || E_tot <= 0 || K_total <= 0 || L < 0 || r < 0)
+        return ORACLE_BAD_ARG;
+    const int has_lora = A13 && B13 && A2 && B2 && token_lora_idx && L > 0 && r > 0;
+    double wv[256], sv[256];
+    for (int b = 0; b < 256; ++b) {
+        wv[b] = e4m3_value((uint8_t)b);
+        sv[b] = ldexp(1.0, b - 127);
+    }
+    int bad = 0;
+#pragma omp parallel
+    {
+        double* xm = (double*)malloc(sizeof(double) * (size_t)H);
+        double* xq = (double*)malloc(sizeof(double) * (size_t)H);
+        double* d = (double*)malloc(sizeof(double) * (size_t)H);
+        double* acc = (double*)malloc(sizeof(double) * (size_t)H);
+        double* scratch = (double*)malloc(sizeof(double) * (4 * (size_t)I + 2 * (size_t)(r > 0 ? r : 1)));
+        if (!xm || !xq || !d || !acc || !scratch) {
+#pragma omp atomic write
+            bad = 1;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int m = 0; m < M; ++m) {
+                int l = has_lora ? token_lora_idx[m] : -1;
+                if (l < -1 || l >= L) l = -1;
+                for (int i = 0; i < H; ++i) xm[i] = bf16_bits_to_double(x[(size_t)m * H + i]);
+                mx_round_trip(xm, H, xq);
+                for (int o = 0; o < H; ++o) acc[o] = 0.0;
+                for (int k = 0; k < K_total; ++k) {
+                    int e = topk_ids[(size_t)m * K_total + k];
+                    double w = (double)topk_w[(size_t)m * K_total + k];
+                    if (e < 0 || e >= E_tot) {
+#pragma omp atomic write
+                        bad = 1;
+                        continue;
+                    }
+                    expert_mx(xq, xm, w13q, w13s, w2q, w2s, A13, B13, A2, B2, e, l, H, I, E_tot, r,
+                              (double)scaling, wv, sv, scratch, d);
+                    for (int o = 0; o < H; ++o) acc[o] += w * d[o];
+                }
+                for (int o = 0; o < H; ++o) y[(size_t)m * H + o] = (double)out_scale * acc[o];
+            }
+        }
+        free(xm);
+        free(xq);
+        free(d);
+        free(acc);
+        free(scratch);
+    }
+    return bad ? ORACLE_BAD_ARG : ORACLE_OK;
+}

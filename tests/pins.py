@@ -325,6 +325,189 @@ def pin_forward_lora_on_shared_slot(lib):
     np.testing.assert_allclose(y, ref, rtol=1e-9, atol=1e-9 * np.abs(ref).max())
 
 
+# ------------------------------------------------------------------ MXFP8 --
+# The MXFP8 oracle follows the OCP Microscaling Formats Specification v1.0
+# (blocks of 32 elements, E8M0 scale, E4M3 elements; conversion: shared
+# exponent floor(log2(max|v|)) - 8, elements rounded to nearest-even and
+# saturated).  The pins below check it against torch's own float8_e4m3fn
+# codec, against a brute-force nearest-value search over the 256 codes,
+# against hand-derived blocks, and (the layer) against a dense vectorised
+# formulation.
+
+def e4m3_table():
+    """Value of every E4M3 code, from torch's float8_e4m3fn (an implementation
+    of the same format that shares nothing with the oracle)."""
+    return torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def brute_mx_block(v):
+    """One block of 32 values: (codes, scale byte) by exhaustive search for
+    the nearest finite E4M3 value of v / 2^shared, ties to the even code."""
+    v = np.asarray(v, np.float64)
+    amax = float(np.abs(v).max())
+    se = -127 if amax == 0.0 else min(127, max(-127, math.frexp(amax)[1] - 1 - 8))
+    x = v * 2.0 ** -se
+    pos = e4m3_table()[:0x7F]          # codes 0x00 .. 0x7E: 0 .. 448
+    codes = np.zeros(32, np.uint8)
+    for i, xi in enumerate(x):
+        a = abs(xi)
+        if a >= 448.0:
+            c = 0x7E
+        else:
+            d = np.abs(pos - a)
+            cand = np.flatnonzero(d == d.min())
+            c = int(cand[0]) if len(cand) == 1 else int(cand[cand % 2 == 0][0])
+        codes[i] = c | (0x80 if math.copysign(1.0, xi) < 0 else 0)
+    return codes, se + 127
+
+
+def brute_mx_round_trip(a):
+    """Rows of values through MXFP8 and back (blocks of 32 along the last
+    axis), with the brute-force quantizer."""
+    a = np.asarray(a, np.float64)
+    out = np.empty_like(a)
+    tab = e4m3_table()
+    for idx in np.ndindex(a.shape[:-1]):
+        for b in range(a.shape[-1] // 32):
+            c, sc = brute_mx_block(a[idx][b * 32:(b + 1) * 32])
+            out[idx][b * 32:(b + 1) * 32] = tab[c] * 2.0 ** (sc - 127)
+    return out
+
+
+def _bf16_bits(v):
+    return torch.tensor(np.asarray(v, np.float64), dtype=torch.float32).to(torch.bfloat16).view(torch.int16) \
+        .numpy().view(np.uint16)
+
+
+def pin_mx_e4m3_values_match_torch(lib):
+    """Every code's value (scale byte 127 = 2^0), the sign of zero included,
+    and the scale bytes as powers of two."""
+    t = e4m3_table()
+    v = oracle.mx_dequantize(np.arange(256, dtype=np.uint8).reshape(8, 32), np.full((8, 1), 127, np.uint8),
+                             lib=lib).reshape(-1)
+    nan = np.isnan(t)
+    assert nan.sum() == 2 and np.array_equal(np.isnan(v), nan)
+    assert np.array_equal(v[~nan], t[~nan])
+    assert np.array_equal(np.signbit(v[~nan]), np.signbit(t[~nan]))
+    one = np.full((1, 32), 0x38, np.uint8)  # 1.0
+    for sc in (0, 1, 100, 127, 200, 254):
+        got = oracle.mx_dequantize(one, np.array([[sc]], np.uint8), lib=lib)
+        assert (got == 2.0 ** (sc - 127)).all()
+
+
+def pin_mx_quantize_golden(lib):
+    """Blocks worked out by hand from the specification's conversion.  The
+    first holds 1.0, so max|v| = 1, the shared exponent is 0 - 8 and the
+    scale byte 119; every element is then scaled by 2^8:
+      1.0          -> 256   = 2^8 * 1.000: code 0x78
+      9.5/256      -> 9.5, halfway between 9 and 10: even mantissa, 10 = 0x52
+      10.5/256     -> 10.5, halfway between 10 and 11: 10 again, 0x52
+      -0.0         -> negative zero, 0x80
+      2^-17        -> 2^-9, the smallest subnormal, 0x01
+      2^-18        -> 2^-10, halfway between 0 and 2^-9: 0, 0x00
+      1.5 * 2^-18  -> 0.75 * 2^-9: 2^-9, 0x01
+      1.9 (bf16 1.8984375) -> 486, above 448: saturated, 0x7E
+    and a block of zeros takes the smallest scale byte, 0."""
+    v = np.zeros((2, 32))
+    v[0, :8] = [1.0, 9.5 / 256, 10.5 / 256, -0.0, 2.0 ** -17, 2.0 ** -18, 1.5 * 2.0 ** -18, 1.9]
+    codes, scales = oracle.mx_quantize(_bf16_bits(v), lib=lib)
+    assert scales.tolist() == [[119], [0]]
+    assert codes[0, :8].tolist() == [0x78, 0x52, 0x52, 0x80, 0x01, 0x00, 0x01, 0x7E]
+    assert (codes[1] == 0).all()
+
+
+def pin_mx_quantize_brute_force(lib):
+    """Random bf16 blocks over many magnitudes, zeros and outliers included,
+    against the exhaustive nearest-value search."""
+    rng = np.random.default_rng(31)
+    rows = []
+    for mag in (1e-30, 1e-6, 3e-3, 1.0, 7.0, 1e4, 1e30):
+        rows.append(rng.standard_normal(32) * mag)
+    r = rng.standard_normal(32)
+    r[rng.integers(0, 32)] = 200.0  # one outlier: the rest fall towards the subnormals
+    rows.append(r)
+    r = rng.standard_normal(32)
+    r[::3] = 0.0
+    rows.append(r)
+    rows.append(rng.choice([-1.0, 1.0], 32) * 2.0 ** rng.integers(-20, 5, 32))
+    bits = _bf16_bits(np.array(rows))
+    codes, scales = oracle.mx_quantize(bits, lib=lib)
+    vals = wl.to_f64(wl.from_bits(bits))
+    for i, row in enumerate(vals):
+        c, sc = brute_mx_block(row)
+        assert scales[i, 0] == sc, (i, scales[i, 0], sc)
+        assert np.array_equal(codes[i], c), (i, codes[i], c)
+
+
+def dense_forward_mx(x, w13q, w13s, w2q, w2s, A13, B13, A2, B2, idx, ids, w, s, out_scale):
+    """The MXFP8 layer as dense vectorised algebra: quantized x and SwiGLU
+    output (brute-force quantizer), weights decoded with torch's E4M3 codec,
+    adapters on the unquantized activations, a dense gate matrix."""
+    tab = e4m3_table()
+    W13 = tab[w13q] * np.repeat(2.0 ** (w13s.astype(np.float64) - 127), 32, axis=-1)
+    W2 = tab[w2q] * np.repeat(2.0 ** (w2s.astype(np.float64) - 127), 32, axis=-1)
+    M, H = x.shape
+    Et, twoI, _ = W13.shape
+    I = twoI // 2
+    G = np.zeros((M, Et))
+    np.add.at(G, (np.repeat(np.arange(M), ids.shape[1]), ids.reshape(-1)), w.reshape(-1))
+    idx = np.full(M, -1) if idx is None else idx
+    xq = brute_mx_round_trip(x)
+    y = np.zeros((M, H))
+    for l in np.unique(idx):
+        rows = idx == l
+        for e in range(Et):
+            if not G[rows, e].any():
+                continue
+            h = xq[rows] @ W13[e].T
+            if l >= 0:
+                h = h + s * (x[rows] @ A13[l, e].T) @ B13[l, e].T
+            a = h[:, :I] * scipy.special.expit(h[:, :I]) * h[:, I:]
+            d = brute_mx_round_trip(a) @ W2[e].T
+            if l >= 0:
+                d = d + s * (a @ A2[l, e].T) @ B2[l, e].T
+            y[rows] += G[rows, e][:, None] * d
+    return out_scale * y
+
+
+def _mx_inputs(seed, M=6, H=64, I=32, E=4, k=2, L=2, r=8):
+    s, inp = _tiny_inputs(seed=seed, M=M, H=H, I=I, E=E, k=k, L=L, r=r)
+    w13q, w13s = oracle.mx_quantize(wl.bits(inp.w13))
+    w2q, w2s = oracle.mx_quantize(wl.bits(inp.w2))
+    return s, inp, (w13q, w13s, w2q, w2s)
+
+
+def _oracle_y_mx(lib, inp, q, ids, w, scaling, lora=True, out_scale=1.0):
+    b = wl.bits
+    use = lora and inp.A13 is not None
+    return oracle.moe_forward_mx(b(inp.x), *q, b(inp.A13) if use else None, b(inp.B13) if use else None,
+                                 b(inp.A2) if use else None, b(inp.B2) if use else None,
+                                 inp.token_lora_idx.numpy() if use else None, ids, w.astype(np.float32),
+                                 scaling, out_scale, lib=lib)
+
+
+def pin_mx_forward_dense(lib):
+    for seed, (H, I, E, k, L, r) in [(41, (64, 32, 4, 2, 2, 8)), (42, (32, 96, 3, 3, 3, 16))]:
+        s, inp, q = _mx_inputs(seed, H=H, I=I, E=E, k=k, L=L, r=r)
+        ids, w = oracle.moe_route(inp.logits.numpy(), None, k, 0, 1, lib=lib)
+        y = _oracle_y_mx(lib, inp, q, ids, w, s.scaling)
+        f = _f64
+        ref = dense_forward_mx(f(inp.x), *q, f(inp.A13), f(inp.B13), f(inp.A2), f(inp.B2),
+                               inp.token_lora_idx.numpy(), ids, w.astype(np.float32).astype(np.float64),
+                               s.scaling, 1.0)
+        np.testing.assert_allclose(y, ref, rtol=1e-9, atol=1e-9 * np.abs(ref).max())
+
+
+def pin_mx_forward_b_zero_is_base(lib):
+    """All adapter B = 0: the MXFP8 layer equals itself without adapters."""
+    s, inp, q = _mx_inputs(43)
+    ids, w = oracle.moe_route(inp.logits.numpy(), None, s.top_k, 0, 1, lib=lib)
+    base = _oracle_y_mx(lib, inp, q, ids, w, s.scaling, lora=False)
+    inp.B13 = torch.zeros_like(inp.B13)
+    inp.B2 = torch.zeros_like(inp.B2)
+    assert np.array_equal(_oracle_y_mx(lib, inp, q, ids, w, s.scaling), base)
+
+
 ALL_PINS = [
     pin_route_softmax_closed_form, pin_route_ties_lower_id, pin_route_softmax_brute_force,
     pin_route_sigmoid_bias_shared, pin_route_golden_shared,
@@ -333,4 +516,6 @@ ALL_PINS = [
     pin_forward_no_adapter_tokens_equal_base, pin_forward_linear_in_scaling,
     pin_forward_token_permutation, pin_forward_shared_fusion_equals_unfused,
     pin_forward_lora_on_shared_slot,
+    pin_mx_e4m3_values_match_torch, pin_mx_quantize_golden, pin_mx_quantize_brute_force,
+    pin_mx_forward_dense, pin_mx_forward_b_zero_is_base,
 ]

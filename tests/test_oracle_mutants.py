@@ -43,6 +43,18 @@ MUTANTS = {
                                "for (long f = slots - 1; f >= 0; --f)\n            if (topk_ids[f] == e)"),
     "align_no_padding": ("while ((pos - start) % block_m != 0) sorted_ids[pos++] = sentinel;", ""),
     "align_tail_not_filled": ("for (long b = pos / block_m; b < max_padded / block_m; ++b) expert_ids[b] = -1;", ""),
+    # MXFP8
+    "mx_shared_exponent_off_by_one": ("se = (e - 1) - 8;", "se = (e - 1) - 7;"),
+    "mx_rounds_toward_zero": ("const double q = rint(a / step) * step;", "const double q = floor(a / step) * step;"),
+    "mx_no_saturation": ("if (!(a < 448.0)) return sign | 0x7E;", "if (!(a < 480.0)) return sign | 0x7E;"),
+    "mx_negative_zero_unsigned": ("if (q == 0.0) return sign;", "if (q == 0.0) return 0;"),
+    "mx_subnormals_flushed": ("if (q < ldexp(1.0, -6)) return sign | (uint8_t)(q / ldexp(1.0, -9));",
+                              "if (q < ldexp(1.0, -6)) return sign;"),
+    "mx_decode_bias_8": ("v = ldexp(1.0 + m / 8.0, E - 7);", "v = ldexp(1.0 + m / 8.0, E - 8);"),
+    "mx_swiglu_output_not_quantized": ("mx_round_trip(a, I, aq);", "for (int j = 0; j < I; ++j) aq[j] = a[j];"),
+    "mx_x_not_quantized": ("mx_round_trip(xm, H, xq);", "for (int i = 0; i < H; ++i) xq[i] = xm[i];"),
+    "mx_adapter_reads_quantized_x": ("expert_mx(xq, xm,", "expert_mx(xq, xq,"),
+    "mx_scale_of_next_block": ("sv[S2[(size_t)o * (I / 32) + j / 32]]", "sv[S2[(size_t)o * (I / 32) + (j / 32 + 1) % (I / 32)]]"),
 }
 
 

@@ -399,56 +399,56 @@ static void mx_round_trip(const double* v, int n, double* out) {
 static void expert_mx(const double* xq, const double* xm, const uint8_t* w13q, const uint8_t* w13s,
                       const uint8_t* w2q, const uint8_t* w2s, const uint16_t* A13, const uint16_t* B13,
                       const uint16_t* A2, const uint16_t* B2, int e, int l, int H, int I, int E_tot, int r,
-                      double scaling, const double* wv, const double* sv, double* scratch, double* d) {
-    double* h = scratch;            /* [2I] */
-    double* a = h + 2 * (size_t)I;  /* [I] */
-    double* aq = a + I;             /* [I] */
-    double* t = aq + I;             /* [r] */
-    double* t2 = t + r;             /* [r] */
+                      double scaling, const double* wv, const double* sv, double* scratch, double* dout) {
+    double* hh = scratch;             /* [2I] gate then up */
+    double* act = hh + 2 * (size_t)I; /* [I] SwiGLU output */
+    double* actq = act + I;           /* [I] the same through MXFP8 */
+    double* ts = actq + I;            /* [r] gate_up shrink */
+    double* ts2 = ts + r;             /* [r] down shrink */
     const uint8_t* Q13 = w13q + (size_t)e * 2 * I * H;
     const uint8_t* S13 = w13s + (size_t)e * 2 * I * (H / 32);
     for (int j = 0; j < 2 * I; ++j) {
-        double s = 0.0;
+        double acc_j = 0.0;
         for (int i = 0; i < H; ++i)
-            s += xq[i] * wv[Q13[(size_t)j * H + i]] * sv[S13[(size_t)j * (H / 32) + i / 32]];
-        h[j] = s;
+            acc_j += xq[i] * wv[Q13[(size_t)j * H + i]] * sv[S13[(size_t)j * (H / 32) + i / 32]];
+        hh[j] = acc_j;
     }
     if (l >= 0) {
-        const uint16_t* A = A13 + ((size_t)l * E_tot + e) * r * H;
-        const uint16_t* B = B13 + ((size_t)l * E_tot + e) * 2 * I * r;
+        const uint16_t* Ash = A13 + ((size_t)l * E_tot + e) * r * H;
+        const uint16_t* Bex = B13 + ((size_t)l * E_tot + e) * 2 * I * r;
         for (int q = 0; q < r; ++q) {
-            double s = 0.0;
-            for (int i = 0; i < H; ++i) s += xm[i] * bf16_bits_to_double(A[(size_t)q * H + i]);
-            t[q] = s;
+            double acc_q = 0.0;
+            for (int i = 0; i < H; ++i) acc_q += xm[i] * bf16_bits_to_double(Ash[(size_t)q * H + i]);
+            ts[q] = acc_q;
         }
         for (int j = 0; j < 2 * I; ++j) {
-            double s = 0.0;
-            for (int q = 0; q < r; ++q) s += t[q] * bf16_bits_to_double(B[(size_t)j * r + q]);
-            h[j] += scaling * s;
+            double acc_j = 0.0;
+            for (int q = 0; q < r; ++q) acc_j += ts[q] * bf16_bits_to_double(Bex[(size_t)j * r + q]);
+            hh[j] += scaling * acc_j;
         }
     }
-    for (int j = 0; j < I; ++j) a[j] = silu(h[j]) * h[I + j];
-    mx_round_trip(a, I, aq);
+    for (int j = 0; j < I; ++j) act[j] = silu(hh[j]) * hh[I + j];
+    mx_round_trip(act, I, actq);
     const uint8_t* Q2 = w2q + (size_t)e * H * I;
     const uint8_t* S2 = w2s + (size_t)e * H * (I / 32);
     for (int o = 0; o < H; ++o) {
-        double s = 0.0;
+        double acc_o = 0.0;
         for (int j = 0; j < I; ++j)
-            s += aq[j] * wv[Q2[(size_t)o * I + j]] * sv[S2[(size_t)o * (I / 32) + j / 32]];
-        d[o] = s;
+            acc_o += actq[j] * wv[Q2[(size_t)o * I + j]] * sv[S2[(size_t)o * (I / 32) + j / 32]];
+        dout[o] = acc_o;
     }
     if (l >= 0) {
-        const uint16_t* A = A2 + ((size_t)l * E_tot + e) * r * I;
-        const uint16_t* B = B2 + ((size_t)l * E_tot + e) * H * r;
+        const uint16_t* Ash = A2 + ((size_t)l * E_tot + e) * r * I;
+        const uint16_t* Bex = B2 + ((size_t)l * E_tot + e) * H * r;
         for (int q = 0; q < r; ++q) {
-            double s = 0.0;
-            for (int j = 0; j < I; ++j) s += a[j] * bf16_bits_to_double(A[(size_t)q * I + j]);
-            t2[q] = s;
+            double acc_q = 0.0;
+            for (int j = 0; j < I; ++j) acc_q += act[j] * bf16_bits_to_double(Ash[(size_t)q * I + j]);
+            ts2[q] = acc_q;
         }
         for (int o = 0; o < H; ++o) {
-            double s = 0.0;
-            for (int q = 0; q < r; ++q) s += t2[q] * bf16_bits_to_double(B[(size_t)o * r + q]);
-            d[o] += scaling * s;
+            double acc_o = 0.0;
+            for (int q = 0; q < r; ++q) acc_o += ts2[q] * bf16_bits_to_double(Bex[(size_t)o * r + q]);
+            dout[o] += scaling * acc_o;
         }
     }
 }
@@ -500,9 +500,9 @@ int oracle_moe_forward_mx(const uint16_t* x, const uint8_t* w13q, const uint8_t*
                     }
                     expert_mx(xq, xm, w13q, w13s, w2q, w2s, A13, B13, A2, B2, e, l, H, I, E_tot, r,
                               (double)scaling, wv, sv, scratch, d);
-                    for (int o = 0; o < H; ++o) acc[o] += w * d[o];
+                    for (int o = 0; o < H; ++o) acc[o] += d[o] * w;
                 }
-                for (int o = 0; o < H; ++o) y[(size_t)m * H + o] = (double)out_scale * acc[o];
+                for (int o = 0; o < H; ++o) y[(size_t)m * H + o] = acc[o] * (double)out_scale;
             }
         }
         free(xm);

@@ -51,7 +51,8 @@ MUTANTS = {
     "mx_subnormals_flushed": ("if (q < ldexp(1.0, -6)) return sign | (uint8_t)(q / ldexp(1.0, -9));",
                               "if (q < ldexp(1.0, -6)) return sign;"),
     "mx_decode_bias_8": ("v = ldexp(1.0 + m / 8.0, E - 7);", "v = ldexp(1.0 + m / 8.0, E - 8);"),
-    "mx_swiglu_output_not_quantized": ("mx_round_trip(a, I, aq);", "for (int j = 0; j < I; ++j) aq[j] = a[j];"),
+    "mx_swiglu_output_not_quantized": ("mx_round_trip(act, I, actq);",
+                                       "for (int j = 0; j < I; ++j) actq[j] = act[j];"),
     "mx_x_not_quantized": ("mx_round_trip(xm, H, xq);", "for (int i = 0; i < H; ++i) xq[i] = xm[i];"),
     "mx_adapter_reads_quantized_x": ("expert_mx(xq, xm,", "expert_mx(xq, xq,"),
     "mx_scale_of_next_block": ("sv[S2[(size_t)o * (I / 32) + j / 32]]", "sv[S2[(size_t)o * (I / 32) + (j / 32 + 1) % (I / 32)]]"),

@@ -304,8 +304,22 @@ int oracle_moe_forward(const uint16_t* x, const uint16_t* w13, const uint16_t* w
  * Readings (not fixed by the pages): the expert weights and the activations
  * that meet them (x for gate_up, the SwiGLU output for down) are MXFP8;
  * the LoRA adapters stay bf16 and read the unquantized activations, as in
- * the bf16 layer.  Everything else is fp64, as above.
+ * the bf16 layer, and the gate_up adapter's shrink result s * (x A13^T)
+ * enters its expand as a bf16 value (rounded to nearest even, through
+ * fp32).  That rounding decides values which the SwiGLU output's MXFP8
+ * quantization then turns into codes -- a decision that both sides must
+ * take from the same numbers.  Everything else is fp64, as above.
  */
+/* fp64 -> fp32 -> bf16, each step rounded to nearest even. */
+static double bf16_round(double v) {
+    float f = (float)v;
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    u += 0x7FFFu + ((u >> 16) & 1u);
+    u &= 0xFFFF0000u;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
 static double e4m3_value(uint8_t b) {
     const int s = b >> 7, E = (b >> 3) & 15, m = b & 7;
     double v;
@@ -363,12 +377,15 @@ static void mx_block(const double* v, uint8_t* codes, uint8_t* scale) {
  * scales [rows, K/32]. */
 int oracle_mx_quantize(const uint16_t* w, long rows, int K, uint8_t* codes, uint8_t* scales) {
     if (rows < 0 || K <= 0 || K % 32) return ORACLE_BAD_ARG;
-    double v[32];
-    for (long r = 0; r < rows; ++r)
+    /* rows are independent: one per thread at a time */
+#pragma omp parallel for schedule(static)
+    for (long r = 0; r < rows; ++r) {
+        double v[32];
         for (int b = 0; b < K / 32; ++b) {
             for (int i = 0; i < 32; ++i) v[i] = bf16_bits_to_double(w[r * K + b * 32 + i]);
             mx_block(v, codes + r * K + b * 32, scales + r * (K / 32) + b);
         }
+    }
     return ORACLE_OK;
 }
 
@@ -419,12 +436,12 @@ static void expert_mx(const double* xq, const double* xm, const uint8_t* w13q, c
         for (int q = 0; q < r; ++q) {
             double acc_q = 0.0;
             for (int i = 0; i < H; ++i) acc_q += xm[i] * bf16_bits_to_double(Ash[(size_t)q * H + i]);
-            ts[q] = acc_q;
+            ts[q] = bf16_round(scaling * acc_q);
         }
         for (int j = 0; j < 2 * I; ++j) {
             double acc_j = 0.0;
             for (int q = 0; q < r; ++q) acc_j += ts[q] * bf16_bits_to_double(Bex[(size_t)j * r + q]);
-            hh[j] += scaling * acc_j;
+            hh[j] += acc_j;
         }
     }
     for (int j = 0; j < I; ++j) act[j] = silu(hh[j]) * hh[I + j];

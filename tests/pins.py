@@ -439,10 +439,16 @@ def pin_mx_quantize_brute_force(lib):
         assert np.array_equal(codes[i], c), (i, codes[i], c)
 
 
+def _to_bf16(a):
+    """Round to bf16 through fp32 (torch's conversions, nearest even)."""
+    return torch.from_numpy(np.asarray(a, np.float64)).to(torch.float32).to(torch.bfloat16).to(torch.float64).numpy()
+
+
 def dense_forward_mx(x, w13q, w13s, w2q, w2s, A13, B13, A2, B2, idx, ids, w, s, out_scale):
     """The MXFP8 layer as dense vectorised algebra: quantized x and SwiGLU
     output (brute-force quantizer), weights decoded with torch's E4M3 codec,
-    adapters on the unquantized activations, a dense gate matrix."""
+    adapters on the unquantized activations (the gate_up shrink result
+    s * x A13^T rounded to bf16 by torch), a dense gate matrix."""
     tab = e4m3_table()
     W13 = tab[w13q] * np.repeat(2.0 ** (w13s.astype(np.float64) - 127), 32, axis=-1)
     W2 = tab[w2q] * np.repeat(2.0 ** (w2s.astype(np.float64) - 127), 32, axis=-1)
@@ -461,7 +467,7 @@ def dense_forward_mx(x, w13q, w13s, w2q, w2s, A13, B13, A2, B2, idx, ids, w, s, 
                 continue
             h = xq[rows] @ W13[e].T
             if l >= 0:
-                h = h + s * (x[rows] @ A13[l, e].T) @ B13[l, e].T
+                h = h + _to_bf16(s * (x[rows] @ A13[l, e].T)) @ B13[l, e].T
             a = h[:, :I] * scipy.special.expit(h[:, :I]) * h[:, I:]
             d = brute_mx_round_trip(a) @ W2[e].T
             if l >= 0:

@@ -55,6 +55,7 @@ MUTANTS = {
                                        "for (int j = 0; j < I; ++j) actq[j] = act[j];"),
     "mx_x_not_quantized": ("mx_round_trip(xm, H, xq);", "for (int i = 0; i < H; ++i) xq[i] = xm[i];"),
     "mx_adapter_reads_quantized_x": ("expert_mx(xq, xm,", "expert_mx(xq, xq,"),
+    "mx_shrink_not_rounded": ("ts[q] = bf16_round(scaling * acc_q);", "ts[q] = scaling * acc_q;"),
     "mx_scale_of_next_block": ("sv[S2[(size_t)o * (I / 32) + j / 32]]", "sv[S2[(size_t)o * (I / 32) + (j / 32 + 1) % (I / 32)]]"),
 }
 

@@ -58,6 +58,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of replaying a graph")
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip the per-workload breakdown that follows the headline measurement")
+    ap.add_argument("--mxfp8", action="store_true", help="the layer with MXFP8 expert weights")
     return ap.parse_args(argv)
 
 
@@ -108,10 +109,11 @@ def workload_config(s: wl.Spec) -> dict:
     return d
 
 
-def algorithmic(s: wl.Spec, ids: np.ndarray, idx) -> dict:
+def algorithmic(s: wl.Spec, ids: np.ndarray, idx, mx: bool = False) -> dict:
     """Bytes each stage must move and flops it must do, from the routed ids:
-    every touched expert's weights once, every touched (adapter, expert)
-    pair's four LoRA matrices once, the activations once."""
+    every touched expert's weights once (bf16, or MXFP8: one byte an element
+    plus one scale byte per 32), every touched (adapter, expert) pair's four
+    LoRA matrices once, the activations once."""
     M, H, I, r = s.M, s.H, s.I, s.r
     S = ids.size
     experts = np.unique(ids)
@@ -125,15 +127,16 @@ def algorithmic(s: wl.Spec, ids: np.ndarray, idx) -> dict:
     else:
         n_pairs = a_slots = 0
     b = 2  # bf16
+    bw = 1 + 1 / 32 if mx else b  # bytes of an expert weight element
     st = {
         # the experts kernel: both projections, their adapter shrink and expand
-        "experts": dict(bytes=n_exp * 3 * I * H * b + n_pairs * r * (2 * H + 3 * I) * b + S * (2 * H + 2 * I) * b,
+        "experts": dict(bytes=n_exp * 3 * I * H * bw + n_pairs * r * (2 * H + 3 * I) * b + S * (2 * H + 2 * I) * b,
                         flops=2.0 * S * 3 * H * I + 2.0 * a_slots * r * (2 * H + 3 * I)),
         "gather": dict(bytes=S * H * b * 2, flops=0.0),
         "combine": dict(bytes=S * H * 4 + M * H * b, flops=2.0 * S * H),
         "align": dict(bytes=S * 4 * 3, flops=0.0),
     }
-    layer_bytes = (n_exp * 3 * I * H * b + n_pairs * r * (2 * H + 3 * I) * b + 2 * M * H * b
+    layer_bytes = (n_exp * 3 * I * H * bw + n_pairs * r * (2 * H + 3 * I) * b + 2 * M * H * b
                    + M * s.E * 4 + S * 8)
     layer_flops = sum(v["flops"] for v in st.values())
     return {"stages": st, "layer_bytes": layer_bytes, "layer_flops": layer_flops, "experts": n_exp,
@@ -326,6 +329,12 @@ SWEEP = (
     ("shared_M128", "shared", {"M": 128}),
     ("stress", "stress", {}),
     ("stress_all_none", "stress", {"lora_mode": "all_none"}),
+    # the same layers with MXFP8 expert weights (E4M3, one E8M0 scale per 32)
+    ("decode_mxfp8", "decode", {"mx": True}),
+    ("prefill_mxfp8", "prefill", {"mx": True}),
+    ("shared_M1_mxfp8", "shared", {"M": 1, "mx": True}),
+    ("shared_M128_mxfp8", "shared", {"M": 128, "mx": True}),
+    ("stress_mxfp8", "stress", {"mx": True}),
 )
 
 
@@ -334,10 +343,11 @@ class LayerRun:
     step (route + forward on a side stream), and CUDA graphs of the step --
     a plain one and one with event nodes at the stage boundaries."""
 
-    def __init__(self, s: wl.Spec, device, use_graph: bool, packed: bool = False):
+    def __init__(self, s: wl.Spec, device, use_graph: bool, packed: bool = False, mx: bool = False):
         import moe_layer_lora_gb300 as ml
         self.ml = ml
         self.s = s
+        self.mx = mx
         self.device = device
         inp = wl.make(s, device=device)
         self.inp = inp
@@ -366,8 +376,15 @@ class LayerRun:
         self.ids = torch.empty((s.M, s.K_total), dtype=torch.int32, device=device)
         self.w = torch.empty((s.M, s.K_total), dtype=torch.float32, device=device)
         self.y = torch.empty((s.M, s.H), dtype=torch.bfloat16, device=device)
-        self.ws = torch.empty(ml.mlora_moe_workspace_size(s.M, s.H, s.I, s.E_tot, s.K_total, L, r),
-                              dtype=torch.uint8, device=device)
+        if mx:
+            # the weights are quantized once, outside every timed region
+            self.q = ml.mlora_mxfp8_quantize_weights(d["w13"], d["w2"])
+            torch.cuda.synchronize(device)
+            d["w13"] = d["w2"] = None
+            wsb = ml.mlora_moe_workspace_size_mxfp8(s.M, s.H, s.I, s.E_tot, s.K_total, L, r)
+        else:
+            wsb = ml.mlora_moe_workspace_size(s.M, s.H, s.I, s.E_tot, s.K_total, L, r)
+        self.ws = torch.empty(wsb, dtype=torch.uint8, device=device)
         self.stream = torch.cuda.Stream(device=device)
         self.ev = [torch.cuda.Event(enable_timing=True) for _ in range(ml.STAGE_EVENTS)]
         for e in self.ev:
@@ -396,6 +413,11 @@ class LayerRun:
         s, d, ml = self.s, self.d, self.ml
         ml.mlora_moe_route(d["logits"], d["bias"], s.top_k, s.scoring, s.renormalize, s.n_shared,
                            s.routed_scaling_factor, topk_ids=self.ids, topk_w=self.w, stream=self.stream)
+        if self.mx:
+            ml.mlora_moe_forward_mxfp8(d["x"], *self.q, d["A13"], d["B13"], d["A2"], d["B2"], d["idx"], self.ids,
+                                       self.w, s.scaling, s.n_shared, s.out_scale, y=self.y, workspace=self.ws,
+                                       stream=self.stream)
+            return
         ml.mlora_moe_forward(d["x"], d["w13"], d["w2"], d["A13"], d["B13"], d["A2"], d["B2"], d["idx"], self.ids,
                              self.w, s.scaling, s.n_shared, s.out_scale, y=self.y, workspace=self.ws,
                              stream=self.stream)
@@ -418,7 +440,7 @@ class LayerRun:
 
     def alg(self):
         return algorithmic(self.s, self.ids.cpu().numpy(),
-                           self.inp.token_lora_idx.numpy() if self.s.has_lora else None)
+                           self.inp.token_lora_idx.numpy() if self.s.has_lora else None, self.mx)
 
     def time(self, flush, steps: int, warmup: int, world: int = 1, clocks=None):
         """W warm-up steps, then K timed steps of the plain graph and K of the
@@ -509,22 +531,26 @@ class LayerRun:
         return e2e_s, self.in_bytes, h_y.numel() * 2
 
 
-def roofline_fields(s: wl.Spec, alg: dict, kernel_ms: float, layer_ms: float, peaks: dict) -> dict:
+def roofline_fields(s: wl.Spec, alg: dict, kernel_ms: float, layer_ms: float, peaks: dict, mx: bool = False) -> dict:
     """The experts kernel's and the whole layer's fraction of the roofline
-    that bounds the workload: bf16 tensor peak for prefill, HBM otherwise."""
+    that bounds the workload: the tensor peak for prefill (bf16; MXFP8: the
+    measured bf16 peak times the nominal fp8 / bf16 ratio of 2), HBM
+    otherwise."""
     st = alg["stages"]["experts"]
     if s.name == "prefill":
+        peak = peaks["bf16_tflops"] * (2.0 if mx else 1.0)
         kernel = st["flops"] / (kernel_ms / 1e3) / 1e12
         layer = alg["layer_flops"] / (layer_ms / 1e3) / 1e12
-        return {"bound": "tensor", "unit": "TFLOP/s", "peak": peaks["bf16_tflops"], "experts_achieved": kernel,
-                "experts_frac": kernel / peaks["bf16_tflops"], "layer_frac": layer / peaks["bf16_tflops"]}
+        return {"bound": "tensor", "unit": "TFLOP/s", "peak": peak, "experts_achieved": kernel,
+                "experts_frac": kernel / peak, "layer_frac": layer / peak,
+                "peak_kind": "measured bf16 x 2 (nominal fp8 ratio)" if mx else "measured bf16"}
     kernel = st["bytes"] / (kernel_ms / 1e3) / 1e9
     layer = alg["layer_bytes"] / (layer_ms / 1e3) / 1e9
     return {"bound": "hbm", "unit": "GB/s", "peak": peaks["hbm_gbs"], "experts_achieved": kernel,
             "experts_frac": kernel / peaks["hbm_gbs"], "layer_frac": layer / peaks["hbm_gbs"]}
 
 
-def workload_entry(s: wl.Spec, t: dict, alg: dict, peaks: dict) -> dict:
+def workload_entry(s: wl.Spec, t: dict, alg: dict, peaks: dict, mx: bool = False) -> dict:
     ms = float(np.mean(t["step_ms"]))
     kernel_ms = t["stage_avg"]["experts"]
     e = {"workload": workload_config(s)["workload"], "M": s.M, "us_per_layer": ms * 1e3,
@@ -532,7 +558,8 @@ def workload_entry(s: wl.Spec, t: dict, alg: dict, peaks: dict) -> dict:
          "stage_us": {k: v * 1e3 for k, v in t["stage_avg"].items()},
          "algorithmic_bytes": alg["layer_bytes"], "algorithmic_flops": alg["layer_flops"],
          "experts_touched": alg["experts"], "adapter_pairs_touched": alg["pairs"]}
-    e.update(roofline_fields(s, alg, kernel_ms, ms, peaks))
+    e["weights"] = "mxfp8" if mx else "bf16"
+    e.update(roofline_fields(s, alg, kernel_ms, ms, peaks, mx))
     return e
 
 
@@ -545,10 +572,12 @@ def run_sweep(args, device, flush, peaks, skip_label=None, skip_entry=None):
         if label == skip_label and skip_entry is not None:
             out[label] = skip_entry
             continue
+        over = dict(over)
+        mx = over.pop("mx", False)
         s = wl.spec(name, **over)
-        run = LayerRun(s, device, not args.no_graph)
+        run = LayerRun(s, device, not args.no_graph, mx=mx)
         t = run.time(flush, steps=args.steps, warmup=max(3, min(args.warmup, 5)))
-        out[label] = workload_entry(s, t, run.alg(), peaks)
+        out[label] = workload_entry(s, t, run.alg(), peaks, mx)
         del run
         torch.cuda.empty_cache()
     return out
@@ -595,7 +624,7 @@ def main(argv=None):
     torch.cuda.set_device(device)
     peaks, peak_src = load_peaks()
     flush = L2Flush(device)
-    run = LayerRun(s, device, not args.no_graph, packed=True)
+    run = LayerRun(s, device, not args.no_graph, packed=True, mx=args.mxfp8)
     clocks = ClockSampler(local_rank)
     t = run.time(flush, args.steps, args.warmup, world, clocks=clocks)
     e2e_s, bi, bo = run.time_e2e(args.steps, args.warmup, world)
@@ -603,20 +632,21 @@ def main(argv=None):
     total_ms, _, _ = aggregate(t["step_ms"], s.M, world, device)
     e2e_s = reduce_max(e2e_s, world, device)
     inp = run.inp
-    headline_entry = workload_entry(s, t, alg, peaks)
+    headline_entry = workload_entry(s, t, alg, peaks, args.mxfp8)
     del run
     torch.cuda.empty_cache()
     workloads = None
     if not args.no_workloads and world == 1 and args.M is None:
-        workloads = run_sweep(args, device, flush, peaks, sweep_label(s, overrides), headline_entry)
+        workloads = run_sweep(args, device, flush, peaks,
+                              sweep_label(s, {**overrides, **({"mx": True} if args.mxfp8 else {})}), headline_entry)
     if rank == 0:
         ms_per_step = total_ms / args.steps
         tokens = s.M * world
         value = tokens / (ms_per_step / 1e3)
         dom_ms = t["stage_avg"]["experts"]
-        rf = roofline_fields(s, alg, dom_ms, ms_per_step, peaks)
+        rf = roofline_fields(s, alg, dom_ms, ms_per_step, peaks, args.mxfp8)
         cpu = None
-        if not args.no_cpu_baseline and world == 1:
+        if not args.no_cpu_baseline and world == 1 and not args.mxfp8:
             cpu = cpu_baseline(inp, args.cpu_seconds)
             cpu.pop("seconds", None)
         cfg = workload_config(s)
@@ -626,7 +656,9 @@ def main(argv=None):
         out = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "us_per_layer": ms_per_step * 1e3,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "mxfp8 (e4m3, e8m0 scales) expert weights, bf16 activations and adapters" if args.mxfp8
+            else "bf16",
             "data": "synthetic (seeded, random-init weights)", "config": cfg,
             "roofline": {"bound": rf["bound"], "kernel": "experts", "achieved": rf["experts_achieved"],
                          "peak": rf["peak"], "unit": rf["unit"], "frac": rf["experts_frac"],

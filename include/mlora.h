@@ -163,6 +163,65 @@ mlora_status mlora_moe_forward(const void* x, const void* w13, const void* w2, c
                                void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * ---- MXFP8 expert weights -------------------------------------------------
+ * "[vllm] vLLM ROCm 환경에서 Shared-Expert Fusion을 통한 MoE 추론 성능 최적화",
+ * section "코드 분석" item 2: the fused layer runs on an MXFP8 experts path.
+ * The pages do not define the format; it is the OCP Microscaling (MX)
+ * specification's MXFP8: along the reduction dimension (H for w13 and x, I
+ * for w2 and the SwiGLU output) blocks of 32 elements share one E8M0 scale
+ * 2^(s-127) (a byte s); elements are FP8 E4M3.  A block converts with
+ * shared exponent floor(log2 max|v|) - 8 (a block of zeros: s = 0) and
+ * elements v / 2^shared rounded to the nearest E4M3 value, ties to even,
+ * saturated to +-448.  In the MXFP8 layer x and the SwiGLU output are
+ * quantized this way on the device before they meet the expert weights; the
+ * LoRA adapters stay bf16 and read the unquantized x and SwiGLU output
+ * (shrink and expand as in the bf16 layer, accumulated with the base
+ * product).  H and I must be multiples of 32.
+ *
+ * Packed scales (the order the tensor cores read them in; `which` 0 is
+ * gate_up, 1 is down): for each expert e, tile slab cb and K-chunk kc of 128,
+ * 1024 bytes = two 512-byte atoms, atom a holding tile rows 128a..128a+127,
+ * row t's scale for K-block kb (0..3) of the chunk at byte
+ * (t % 32) * 16 + ((t % 128) / 32) * 4 + kb of its atom.  gate_up: slabs of
+ * 96 gate + 96 up rows, cb in [0, ceil(I/96)), kc in [0, ceil(H/128)); tile
+ * row t < 96 is w13 row cb*96 + t (gate), t >= 96 is row I + cb*96 + t - 96
+ * (up).  down: slabs of 192 rows of w2, cb in [0, ceil(H/192)), kc in
+ * [0, ceil(I/128)); tile row t is w2 row cb*192 + t.  Bytes of rows or
+ * blocks past the matrix are 0.
+ */
+
+/* Bytes of the packed scales of the gate_up (which = 0) or down (which = 1)
+ * weights; 0 for invalid sizes. */
+size_t mlora_mxfp8_scales_size(int E_tot, int H, int I, int which);
+
+/*
+ * Quantize bf16 expert weights to MXFP8 on the device (done once, when the
+ * weights are loaded): w13 [E_tot, 2I, H] -> w13_q [E_tot, 2I, H] E4M3
+ * codes (bytes, the weights' own layout) and w13_s packed scales
+ * (mlora_mxfp8_scales_size(..., 0) bytes); w2 [E_tot, H, I] -> w2_q and
+ * w2_s likewise.  All buffers are caller-owned device memory, 16-byte
+ * aligned.  Enqueued on `stream`; nothing is allocated.
+ */
+mlora_status mlora_mxfp8_quantize_weights(const void* w13, const void* w2, int E_tot, int H, int I, void* w13_q,
+                                          void* w13_s, void* w2_q, void* w2_s, void* stream);
+
+/* Workspace bytes of mlora_moe_forward_mxfp8 (as mlora_moe_workspace_size). */
+size_t mlora_moe_workspace_size_mxfp8(int M, int H, int I, int E_tot, int K_total, int L, int rank);
+
+/*
+ * The layer of mlora_moe_forward with MXFP8 expert weights (w13_q, w13_s,
+ * w2_q, w2_s from mlora_mxfp8_quantize_weights); every other argument,
+ * constraint and convention as there, plus H and I multiples of 32.  The
+ * expert tiles are 192 weight rows wide.
+ */
+mlora_status mlora_moe_forward_mxfp8(const void* x, const void* w13_q, const void* w13_s, const void* w2_q,
+                                     const void* w2_s, const void* A13, const void* B13, const void* A2,
+                                     const void* B2, const int32_t* token_lora_idx, const int32_t* topk_ids,
+                                     const float* topk_w, int M, int H, int I, int E_tot, int K_total, int L,
+                                     int rank, float scaling, int n_shared, float out_scale, void* y,
+                                     void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * mlora_moe_forward_static -- the same layer as mlora_moe_forward, for
  * callers that cannot allocate device memory where they run it (their
  * device memory belongs to another allocator they must not bypass, they may

@@ -19,11 +19,15 @@ from ._lib import (  # noqa: F401
     mlora_moe_align,
     mlora_moe_align_max_padded,
     mlora_moe_forward,
+    mlora_moe_forward_mxfp8,
     mlora_moe_forward_static,
     mlora_moe_read_status,
     mlora_moe_read_status_static,
     mlora_moe_route,
     mlora_moe_workspace_size,
+    mlora_moe_workspace_size_mxfp8,
+    mlora_mxfp8_quantize_weights,
+    mlora_mxfp8_scales_size,
     mlora_set_stage_events,
     mlora_set_wait_test,
     mlora_status_string,

@@ -81,6 +81,14 @@ def load(path: str = LIB_PATH):
     lib.mlora_moe_forward_static.restype = i
     lib.mlora_moe_read_status_static.argtypes = [ctypes.POINTER(ctypes.c_uint32), P]
     lib.mlora_moe_read_status_static.restype = i
+    lib.mlora_mxfp8_scales_size.argtypes = [i] * 4
+    lib.mlora_mxfp8_scales_size.restype = sz
+    lib.mlora_mxfp8_quantize_weights.argtypes = [P, P, i, i, i, P, P, P, P, P]
+    lib.mlora_mxfp8_quantize_weights.restype = i
+    lib.mlora_moe_workspace_size_mxfp8.argtypes = [i] * 7
+    lib.mlora_moe_workspace_size_mxfp8.restype = sz
+    lib.mlora_moe_forward_mxfp8.argtypes = [P] * 12 + [i] * 7 + [f, i, f, P, P, sz, P]
+    lib.mlora_moe_forward_mxfp8.restype = i
     _lib = lib
     return lib
 
@@ -140,9 +148,11 @@ def _need(t, dtype, name: str, shape=None, device=None):
     _need_place(t, name, device)
 
 
-def _layer_args(x, w13, w2, A13, B13, A2, B2, token_lora_idx, topk_ids, topk_w, y):
+def _layer_args(x, w13, w2, A13, B13, A2, B2, token_lora_idx, topk_ids, topk_w, y, weight_dtype=torch.bfloat16,
+                extra=()):
     """Checks the layer's tensors against each other; returns
-    (M, H, I, E_tot, K', L, rank, lora)."""
+    (M, H, I, E_tot, K', L, rank, lora).  `extra`: more (tensor, dtype,
+    name, shape) checks (shape may be a callable of (E_tot, H, I))."""
     if not isinstance(x, torch.Tensor) or x.dim() != 2 or not isinstance(w13, torch.Tensor) or w13.dim() != 3:
         raise ValueError("x must be [M, H] and w13 [E_tot, 2I, H]")
     M, H = x.shape
@@ -153,9 +163,10 @@ def _layer_args(x, w13, w2, A13, B13, A2, B2, token_lora_idx, topk_ids, topk_w, 
     if not isinstance(topk_ids, torch.Tensor) or topk_ids.dim() != 2:
         raise ValueError("topk_ids must be [M, K']")
     KT = topk_ids.shape[1]
-    checks = [(x, torch.bfloat16, "x", (M, H)), (w13, torch.bfloat16, "w13", (E_tot, 2 * I, H)),
-              (w2, torch.bfloat16, "w2", (E_tot, H, I)), (topk_ids, torch.int32, "topk_ids", (M, KT)),
+    checks = [(x, torch.bfloat16, "x", (M, H)), (w13, weight_dtype, "w13", (E_tot, 2 * I, H)),
+              (w2, weight_dtype, "w2", (E_tot, H, I)), (topk_ids, torch.int32, "topk_ids", (M, KT)),
               (topk_w, torch.float32, "topk_w", (M, KT))]
+    checks += [(t, dt, name, shape(E_tot, H, I) if callable(shape) else shape) for t, dt, name, shape in extra]
     if y is not None:
         checks.append((y, torch.bfloat16, "y", (M, H)))
     given = [t is not None for t in (A13, B13, A2, B2, token_lora_idx)]
@@ -255,6 +266,68 @@ def mlora_moe_forward(x, w13, w2, A13, B13, A2, B2, token_lora_idx, topk_ids, to
             _ptr(topk_ids), _ptr(topk_w), M, H, I, E_tot, KT, L, r, float(scaling), int(n_shared),
             float(out_scale), _ptr(y), _ptr(workspace), workspace.numel(), _stream(stream, x.device))
     _check("mlora_moe_forward", st)
+    return y
+
+
+def mlora_mxfp8_scales_size(E_tot: int, H: int, I: int, which: int) -> int:
+    return int(load().mlora_mxfp8_scales_size(E_tot, H, I, which))
+
+
+def mlora_mxfp8_quantize_weights(w13: torch.Tensor, w2: torch.Tensor, stream=None):
+    """bf16 expert weights to MXFP8 on their device: returns (w13_q, w13_s,
+    w2_q, w2_s), E4M3 codes in the weights' layout and packed E8M0 scales
+    (see include/mlora.h)."""
+    if not isinstance(w13, torch.Tensor) or w13.dim() != 3 or not isinstance(w2, torch.Tensor) or w2.dim() != 3:
+        raise ValueError("w13 must be [E_tot, 2I, H] and w2 [E_tot, H, I]")
+    E_tot, twoI, H = w13.shape
+    I = twoI // 2
+    _need(w13, torch.bfloat16, "w13", (E_tot, 2 * I, H))
+    _need(w2, torch.bfloat16, "w2", (E_tot, H, I), w13.device)
+    n13, n2 = mlora_mxfp8_scales_size(E_tot, H, I, 0), mlora_mxfp8_scales_size(E_tot, H, I, 1)
+    if not n13 or not n2:
+        raise ValueError(f"MXFP8 needs H and I multiples of 32 (H={H}, I={I})")
+    dev = w13.device
+    w13_q = torch.empty((E_tot, 2 * I, H), dtype=torch.uint8, device=dev)
+    w2_q = torch.empty((E_tot, H, I), dtype=torch.uint8, device=dev)
+    w13_s = torch.empty(n13, dtype=torch.uint8, device=dev)
+    w2_s = torch.empty(n2, dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        st = load().mlora_mxfp8_quantize_weights(_ptr(w13), _ptr(w2), E_tot, H, I, _ptr(w13_q), _ptr(w13_s),
+                                                 _ptr(w2_q), _ptr(w2_s), _stream(stream, dev))
+    _check("mlora_mxfp8_quantize_weights", st)
+    return w13_q, w13_s, w2_q, w2_s
+
+
+def mlora_moe_workspace_size_mxfp8(M: int, H: int, I: int, E_tot: int, K_total: int, L: int, rank: int) -> int:
+    return int(load().mlora_moe_workspace_size_mxfp8(M, H, I, E_tot, K_total, L, rank))
+
+
+def mlora_moe_forward_mxfp8(x, w13_q, w13_s, w2_q, w2_s, A13, B13, A2, B2, token_lora_idx, topk_ids, topk_w,
+                            scaling: float, n_shared: int = 0, out_scale: float = 1.0,
+                            y: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                            stream=None):
+    """The fused MoE-LoRA layer with MXFP8 expert weights (from
+    mlora_mxfp8_quantize_weights); returns y [M, H] bf16."""
+    extra = [(w13_s, torch.uint8, "w13_s", lambda E, H, I: (mlora_mxfp8_scales_size(E, H, I, 0),)),
+             (w2_s, torch.uint8, "w2_s", lambda E, H, I: (mlora_mxfp8_scales_size(E, H, I, 1),))]
+    M, H, I, E_tot, KT, L, r, lora = _layer_args(x, w13_q, w2_q, A13, B13, A2, B2, token_lora_idx, topk_ids,
+                                                 topk_w, y, weight_dtype=torch.uint8, extra=extra)
+    if y is None:
+        y = torch.empty((M, H), dtype=torch.bfloat16, device=x.device)
+    need = mlora_moe_workspace_size_mxfp8(M, H, I, E_tot, KT, L, r)
+    if need == 0:
+        raise ValueError(f"invalid MXFP8 layer sizes (H={H}, I={I} must be multiples of 32)")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    _need(workspace, torch.uint8, "workspace", None, x.device)
+    with torch.cuda.device(x.device):
+        st = load().mlora_moe_forward_mxfp8(
+            _ptr(x), _ptr(w13_q), _ptr(w13_s), _ptr(w2_q), _ptr(w2_s), _ptr(A13) if lora else None,
+            _ptr(B13) if lora else None, _ptr(A2) if lora else None, _ptr(B2) if lora else None,
+            _ptr(token_lora_idx) if lora else None, _ptr(topk_ids), _ptr(topk_w), M, H, I, E_tot, KT, L, r,
+            float(scaling), int(n_shared), float(out_scale), _ptr(y), _ptr(workspace), workspace.numel(),
+            _stream(stream, x.device))
+    _check("mlora_moe_forward_mxfp8", st)
     return y
 
 

@@ -26,6 +26,7 @@
 #include <mutex>
 
 #include "internal.cuh"
+#include "mx.cuh"
 
 namespace mlora {
 
@@ -52,13 +53,19 @@ EncodeTiledFn encode_fn() {
 // bf16 tensor map with 128-byte swizzle; dims innermost first, strides in
 // bytes for dims 1..rank-1.
 bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
-              const cuuint32_t* box) {
+              const cuuint32_t* box, CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank), const_cast<void*>(base), dims,
-              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return fn(m, dtype, static_cast<cuuint32_t>(rank), const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// E4M3 bytes (MXFP8 layer)
+bool make_map_u8(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+                 const cuuint32_t* box) {
+    return make_map(m, base, rank, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_UINT8);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -139,8 +146,11 @@ int device_sm_count() {
     return n;
 }
 
-Sizes make_sizes(int M, int H, int I, int E_tot, int K_total, int L, int rank) {
+Sizes make_sizes(int M, int H, int I, int E_tot, int K_total, int L, int rank, bool mx) {
     Sizes z{};
+    z.mx = mx;
+    z.nkc0 = static_cast<int>(mx_chunks(0, H, I));
+    z.nkc1 = static_cast<int>(mx_chunks(1, H, I));
     z.M = M;
     z.H = H;
     z.I = I;
@@ -155,8 +165,9 @@ Sizes make_sizes(int M, int H, int I, int E_tot, int K_total, int L, int rank) {
     z.cap = z.lora ? std::min(L, kBlockM) : 0;
     z.max_lt = z.max_blocks * z.cap;
     // adapters per shrink group tile: up to 256 stacked rank rows (the MMA's
-    // N), at most 4 so that a block's shrink spreads over more SMs
-    z.gsize = z.lora ? std::min(4, 256 / ((rank + 15) / 16 * 16)) : 1;
+    // N; 192, the accumulator width, in the MXFP8 layer), at most 4 so that
+    // a block's shrink spreads over more SMs
+    z.gsize = z.lora ? std::min(4, (mx ? kMxWidth : 256) / ((rank + 15) / 16 * 16)) : 1;
     return z;
 }
 
@@ -192,8 +203,18 @@ Workspace carve_workspace(const Sizes& z, void* base) {
         w.gt_block = reinterpret_cast<int32_t*>(take(4 * z.max_lt));
         w.gt_first = reinterpret_cast<int32_t*>(take(4 * z.max_lt));
     }
-    w.x_perm = take(2 * static_cast<size_t>(z.max_padded) * z.H);
-    w.act = take(2 * static_cast<size_t>(z.max_padded) * z.I);
+    // bf16 token rows: the base GEMMs' A (bf16 layer) or the shrinks' (adapters)
+    if (!z.mx || z.lora) {
+        w.x_perm = take(2 * static_cast<size_t>(z.max_padded) * z.H);
+        w.act = take(2 * static_cast<size_t>(z.max_padded) * z.I);
+    }
+    if (z.mx) {
+        // MXFP8 token rows and their scale atoms (one per 128 rows and K-chunk)
+        w.x_q = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(z.max_padded) * z.H));
+        w.x_s = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(z.max_blocks) * z.nkc0 * kMxAtom));
+        w.act_q = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(z.max_padded) * z.I));
+        w.act_s = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(z.max_blocks) * z.nkc1 * kMxAtom));
+    }
     if (z.lora) {
         w.lora_t13 = take(2 * static_cast<size_t>(z.max_lt) * kBlockM * kLoraTileCols);
         w.lora_t2 = take(2 * static_cast<size_t>(z.max_lt) * kBlockM * kLoraTileCols);
@@ -259,15 +280,17 @@ mlora_status mlora_moe_align(const int32_t* topk_ids, int M, int K_total, int E_
                                     nullptr, nullptr, static_cast<cudaStream_t>(stream)));
 }
 
-static mlora_status check_forward_sizes(int M, int H, int I, int E_tot, int K_total, int L, int rank) {
+static mlora_status check_forward_sizes(int M, int H, int I, int E_tot, int K_total, int L, int rank,
+                                        bool mx = false) {
     if (M < 0 || H < 8 || I < 8 || (H % 8) || (I % 8) || E_tot < 1 || E_tot > MLORA_MAX_EXPERTS || K_total < 1 ||
         K_total > MLORA_MAX_TOPK || L < 0 || rank < 0)
         return MLORA_ERR_SHAPE;
+    if (mx && (H % kMxBlock || I % kMxBlock)) return MLORA_ERR_SHAPE;
     if (L > 0 && rank > 0 && (rank % 8 || rank > MLORA_MAX_RANK)) return MLORA_ERR_UNSUPPORTED;
     const long S = static_cast<long>(M) * K_total;
     if (S + static_cast<long>(E_tot) * kBlockM >= 0x7fffffffL) return MLORA_ERR_SHAPE;
     if (static_cast<long>(L) * E_tot >= 0x7fffffffL) return MLORA_ERR_SHAPE;
-    const Sizes z = make_sizes(M, H, I, E_tot, K_total, L, rank);
+    const Sizes z = make_sizes(M, H, I, E_tot, K_total, L, rank, mx);
     if (z.max_lt * kBlockM >= 0x7fffffffL) return MLORA_ERR_SHAPE;
     return MLORA_OK;
 }
@@ -277,17 +300,69 @@ size_t mlora_moe_workspace_size(int M, int H, int I, int E_tot, int K_total, int
     return carve_workspace(make_sizes(M, H, I, E_tot, K_total, L, rank), nullptr).bytes;
 }
 
-mlora_status mlora_moe_forward(const void* x, const void* w13, const void* w2, const void* A13, const void* B13,
-                               const void* A2, const void* B2, const int32_t* token_lora_idx,
-                               const int32_t* topk_ids, const float* topk_w, int M, int H, int I, int E_tot,
-                               int K_total, int L, int rank, float scaling, int n_shared, float out_scale, void* y,
-                               void* workspace, size_t workspace_bytes, void* stream) {
+size_t mlora_moe_workspace_size_mxfp8(int M, int H, int I, int E_tot, int K_total, int L, int rank) {
+    if (check_forward_sizes(M, H, I, E_tot, K_total, L, rank, true) != MLORA_OK) return 0;
+    return carve_workspace(make_sizes(M, H, I, E_tot, K_total, L, rank, true), nullptr).bytes;
+}
+
+size_t mlora_mxfp8_scales_size(int E_tot, int H, int I, int which) {
+    if (E_tot < 1 || E_tot > MLORA_MAX_EXPERTS || H < kMxBlock || I < kMxBlock || H % kMxBlock || I % kMxBlock ||
+        (which != 0 && which != 1))
+        return 0;
+    return static_cast<size_t>(E_tot) * mx_slabs(which, H, I) * mx_chunks(which, H, I) * kMxTileScaleBytes;
+}
+
+mlora_status mlora_mxfp8_quantize_weights(const void* w13, const void* w2, int E_tot, int H, int I, void* w13_q,
+                                          void* w13_s, void* w2_q, void* w2_s, void* stream) {
+    const size_t s13 = mlora_mxfp8_scales_size(E_tot, H, I, 0), s2 = mlora_mxfp8_scales_size(E_tot, H, I, 1);
+    if (!s13 || !s2) return MLORA_ERR_SHAPE;
+    const void* ptrs[] = {w13, w2, w13_q, w13_s, w2_q, w2_s};
+    for (const void* ptr : ptrs)
+        if (!ptr || !aligned16(ptr)) return MLORA_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (foreign_device_memory(s, {w13, w2, w13_q, w13_s, w2_q, w2_s})) return MLORA_ERR_INVALID_ARG;
+    cudaError_t err;
+    // bytes of the packed scales that no weight row fills (ragged last slab
+    // or K-chunk) read as 2^-127
+    if ((err = cudaMemsetAsync(w13_s, 0, s13, s)) != cudaSuccess) return cuda_fail(err, "scales");
+    if ((err = cudaMemsetAsync(w2_s, 0, s2, s)) != cudaSuccess) return cuda_fail(err, "scales");
+    err = launch_mx_quantize_weights(w13, 2L * I * E_tot, H, 0, H, I, static_cast<uint8_t*>(w13_q),
+                                     static_cast<uint8_t*>(w13_s), s);
+    if (err != cudaSuccess) return cuda_fail(err, "quantize w13");
+    err = launch_mx_quantize_weights(w2, static_cast<long>(H) * E_tot, I, 1, H, I, static_cast<uint8_t*>(w2_q),
+                                     static_cast<uint8_t*>(w2_s), s);
+    if (err != cudaSuccess) return cuda_fail(err, "quantize w2");
+    return MLORA_OK;
+}
+
+namespace {
+
+// MXFP8 expert weights of a forward (null: the bf16 layer).
+struct MxWeights {
+    const void* w13_q;
+    const void* w13_s;
+    const void* w2_q;
+    const void* w2_s;
+};
+
+mlora_status forward_impl(const void* x, const void* w13, const void* w2, const MxWeights* mxw, const void* A13,
+                          const void* B13, const void* A2, const void* B2, const int32_t* token_lora_idx,
+                          const int32_t* topk_ids, const float* topk_w, int M, int H, int I, int E_tot, int K_total,
+                          int L, int rank, float scaling, int n_shared, float out_scale, void* y, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+    const bool mx = mxw != nullptr;
     const bool lora = A13 && B13 && A2 && B2 && token_lora_idx && L > 0 && rank > 0;
     const int L_eff = lora ? L : 0, r_eff = lora ? rank : 0;
-    mlora_status st = check_forward_sizes(M, H, I, E_tot, K_total, L, rank);
+    mlora_status st = check_forward_sizes(M, H, I, E_tot, K_total, L, rank, mx);
     if (st != MLORA_OK) return st;
     if (n_shared < 0 || n_shared >= K_total || n_shared >= E_tot) return MLORA_ERR_SHAPE;
     if (M == 0) return MLORA_OK;
+    if (mx) {
+        w13 = mxw->w13_q;
+        w2 = mxw->w2_q;
+        if (!mxw->w13_s || !mxw->w2_s || !aligned16(mxw->w13_s) || !aligned16(mxw->w2_s))
+            return MLORA_ERR_INVALID_ARG;
+    }
     if (!x || !w13 || !w2 || !topk_ids || !topk_w || !y) return MLORA_ERR_INVALID_ARG;
     const void* ptrs[] = {x, w13, w2, topk_ids, topk_w, y};
     for (const void* ptr : ptrs)
@@ -298,10 +373,11 @@ mlora_status mlora_moe_forward(const void* x, const void* w13, const void* w2, c
             if (!aligned16(ptr)) return MLORA_ERR_INVALID_ARG;
         if (reinterpret_cast<uintptr_t>(token_lora_idx) & 3u) return MLORA_ERR_INVALID_ARG;
     }
-    if (foreign_device_memory(static_cast<cudaStream_t>(stream), {x, w13, w2, topk_ids, topk_w, y, workspace,
-                                                                  lora ? A13 : nullptr, lora ? token_lora_idx : nullptr}))
+    if (foreign_device_memory(static_cast<cudaStream_t>(stream),
+                              {x, w13, w2, topk_ids, topk_w, y, workspace, lora ? A13 : nullptr,
+                               lora ? token_lora_idx : nullptr, mx ? mxw->w13_s : nullptr}))
         return MLORA_ERR_INVALID_ARG;
-    const Sizes z = make_sizes(M, H, I, E_tot, K_total, L_eff, r_eff);
+    const Sizes z = make_sizes(M, H, I, E_tot, K_total, L_eff, r_eff, mx);
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return MLORA_ERR_WORKSPACE;
     const Workspace ws = carve_workspace(z, workspace);
     if (workspace_bytes < ws.bytes) return MLORA_ERR_WORKSPACE;
@@ -315,13 +391,6 @@ mlora_status mlora_moe_forward(const void* x, const void* w13, const void* w2, c
     {
         const cuuint32_t bx[2] = {64, kRowBox};
         const cuuint32_t bxf[2] = {64, 128};
-        const cuuint64_t dx[2] = {H_, MP}, sx[1] = {H_ * 2};
-        ok &= make_map(&up.tm_a, ws.x_perm, 2, dx, sx, bx);
-        ok &= make_map(&up.tm_a_full, ws.x_perm, 2, dx, sx, bxf);
-        const cuuint64_t da[2] = {I_, MP}, sa[1] = {I_ * 2};
-        ok &= make_map(&dn.tm_a, ws.act, 2, da, sa, bx);
-        ok &= make_map(&dn.tm_a_full, ws.act, 2, da, sa, bxf);
-        const cuuint64_t d13[4] = {H_, I_, 2, E_}, s13[3] = {H_ * 2, I_ * H_ * 2, 2 * I_ * H_ * 2};
         // a gate_up tile of width n takes n/2 gate and n/2 up rows, a down tile n rows
         cuuint32_t b13[kTileWidths][4], b2[kTileWidths][3];
         for (int wc = 0; wc < kTileWidths; ++wc) {
@@ -329,10 +398,35 @@ mlora_status mlora_moe_forward(const void* x, const void* w13, const void* w2, c
             b13[wc][0] = 64, b13[wc][1] = n / 2, b13[wc][2] = 1, b13[wc][3] = 1;
             b2[wc][0] = 64, b2[wc][1] = n, b2[wc][2] = 1;
         }
-        const cuuint64_t d2[3] = {I_, H_, E_}, s2[2] = {I_ * 2, H_ * I_ * 2};
-        for (int wc = 0; wc < kTileWidths; ++wc) {
-            ok &= make_map(&up.tm_b[wc], w13, 4, d13, s13, b13[wc]);
-            ok &= make_map(&dn.tm_b[wc], w2, 3, d2, s2, b2[wc]);
+        if (ws.x_perm) {
+            const cuuint64_t dx[2] = {H_, MP}, sx[1] = {H_ * 2};
+            ok &= make_map(&up.tm_a, ws.x_perm, 2, dx, sx, bx);
+            ok &= make_map(&up.tm_a_full, ws.x_perm, 2, dx, sx, bxf);
+            const cuuint64_t da[2] = {I_, MP}, sa[1] = {I_ * 2};
+            ok &= make_map(&dn.tm_a, ws.act, 2, da, sa, bx);
+            ok &= make_map(&dn.tm_a_full, ws.act, 2, da, sa, bxf);
+        }
+        if (mx) {
+            const cuuint32_t qb[2] = {kMxChunk, kRowBox}, qbf[2] = {kMxChunk, 128};
+            const cuuint64_t dx[2] = {H_, MP}, sx[1] = {H_};
+            ok &= make_map_u8(&up.tm_aq, ws.x_q, 2, dx, sx, qb);
+            ok &= make_map_u8(&up.tm_aq_full, ws.x_q, 2, dx, sx, qbf);
+            const cuuint64_t da[2] = {I_, MP}, sa[1] = {I_};
+            ok &= make_map_u8(&dn.tm_aq, ws.act_q, 2, da, sa, qb);
+            ok &= make_map_u8(&dn.tm_aq_full, ws.act_q, 2, da, sa, qbf);
+            const cuuint64_t d13[4] = {H_, I_, 2, E_}, s13[3] = {H_, I_ * H_, 2 * I_ * H_};
+            const cuuint32_t q13[4] = {kMxChunk, kMxHalf, 1, 1};
+            ok &= make_map_u8(&up.tm_bq, w13, 4, d13, s13, q13);
+            const cuuint64_t d2[3] = {I_, H_, E_}, s2[2] = {I_, H_ * I_};
+            const cuuint32_t q2[3] = {kMxChunk, kMxWidth, 1};
+            ok &= make_map_u8(&dn.tm_bq, w2, 3, d2, s2, q2);
+        } else {
+            const cuuint64_t d13[4] = {H_, I_, 2, E_}, s13[3] = {H_ * 2, I_ * H_ * 2, 2 * I_ * H_ * 2};
+            const cuuint64_t d2[3] = {I_, H_, E_}, s2[2] = {I_ * 2, H_ * I_ * 2};
+            for (int wc = 0; wc < kTileWidths; ++wc) {
+                ok &= make_map(&up.tm_b[wc], w13, 4, d13, s13, b13[wc]);
+                ok &= make_map(&dn.tm_b[wc], w2, 3, d2, s2, b2[wc]);
+            }
         }
         if (lora) {
             const cuuint64_t R = rank, LE = static_cast<cuuint64_t>(L) * E_tot;
@@ -371,6 +465,17 @@ mlora_status mlora_moe_forward(const void* x, const void* w13, const void* w2, c
     dn.K = I;
     dn.n_out = H;
     dn.ncb = (H + 255) / 256;
+    if (mx) {
+        up.a_scales = ws.x_s;
+        up.b_scales = static_cast<const uint8_t*>(mxw->w13_s);
+        up.out_q = ws.act_q;
+        up.out_s = ws.act_s;
+        up.nkc = z.nkc0;
+        dn.a_scales = ws.act_s;
+        dn.b_scales = static_cast<const uint8_t*>(mxw->w2_s);
+        dn.nkc = z.nkc1;
+    }
+    gp.mx = mx ? 1 : 0;
     gp.n_pad = ws.n_pad;
     gp.expert_ids = ws.expert_ids;
     gp.blk_rows = ws.blk_rows;
@@ -425,7 +530,7 @@ mlora_status mlora_moe_forward(const void* x, const void* w13, const void* w2, c
         ex.gt_first = ws.gt_first;
         ex.gt_total = ws.gt_total;
     }
-    if (align_small_fits(z.S, E_tot, kBlockM, z.max_padded, &ex, true)) {
+    if (!mx && align_small_fits(z.S, E_tot, kBlockM, z.max_padded, &ex, true)) {
         // small batches: align and the row gather in one launch (stage
         // boundaries 1 and 2 coincide)
         const GatherArgs ga{x, ws.x_perm, H, K_total};
@@ -438,8 +543,12 @@ mlora_status mlora_moe_forward(const void* x, const void* w13, const void* w2, c
                            ws.status, &ex, s);
         if (err != cudaSuccess) return cuda_fail(err, "align");
         if ((err = mark_stage(1, s)) != cudaSuccess) return cuda_fail(err, "stage event");
-        err = launch_gather_rows(x, H, ws.sorted_ids, ws.n_pad, z.S, K_total, z.max_padded, ws.x_perm, ws.status,
-                                 s);
+        if (mx)
+            err = launch_mx_gather(x, H, K_total, ws.sorted_ids, ws.n_pad, z.S, z.max_padded, ws.x_q, ws.x_s,
+                                   ws.x_perm, ws.status, s);
+        else
+            err = launch_gather_rows(x, H, ws.sorted_ids, ws.n_pad, z.S, K_total, z.max_padded, ws.x_perm,
+                                     ws.status, s);
         if (err != cudaSuccess) return cuda_fail(err, "gather");
     }
     if ((err = mark_stage(2, s)) != cudaSuccess) return cuda_fail(err, "stage event");
@@ -452,6 +561,29 @@ mlora_status mlora_moe_forward(const void* x, const void* w13, const void* w2, c
     if (err != cudaSuccess) return cuda_fail(err, "combine");
     if ((err = mark_stage(4, s)) != cudaSuccess) return cuda_fail(err, "stage event");
     return MLORA_OK;
+}
+
+}  // namespace
+
+mlora_status mlora_moe_forward(const void* x, const void* w13, const void* w2, const void* A13, const void* B13,
+                               const void* A2, const void* B2, const int32_t* token_lora_idx,
+                               const int32_t* topk_ids, const float* topk_w, int M, int H, int I, int E_tot,
+                               int K_total, int L, int rank, float scaling, int n_shared, float out_scale, void* y,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+    return forward_impl(x, w13, w2, nullptr, A13, B13, A2, B2, token_lora_idx, topk_ids, topk_w, M, H, I, E_tot,
+                        K_total, L, rank, scaling, n_shared, out_scale, y, workspace, workspace_bytes, stream);
+}
+
+mlora_status mlora_moe_forward_mxfp8(const void* x, const void* w13_q, const void* w13_s, const void* w2_q,
+                                     const void* w2_s, const void* A13, const void* B13, const void* A2,
+                                     const void* B2, const int32_t* token_lora_idx, const int32_t* topk_ids,
+                                     const float* topk_w, int M, int H, int I, int E_tot, int K_total, int L,
+                                     int rank, float scaling, int n_shared, float out_scale, void* y,
+                                     void* workspace, size_t workspace_bytes, void* stream) {
+    const MxWeights mxw{w13_q, w13_s, w2_q, w2_s};
+    return forward_impl(x, nullptr, nullptr, &mxw, A13, B13, A2, B2, token_lora_idx, topk_ids, topk_w, M, H, I,
+                        E_tot, K_total, L, rank, scaling, n_shared, out_scale, y, workspace, workspace_bytes,
+                        stream);
 }
 
 mlora_status mlora_set_stage_events(void* const* events, int count) {

@@ -57,6 +57,7 @@
 #include <atomic>
 
 #include "internal.cuh"
+#include "mx.cuh"
 #include "ptx.cuh"
 
 namespace mlora {
@@ -70,7 +71,21 @@ constexpr int kBN = 256;                                         // weight rows 
 // flight.
 constexpr int kStages = 4;
 constexpr int kSmallStages = 6;
-constexpr int kMaxStages = kSmallStages > kStages ? kSmallStages : kStages;  // barrier arrays
+// MXFP8 stages: A rows x 128 E4M3 (16 KiB for a full block, 4 KiB for one
+// 32-row box), B 192 x 128 E4M3 (24 KiB), then the stage's scale atoms
+// (512 B for A, 1 KiB for B), rounded up to the 1 KiB swizzle atom
+constexpr int kMxBBytes = kMxWidth * kMxChunk;
+constexpr int kMxStageBytes = (16384 + kMxBBytes + 3 * kMxAtom + 1023) / 1024 * 1024;  // 42 KiB
+constexpr int kMxStages = 5;
+constexpr int kMxSmallStageBytes = (4096 + kMxBBytes + 3 * kMxAtom + 1023) / 1024 * 1024;  // 30 KiB
+constexpr int kMxSmallStages = 7;
+constexpr int kMaxStages = 7;  // barrier arrays: the deepest ring
+static_assert(kMaxStages >= kStages && kMaxStages >= kSmallStages && kMaxStages >= kMxStages &&
+                  kMaxStages >= kMxSmallStages, "barrier arrays");
+// MXFP8 tensor memory: two 192-column accumulators, then two slots of
+// scale factors (A at +0, B at +32 -- 32-column aligned -- of each 64)
+constexpr int kMxAccCols = kMxWidth;
+constexpr int kMxSfCol0 = 2 * kMxAccCols;
 constexpr int kTileRing = 4;                                     // claimed tiles handed from producer to consumers
 constexpr int kATileBytes = kBlockM * kBlockK * 2;               // 16 KiB
 constexpr int kStageBytes = kATileBytes + kBN * kBlockK * 2;     // 48 KiB
@@ -81,6 +96,8 @@ constexpr int kAccCols = kBN;
 constexpr int kTmemCols = 2 * kBN;
 constexpr int kSmemBytes = kRingBytes + 1024 /* alignment slack */ + 256 /* barriers */;
 static_assert(kStages * kStageBytes <= kRingBytes && kSmallStages * kSmallStageBytes <= kRingBytes, "ring");
+static_assert(kMxStages * kMxStageBytes <= kRingBytes && kMxSmallStages * kMxSmallStageBytes <= kRingBytes, "ring");
+static_assert(kMxSfCol0 + 2 * 64 <= 512, "tensor memory");
 // one CTA per SM: each CTA allocates all 512 TMEM columns, so two CTAs of
 // this kernel on one SM would wait on each other
 static_assert(2 * kSmemBytes > 228 * 1024, "the experts kernel must not fit twice on an SM");
@@ -271,7 +288,8 @@ struct Ctx {
         : p(&prm), smem(sm), L(sm), tmem_base(tmem), lim(prm.wait_limit) {
         nblocks = *prm.n_pad / kBlockM;
         ns = prm.has_lora ? *prm.gt_total : 0;
-        gm.wc = choose_width(nblocks, prm.side[0].n_out, prm.side[1].n_out, gridDim.x);
+        // MXFP8 launches use 192-row tiles: the packed weight scales follow them
+        gm.wc = prm.mx ? 1 : choose_width(nblocks, prm.side[0].n_out, prm.side[1].n_out, gridDim.x);
         gm.bn = tile_width(gm.wc);
         gm.half = gm.bn / 2;
         gm.ncb0 = (prm.side[0].n_out + gm.half - 1) / gm.half;
@@ -288,7 +306,7 @@ struct Ctx {
 // TMA producer (one thread): claims tiles, hands them on through the tile
 // ring and streams their operands into a ring of nst stages of stb bytes,
 // the first ab of each holding A rows.
-template <int nst, uint32_t stb, uint32_t ab>
+template <int nst, uint32_t stb, uint32_t ab, bool kMx>
 __device__ __forceinline__ void producer(const Ctx& c, long first_tile) {
     const GemmParams& p = *c.p;
     uint64_t* const full = c.L.full;
@@ -347,6 +365,8 @@ __device__ __forceinline__ void producer(const Ctx& c, long first_tile) {
         const uint32_t a_bytes = static_cast<uint32_t>(nbox) * kRowBox * kBlockK * 2;
         const int32_t* lora_list = p.blk_lora + static_cast<long>(tc.b) * p.cap;
         const int nk = (sd.K + kBlockK - 1) / kBlockK;
+        // base tiles of the MXFP8 layer: K-chunks of 128 E4M3
+        const int nk_base = kMx ? sd.nkc : nk;
         const CUtensorMap* bmap = &sd.tm_b[gm.wc];
         const CUtensorMap* lbmap = &sd.tm_lb[gm.wc];
         if (tc.shrink) {
@@ -383,16 +403,41 @@ __device__ __forceinline__ void producer(const Ctx& c, long first_tile) {
             }
             continue;
         }
-        for (int kb = 0; kb < nk; ++kb, ++it) {
+        for (int kb = 0; kb < nk_base; ++kb, ++it) {
             const int s = static_cast<int>(it % nst);
             const uint32_t phs = static_cast<uint32_t>(it / nst) & 1u;
             if (!mbar_wait(&empty[s], phs ^ 1u, abort_flag, p.status, lim)) {
                 ok = false;
                 break;
             }
-            if (kb + 3 >= nk) claim();
+            if (kb + 3 >= nk_base) claim();
             uint8_t* sa = smem + s * stb;
             uint8_t* sb = sa + ab;
+            if (kMx) {
+                // E4M3 A and B rows of K-chunk kb (128 bytes a row), then the
+                // chunk's scale atoms: A's from the activations' atoms, B's
+                // from the packed weight scales of this slab
+                uint8_t* sf = sb + kMxBBytes;
+                const int kx = kb * kMxChunk;
+                mbar_arrive_expect_tx(&full[s], a_bytes + gm.bn * kMxChunk + 3 * kMxAtom);
+                if (tc.kind == kGateUp) {
+                    tma_load_4d(sb, &sd.tm_bq, &full[s], kx, tc.cb * gm.half, 0, tc.e);
+                    tma_load_4d(sb + gm.half * kMxChunk, &sd.tm_bq, &full[s], kx, tc.cb * gm.half, 1, tc.e);
+                } else {
+                    tma_load_3d(sb, &sd.tm_bq, &full[s], kx, tc.cb * gm.bn, tc.e);
+                }
+                if (full_block)
+                    tma_load_2d(sa, &sd.tm_aq_full, &full[s], kx, row0);
+                else
+                    for (int i = 0; i < nbox; ++i)
+                        tma_load_2d(sa + i * kRowBox * kMxChunk, &sd.tm_aq, &full[s], kx, row0 + i * kRowBox);
+                const long ncb = tc.side ? gm.ncb1 : gm.ncb0;
+                bulk_load(sf, sd.a_scales + (static_cast<size_t>(tc.b) * sd.nkc + kb) * kMxAtom, kMxAtom, &full[s]);
+                bulk_load(sf + kMxAtom,
+                          sd.b_scales + ((static_cast<size_t>(tc.e) * ncb + tc.cb) * sd.nkc + kb) * kMxTileScaleBytes,
+                          kMxTileScaleBytes, &full[s]);
+                continue;
+            }
             const int k0 = kb * kBlockK;
             if (tc.kind == kGateUp) {
                 mbar_arrive_expect_tx(&full[s], a_bytes + gm.bn * kBlockK * 2);
@@ -450,7 +495,7 @@ __device__ __forceinline__ void producer(const Ctx& c, long first_tile) {
 }
 
 // MMA issuer (one thread), over the same ring geometry as the producer.
-template <int nst, uint32_t stb, uint32_t ab>
+template <int nst, uint32_t stb, uint32_t ab, bool kMx>
 __device__ __forceinline__ void mma_issuer(const Ctx& c) {
     const GemmParams& p = *c.p;
     uint64_t* const full = c.L.full;
@@ -473,6 +518,7 @@ __device__ __forceinline__ void mma_issuer(const Ctx& c) {
     const uint32_t tmem_base = c.tmem_base;
     const uint32_t idesc_base = umma_idesc_bf16(128, gm.bn);
     long it = 0;  // stages consumed
+    uint32_t sf_slot = 0;  // MXFP8: scale slot of the next base stage
     bool ok = true;
     for (int lt = 0; ok; ++lt) {
         const int ts = lt % kTileRing;
@@ -488,7 +534,7 @@ __device__ __forceinline__ void mma_issuer(const Ctx& c) {
             break;
         }
         tc_fence_after();
-        const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kAccCols);
+        const uint32_t d = tmem_base + static_cast<uint32_t>(acc * (kMx ? kMxAccCols : kAccCols));
         // a down tile whose slab runs past H multiplies only the
         // valid weight rows (rounded up to the MMA's N granule of 16)
         const int dn_valid = p.side[1].n_out - tc.cb * gm.bn;
@@ -525,7 +571,10 @@ __device__ __forceinline__ void mma_issuer(const Ctx& c) {
             umma_commit(&tfull[acc]);
             continue;
         }
-        for (int kb = 0; kb < nk; ++kb, ++it) {
+        const int nk_base = kMx ? p.side[tc.side].nkc : nk;
+        // MXFP8: N of the block-scaled MMA (the trimmed last down slab as above)
+        const int n_mx = (tc.kind == kDown && dn_valid < gm.bn) ? (dn_valid + 15) / 16 * 16 : gm.bn;
+        for (int kb = 0; kb < nk_base; ++kb, ++it) {
             const int s = static_cast<int>(it % nst);
             if (!mbar_wait(&full[s], static_cast<uint32_t>(it / nst) & 1u, abort_flag, p.status, lim)) {
                 ok = false;
@@ -535,9 +584,27 @@ __device__ __forceinline__ void mma_issuer(const Ctx& c) {
             const uint32_t a_addr = smem_u32(smem + s * stb);
             const uint64_t ad = umma_desc_sw128(a_addr);
             const uint64_t bd = umma_desc_sw128(a_addr + ab);
+            if (kMx) {
+                // the stage's scale atoms into tensor memory (ordered before
+                // the MMAs that read them, and after the earlier MMAs that
+                // read the same slot), then four K = 32 block-scaled MMAs,
+                // each taking its byte of every scale word
+                const uint32_t sf_smem = a_addr + ab + kMxBBytes;
+                const uint32_t sfa = tmem_base + kMxSfCol0 + 64 * (sf_slot & 1u);
+                const uint32_t sfb = sfa + 32;
+                ++sf_slot;
+                tmem_cp_32x128b_x4(sfa, smem_desc_plain(sf_smem, 128, 128));
+                tmem_cp_32x128b_x4(sfb, smem_desc_plain(sf_smem + kMxAtom, 128, 128));
+                tmem_cp_32x128b_x4(sfb + 4, smem_desc_plain(sf_smem + 2 * kMxAtom, 128, 128));
 #pragma unroll
-            for (int k = 0; k < kBlockK / 16; ++k)
-                umma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+                for (int k = 0; k < kMxChunk / 32; ++k)
+                    umma_mx(d, ad + 2 * k, bd + 2 * k, umma_idesc_mx(128, n_mx, k), sfa, sfb,
+                            (kb | k) != 0 ? 1u : 0u);
+            } else {
+#pragma unroll
+                for (int k = 0; k < kBlockK / 16; ++k)
+                    umma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+            }
             umma_commit(&empty[s]);
         }
         if (!ok) break;
@@ -567,6 +634,7 @@ __device__ __forceinline__ void mma_issuer(const Ctx& c) {
 
 // Epilogue (warps 2-5): drains the TMEM accumulators, writes shrink tiles,
 // act rows or slot rows and publishes the per-block counters.
+template <bool kMx>
 __device__ __forceinline__ void epilogue(const Ctx& c) {
     const GemmParams& p = *c.p;
     uint64_t* const tfull = c.L.tfull;
@@ -600,7 +668,7 @@ __device__ __forceinline__ void epilogue(const Ctx& c) {
         const int acc = lt & 1;
         if (!mbar_wait(&tfull[acc], static_cast<uint32_t>(lt >> 1) & 1u, abort_flag, p.status, lim)) break;
         tc_fence_after();
-        const uint32_t tb = tmem_base + static_cast<uint32_t>(acc * kAccCols) +
+        const uint32_t tb = tmem_base + static_cast<uint32_t>(acc * (kMx ? kMxAccCols : kAccCols)) +
                             (static_cast<uint32_t>(q * 32) << 16);
         const int prow = tc.b * kBlockM + row;
         int32_t* publish = nullptr;  // counter to bump once all 128 threads wrote
@@ -645,17 +713,42 @@ __device__ __forceinline__ void epilogue(const Ctx& c) {
                 tmem_ld32(tb + c, g);
                 tmem_ld32(tb + gm.half + c, u);
                 if (real) {
+                    // the SwiGLU output in place of g
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        const int col = j0 + c + 8 * v;
-                        if (col < sd.n_out) {
-                            uint4 o;
-                            o.x = pack_bf16x2(silu(g[8 * v + 0]) * u[8 * v + 0], silu(g[8 * v + 1]) * u[8 * v + 1]);
-                            o.y = pack_bf16x2(silu(g[8 * v + 2]) * u[8 * v + 2], silu(g[8 * v + 3]) * u[8 * v + 3]);
-                            o.z = pack_bf16x2(silu(g[8 * v + 4]) * u[8 * v + 4], silu(g[8 * v + 5]) * u[8 * v + 5]);
-                            o.w = pack_bf16x2(silu(g[8 * v + 6]) * u[8 * v + 6], silu(g[8 * v + 7]) * u[8 * v + 7]);
-                            *reinterpret_cast<uint4*>(act + col) = o;
+                    for (int i = 0; i < 32; ++i) g[i] = silu(g[i]) * u[i];
+                    // bf16 rows: the down GEMM's A (bf16 layer) or the down
+                    // shrink's (adapters)
+                    if (!kMx || p.has_lora) {
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            const int col = j0 + c + 8 * v;
+                            if (col < sd.n_out) {
+                                uint4 o;
+                                o.x = pack_bf16x2(g[8 * v + 0], g[8 * v + 1]);
+                                o.y = pack_bf16x2(g[8 * v + 2], g[8 * v + 3]);
+                                o.z = pack_bf16x2(g[8 * v + 4], g[8 * v + 5]);
+                                o.w = pack_bf16x2(g[8 * v + 6], g[8 * v + 7]);
+                                *reinterpret_cast<uint4*>(act + col) = o;
+                            }
                         }
+                    }
+                    if (kMx) {
+                        // MXFP8 rows for the down GEMM: one block of 32 (I is a
+                        // multiple of 32), its codes and its scale byte
+                        uint4 q0, q1;
+                        const uint8_t sc = mx_quantize32(g, q0, q1);
+                        const int col = j0 + c;
+                        uint4* dq = reinterpret_cast<uint4*>(sd.out_q + static_cast<size_t>(prow) * sd.n_out + col);
+                        dq[0] = q0;
+                        dq[1] = q1;
+                        uint8_t* atoms = sd.out_s + static_cast<size_t>(tc.b) * p.side[1].nkc * kMxAtom;
+                        atoms[(col / kMxChunk) * kMxAtom + mx_atom_byte(row, (col % kMxChunk) / kMxBlock)] = sc;
+                        // after the last block of I: the rest of its K-chunk
+                        // reads as zero data, with a zero scale byte rather
+                        // than a stale NaN one
+                        if (col + kMxBlock == sd.n_out)
+                            for (int kb = (col % kMxChunk) / kMxBlock + 1; kb < kMxChunk / kMxBlock; ++kb)
+                                atoms[(col / kMxChunk) * kMxAtom + mx_atom_byte(row, kb)] = 0;
                     }
                 }
             }
@@ -702,6 +795,7 @@ __device__ __forceinline__ void epilogue(const Ctx& c) {
     }
 }
 
+template <bool kMx>
 __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_constant__ GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -736,9 +830,18 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
         *abort_flag = 0;
         fence_barrier_init();
         for (int sd = 0; sd < 2; ++sd) {
-            prefetch_tensormap(&p.side[sd].tm_a);
-            prefetch_tensormap(&p.side[sd].tm_a_full);
-            for (int wc = 0; wc < kTileWidths; ++wc) prefetch_tensormap(&p.side[sd].tm_b[wc]);
+            // (the MXFP8 layer has bf16 token rows only for the adapters)
+            if (!kMx || p.has_lora) {
+                prefetch_tensormap(&p.side[sd].tm_a);
+                prefetch_tensormap(&p.side[sd].tm_a_full);
+            }
+            if (!kMx)
+                for (int wc = 0; wc < kTileWidths; ++wc) prefetch_tensormap(&p.side[sd].tm_b[wc]);
+            if (kMx) {
+                prefetch_tensormap(&p.side[sd].tm_aq);
+                prefetch_tensormap(&p.side[sd].tm_aq_full);
+                prefetch_tensormap(&p.side[sd].tm_bq);
+            }
             if (p.has_lora) {
                 prefetch_tensormap(&p.side[sd].tm_sa);
                 for (int wc = 0; wc < kTileWidths; ++wc) prefetch_tensormap(&p.side[sd].tm_lb[wc]);
@@ -768,22 +871,25 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
     // the ring holds 6 stages instead of 4.  Only the two ring roles are
     // compiled per geometry; the epilogue exists once.
     const bool small_a = *p.max_rows <= kRowBox;
+    constexpr int nst_s = kMx ? kMxSmallStages : kSmallStages, nst_f = kMx ? kMxStages : kStages;
+    constexpr uint32_t stb_s = kMx ? kMxSmallStageBytes : kSmallStageBytes;
+    constexpr uint32_t stb_f = kMx ? kMxStageBytes : kStageBytes;
     if (warp == 0) {
         if ((threadIdx.x & 31) == 0) {
             if (small_a)
-                producer<kSmallStages, kSmallStageBytes, kSmallATileBytes>(c, first_tile);
+                producer<nst_s, stb_s, kSmallATileBytes, kMx>(c, first_tile);
             else
-                producer<kStages, kStageBytes, kATileBytes>(c, first_tile);
+                producer<nst_f, stb_f, kATileBytes, kMx>(c, first_tile);
         }
     } else if (warp == 1) {
         if ((threadIdx.x & 31) == 0) {
             if (small_a)
-                mma_issuer<kSmallStages, kSmallStageBytes, kSmallATileBytes>(c);
+                mma_issuer<nst_s, stb_s, kSmallATileBytes, kMx>(c);
             else
-                mma_issuer<kStages, kStageBytes, kATileBytes>(c);
+                mma_issuer<nst_f, stb_f, kATileBytes, kMx>(c);
         }
     } else {
-        epilogue(c);
+        epilogue<kMx>(c);
     }
 
     __syncthreads();
@@ -797,19 +903,23 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
 
 cudaError_t launch_experts(const GemmParams& p, long max_tiles, cudaStream_t s) {
     if (max_tiles <= 0) return cudaSuccess;
-    static std::atomic<unsigned long long> attr_done{0};  // one bit per device (shared by host threads)
+    static std::atomic<unsigned long long> attr_done[2];  // one bit per device (shared by host threads)
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
-    if (!(attr_done.load(std::memory_order_relaxed) & bit) || !bit) {
-        err = cudaFuncSetAttribute(experts_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    const int v = p.mx ? 1 : 0;
+    if (!(attr_done[v].load(std::memory_order_relaxed) & bit) || !bit) {
+        err = cudaFuncSetAttribute(p.mx ? experts_kernel<true> : experts_kernel<false>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (err != cudaSuccess) return err;
-        attr_done.fetch_or(bit, std::memory_order_relaxed);
+        attr_done[v].fetch_or(bit, std::memory_order_relaxed);
     }
     long grid = device_sm_count();
     if (grid > max_tiles) grid = max_tiles;
-    return launch_pdl(experts_kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads), kSmemBytes, s, p);
+    if (p.mx)
+        return launch_pdl(experts_kernel<true>, dim3(static_cast<unsigned>(grid)), dim3(kThreads), kSmemBytes, s, p);
+    return launch_pdl(experts_kernel<false>, dim3(static_cast<unsigned>(grid)), dim3(kThreads), kSmemBytes, s, p);
 }
 
 }  // namespace mlora

@@ -60,6 +60,10 @@ struct Workspace {
     void* lora_t13;        // [max_lt * 128, 64] bf16: s * x A13^T, one masked LoRA tile per (block, adapter)
     void* lora_t2;         // [max_lt * 128, 64] bf16: s * act A2^T, the same for the down projection
     void* y_slot;          // [M*K', H] fp32: each slot's expert output
+    uint8_t* x_q;          // MXFP8 layer: [max_padded, H] E4M3 x rows in sorted order
+    uint8_t* x_s;          // [max_blocks][ceil(H/128)][512] their scale atoms
+    uint8_t* act_q;        // [max_padded, I] E4M3 SwiGLU rows
+    uint8_t* act_s;        // [max_blocks][ceil(I/128)][512] their scale atoms
     size_t bytes;
 };
 
@@ -72,9 +76,11 @@ struct Sizes {
     int cap;          // adapters per block list: min(L, kBlockM)
     int gsize;        // adapters per shrink group tile: 256 / rank rounded up to 16
     long max_lt;
+    bool mx;          // MXFP8 expert weights
+    int nkc0, nkc1;   // K-chunks of 128 of H and of I (MXFP8)
 };
 
-Sizes make_sizes(int M, int H, int I, int E_tot, int K_total, int L, int rank);
+Sizes make_sizes(int M, int H, int I, int E_tot, int K_total, int L, int rank, bool mx = false);
 Workspace carve_workspace(const Sizes& z, void* base);  // base == nullptr: sizing only
 
 long align_max_padded(long S, int E_tot, int block_m);
@@ -143,6 +149,18 @@ struct alignas(128) GemmSide {
     CUtensorMap tm_lb[kTileWidths];
     CUtensorMap tm_t;       // this side's LoRA tiles [tiles*128, 64], box {64, kRowBox}
     CUtensorMap tm_t_full;  // box {64, 128}
+    // MXFP8 layer only: E4M3 token rows (x codes / act codes [rows, K]),
+    // box {128, kRowBox} and {128, 128}; E4M3 weight rows (w13 codes view
+    // {H, I, 2, E_tot}, box {128, 96, 1, 1} / w2 codes {I, H, E_tot}, box
+    // {128, 192, 1})
+    CUtensorMap tm_aq;
+    CUtensorMap tm_aq_full;
+    CUtensorMap tm_bq;
+    const uint8_t* a_scales;  // token-row scale atoms [max_blocks][nkc][512]
+    const uint8_t* b_scales;  // packed weight scales [E_tot][slabs][nkc][1024]
+    uint8_t* out_q;           // gate_up side: act codes [rows, I]
+    uint8_t* out_s;           // gate_up side: act scale atoms [max_blocks][ceil(I/128)][512]
+    int nkc;                  // K-chunks of 128 (MXFP8)
     void* lora_t;           // LoRA tiles: written by the shrink tiles, read by the expand stages
     int32_t* done;          // per block: finished shrink tiles (zero at launch)
     void* out;              // act [rows, I] bf16 / y_slot [M*K', H] fp32
@@ -178,6 +196,7 @@ struct alignas(128) GemmParams {
     int rank;
     int S;              // sentinel slot value M*K'
     int has_lora;
+    int mx;             // MXFP8 expert weights (fixed 192-row tiles)
     float scaling;
 };
 
@@ -185,6 +204,15 @@ struct alignas(128) GemmParams {
 // tiles, gate_up tiles (+ expand, SwiGLU), down shrink tiles, down tiles
 // (+ expand); see gemm.cu.
 cudaError_t launch_experts(const GemmParams& p, long max_tiles, cudaStream_t s);
+
+// MXFP8 (mxfp8.cu): weights to E4M3 codes and packed scales; the row gather
+// of the MXFP8 layer (x rows quantized into sorted order, plus the bf16 rows
+// the adapters' shrink reads when x_perm is set).
+cudaError_t launch_mx_quantize_weights(const void* w, long rows, int K, int which, int H, int I, uint8_t* codes,
+                                       uint8_t* packed_scales, cudaStream_t s);
+cudaError_t launch_mx_gather(const void* x, int H, int K_total, const int32_t* sorted, const int32_t* n_pad,
+                             long S, long max_padded, uint8_t* x_q, uint8_t* x_s, void* x_perm, uint32_t* status,
+                             cudaStream_t s);
 
 int device_sm_count();
 

@@ -1,0 +1,76 @@
+// mx.cuh -- MXFP8 (OCP Microscaling Formats v1.0: blocks of 32 elements
+// along the reduction dimension, one E8M0 scale 2^(s-127) per block, FP8
+// E4M3 elements) for the layer's MXFP8 expert path, and the layout of the
+// scale factors the tensor cores read.
+//
+// Conversion of a block, as the specification defines it: shared exponent
+// = floor(log2(max |v|)) - 8 (8: the exponent of E4M3's largest normal,
+// 448), clamped to >= -127 (a block of zeros or subnormals gets -127);
+// element = v / 2^shared rounded to the nearest E4M3 value (ties to even)
+// and saturated to +-448 -- one cvt.rn.satfinite.e4m3x2.f32 per pair.
+#pragma once
+#include <stdint.h>
+
+namespace mlora {
+
+constexpr int kMxBlock = 32;       // elements per scale
+constexpr int kMxChunk = 128;      // K per pipeline stage: one 128-byte swizzle row of E4M3
+constexpr int kMxAtom = 512;       // scale bytes of 128 rows x one K-chunk (4 blocks)
+constexpr int kMxWidth = 192;      // weight rows per MXFP8 tile (gate_up: 96 gate + 96 up)
+constexpr int kMxHalf = kMxWidth / 2;
+constexpr int kMxTileScaleBytes = 2 * kMxAtom;  // a tile's weight scales per K-chunk (rows 0-127, 128-191)
+
+// Byte of row r (0..127) and K-block kb (0..3) inside a 512-byte atom.  The
+// atom is 32 rows of 16 bytes: row r % 32 holds rows r, r+32, r+64, r+96,
+// four bytes (one per K-block) each.  tcgen05.cp 32x128b.warpx4 puts it in
+// tensor memory where the block-scaled MMA reads it: A row m at lane m,
+// column m / 32; B row n at lane n % 32 (every lane quarter), column n / 32.
+__host__ __device__ constexpr int mx_atom_byte(int r, int kb) { return (r % 32) * 16 + (r / 32) * 4 + kb; }
+
+// Packed weight scales.  gate_up: for each expert e, tile slab cb of
+// kMxHalf gate and kMxHalf up rows, K-chunk kc of H: kMxTileScaleBytes;
+// tile row n < 96 is gate row cb*96 + n, n >= 96 up row I + cb*96 + n - 96.
+// down: for each expert, slab cb of kMxWidth rows of w2, K-chunk kc of I.
+__host__ __device__ constexpr long mx_slabs(int which, int H, int I) {
+    return which == 0 ? (I + kMxHalf - 1) / kMxHalf : (H + kMxWidth - 1) / kMxWidth;
+}
+__host__ __device__ constexpr long mx_chunks(int which, int H, int I) {
+    return which == 0 ? (H + kMxChunk - 1) / kMxChunk : (I + kMxChunk - 1) / kMxChunk;
+}
+
+#ifdef __CUDACC__
+// Shared exponent of a block whose largest magnitude is amax (>= 0).
+__device__ __forceinline__ int mx_shared_exp(float amax) {
+    const int field = (__float_as_int(amax) >> 23) & 0xff;
+    return field == 0 ? -127 : max(-127, field - 127 - 8);
+}
+
+// 2^-se exactly, for se in [-127, 119] (every finite fp32 block).
+__device__ __forceinline__ float mx_inv_scale(int se) { return __int_as_float((127 - se) << 23); }
+
+// Four values to four E4M3 codes, byte i = code of the i-th value.
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
+    uint32_t lo, hi;
+    asm("{.reg .b16 t;\n\tcvt.rn.satfinite.e4m3x2.f32 t, %2, %1;\n\tcvt.u32.u16 %0, t;}" : "=r"(lo) : "f"(a), "f"(b));
+    asm("{.reg .b16 t;\n\tcvt.rn.satfinite.e4m3x2.f32 t, %2, %1;\n\tcvt.u32.u16 %0, t;}" : "=r"(hi) : "f"(c), "f"(d));
+    return lo | (hi << 16);
+}
+
+// One block of 32 values (already in registers) to 32 codes (two uint4,
+// bytes in element order) and its scale byte.
+__device__ __forceinline__ uint8_t mx_quantize32(const float (&v)[32], uint4& q0, uint4& q1) {
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    const int se = mx_shared_exp(amax);
+    const float inv = mx_inv_scale(se);
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i] = e4m3x4(v[4 * i] * inv, v[4 * i + 1] * inv, v[4 * i + 2] * inv, v[4 * i + 3] * inv);
+    q0 = make_uint4(w[0], w[1], w[2], w[3]);
+    q1 = make_uint4(w[4], w[5], w[6], w[7]);
+    return static_cast<uint8_t>(se + 127);
+}
+#endif
+
+}  // namespace mlora

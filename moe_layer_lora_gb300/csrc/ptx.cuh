@@ -95,6 +95,16 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, u
         : "memory");
 }
 
+// Untiled bulk copy of `bytes` (a multiple of 16; both addresses 16-byte
+// aligned) from global to shared memory, completing on `bar`.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -128,6 +138,51 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint6
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+
+// Shared-memory descriptor of an unswizzled operand: core matrices of 8
+// rows x 16 bytes, `lbo` / `sbo` bytes apart along K / along the rows.
+__device__ __forceinline__ uint64_t smem_desc_plain(uint32_t smem_addr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((smem_addr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1u) << 46;  // descriptor version (tcgen05); layout: no swizzle
+    return d;
+}
+
+// Instruction descriptor, kind::mxf8f6f4 with block scaling: E4M3 A and B
+// (format code 0, K-major), E8M0 scales (bit 23), one scale per 32 of K;
+// the scale byte used by the instruction's K-block is picked by the A / B
+// scale-factor ids (bits 29-30 / 4-5).
+__host__ __device__ constexpr uint32_t umma_idesc_mx(int M, int N, int sf_id) {
+    return (static_cast<uint32_t>(sf_id) << 4)         // B scale-factor id
+           | (1u << 23)                                  // scale format: E8M0
+           | (static_cast<uint32_t>(N >> 3) << 17)       // N / 8
+           | (static_cast<uint32_t>(M >> 4) << 24)       // M / 16
+           | (static_cast<uint32_t>(sf_id) << 29);       // A scale-factor id
+}
+
+// D (+)= (A * 2^sfA) (B * 2^sfB)^T over K = 32, A and B E4M3 in shared
+// memory, scales in tensor memory: A row m at lane m, column sfa + m/32;
+// B row n at lane n % 32 of every lane quarter, column sfb + n/32; byte =
+// the instruction's scale-factor id.
+__device__ __forceinline__ void umma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                        uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate));
+}
+
+// 32 rows x 16 bytes of shared memory (an unswizzled descriptor) into 32
+// lanes x 4 columns of tensor memory, repeated in all four lane quarters:
+// row r lands in lanes r, 32 + r, 64 + r, 96 + r.  Ordered with the MMAs the
+// same thread issues.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {

@@ -111,3 +111,23 @@ def test_workspace_size(lib):
     assert base % 256 == 0 and with_lora % 256 == 0
     assert ml.mlora_moe_workspace_size(64, 2881, 2880, 32, 4, 0, 0) == 0
     assert ml.mlora_moe_workspace_size(8192, 2880, 2880, 32, 4, 8, 32) < 2 << 30
+
+
+def test_mxfp8_sizes(lib):
+    """MXFP8 needs H and I multiples of 32; sizes of the packed scales."""
+    assert lib.mlora_mxfp8_scales_size(4, 72, 64, 0) == 0         # H not a multiple of 32
+    assert lib.mlora_mxfp8_scales_size(4, 64, 64, 2) == 0         # which is 0 or 1
+    assert lib.mlora_moe_workspace_size_mxfp8(4, 64, 40, 4, 2, 0, 0) == 0
+    # gate_up: 32 experts x ceil(2880/96) slabs x ceil(2880/128) chunks x 1024 bytes
+    assert lib.mlora_mxfp8_scales_size(32, 2880, 2880, 0) == 32 * 30 * 23 * 1024
+    assert lib.mlora_mxfp8_scales_size(32, 2880, 2880, 1) == 32 * 15 * 23 * 1024
+    assert ml.mlora_moe_workspace_size_mxfp8(64, 2880, 2880, 32, 4, 8, 16) > 0
+
+
+def test_mxfp8_forward_validation(lib):
+    P = ctypes.c_void_p(4096)
+    f = lib.mlora_moe_forward_mxfp8
+    args = [P] * 5 + [None] * 5 + [P, P]
+    assert f(*args, 4, 72, 64, 4, 2, 0, 0, 1.0, 0, 1.0, P, ctypes.c_void_p(1 << 20), 1 << 30, None) == 2
+    null_scales = [P, P, None, P, None] + [None] * 5 + [P, P]
+    assert f(*null_scales, 4, 64, 64, 4, 2, 0, 0, 1.0, 0, 1.0, P, ctypes.c_void_p(1 << 20), 1 << 30, None) == 1

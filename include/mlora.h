@@ -303,6 +303,34 @@ mlora_status mlora_set_stage_events(void* const* events, int count);
  */
 mlora_status mlora_set_wait_test(long long wait_limit_cycles, int stall);
 
+/*
+ * Tile configuration of the experts kernel ("Amazon SageMaker 및 Amazon
+ * Bedrock에서 vLLM을 활용한 MoE 모델 Multi-LoRA 서빙 최적화", section "섹션별
+ * 상세" paragraph 4: block and split parameters found per deployment and
+ * loaded automatically).  Each bf16 forward picks, for the number of
+ * 128-slot blocks it finds on the device, a tile width of 256, 192 or 128
+ * weight rows (width class 0, 1, 2), and a shrink group size (adapters per
+ * shrink tile, 1-4): from the library's tuned table for the layer's shape
+ * (H, I, E_tot, K', rank) when it has a row for it, else from the wave rule
+ * (fill the grid's SMs with each projection's tiles) and at most 4
+ * adapters (256 stacked rank rows) a group.  The table is written by the
+ * offline tuner (python -m moe_layer_lora_gb300.autotune) and compiled in.
+ * Neither choice changes any output bit: every output element sums the same
+ * products in the same order.
+ *
+ * mlora_set_tile_config: for the calling host thread, force the width class
+ * (-1: table or rule) and the shrink group size (0: table or rule; clamped to
+ * what the rank allows) of later forwards -- the tuner's hook.  MXFP8
+ * layers keep their 192-row width.  MLORA_ERR_INVALID_ARG out of range.
+ *
+ * mlora_tile_config: the width class and group size a bf16 layer of this
+ * shape would use for `nblocks` blocks on a grid of `grid` CTAs (one per
+ * SM), and whether a tuned row applied (*tuned, may be NULL).  Host only.
+ */
+mlora_status mlora_set_tile_config(int width_class, int gsize);
+mlora_status mlora_tile_config(int H, int I, int E_tot, int K_total, int rank, int nblocks, int grid,
+                               int* width_class, int* gsize, int* tuned);
+
 /* Static, human-readable name of a status code. */
 const char* mlora_status_string(mlora_status status);
 

@@ -29,6 +29,8 @@ from ._lib import (  # noqa: F401
     mlora_mxfp8_quantize_weights,
     mlora_mxfp8_scales_size,
     mlora_set_stage_events,
+    mlora_set_tile_config,
+    mlora_tile_config,
     mlora_set_wait_test,
     mlora_status_string,
     STAGE_EVENTS,

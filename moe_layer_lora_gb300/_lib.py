@@ -89,6 +89,11 @@ def load(path: str = LIB_PATH):
     lib.mlora_moe_workspace_size_mxfp8.restype = sz
     lib.mlora_moe_forward_mxfp8.argtypes = [P] * 12 + [i] * 7 + [f, i, f, P, P, sz, P]
     lib.mlora_moe_forward_mxfp8.restype = i
+    lib.mlora_set_tile_config.argtypes = [i, i]
+    lib.mlora_set_tile_config.restype = i
+    ip = ctypes.POINTER(ctypes.c_int)
+    lib.mlora_tile_config.argtypes = [i] * 7 + [ip, ip, ip]
+    lib.mlora_tile_config.restype = i
     _lib = lib
     return lib
 
@@ -392,6 +397,22 @@ def mlora_set_wait_test(wait_limit_cycles: int, stall: bool) -> None:
     kernel's waits and, with stall, a first wait on a flag nothing sets.
     (0, False) restores the defaults."""
     _check("mlora_set_wait_test", load().mlora_set_wait_test(int(wait_limit_cycles), 1 if stall else 0))
+
+
+def mlora_set_tile_config(width_class: int = -1, gsize: int = 0) -> None:
+    """Force, for this thread's later forwards, the experts kernel's tile
+    width class (0: 256, 1: 192, 2: 128 weight rows; -1: tuned table or
+    rule) and shrink group size (0: table or rule) -- the tuner's hook."""
+    _check("mlora_set_tile_config", load().mlora_set_tile_config(int(width_class), int(gsize)))
+
+
+def mlora_tile_config(H: int, I: int, E_tot: int, K_total: int, rank: int, nblocks: int, grid: int):
+    """(width class, shrink group size, tuned) a bf16 layer of this shape
+    uses for nblocks blocks on a grid of `grid` CTAs."""
+    wc, g, t = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+    _check("mlora_tile_config", load().mlora_tile_config(H, I, E_tot, K_total, rank, nblocks, grid,
+                                                         ctypes.byref(wc), ctypes.byref(g), ctypes.byref(t)))
+    return wc.value, g.value, bool(t.value)
 
 
 def mlora_status_string(status: int) -> str:

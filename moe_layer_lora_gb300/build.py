@@ -49,7 +49,8 @@ def build(verbose: bool = False, extra_flags=(), checked: bool = False) -> str:
         extra_flags = (*extra_flags, "-DMLORA_CHECK_BOUNDS")
     os.makedirs(build_dir, exist_ok=True)
     sources = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
-    headers = glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h"))
+    headers = (glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.inc")) +
+               glob.glob(os.path.join(INCLUDE, "*.h")))
     objs = []
     jobs = []
     for src in sources:

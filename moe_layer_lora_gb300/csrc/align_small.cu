@@ -27,6 +27,7 @@
 #include <atomic>
 
 #include "internal.cuh"
+#include "mx.cuh"
 #include "ptx.cuh"
 
 namespace mlora {
@@ -74,7 +75,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     align_small_kernel(const int32_t* __restrict__ ids, int S, int E_tot, int BM, int max_padded,
                        int32_t* __restrict__ sorted, int32_t* __restrict__ expert_ids,
                        int32_t* __restrict__ n_pad_out, uint32_t* __restrict__ status, AlignExtra ex,
-                       const uint4* __restrict__ x, int H8, int K_total, uint4* __restrict__ x_perm) {
+                       const uint4* __restrict__ x, int H8, int K_total, uint4* __restrict__ x_perm,
+                       uint8_t* __restrict__ x_q, uint8_t* __restrict__ x_s) {
     extern __shared__ int smem_i[];
     int* wcnt = smem_i;                  // [kWarps][E_tot] a warp's slots per expert, then its first offset
     int* tot = wcnt + kWarps * E_tot;    // [E_tot] slots per expert
@@ -220,8 +222,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
 
     // 4. this CTA's x rows into their sorted positions: one warp per row,
-    //    four 16-byte loads in flight per lane
-    if (kGather) {
+    //    four 16-byte loads in flight per lane (MXFP8 layer: the rows
+    //    quantized, and copied in bf16 only when adapters read them)
+    if (kGather && x_q) {
+        const int n = scratch[50];
+        const int nchunk = (8 * H8 + kMxChunk - 1) / kMxChunk;
+        for (int i = warp; i < n; i += kWarps) {
+            const int pos = glist[2 * i];
+            mx_gather_row(x + static_cast<size_t>(glist[2 * i + 1]) * H8, 8 * H8, pos % kBlockM,
+                          x_q + static_cast<size_t>(pos) * 8 * H8,
+                          x_s + static_cast<size_t>(pos / kBlockM) * nchunk * kMxAtom,
+                          x_perm ? x_perm + static_cast<size_t>(pos) * H8 : nullptr, lane);
+        }
+    } else if (kGather) {
         const int n = scratch[50];
         for (int i = warp; i < n; i += kWarps) {
             const int pos = glist[2 * i];
@@ -311,7 +324,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <bool kWithLora, bool kGather>
 cudaError_t launch_variant(int variant, const cudaLaunchConfig_t& cfg, const int32_t* ids, int S, int E_tot, int BM,
                            int max_padded, int32_t* sorted, int32_t* expert_ids, int32_t* n_pad, uint32_t* status,
-                           const AlignExtra& ex, const uint4* x, int H8, int K_total, uint4* x_perm) {
+                           const AlignExtra& ex, const uint4* x, int H8, int K_total, uint4* x_perm,
+                           uint8_t* x_q, uint8_t* x_s) {
     static std::atomic<unsigned long long> attr_set[4];  // one bit per device (shared by host threads)
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
@@ -324,7 +338,7 @@ cudaError_t launch_variant(int variant, const cudaLaunchConfig_t& cfg, const int
         attr_set[variant].fetch_or(bit, std::memory_order_relaxed);
     }
     return cudaLaunchKernelEx(&cfg, align_small_kernel<kWithLora, kGather>, ids, S, E_tot, BM, max_padded, sorted,
-                              expert_ids, n_pad, status, ex, x, H8, K_total, x_perm);
+                              expert_ids, n_pad, status, ex, x, H8, K_total, x_perm, x_q, x_s);
 }
 
 }  // namespace
@@ -356,6 +370,8 @@ cudaError_t launch_align_small(const int32_t* ids, long S, int E_tot, int block_
     uint4* x_perm = g ? static_cast<uint4*>(gather->x_perm) : nullptr;
     const int H8 = g ? gather->H / 8 : 0;
     const int K_total = g ? gather->K_total : 1;
+    uint8_t* x_q = g ? gather->x_q : nullptr;
+    uint8_t* x_s = g ? gather->x_s : nullptr;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreads);
@@ -370,14 +386,14 @@ cudaError_t launch_align_small(const int32_t* ids, long S, int E_tot, int block_
     cudaError_t err;
     if (with_lora)
         err = g ? launch_variant<true, true>(3, cfg, ids, Si, E_tot, block_m, mpi, sorted, expert_ids, n_pad, status,
-                                             ex, x, H8, K_total, x_perm)
+                                             ex, x, H8, K_total, x_perm, x_q, x_s)
                 : launch_variant<true, false>(2, cfg, ids, Si, E_tot, block_m, mpi, sorted, expert_ids, n_pad,
-                                              status, ex, x, H8, K_total, x_perm);
+                                              status, ex, x, H8, K_total, x_perm, x_q, x_s);
     else
         err = g ? launch_variant<false, true>(1, cfg, ids, Si, E_tot, block_m, mpi, sorted, expert_ids, n_pad,
-                                              status, ex, x, H8, K_total, x_perm)
+                                              status, ex, x, H8, K_total, x_perm, x_q, x_s)
                 : launch_variant<false, false>(0, cfg, ids, Si, E_tot, block_m, mpi, sorted, expert_ids, n_pad,
-                                               status, ex, x, H8, K_total, x_perm);
+                                               status, ex, x, H8, K_total, x_perm, x_q, x_s);
     if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }

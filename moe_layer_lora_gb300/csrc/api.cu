@@ -74,6 +74,22 @@ size_t round256(size_t b) { return (b + 255) & ~size_t(255); }
 
 mlora_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MLORA_OK : MLORA_ERR_CUDA; }
 
+// Tuned tile widths and shrink group sizes per layer shape (tuned_tiles.inc,
+// written by the offline tuner); the last row (H = 0) ends the table.
+struct TunedShape {
+    int H, I, E_tot, K_total, rank;
+    int8_t wc[kWidthBuckets];
+    int gsize;
+};
+const TunedShape kTunedShapes[] = {
+#include "tuned_tiles.inc"
+    {0, 0, 0, 0, 0, {0}, 0},
+};
+
+// tile override for the tuner (mlora_set_tile_config), per host thread
+thread_local int g_force_wc = -1;
+thread_local int g_force_gsize = 0;
+
 thread_local cudaEvent_t g_stage_events[MLORA_STAGE_EVENTS];
 thread_local bool g_stage_events_on = false;
 // wait-limit test hook (mlora_set_wait_test)
@@ -127,6 +143,31 @@ bool foreign_device_memory(cudaStream_t s, std::initializer_list<const void*> pt
         if (a.type == cudaMemoryTypeDevice && a.device != dev) return true;
     }
     return false;
+}
+
+// The tile width table (per block-count bucket; -1 = the wave rule) and the
+// shrink group size a layer of this shape uses: the thread's override if
+// set, else the tuned row of this shape, else the rules.  MXFP8 layers keep
+// their fixed width.  Returns whether a tuned row applied.
+bool resolve_tiles(int H, int I, int E_tot, int K_total, int rank, bool mx, int8_t* table, int* gsize) {
+    for (int b = 0; b < kWidthBuckets; ++b) table[b] = -1;
+    bool tuned = false;
+    const int rp = (rank + 15) / 16 * 16;
+    const int gmax = rank > 0 ? std::min(4, (mx ? kMxWidth : 256) / rp) : 1;
+    for (const TunedShape* t = kTunedShapes; t->H; ++t) {
+        if (t->H == H && t->I == I && t->E_tot == E_tot && t->K_total == K_total && t->rank == rank) {
+            tuned = true;
+            if (!mx)
+                for (int b = 0; b < kWidthBuckets; ++b)
+                    table[b] = t->wc[b] >= 0 && t->wc[b] < kTileWidths ? t->wc[b] : -1;
+            if (t->gsize > 0) *gsize = std::min(t->gsize, gmax);
+            break;
+        }
+    }
+    if (g_force_wc >= 0 && !mx)
+        for (int b = 0; b < kWidthBuckets; ++b) table[b] = static_cast<int8_t>(g_force_wc);
+    if (g_force_gsize > 0 && rank > 0) *gsize = std::min(g_force_gsize, gmax);
+    return tuned;
 }
 
 }  // namespace
@@ -377,13 +418,16 @@ mlora_status forward_impl(const void* x, const void* w13, const void* w2, const 
                               {x, w13, w2, topk_ids, topk_w, y, workspace, lora ? A13 : nullptr,
                                lora ? token_lora_idx : nullptr, mx ? mxw->w13_s : nullptr}))
         return MLORA_ERR_INVALID_ARG;
-    const Sizes z = make_sizes(M, H, I, E_tot, K_total, L_eff, r_eff, mx);
+    Sizes z = make_sizes(M, H, I, E_tot, K_total, L_eff, r_eff, mx);
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return MLORA_ERR_WORKSPACE;
     const Workspace ws = carve_workspace(z, workspace);
     if (workspace_bytes < ws.bytes) return MLORA_ERR_WORKSPACE;
 
     // ---- tensor maps (dims innermost first) ----
     GemmParams gp{};
+    // tile widths and shrink group size: tuned table or rules (the group
+    // size does not change the workspace layout)
+    resolve_tiles(H, I, E_tot, K_total, r_eff, mx, gp.width_table, &z.gsize);
     GemmSide& up = gp.side[0];
     GemmSide& dn = gp.side[1];
     const cuuint64_t H_ = H, I_ = I, E_ = E_tot, MP = z.max_padded;
@@ -530,10 +574,10 @@ mlora_status forward_impl(const void* x, const void* w13, const void* w2, const 
         ex.gt_first = ws.gt_first;
         ex.gt_total = ws.gt_total;
     }
-    if (!mx && align_small_fits(z.S, E_tot, kBlockM, z.max_padded, &ex, true)) {
+    if (align_small_fits(z.S, E_tot, kBlockM, z.max_padded, &ex, true)) {
         // small batches: align and the row gather in one launch (stage
         // boundaries 1 and 2 coincide)
-        const GatherArgs ga{x, ws.x_perm, H, K_total};
+        const GatherArgs ga{x, ws.x_perm, H, K_total, ws.x_q, ws.x_s};
         err = launch_align_small(topk_ids, z.S, E_tot, kBlockM, z.max_padded, ws.sorted_ids, ws.expert_ids,
                                  ws.n_pad, ws.status, &ex, &ga, s);
         if (err != cudaSuccess) return cuda_fail(err, "align + gather");
@@ -597,6 +641,28 @@ mlora_status mlora_set_stage_events(void* const* events, int count) {
         g_stage_events[i] = static_cast<cudaEvent_t>(events[i]);
     }
     g_stage_events_on = true;
+    return MLORA_OK;
+}
+
+mlora_status mlora_set_tile_config(int width_class, int gsize) {
+    if (width_class < -1 || width_class >= kTileWidths || gsize < 0 || gsize > 4) return MLORA_ERR_INVALID_ARG;
+    g_force_wc = width_class;
+    g_force_gsize = gsize;
+    return MLORA_OK;
+}
+
+mlora_status mlora_tile_config(int H, int I, int E_tot, int K_total, int rank, int nblocks, int grid,
+                               int* width_class, int* gsize, int* tuned) {
+    if (!width_class || !gsize || H < 8 || I < 8 || E_tot < 1 || K_total < 1 || rank < 0 || nblocks < 1 || grid < 1)
+        return MLORA_ERR_INVALID_ARG;
+    const Sizes z = make_sizes(1, H, I, E_tot, K_total, rank > 0 ? 1 : 0, rank);
+    int8_t table[kWidthBuckets];
+    int g = z.gsize;
+    const bool t = resolve_tiles(H, I, E_tot, K_total, rank, false, table, &g);
+    const int tw = table[width_bucket(nblocks)];
+    *width_class = tw >= 0 ? tw : choose_width(nblocks, I, H, grid);
+    *gsize = g;
+    if (tuned) *tuned = t ? 1 : 0;
     return MLORA_OK;
 }
 

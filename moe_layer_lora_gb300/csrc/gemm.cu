@@ -156,31 +156,6 @@ struct Geom {
     int ncb1;    // column slabs per block, down
 };
 
-// The tile width of a launch with nblocks blocks on a grid of `grid` CTAs.
-// One SM streams weights at a rate of its own (~44 GB/s measured, about
-// the HBM rate divided by the SM count), so a phase whose tiles do not fill
-// whole waves of the grid leaves HBM idle.  With at most two waves of wide
-// gate_up tiles, the width that minimises (waves of gate_up tiles) x (bytes
-// per gate_up tile) + the same for down is taken, the wider on a tie;
-// larger batches keep wide tiles.
-__device__ __forceinline__ int choose_width(int nblocks, int I, int H, long grid) {
-    const long wide = static_cast<long>(nblocks) * ((I + 127) / 128);
-    if (wide > 2 * grid) return 0;
-    int best = 0;
-    long best_cost = -1;
-    for (int wc = 0; wc < kTileWidths; ++wc) {
-        const int n = tile_width(wc);
-        const long tg = static_cast<long>(nblocks) * ((I + n / 2 - 1) / (n / 2));
-        const long td = static_cast<long>(nblocks) * ((H + n - 1) / n);
-        const long cost = ((tg + grid - 1) / grid) * n * static_cast<long>(H) + ((td + grid - 1) / grid) * n * static_cast<long>(I);
-        if (best_cost < 0 || cost < best_cost) {
-            best = wc;
-            best_cost = cost;
-        }
-    }
-    return best;
-}
-
 // Phase boundaries of the tile sequence.
 struct Phases {
     long s1, g, s2, d;  // ends of phases 1..4
@@ -288,8 +263,12 @@ struct Ctx {
         : p(&prm), smem(sm), L(sm), tmem_base(tmem), lim(prm.wait_limit) {
         nblocks = *prm.n_pad / kBlockM;
         ns = prm.has_lora ? *prm.gt_total : 0;
-        // MXFP8 launches use 192-row tiles: the packed weight scales follow them
-        gm.wc = prm.mx ? 1 : choose_width(nblocks, prm.side[0].n_out, prm.side[1].n_out, gridDim.x);
+        // MXFP8 launches use 192-row tiles (the packed weight scales follow
+        // them); otherwise the tuned table's width for this many blocks, else
+        // the wave rule
+        const int tuned = prm.width_table[width_bucket(nblocks)];
+        gm.wc = prm.mx ? 1
+                       : tuned >= 0 ? tuned : choose_width(nblocks, prm.side[0].n_out, prm.side[1].n_out, gridDim.x);
         gm.bn = tile_width(gm.wc);
         gm.half = gm.bn / 2;
         gm.ncb0 = (prm.side[0].n_out + gm.half - 1) / gm.half;

@@ -15,6 +15,41 @@ constexpr int kBlockM = MLORA_FORWARD_BLOCK_M;  // token rows per GEMM tile (MMA
 constexpr int kBlockK = 64;                     // bf16 elements per 128-byte swizzle row
 constexpr int kTileWidths = 3;                   // weight rows per experts tile: 256, 192 or 128
 __host__ __device__ constexpr int tile_width(int wc) { return 256 - 64 * wc; }
+// Tuned tile widths are kept per power-of-two bucket of a launch's block
+// count: bucket b holds [2^b, 2^(b+1)) blocks, the last one everything above.
+constexpr int kWidthBuckets = 16;
+__host__ __device__ inline int width_bucket(int nblocks) {
+    int b = 0;
+    while (b + 1 < kWidthBuckets && (nblocks >> (b + 1)) > 0) ++b;
+    return b;
+}
+
+// The tile width of a launch with nblocks blocks (I, H the projections'
+// output widths) on a grid of `grid` CTAs when no tuned table applies.  One
+// SM streams weights at a rate of its own (~44 GB/s measured, about the HBM
+// rate divided by the SM count), so a phase whose tiles do not fill whole
+// waves of the grid leaves HBM idle.  With at most two waves of wide
+// gate_up tiles, the width that minimises (waves of gate_up tiles) x (bytes
+// per gate_up tile) + the same for down is taken, the wider on a tie;
+// larger batches keep wide tiles.
+__host__ __device__ inline int choose_width(int nblocks, int I, int H, long grid) {
+    const long wide = static_cast<long>(nblocks) * ((I + 127) / 128);
+    if (wide > 2 * grid) return 0;
+    int best = 0;
+    long best_cost = -1;
+    for (int wc = 0; wc < kTileWidths; ++wc) {
+        const int n = tile_width(wc);
+        const long tg = static_cast<long>(nblocks) * ((I + n / 2 - 1) / (n / 2));
+        const long td = static_cast<long>(nblocks) * ((H + n - 1) / n);
+        const long cost =
+            ((tg + grid - 1) / grid) * n * static_cast<long>(H) + ((td + grid - 1) / grid) * n * static_cast<long>(I);
+        if (best_cost < 0 || cost < best_cost) {
+            best = wc;
+            best_cost = cost;
+        }
+    }
+    return best;
+}
 constexpr int kLoraTileCols = 64;               // shrink result row, padded to one swizzle row
 constexpr int kRowBox = 32;                     // token rows per TMA box of an A operand
 constexpr long long kWaitCycles = 4000000000LL;  // default spin limit of a device wait (~2 s at 2 GHz)
@@ -120,9 +155,11 @@ cudaError_t launch_align(const int32_t* ids, long S, int E_tot, int block_m, lon
 constexpr long kSmallMaxSlots = 2048;
 struct GatherArgs {
     const void* x;  // [M, H] bf16
-    void* x_perm;   // [max_padded, H] bf16
+    void* x_perm;   // [max_padded, H] bf16 (may be null in the MXFP8 layer without adapters)
     int H;
     int K_total;
+    uint8_t* x_q;   // MXFP8 layer: [max_padded, H] E4M3 rows, else null
+    uint8_t* x_s;   // MXFP8 layer: [max_blocks][ceil(H/128)][512] scale atoms
 };
 bool align_small_fits(long S, int E_tot, int block_m, long max_padded, const AlignExtra* extra, bool gather);
 cudaError_t launch_align_small(const int32_t* ids, long S, int E_tot, int block_m, long max_padded, int32_t* sorted,
@@ -197,6 +234,8 @@ struct alignas(128) GemmParams {
     int S;              // sentinel slot value M*K'
     int has_lora;
     int mx;             // MXFP8 expert weights (fixed 192-row tiles)
+    // tuned tile width class per block-count bucket (-1: the rule, choose_width)
+    int8_t width_table[kWidthBuckets];
     float scaling;
 };
 

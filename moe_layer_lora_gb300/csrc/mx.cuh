@@ -10,6 +10,9 @@
 // and saturated to +-448 -- one cvt.rn.satfinite.e4m3x2.f32 per pair.
 #pragma once
 #include <stdint.h>
+#ifdef __CUDACC__
+#include <cuda_bf16.h>
+#endif
 
 namespace mlora {
 
@@ -70,6 +73,48 @@ __device__ __forceinline__ uint8_t mx_quantize32(const float (&v)[32], uint4& q0
     q0 = make_uint4(w[0], w[1], w[2], w[3]);
     q1 = make_uint4(w[4], w[5], w[6], w[7]);
     return static_cast<uint8_t>(se + 127);
+}
+
+// One routed x row into sorted position p (row r = p % 128 of its block):
+// each lane takes whole blocks of 32 of the bf16 row `src`, writes their
+// E4M3 codes to q_row and their scale bytes into the block's atoms
+// (atoms[kc * 512 + ...], kc = the K-chunk); the bf16 row is copied to
+// bf_row too when it is set.  Blocks of the last K-chunk past H get a zero
+// scale byte (their data reads as zero), never a stale one.
+__device__ __forceinline__ void mx_gather_row(const uint4* __restrict__ src, int H, int r, uint8_t* __restrict__ q_row,
+                                              uint8_t* __restrict__ atoms, uint4* __restrict__ bf_row, int lane) {
+    const int nblk = H / kMxBlock;
+    const int per_chunk = kMxChunk / kMxBlock;
+    for (int b = lane; b < nblk; b += 32) {
+        uint4 raw[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) raw[q] = __ldg(src + b * 4 + q);
+        if (bf_row) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) bf_row[b * 4 + q] = raw[q];
+        }
+        float v[32];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw[q]);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 t = __bfloat1622float2(h[i]);
+                v[8 * q + 2 * i] = t.x;
+                v[8 * q + 2 * i + 1] = t.y;
+            }
+        }
+        uint4 q0, q1;
+        const uint8_t sc = mx_quantize32(v, q0, q1);
+        uint4* dq = reinterpret_cast<uint4*>(q_row + b * kMxBlock);
+        dq[0] = q0;
+        dq[1] = q1;
+        atoms[(b / per_chunk) * kMxAtom + mx_atom_byte(r, b % per_chunk)] = sc;
+    }
+    if (lane == 0) {
+        const int nchunk = (H + kMxChunk - 1) / kMxChunk;
+        for (int b = nblk; b < nchunk * per_chunk; ++b) atoms[(b / per_chunk) * kMxAtom + mx_atom_byte(r, b % per_chunk)] = 0;
+    }
 }
 #endif
 

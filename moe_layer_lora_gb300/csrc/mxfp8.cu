@@ -92,39 +92,14 @@ __global__ void __launch_bounds__(256) mx_gather_kernel(const uint4* __restrict_
     const int lane = threadIdx.x & 31;
     const int warps = blockDim.x >> 5;
     const int np = *n_pad;
-    const int nblk = H / kMxBlock;
     const int nchunk = (H + kMxChunk - 1) / kMxChunk;
     for (int p = blockIdx.x * warps + (threadIdx.x >> 5); p < np; p += gridDim.x * warps) {
         if (!MLORA_IN_BOUNDS(p < max_padded, status)) break;
         const int f = sorted[p];
         if (f >= S) continue;  // padding row: its outputs are discarded
-        const uint4* src = x + static_cast<size_t>(f / K_total) * (H / 8);
-        const int blk = p / kBlockM, r = p % kBlockM;
-        for (int b = lane; b < nblk; b += 32) {
-            uint4 raw[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) raw[q] = __ldg(src + b * 4 + q);
-            if (x_perm) {
-                uint4* d = x_perm + static_cast<size_t>(p) * (H / 8) + b * 4;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) d[q] = raw[q];
-            }
-            float v[32];
-            bf16x32_to_f32(raw, v);
-            uint4 q0, q1;
-            const uint8_t sc = mx_quantize32(v, q0, q1);
-            uint4* dq = reinterpret_cast<uint4*>(x_q + static_cast<size_t>(p) * H + b * kMxBlock);
-            dq[0] = q0;
-            dq[1] = q1;
-            x_s[(static_cast<size_t>(blk) * nchunk + b / (kMxChunk / kMxBlock)) * kMxAtom +
-                mx_atom_byte(r, b % (kMxChunk / kMxBlock))] = sc;
-        }
-        // blocks of the last K-chunk past H: their data reads as zero (TMA
-        // fill), and their scale byte must not be a stale NaN
-        if (lane == 0)
-            for (int b = nblk; b < nchunk * (kMxChunk / kMxBlock); ++b)
-                x_s[(static_cast<size_t>(blk) * nchunk + b / (kMxChunk / kMxBlock)) * kMxAtom +
-                    mx_atom_byte(r, b % (kMxChunk / kMxBlock))] = 0;
+        mx_gather_row(x + static_cast<size_t>(f / K_total) * (H / 8), H, p % kBlockM, x_q + static_cast<size_t>(p) * H,
+                      x_s + static_cast<size_t>(p / kBlockM) * nchunk * kMxAtom,
+                      x_perm ? x_perm + static_cast<size_t>(p) * (H / 8) : nullptr, lane);
     }
 }
 

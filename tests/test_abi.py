@@ -2,6 +2,7 @@
 include/mlora.h declares, and rejects bad arguments on the host before any
 CUDA call (only calls that fail validation or are no-ops run here)."""
 import ctypes
+import os
 
 import pytest
 
@@ -131,3 +132,46 @@ def test_mxfp8_forward_validation(lib):
     assert f(*args, 4, 72, 64, 4, 2, 0, 0, 1.0, 0, 1.0, P, ctypes.c_void_p(1 << 20), 1 << 30, None) == 2
     null_scales = [P, P, None, P, None] + [None] * 5 + [P, P]
     assert f(*null_scales, 4, 64, 64, 4, 2, 0, 0, 1.0, 0, 1.0, P, ctypes.c_void_p(1 << 20), 1 << 30, None) == 1
+
+
+def test_tile_config_rule_and_hook(lib):
+    """Without a tuned row the wave rule picks the width: narrow tiles for
+    few blocks, 256 once the gate_up tiles fill two waves; the shrink group
+    holds at most 4 adapters and 256 stacked rank rows.  The tuner's hook
+    forces both and rejects values out of range."""
+    H, I, E, K = 2880, 2880, 32, 4
+    assert ml.mlora_tile_config(H, I, E, K, 16, 1, 152)[:2] == (2, 4)
+    assert ml.mlora_tile_config(H, I, E, K, 16, 64, 152)[:2] == (0, 4)
+    assert ml.mlora_tile_config(H, I, E, K, 64, 64, 152)[1] == 4
+    assert ml.mlora_tile_config(H, I, E, K, 0, 64, 152)[1] == 1
+    try:
+        ml.mlora_set_tile_config(1, 2)
+        assert ml.mlora_tile_config(H, I, E, K, 16, 64, 152)[:2] == (1, 2)
+        ml.mlora_set_tile_config(2, 4)
+        # rank 64: four adapters would stack 256 rows, within the limit
+        assert ml.mlora_tile_config(H, I, E, K, 64, 3, 152)[:2] == (2, 4)
+    finally:
+        ml.mlora_set_tile_config(-1, 0)
+    assert lib.mlora_set_tile_config(3, 0) == 1
+    assert lib.mlora_set_tile_config(-2, 0) == 1
+    assert lib.mlora_set_tile_config(0, 5) == 1
+
+
+def test_tuned_table_rows_are_valid():
+    """Every row of the compiled-in tuned table names width classes in
+    range (or -1) and a group size the rank allows; the library reports the
+    row as applied for its shape."""
+    import re
+    path = os.path.join(os.path.dirname(_lib.LIB_PATH), "csrc", "tuned_tiles.inc")
+    rows = re.findall(r"^\{(\d+), (\d+), (\d+), (\d+), (\d+), \{([-\d, ]+)\}, (\d+)\},", open(path).read(), re.M)
+    for H, I, E, K, r, tab, g in rows:
+        H, I, E, K, r, g = map(int, (H, I, E, K, r, g))
+        wcs = [int(v) for v in tab.split(",")]
+        assert len(wcs) == 16 and all(-1 <= v <= 2 for v in wcs)
+        rp = (r + 15) // 16 * 16
+        assert g == 0 or (1 <= g <= 4 and (r == 0 or g * rp <= 256))
+        for b, v in enumerate(wcs):
+            wc, gs, tuned = ml.mlora_tile_config(H, I, E, K, r, 1 << b, 152)
+            assert tuned
+            if v >= 0:
+                assert wc == v

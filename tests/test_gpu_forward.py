@@ -492,3 +492,23 @@ def test_random_wide_layers(over):
     s = wl.spec("tiny", **over)
     rows = gu.sample_rows(s.M, 6, seed=over["seed"], must=(0, s.M - 1))
     _layer(s, rows=rows, label=str(over))
+
+
+@pytest.mark.parametrize("name,M", [("decode", 4), ("decode", 64), ("stress", 96), ("shared", 32)])
+def test_tile_configurations_change_no_bit(name, M):
+    """The tuner's choices (tile width, shrink group size) never change an
+    output bit: every forced configuration equals the library's own choice,
+    which matches the oracle."""
+    s = wl.spec(name, M=M)
+    inp, d, ids, w, y, ids_ref, w_ref, _ = _layer(s)
+    rp = (s.r + 15) // 16 * 16 if s.has_lora else 0
+    groups = [g for g in (1, 2, 4) if g * rp <= 256] if s.has_lora else [0]
+    try:
+        for wc in range(3):
+            for g in groups:
+                ml.mlora_set_tile_config(wc, g)
+                yf = gu.gpu_forward(d, ids, w)
+                torch.cuda.synchronize()
+                assert torch.equal(yf, y), (wc, g)
+    finally:
+        ml.mlora_set_tile_config(-1, 0)

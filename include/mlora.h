@@ -331,6 +331,33 @@ mlora_status mlora_set_tile_config(int width_class, int gsize);
 mlora_status mlora_tile_config(int H, int I, int E_tot, int K_total, int rank, int nblocks, int grid,
                                int* width_class, int* gsize, int* tuned);
 
+/*
+ * CTA-pair mode of the bf16 experts kernel (opt-in).  The experts kernel
+ * runs as clusters of two CTAs on two SMs, each pair sharing 256-row MMAs
+ * (tcgen05 cta_group::2) over two 128-slot blocks of one expert: each SM
+ * loads its own block's token rows and half of the tile's 256 weight rows,
+ * two K-chunks of 64 per copy, so a stage brings a third fewer bytes per
+ * MMA and the producer issues half as many copies.  Align then pads every
+ * expert's blocks to an even count (the second block of a pair may hold no
+ * rows), which the workspace size accounts for: mlora_moe_workspace_size
+ * reports the size for the mode in effect on the calling thread when it is
+ * called.  Tiles are 256 weight rows wide in this mode, and a block's
+ * shrink tiles occupy both SMs of a pair.  On prefill-sized layers the pair
+ * kernel runs its MMAs faster but computes more padded rows, and the
+ * adapter work costs more, so it is off by default.  With finite adapter
+ * weights the mode changes no output bit except, possibly, the sign of an
+ * exact zero: an adapter's expand adds zero products to the rows of a
+ * pair's block that does not use it (a non-finite expand weight then turns
+ * them into NaN).
+ *
+ * mlora_set_pair_mode: for the calling host thread, 1 runs later bf16
+ * forwards in pair mode, 0 (default) with one CTA per SM; the MXFP8 layer
+ * never pairs.  MLORA_ERR_INVALID_ARG for other values.
+ * mlora_pair_mode: the calling thread's mode (1 or 0).  Host only.
+ */
+mlora_status mlora_set_pair_mode(int on);
+int mlora_pair_mode(void);
+
 /* Static, human-readable name of a status code. */
 const char* mlora_status_string(mlora_status status);
 

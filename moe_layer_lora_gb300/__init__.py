@@ -30,6 +30,8 @@ from ._lib import (  # noqa: F401
     mlora_mxfp8_scales_size,
     mlora_set_stage_events,
     mlora_set_tile_config,
+    mlora_set_pair_mode,
+    mlora_pair_mode,
     mlora_tile_config,
     mlora_set_wait_test,
     mlora_status_string,

@@ -94,6 +94,10 @@ def load(path: str = LIB_PATH):
     ip = ctypes.POINTER(ctypes.c_int)
     lib.mlora_tile_config.argtypes = [i] * 7 + [ip, ip, ip]
     lib.mlora_tile_config.restype = i
+    lib.mlora_set_pair_mode.argtypes = [i]
+    lib.mlora_set_pair_mode.restype = i
+    lib.mlora_pair_mode.argtypes = []
+    lib.mlora_pair_mode.restype = i
     _lib = lib
     return lib
 
@@ -413,6 +417,18 @@ def mlora_tile_config(H: int, I: int, E_tot: int, K_total: int, rank: int, nbloc
     _check("mlora_tile_config", load().mlora_tile_config(H, I, E_tot, K_total, rank, nblocks, grid,
                                                          ctypes.byref(wc), ctypes.byref(g), ctypes.byref(t)))
     return wc.value, g.value, bool(t.value)
+
+
+def mlora_set_pair_mode(on: bool) -> None:
+    """For this thread's later bf16 forwards: run the experts kernel as CTA
+    pairs (True) or one CTA per SM (False, the default).  Query workspace
+    sizes after setting it."""
+    _check("mlora_set_pair_mode", load().mlora_set_pair_mode(1 if on else 0))
+
+
+def mlora_pair_mode() -> bool:
+    """Whether this thread's bf16 forwards run as CTA pairs."""
+    return bool(load().mlora_pair_mode())
 
 
 def mlora_status_string(status: int) -> str:

@@ -254,8 +254,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // 2. exclusive scan of the padded counts (E_tot <= 1024: one expert per
     //    thread), the block -> expert map and the real rows of each block
+    //    (pair_pad: padded to whole pairs of blocks, the second of a pair
+    //    possibly empty)
+    const int PB = ex.pair_pad ? 2 * BM : BM;
     const int c = tid < E_tot ? tot[tid] : 0;
-    const int padded = (c + BM - 1) / BM * BM;
+    const int padded = (c + PB - 1) / PB * PB;
     int total;
     const int start = block_exclusive_scan(padded, scratch, &total);
     if (tid < E_tot) {
@@ -267,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int b = start / BM; b < (start + padded) / BM; ++b) {
             if (!MLORA_IN_BOUNDS(b < max_padded / BM, status)) break;
             expert_ids[b] = tid;
-            if (ex.blk_rows) ex.blk_rows[b] = min(BM, c - (b - start / BM) * BM);
+            if (ex.blk_rows) ex.blk_rows[b] = max(0, min(BM, c - (b - start / BM) * BM));
         }
     }
     if (crank == 0) {
@@ -281,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 3. per-expert padding, one warp per expert
     for (int e = warp * ncl + crank; e < E_tot; e += kWarps * ncl) {
         const int n = tot[e];
-        const int pad_end = first[e] + (n + BM - 1) / BM * BM;
+        const int pad_end = first[e] + (n + PB - 1) / PB * PB;
         for (int p = first[e] + n + lane; p < pad_end; p += 32) {
             if (!MLORA_IN_BOUNDS(p < max_padded, status)) break;
             if (staged) {

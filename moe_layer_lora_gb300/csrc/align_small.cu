@@ -352,6 +352,8 @@ size_t align_small_smem(long S, int E_tot, int block_m, long max_padded, bool wi
 
 bool align_small_fits(long S, int E_tot, int block_m, long max_padded, const AlignExtra* extra, bool gather) {
     const bool with_lora = extra && extra->token_lora_idx;
+    // (blocks padded to pairs: the cluster kernel only)
+    if (extra && extra->pair_pad) return false;
     if (S < 1 || S > kSmallMaxSlots || E_tot > 2 * kThreads) return false;
     if (with_lora && (extra->L > 32767 || block_m != MLORA_FORWARD_BLOCK_M)) return false;
     return align_small_smem(S, E_tot, block_m, max_padded, with_lora, gather) <= static_cast<size_t>(kMaxSmem);

@@ -89,6 +89,7 @@ const TunedShape kTunedShapes[] = {
 // tile override for the tuner (mlora_set_tile_config), per host thread
 thread_local int g_force_wc = -1;
 thread_local int g_force_gsize = 0;
+thread_local bool g_pair_mode = false;
 
 thread_local cudaEvent_t g_stage_events[MLORA_STAGE_EVENTS];
 thread_local bool g_stage_events_on = false;
@@ -187,6 +188,8 @@ int device_sm_count() {
     return n;
 }
 
+bool use_pair_mode(bool mx) { return g_pair_mode && !mx; }
+
 Sizes make_sizes(int M, int H, int I, int E_tot, int K_total, int L, int rank, bool mx) {
     Sizes z{};
     z.mx = mx;
@@ -201,7 +204,8 @@ Sizes make_sizes(int M, int H, int I, int E_tot, int K_total, int L, int rank, b
     z.rank = rank;
     z.lora = L > 0 && rank > 0;
     z.S = static_cast<long>(M) * K_total;
-    z.max_padded = align_max_padded(z.S, E_tot, kBlockM);
+    z.pair = use_pair_mode(mx);
+    z.max_padded = align_max_padded(z.S, E_tot, z.pair ? 2 * kBlockM : kBlockM);
     z.max_blocks = z.max_padded / kBlockM;
     z.cap = z.lora ? std::min(L, kBlockM) : 0;
     z.max_lt = z.max_blocks * z.cap;
@@ -435,13 +439,17 @@ mlora_status forward_impl(const void* x, const void* w13, const void* w2, const 
     {
         const cuuint32_t bx[2] = {64, kRowBox};
         const cuuint32_t bxf[2] = {64, 128};
-        // a gate_up tile of width n takes n/2 gate and n/2 up rows, a down tile n rows
+        // a gate_up tile of width n takes n/2 gate and n/2 up rows (one box
+        // over both halves: gate rows, then up rows), a down tile n rows.
+        // CTA pairs (256-row tiles only) load one half per CTA: width class
+        // 1's slot holds that 128-row half box instead.
         cuuint32_t b13[kTileWidths][4], b2[kTileWidths][3];
         for (int wc = 0; wc < kTileWidths; ++wc) {
             const cuuint32_t n = static_cast<cuuint32_t>(tile_width(wc));
-            b13[wc][0] = 64, b13[wc][1] = n / 2, b13[wc][2] = 1, b13[wc][3] = 1;
+            b13[wc][0] = 64, b13[wc][1] = n / 2, b13[wc][2] = 2, b13[wc][3] = 1;
             b2[wc][0] = 64, b2[wc][1] = n, b2[wc][2] = 1;
         }
+        if (z.pair) b13[1][1] = 128, b13[1][2] = 1;
         if (ws.x_perm) {
             const cuuint64_t dx[2] = {H_, MP}, sx[1] = {H_ * 2};
             ok &= make_map(&up.tm_a, ws.x_perm, 2, dx, sx, bx);
@@ -453,23 +461,43 @@ mlora_status forward_impl(const void* x, const void* w13, const void* w2, const 
         if (mx) {
             const cuuint32_t qb[2] = {kMxChunk, kRowBox}, qbf[2] = {kMxChunk, 128};
             const cuuint64_t dx[2] = {H_, MP}, sx[1] = {H_};
-            ok &= make_map_u8(&up.tm_aq, ws.x_q, 2, dx, sx, qb);
-            ok &= make_map_u8(&up.tm_aq_full, ws.x_q, 2, dx, sx, qbf);
+            ok &= make_map_u8(&up.tm_ax, ws.x_q, 2, dx, sx, qb);
+            ok &= make_map_u8(&up.tm_ax_full, ws.x_q, 2, dx, sx, qbf);
             const cuuint64_t da[2] = {I_, MP}, sa[1] = {I_};
-            ok &= make_map_u8(&dn.tm_aq, ws.act_q, 2, da, sa, qb);
-            ok &= make_map_u8(&dn.tm_aq_full, ws.act_q, 2, da, sa, qbf);
+            ok &= make_map_u8(&dn.tm_ax, ws.act_q, 2, da, sa, qb);
+            ok &= make_map_u8(&dn.tm_ax_full, ws.act_q, 2, da, sa, qbf);
             const cuuint64_t d13[4] = {H_, I_, 2, E_}, s13[3] = {H_, I_ * H_, 2 * I_ * H_};
-            const cuuint32_t q13[4] = {kMxChunk, kMxHalf, 1, 1};
-            ok &= make_map_u8(&up.tm_bq, w13, 4, d13, s13, q13);
+            const cuuint32_t q13[4] = {kMxChunk, kMxHalf, 2, 1};
+            ok &= make_map_u8(&up.tm_bx, w13, 4, d13, s13, q13);
             const cuuint64_t d2[3] = {I_, H_, E_}, s2[2] = {I_, H_ * I_};
             const cuuint32_t q2[3] = {kMxChunk, kMxWidth, 1};
-            ok &= make_map_u8(&dn.tm_bq, w2, 3, d2, s2, q2);
+            ok &= make_map_u8(&dn.tm_bx, w2, 3, d2, s2, q2);
         } else {
             const cuuint64_t d13[4] = {H_, I_, 2, E_}, s13[3] = {H_ * 2, I_ * H_ * 2, 2 * I_ * H_ * 2};
             const cuuint64_t d2[3] = {I_, H_, E_}, s2[2] = {I_ * 2, H_ * I_ * 2};
             for (int wc = 0; wc < kTileWidths; ++wc) {
                 ok &= make_map(&up.tm_b[wc], w13, 4, d13, s13, b13[wc]);
                 ok &= make_map(&dn.tm_b[wc], w2, 3, d2, s2, b2[wc]);
+            }
+        }
+        if (z.pair && !mx) {
+            // CTA pairs: two K-chunks of 64 per copy, through views with a
+            // chunk dimension of stride 128 B over the whole chunks of K
+            // (at least two of them; otherwise every stage uses the 2D maps)
+            const cuuint32_t bxc[3] = {64, 128, 2};
+            if (H_ / 64 >= 2) {
+                const cuuint64_t dx[3] = {64, MP, H_ / 64}, sx[2] = {H_ * 2, 128};
+                ok &= make_map(&up.tm_ax_full, ws.x_perm, 3, dx, sx, bxc);
+                const cuuint64_t dw[5] = {64, I_, 2, E_, H_ / 64}, sw[4] = {H_ * 2, I_ * H_ * 2, 2 * I_ * H_ * 2, 128};
+                const cuuint32_t bw[5] = {64, 128, 1, 1, 2};
+                ok &= make_map(&up.tm_bx, w13, 5, dw, sw, bw);
+            }
+            if (I_ / 64 >= 2) {
+                const cuuint64_t da[3] = {64, MP, I_ / 64}, sa[2] = {I_ * 2, 128};
+                ok &= make_map(&dn.tm_ax_full, ws.act, 3, da, sa, bxc);
+                const cuuint64_t dw[4] = {64, H_, E_, I_ / 64}, sw[3] = {I_ * 2, H_ * I_ * 2, 128};
+                const cuuint32_t bw[4] = {64, 128, 1, 2};
+                ok &= make_map(&dn.tm_bx, w2, 4, dw, sw, bw);
             }
         }
         if (lora) {
@@ -520,6 +548,7 @@ mlora_status forward_impl(const void* x, const void* w13, const void* w2, const 
         dn.nkc = z.nkc1;
     }
     gp.mx = mx ? 1 : 0;
+    gp.pair = z.pair ? 1 : 0;
     gp.n_pad = ws.n_pad;
     gp.expert_ids = ws.expert_ids;
     gp.blk_rows = ws.blk_rows;
@@ -560,6 +589,7 @@ mlora_status forward_impl(const void* x, const void* w13, const void* w2, const 
     ex.lt_cap = z.max_lt;
     ex.max_rows = ws.max_rows;
     ex.blk_rows = ws.blk_rows;
+    ex.pair_pad = z.pair ? 1 : 0;
     if (lora) {
         ex.token_lora_idx = token_lora_idx;
         ex.L = L;
@@ -643,6 +673,14 @@ mlora_status mlora_set_stage_events(void* const* events, int count) {
     g_stage_events_on = true;
     return MLORA_OK;
 }
+
+mlora_status mlora_set_pair_mode(int on) {
+    if (on != 0 && on != 1) return MLORA_ERR_INVALID_ARG;
+    g_pair_mode = on != 0;
+    return MLORA_OK;
+}
+
+int mlora_pair_mode(void) { return g_pair_mode ? 1 : 0; }
 
 mlora_status mlora_set_tile_config(int width_class, int gsize) {
     if (width_class < -1 || width_class >= kTileWidths || gsize < 0 || gsize > 4) return MLORA_ERR_INVALID_ARG;

@@ -79,9 +79,15 @@ constexpr int kMxStageBytes = (16384 + kMxBBytes + 3 * kMxAtom + 1023) / 1024 * 
 constexpr int kMxStages = 5;
 constexpr int kMxSmallStageBytes = (4096 + kMxBBytes + 3 * kMxAtom + 1023) / 1024 * 1024;  // 30 KiB
 constexpr int kMxSmallStages = 7;
+// CTA-pair stages: two K-chunks of 64 (a copy moves both, so that the
+// producer issues half as many copies per MMA): the CTA's A rows (2 x 16
+// KiB), then its 128 of the tile's 256 weight rows (2 x 16 KiB)
+constexpr int kPairABytes = 2 * 16384;
+constexpr int kPairStageBytes = kPairABytes + 2 * 128 * 64 * 2;  // 64 KiB
+constexpr int kPairStages = 3;
 constexpr int kMaxStages = 7;  // barrier arrays: the deepest ring
 static_assert(kMaxStages >= kStages && kMaxStages >= kSmallStages && kMaxStages >= kMxStages &&
-                  kMaxStages >= kMxSmallStages, "barrier arrays");
+                  kMaxStages >= kMxSmallStages && kMaxStages >= kPairStages, "barrier arrays");
 // MXFP8 tensor memory: two 192-column accumulators, then two slots of
 // scale factors (A at +0, B at +32 -- 32-column aligned -- of each 64)
 constexpr int kMxAccCols = kMxWidth;
@@ -91,11 +97,13 @@ constexpr int kATileBytes = kBlockM * kBlockK * 2;               // 16 KiB
 constexpr int kStageBytes = kATileBytes + kBN * kBlockK * 2;     // 48 KiB
 constexpr int kSmallATileBytes = kRowBox * kBlockK * 2;          // 4 KiB
 constexpr int kSmallStageBytes = kSmallATileBytes + kBN * kBlockK * 2;  // 36 KiB
-constexpr int kRingBytes = kSmallStages * kSmallStageBytes;      // 216 KiB >= kStages * kStageBytes
+constexpr int kRingBytes = kSmallStages * kSmallStageBytes;      // 216 KiB
 constexpr int kAccCols = kBN;
 constexpr int kTmemCols = 2 * kBN;
 constexpr int kSmemBytes = kRingBytes + 1024 /* alignment slack */ + 256 /* barriers */;
 static_assert(kStages * kStageBytes <= kRingBytes && kSmallStages * kSmallStageBytes <= kRingBytes, "ring");
+static_assert(kSmemBytes <= 227 * 1024, "shared memory of a CTA");
+static_assert(kStages * kStageBytes <= kRingBytes && kPairStages * kPairStageBytes <= kRingBytes, "ring");
 static_assert(kMxStages * kMxStageBytes <= kRingBytes && kMxSmallStages * kMxSmallStageBytes <= kRingBytes, "ring");
 static_assert(kMxSfCol0 + 2 * 64 <= 512, "tensor memory");
 // one CTA per SM: each CTA allocates all 512 TMEM columns, so two CTAs of
@@ -134,6 +142,13 @@ __device__ bool wait_counter(const int32_t* flag, int target, volatile int* abor
     }
 }
 
+// One look at a counter, no ordering: whether a wait on it would pass now.
+__device__ __forceinline__ bool counter_reached(const int32_t* flag, int target) {
+    int v;
+    asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+    return v >= target;
+}
+
 struct Tile {
     int kind;
     int side;  // 0: gate_up projection, 1: down projection
@@ -143,6 +158,7 @@ struct Tile {
     int e;     // expert
     int i0;    // first adapter of the group in the block's list (shrink tiles)
     int g;     // adapters in the group (shrink tiles)
+    bool rowless;  // CTA pair: this CTA holds none of the tile's token rows (the odd CTA of a shrink tile)
 };
 
 // Tile width of a launch: 256 weight rows (gate_up: 128 gate + 128 up),
@@ -161,8 +177,12 @@ struct Phases {
     long s1, g, s2, d;  // ends of phases 1..4
 };
 
+// Tile `tile` of the sequence.  Base tiles run over units of rows: blocks,
+// or in pair mode pairs of blocks (2u, 2u+1), where t.b is the block of
+// this CTA (cluster rank `rank`); shrink tiles run over one block, whose
+// rows the even CTA of a pair holds.
 __device__ __forceinline__ Tile decode_tile(const GemmParams& p, const Geom& gm, long tile, const Phases& ph, int ns,
-                                            int nblocks) {
+                                            int nunits, int pair, uint32_t rank) {
     Tile t;
     long u;
     if (tile < ph.s1) {
@@ -188,13 +208,16 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, const Geom& gm,
         t.i0 = p.gt_first[v];
         t.g = min(p.gsize, p.blk_nad[t.b] - t.i0);
         t.cb = 0;
+        t.rowless = pair && rank != 0;
     } else {
         const int ncb = t.side ? gm.ncb1 : gm.ncb0;
         const int bu = static_cast<int>(u / ncb);
         t.cb = static_cast<int>(u - static_cast<long>(bu) * ncb);
-        t.b = nblocks - 1 - bu;
+        const int unit = nunits - 1 - bu;
+        t.b = pair ? 2 * unit + static_cast<int>(rank) : unit;
         t.i0 = 0;
         t.g = 0;
+        t.rowless = false;
     }
     t.e = p.expert_ids[t.b];
     return t;
@@ -254,6 +277,9 @@ struct Ctx {
     Geom gm;
     Phases ph;
     int nblocks;
+    int nunits;       // row units of the base tiles: blocks, or pairs of blocks
+    int pair;         // CTA-pair launch
+    uint32_t rank;    // cluster rank in a pair (0: the CTA that issues the MMAs)
     int ns;           // shrink tiles per projection
     int rp;           // rank padded to the MMA's N granule
     int lora_ksteps;  // expand K-steps of 16
@@ -262,21 +288,27 @@ struct Ctx {
     __device__ __forceinline__ Ctx(const GemmParams& prm, uint8_t* sm, uint32_t tmem)
         : p(&prm), smem(sm), L(sm), tmem_base(tmem), lim(prm.wait_limit) {
         nblocks = *prm.n_pad / kBlockM;
+        pair = prm.pair;
+        rank = pair ? cluster_ctarank() : 0u;
+        // (align pads every expert to whole pairs of blocks in pair mode)
+        nunits = pair ? nblocks / 2 : nblocks;
         ns = prm.has_lora ? *prm.gt_total : 0;
         // MXFP8 launches use 192-row tiles (the packed weight scales follow
-        // them); otherwise the tuned table's width for this many blocks, else
-        // the wave rule
+        // them), CTA pairs 256-row tiles; otherwise the tuned table's width
+        // for this many blocks, else the wave rule
         const int tuned = prm.width_table[width_bucket(nblocks)];
-        gm.wc = prm.mx ? 1
-                       : tuned >= 0 ? tuned : choose_width(nblocks, prm.side[0].n_out, prm.side[1].n_out, gridDim.x);
+        gm.wc = prm.mx     ? 1
+                : pair     ? 0
+                : tuned >= 0 ? tuned
+                             : choose_width(nblocks, prm.side[0].n_out, prm.side[1].n_out, gridDim.x);
         gm.bn = tile_width(gm.wc);
         gm.half = gm.bn / 2;
         gm.ncb0 = (prm.side[0].n_out + gm.half - 1) / gm.half;
         gm.ncb1 = (prm.side[1].n_out + gm.bn - 1) / gm.bn;
         ph.s1 = ns;
-        ph.g = ph.s1 + static_cast<long>(nblocks) * gm.ncb0;
+        ph.g = ph.s1 + static_cast<long>(nunits) * gm.ncb0;
         ph.s2 = ph.g + ns;
-        ph.d = ph.s2 + static_cast<long>(nblocks) * gm.ncb1;
+        ph.d = ph.s2 + static_cast<long>(nunits) * gm.ncb1;
         rp = (prm.rank + 15) / 16 * 16;
         lora_ksteps = (prm.rank + 15) / 16;
     }
@@ -295,7 +327,6 @@ __device__ __forceinline__ void producer(const Ctx& c, long first_tile) {
     long long* const tile_ring = c.L.tile_ring;
     volatile int* const abort_flag = c.L.abort_flag;
     const long long lim = c.lim;
-    const int nblocks = c.nblocks;
     const int ns = c.ns;
     const Geom& gm = c.gm;
     const Phases& ph = c.ph;
@@ -328,15 +359,9 @@ __device__ __forceinline__ void producer(const Ctx& c, long first_tile) {
         tile_ring[ts] = have ? tile : -1;
         mbar_arrive(&tile_full[ts]);
         if (!have) break;
-        const Tile tc = decode_tile(p, gm, tile, ph, ns, nblocks);
+        const Tile tc = decode_tile(p, gm, tile, ph, ns, c.nunits, 0, 0u);
         const GemmSide& sd = p.side[tc.side];
         const int row0 = tc.b * kBlockM;
-        // the down side reads act rows, complete once the block's
-        // gate_up tiles all are
-        if (tc.side == 1 && !wait_counter(p.act_done + tc.b, gm.ncb0, abort_flag, p.status, lim)) {
-            ok = false;
-            break;
-        }
         // only the block's real rows are loaded; the MMA rows past
         // them hold stale data and feed only discarded output rows
         const int nbox = (p.blk_rows[tc.b] + kRowBox - 1) / kRowBox;
@@ -348,6 +373,75 @@ __device__ __forceinline__ void producer(const Ctx& c, long first_tile) {
         const int nk_base = kMx ? sd.nkc : nk;
         const CUtensorMap* bmap = &sd.tm_b[gm.wc];
         const CUtensorMap* lbmap = &sd.tm_lb[gm.wc];
+        // a base stage: the tile's weight rows of K-chunk kb (B; in the
+        // MXFP8 layer E4M3 rows of 128 bytes, then the chunk's packed
+        // weight scales) and the block's token rows (A; MXFP8: then the
+        // chunk's scale atom of the activations)
+        const long ncb = tc.side ? gm.ncb1 : gm.ncb0;
+        const uint8_t* b_scales = kMx ? sd.b_scales + (static_cast<size_t>(tc.e) * ncb + tc.cb) * sd.nkc * kMxTileScaleBytes
+                                      : nullptr;
+        const uint32_t b_stage = kMx ? gm.bn * kMxChunk + kMxTileScaleBytes : gm.bn * kBlockK * 2;
+        const uint32_t a_stage = kMx ? a_bytes + kMxAtom : a_bytes;
+        auto load_b = [&](int s, int kb) {
+            uint8_t* sb = smem + s * stb + ab;
+            const CUtensorMap* map = kMx ? &sd.tm_bx : bmap;
+            const int k0 = kb * (kMx ? kMxChunk : kBlockK);
+            if (tc.kind == kGateUp) {
+                // one box over the slab's gate rows and then its up rows
+                tma_load_4d(sb, map, &full[s], k0, tc.cb * gm.half, 0, tc.e);
+            } else {
+                tma_load_3d(sb, map, &full[s], k0, tc.cb * gm.bn, tc.e);
+            }
+            if (kMx)
+                bulk_load(sb + kMxBBytes + kMxAtom, b_scales + static_cast<size_t>(kb) * kMxTileScaleBytes,
+                          kMxTileScaleBytes, &full[s]);
+        };
+        auto load_a = [&](int s, int kb) {
+            uint8_t* sa = smem + s * stb;
+            const int k0 = kb * (kMx ? kMxChunk : kBlockK);
+            const CUtensorMap* full_map = kMx ? &sd.tm_ax_full : &sd.tm_a_full;
+            const CUtensorMap* box_map = kMx ? &sd.tm_ax : &sd.tm_a;
+            if (full_block)
+                tma_load_2d(sa, full_map, &full[s], k0, row0);
+            else
+                for (int i = 0; i < nbox; ++i)
+                    tma_load_2d(sa + i * kRowBox * 128, box_map, &full[s], k0, row0 + i * kRowBox);
+            if (kMx)
+                bulk_load(sa + ab + kMxBBytes, sd.a_scales + (static_cast<size_t>(tc.b) * sd.nkc + kb) * kMxAtom, kMxAtom,
+                          &full[s]);
+        };
+        // stages whose weight rows went out before the act wait below
+        int pre = 0;
+        if (tc.side == 1) {
+            // the down side reads act rows, complete once the block's
+            // gate_up tiles all are; the weight rows do not depend on
+            // them, so while the block's last gate_up tiles finish, the
+            // first stages' weight rows stream into the ring (an L2
+            // prefetch of the rest measured slower: prefetches ahead of
+            // the ring cut the stream rate of every SM by a quarter)
+            const int32_t* act_done = p.act_done + tc.b;
+            if (!tc.shrink && !counter_reached(act_done, gm.ncb0)) {
+                const int npre = min(nk_base, nst);
+                for (; pre < npre; ++pre) {
+                    const long j = it + pre;
+                    const int s = static_cast<int>(j % nst);
+                    if (!mbar_wait(&empty[s], (static_cast<uint32_t>(j / nst) & 1u) ^ 1u, abort_flag, p.status, lim)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_expect_tx(&full[s], b_stage);
+                    load_b(s, pre);
+                }
+            }
+            if (ok && !wait_counter(act_done, gm.ncb0, abort_flag, p.status, lim)) ok = false;
+            if (!ok) {
+                // the stages armed above complete once their weight rows
+                // land, so the drain below finds every issued copy
+                for (int q = 0; q < pre; ++q) mbar_arrive(&full[(it + q) % nst]);
+                it += pre;
+                break;
+            }
+        }
         if (tc.shrink) {
             // several K-chunks per stage: the shrink's operands are
             // small, and a stage of one chunk leaves the copy
@@ -385,53 +479,20 @@ __device__ __forceinline__ void producer(const Ctx& c, long first_tile) {
         for (int kb = 0; kb < nk_base; ++kb, ++it) {
             const int s = static_cast<int>(it % nst);
             const uint32_t phs = static_cast<uint32_t>(it / nst) & 1u;
-            if (!mbar_wait(&empty[s], phs ^ 1u, abort_flag, p.status, lim)) {
+            if (kb >= pre && !mbar_wait(&empty[s], phs ^ 1u, abort_flag, p.status, lim)) {
                 ok = false;
                 break;
             }
             if (kb + 3 >= nk_base) claim();
-            uint8_t* sa = smem + s * stb;
-            uint8_t* sb = sa + ab;
-            if (kMx) {
-                // E4M3 A and B rows of K-chunk kb (128 bytes a row), then the
-                // chunk's scale atoms: A's from the activations' atoms, B's
-                // from the packed weight scales of this slab
-                uint8_t* sf = sb + kMxBBytes;
-                const int kx = kb * kMxChunk;
-                mbar_arrive_expect_tx(&full[s], a_bytes + gm.bn * kMxChunk + 3 * kMxAtom);
-                if (tc.kind == kGateUp) {
-                    tma_load_4d(sb, &sd.tm_bq, &full[s], kx, tc.cb * gm.half, 0, tc.e);
-                    tma_load_4d(sb + gm.half * kMxChunk, &sd.tm_bq, &full[s], kx, tc.cb * gm.half, 1, tc.e);
-                } else {
-                    tma_load_3d(sb, &sd.tm_bq, &full[s], kx, tc.cb * gm.bn, tc.e);
-                }
-                if (full_block)
-                    tma_load_2d(sa, &sd.tm_aq_full, &full[s], kx, row0);
-                else
-                    for (int i = 0; i < nbox; ++i)
-                        tma_load_2d(sa + i * kRowBox * kMxChunk, &sd.tm_aq, &full[s], kx, row0 + i * kRowBox);
-                const long ncb = tc.side ? gm.ncb1 : gm.ncb0;
-                bulk_load(sf, sd.a_scales + (static_cast<size_t>(tc.b) * sd.nkc + kb) * kMxAtom, kMxAtom, &full[s]);
-                bulk_load(sf + kMxAtom,
-                          sd.b_scales + ((static_cast<size_t>(tc.e) * ncb + tc.cb) * sd.nkc + kb) * kMxTileScaleBytes,
-                          kMxTileScaleBytes, &full[s]);
-                continue;
-            }
-            const int k0 = kb * kBlockK;
-            if (tc.kind == kGateUp) {
-                mbar_arrive_expect_tx(&full[s], a_bytes + gm.bn * kBlockK * 2);
-                tma_load_4d(sb, bmap, &full[s], k0, tc.cb * gm.half, 0, tc.e);
-                tma_load_4d(sb + gm.half * kBlockK * 2, bmap, &full[s], k0, tc.cb * gm.half, 1, tc.e);
+            if (kb < pre) {
+                mbar_arrive_expect_tx(&full[s], a_stage);
             } else {
-                mbar_arrive_expect_tx(&full[s], a_bytes + gm.bn * kBlockK * 2);
-                tma_load_3d(sb, bmap, &full[s], k0, tc.cb * gm.bn, tc.e);
+                mbar_arrive_expect_tx(&full[s], a_stage + b_stage);
+                load_b(s, kb);
             }
-            if (full_block)
-                tma_load_2d(sa, &sd.tm_a_full, &full[s], k0, row0);
-            else
-                for (int i = 0; i < nbox; ++i)
-                    tma_load_2d(sa + i * kRowBox * kBlockK * 2, &sd.tm_a, &full[s], k0, row0 + i * kRowBox);
+            load_a(s, kb);
         }
+
         if (!ok || !p.has_lora) continue;
         const int nad = p.blk_nad[tc.b];
         if (nad == 0) continue;
@@ -454,7 +515,6 @@ __device__ __forceinline__ void producer(const Ctx& c, long first_tile) {
             mbar_arrive_expect_tx(&full[s], a_bytes + gm.bn * kBlockK * 2);
             if (tc.kind == kGateUp) {
                 tma_load_4d(sb, lbmap, &full[s], 0, tc.cb * gm.half, 0, le);
-                tma_load_4d(sb + gm.half * kBlockK * 2, lbmap, &full[s], 0, tc.cb * gm.half, 1, le);
             } else {
                 tma_load_3d(sb, lbmap, &full[s], 0, tc.cb * gm.bn, le);
             }
@@ -487,7 +547,6 @@ __device__ __forceinline__ void mma_issuer(const Ctx& c) {
     long long* const tile_ring = c.L.tile_ring;
     volatile int* const abort_flag = c.L.abort_flag;
     const long long lim = c.lim;
-    const int nblocks = c.nblocks;
     const int ns = c.ns;
     const Geom& gm = c.gm;
     const Phases& ph = c.ph;
@@ -505,7 +564,7 @@ __device__ __forceinline__ void mma_issuer(const Ctx& c) {
         const long tile = tile_ring[ts];
         mbar_arrive(&tile_empty[ts]);
         if (tile < 0) break;
-        const Tile tc = decode_tile(p, gm, tile, ph, ns, nblocks);
+        const Tile tc = decode_tile(p, gm, tile, ph, ns, c.nunits, 0, 0u);
         const int nk = (p.side[tc.side].K + kBlockK - 1) / kBlockK;
         const int acc = lt & 1;
         if (!mbar_wait(&tempty[acc], (static_cast<uint32_t>(lt >> 1) & 1u) ^ 1u, abort_flag, p.status, lim)) {
@@ -611,9 +670,402 @@ __device__ __forceinline__ void mma_issuer(const Ctx& c) {
     drain_wait(drain, 0, lim);
 }
 
+// Bytes of the token rows a CTA loads for block b: whole 32-row boxes
+// covering its real rows (one 128-row box when the block is full).
+__device__ __forceinline__ uint32_t block_a_bytes(const GemmParams& p, int b) {
+    const int nbox = (p.blk_rows[b] + kRowBox - 1) / kRowBox;
+    return static_cast<uint32_t>(nbox) * kRowBox * kBlockK * 2;
+}
+
+// Adapters of a pair of blocks: the ascending union of their lists.
+__device__ __forceinline__ int pair_union_count(const GemmParams& p, int b0) {
+    const int n0 = p.blk_nad[b0], n1 = p.blk_nad[b0 + 1];
+    const int32_t* l0 = p.blk_lora + static_cast<long>(b0) * p.cap;
+    const int32_t* l1 = l0 + p.cap;
+    int i0 = 0, i1 = 0, n = 0;
+    while (i0 < n0 || i1 < n1) {
+        const int a = i0 < n0 ? l0[i0] : 0x7fffffff, b = i1 < n1 ? l1[i1] : 0x7fffffff;
+        const int l = min(a, b);
+        i0 += a == l;
+        i1 += b == l;
+        ++n;
+    }
+    return n;
+}
+
+// TMA producer of a CTA pair (one thread in each CTA).  The even CTA claims
+// the tiles and hands each to the rings of both CTAs.  Each CTA streams its
+// own block's token rows (A) and its 128 of the tile's 256 weight rows (B:
+// the gate rows of a gate_up slab in the even CTA, the up rows in the odd
+// one; the first or second half of a down slab) into its own stage ring;
+// every copy completes on the even CTA's stage barrier, whose one arrival
+// (the even CTA's) announces the bytes of both.  Shrink tiles: the even CTA
+// holds the block's rows, the adapters' rank rows are split between the two
+// (a group of odd size gets a zero adapter in the odd CTA).  Expand stages
+// run over the union of the two blocks' adapters; a block without the
+// stage's adapter loads zero rows (a box at a negative row reads as zero).
+template <int nst, uint32_t stb, uint32_t ab>
+__device__ __forceinline__ void producer_pair(const Ctx& c, long first_tile) {
+    const GemmParams& p = *c.p;
+    uint64_t* const full = c.L.full;
+    uint64_t* const empty = c.L.empty;
+    uint64_t* const tile_full = c.L.tile_full;
+    uint64_t* const tile_empty = c.L.tile_empty;
+    long long* const tile_ring = c.L.tile_ring;
+    volatile int* const abort_flag = c.L.abort_flag;
+    const long long lim = c.lim;
+    const Geom& gm = c.gm;
+    const long ntiles = c.ph.d;
+    const int rp = c.rp;
+    uint8_t* const smem = c.smem;
+    const uint32_t rank = c.rank;
+    const bool lead = rank == 0;
+    long it = 0;  // stages issued
+    bool ok = true;
+    long tile = first_tile, next = -1;
+    auto claim = [&]() {
+        if (lead && next < 0) next = atomicAdd(p.tile_next, 1);
+    };
+    if (p.stall_flag && !wait_counter(p.stall_flag, 1, abort_flag, p.status, lim)) ok = false;
+    for (int jt = 0; ok; ++jt, tile = next, next = -1) {
+        const int ts = jt % kTileRing;
+        const uint32_t tph = static_cast<uint32_t>(jt / kTileRing) & 1u;
+        if (lead) {
+            // the slot is free once its readers in both CTAs arrived
+            if (!mbar_wait_cluster(&tile_empty[ts], tph ^ 1u, abort_flag, p.status, lim)) {
+                ok = false;
+                break;
+            }
+            const bool have = tile >= 0 && tile < ntiles;
+            const long v = have ? tile : -1;
+            tile_ring[ts] = v;
+            st_cluster_s64(mapa_shared(&tile_ring[ts], 1), v);
+            mbar_arrive(&tile_full[ts]);
+            mbar_arrive_cluster(mapa_shared(&tile_full[ts], 1));
+            if (!have) break;
+        } else {
+            if (!mbar_wait_cluster(&tile_full[ts], tph, abort_flag, p.status, lim)) {
+                ok = false;
+                break;
+            }
+            tile = tile_ring[ts];
+            mbar_arrive_cluster(mapa_shared(&tile_empty[ts], 0));
+            if (tile < 0) break;
+        }
+        const Tile tc = decode_tile(p, gm, tile, c.ph, c.ns, c.nunits, 1, rank);
+        const GemmSide& sd = p.side[tc.side];
+        const int nk = (sd.K + kBlockK - 1) / kBlockK;
+        const int32_t* lora_list = p.blk_lora + static_cast<long>(tc.b) * p.cap;
+        if (tc.shrink) {
+            // the down shrink reads act rows (the even CTA's)
+            if (tc.side == 1 && lead && !wait_counter(p.act_done + tc.b, gm.ncb0, abort_flag, p.status, lim)) {
+                ok = false;
+                break;
+            }
+            const uint32_t a0 = block_a_bytes(p, tc.b);
+            const int nbox = static_cast<int>(a0 / (kRowBox * kBlockK * 2));
+            const bool full_block = nbox * kRowBox == kBlockM;
+            const int row0 = tc.b * kBlockM;
+            const int g2 = (tc.g + 1) / 2;  // adapters per CTA
+            const uint32_t bh = static_cast<uint32_t>(g2) * rp * kBlockK * 2;
+            const uint32_t chunk = a0 + bh;  // the same layout in both CTAs
+            const int cps = shrink_chunks(a0, bh, stb);
+            for (int kb0 = 0; kb0 < nk; kb0 += cps, ++it) {
+                const int s = static_cast<int>(it % nst);
+                if (!mbar_wait(&empty[s], (static_cast<uint32_t>(it / nst) & 1u) ^ 1u, abort_flag, p.status, lim)) {
+                    ok = false;
+                    break;
+                }
+                const int nc = min(cps, nk - kb0);
+                if (kb0 + nc >= nk) claim();
+                if (lead) mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(nc) * (a0 + 2 * bh));
+                const uint32_t fb = mapa_shared(&full[s], 0);
+                for (int cc = 0; cc < nc; ++cc) {
+                    uint8_t* ca = smem + s * stb + cc * chunk;
+                    const int k0 = (kb0 + cc) * kBlockK;
+                    for (int i = 0; i < g2; ++i) {
+                        const int ai = static_cast<int>(rank) * g2 + i;
+                        const int le = ai < tc.g ? lora_list[tc.i0 + ai] * p.E_tot + tc.e : -1;
+                        tma_load_3d_pair(ca + a0 + i * rp * kBlockK * 2, &sd.tm_sa, fb, k0, 0, le);
+                    }
+                    if (lead) {
+                        if (full_block)
+                            tma_load_2d_pair(ca, &sd.tm_a_full, fb, k0, row0);
+                        else
+                            for (int i = 0; i < nbox; ++i)
+                                tma_load_2d_pair(ca + i * kRowBox * kBlockK * 2, &sd.tm_a, fb, k0,
+                                                 row0 + i * kRowBox);
+                    }
+                }
+            }
+            continue;
+        }
+        const int b0 = tc.b & ~1;  // the pair's blocks: b0 (even CTA), b0 + 1
+        const uint32_t a_mine = block_a_bytes(p, tc.b);
+        constexpr uint32_t kChunkB = 128 * kBlockK * 2;  // a CTA's weight rows of one K-chunk
+        // a stage: two chunks of both CTAs' token rows and weight halves
+        const uint32_t stage_bytes = 2 * (block_a_bytes(p, b0) + block_a_bytes(p, b0 + 1) + 2 * kChunkB);
+        const int nbox = static_cast<int>(a_mine / (kRowBox * kBlockK * 2));
+        const bool full_block = nbox * kRowBox == kBlockM;
+        const int row0 = tc.b * kBlockM;
+        const int nst2 = (nk + 1) / 2;  // stages of two chunks (the last one's second may lie past K)
+        const int kwhole = sd.K / kBlockK;
+        // stage j copies chunks 2j and 2j+1 with one copy per operand when
+        // both are whole chunks of K, or the second lies entirely past K
+        // (the view's zero fill); the stage holding a partial last chunk
+        // copies chunk by chunk through the 2D maps
+        auto view_ok = [&](int j) {
+            const int c1 = 2 * j + 1;
+            return kwhole >= 2 && (c1 < kwhole || (c1 == kwhole && kwhole == nk));
+        };
+        // (a pair launch keeps the 128-row half boxes of the gate_up weights
+        // and expand weights in width class 1's map slot)
+        auto load_b = [&](int s, int j, uint32_t fb) {
+            uint8_t* sb = smem + s * stb + ab;
+            if (view_ok(j)) {
+                if (tc.kind == kGateUp)
+                    tma_load_5d_pair(sb, &sd.tm_bx, fb, 0, tc.cb * 128, static_cast<int>(rank), tc.e, 2 * j);
+                else
+                    tma_load_4d_pair(sb, &sd.tm_bx, fb, 0, tc.cb * 256 + static_cast<int>(rank) * 128, tc.e, 2 * j);
+                return;
+            }
+            for (int cc = 0; cc < 2; ++cc) {
+                const int k0 = (2 * j + cc) * kBlockK;
+                if (tc.kind == kGateUp)
+                    tma_load_4d_pair(sb + cc * kChunkB, &sd.tm_b[1], fb, k0, tc.cb * 128, static_cast<int>(rank),
+                                     tc.e);
+                else
+                    tma_load_3d_pair(sb + cc * kChunkB, &sd.tm_b[2], fb, k0,
+                                     tc.cb * 256 + static_cast<int>(rank) * 128, tc.e);
+            }
+        };
+        auto load_a = [&](int s, int j, uint32_t fb) {
+            uint8_t* sa = smem + s * stb;
+            if (nbox == 0) return;
+            if (full_block && view_ok(j)) {
+                tma_load_3d_pair(sa, &sd.tm_ax_full, fb, 0, row0, 2 * j);
+                return;
+            }
+            for (int cc = 0; cc < 2; ++cc) {
+                const int k0 = (2 * j + cc) * kBlockK;
+                uint8_t* ca = sa + cc * (kPairABytes / 2);
+                if (full_block)
+                    tma_load_2d_pair(ca, &sd.tm_a_full, fb, k0, row0);
+                else
+                    for (int i = 0; i < nbox; ++i)
+                        tma_load_2d_pair(ca + i * kRowBox * kBlockK * 2, &sd.tm_a, fb, k0, row0 + i * kRowBox);
+            }
+        };
+        int pre = 0;  // stages whose weight rows went out before the act wait
+        if (tc.side == 1) {
+            const int32_t* act_done = p.act_done + tc.b;
+            if (!counter_reached(act_done, gm.ncb0)) {
+                const int npre = min(nst2, nst);
+                for (; pre < npre; ++pre) {
+                    const long j = it + pre;
+                    const int s = static_cast<int>(j % nst);
+                    if (!mbar_wait(&empty[s], (static_cast<uint32_t>(j / nst) & 1u) ^ 1u, abort_flag, p.status, lim)) {
+                        ok = false;
+                        break;
+                    }
+                    if (lead) mbar_arrive_expect_tx(&full[s], stage_bytes);
+                    load_b(s, pre, mapa_shared(&full[s], 0));
+                }
+            }
+            if (ok && !wait_counter(act_done, gm.ncb0, abort_flag, p.status, lim)) ok = false;
+            if (!ok) {
+                it += pre;
+                break;
+            }
+        }
+        for (int j = 0; j < nst2; ++j, ++it) {
+            const int s = static_cast<int>(it % nst);
+            const uint32_t fb = mapa_shared(&full[s], 0);
+            if (j >= pre) {
+                if (!mbar_wait(&empty[s], (static_cast<uint32_t>(it / nst) & 1u) ^ 1u, abort_flag, p.status, lim)) {
+                    ok = false;
+                    break;
+                }
+                if (lead) mbar_arrive_expect_tx(&full[s], stage_bytes);
+                load_b(s, j, fb);
+            }
+            if (j + 2 >= nst2) claim();
+            load_a(s, j, fb);
+        }
+        if (!ok || !p.has_lora) continue;
+        const int n0 = p.blk_nad[b0], n1 = p.blk_nad[b0 + 1];
+        if (n0 + n1 == 0) continue;
+        // this block's LoRA tiles: every shrink tile of the block and side
+        const int nmine = rank ? n1 : n0;
+        if (nmine > 0 && !wait_counter(sd.done + tc.b, (nmine + p.gsize - 1) / p.gsize, abort_flag, p.status, lim)) {
+            ok = false;
+            break;
+        }
+        const int32_t* l0 = p.blk_lora + static_cast<long>(b0) * p.cap;
+        const int32_t* l1 = l0 + p.cap;
+        const int lt0 = p.blk_lt_start[tc.b];
+        const CUtensorMap* lb = tc.kind == kGateUp ? &sd.tm_lb[1] : &sd.tm_lb[2];
+        int i0 = 0, i1 = 0;
+        while (i0 < n0 || i1 < n1) {
+            const int a = i0 < n0 ? l0[i0] : 0x7fffffff, b = i1 < n1 ? l1[i1] : 0x7fffffff;
+            const int l = min(a, b);
+            const int mine = rank ? (b == l ? i1 : -1) : (a == l ? i0 : -1);
+            const int s = static_cast<int>(it % nst);
+            if (!mbar_wait(&empty[s], (static_cast<uint32_t>(it / nst) & 1u) ^ 1u, abort_flag, p.status, lim)) {
+                ok = false;
+                break;
+            }
+            const uint32_t fb = mapa_shared(&full[s], 0);
+            if (lead) mbar_arrive_expect_tx(&full[s], block_a_bytes(p, b0) + block_a_bytes(p, b0 + 1) + 2 * kChunkB);
+            uint8_t* sa = smem + s * stb;
+            const int le = l * p.E_tot + tc.e;
+            if (tc.kind == kGateUp)
+                tma_load_4d_pair(sa + ab, lb, fb, 0, tc.cb * 128, static_cast<int>(rank), le);
+            else
+                tma_load_3d_pair(sa + ab, lb, fb, 0, tc.cb * 256 + static_cast<int>(rank) * 128, le);
+            if (full_block)
+                tma_load_2d_pair(sa, &sd.tm_t_full, fb, 0, mine >= 0 ? (lt0 + mine) * kBlockM : -kBlockM);
+            else
+                for (int j = 0; j < nbox; ++j)
+                    tma_load_2d_pair(sa + j * kRowBox * kBlockK * 2, &sd.tm_t, fb, 0,
+                                     mine >= 0 ? (lt0 + mine) * kBlockM + j * kRowBox : -kRowBox);
+            i0 += a == l;
+            i1 += b == l;
+            ++it;
+        }
+    }
+    // after an abort the even CTA waits (bounded) for the stages issued: each
+    // barrier counts the bytes of both CTAs' copies; the odd CTA's copies
+    // land before the pair passes its final cluster barrier
+    if (!ok && lead) {
+        for (long j = it > nst ? it - nst : 0; j < it; ++j)
+            drain_wait(&full[j % nst], static_cast<uint32_t>(j / nst) & 1u, lim);
+    }
+}
+
+// MMA issuer of a CTA pair (one thread of the even CTA): the 256-row MMAs
+// (cta_group::2) of every tile, each stage's completion signalled to the
+// stage's empty barrier in both CTAs and each finished accumulator to both
+// CTAs' epilogues.
+template <int nst, uint32_t stb, uint32_t ab>
+__device__ __forceinline__ void mma_issuer_pair(const Ctx& c) {
+    const GemmParams& p = *c.p;
+    uint64_t* const full = c.L.full;
+    uint64_t* const empty = c.L.empty;
+    uint64_t* const tfull = c.L.tfull;
+    uint64_t* const tempty = c.L.tempty;
+    uint64_t* const drain = c.L.drain;
+    uint64_t* const tile_full = c.L.tile_full;
+    uint64_t* const tile_empty = c.L.tile_empty;
+    long long* const tile_ring = c.L.tile_ring;
+    volatile int* const abort_flag = c.L.abort_flag;
+    const long long lim = c.lim;
+    const Geom& gm = c.gm;
+    const int rp = c.rp;
+    const int lora_ksteps = c.lora_ksteps;
+    uint8_t* const smem = c.smem;
+    const uint32_t tmem_base = c.tmem_base;
+    const uint32_t idesc_base = umma_idesc_bf16(256, 256);
+    long it = 0;  // stages consumed
+    bool ok = true;
+    for (int lt = 0; ok; ++lt) {
+        const int ts = lt % kTileRing;
+        if (!mbar_wait(&tile_full[ts], static_cast<uint32_t>(lt / kTileRing) & 1u, abort_flag, p.status, lim)) break;
+        const long tile = tile_ring[ts];
+        mbar_arrive(&tile_empty[ts]);
+        if (tile < 0) break;
+        const Tile tc = decode_tile(p, gm, tile, c.ph, c.ns, c.nunits, 1, 0u);
+        const int nk = (p.side[tc.side].K + kBlockK - 1) / kBlockK;
+        const int acc = lt & 1;
+        // both CTAs' epilogues drained this accumulator
+        if (!mbar_wait_cluster(&tempty[acc], (static_cast<uint32_t>(lt >> 1) & 1u) ^ 1u, abort_flag, p.status,
+                               lim)) {
+            ok = false;
+            break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kAccCols);
+        if (tc.shrink) {
+            const uint32_t a0 = block_a_bytes(p, tc.b);
+            const int g2 = (tc.g + 1) / 2;
+            const uint32_t bh = static_cast<uint32_t>(g2) * rp * kBlockK * 2;
+            const uint32_t chunk = a0 + bh;
+            const int cps = shrink_chunks(a0, bh, stb);
+            const uint32_t idesc = umma_idesc_bf16(256, 2 * g2 * rp);
+            for (int kb0 = 0; kb0 < nk; kb0 += cps, ++it) {
+                const int s = static_cast<int>(it % nst);
+                if (!mbar_wait(&full[s], static_cast<uint32_t>(it / nst) & 1u, abort_flag, p.status, lim)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const int nc = min(cps, nk - kb0);
+                for (int cc = 0; cc < nc; ++cc) {
+                    const uint32_t a_addr = smem_u32(smem + s * stb + cc * chunk);
+                    const uint64_t ad = umma_desc_sw128(a_addr);
+                    const uint64_t bd = umma_desc_sw128(a_addr + a0);
+#pragma unroll
+                    for (int k = 0; k < kBlockK / 16; ++k)
+                        umma_bf16_pair(d, ad + 2 * k, bd + 2 * k, idesc, (kb0 | cc | k) != 0 ? 1u : 0u);
+                }
+                umma_commit_pair(&empty[s], 3);
+            }
+            if (!ok) break;
+            umma_commit_pair(&tfull[acc], 3);
+            continue;
+        }
+        // base stages: two K-chunks each (the last stage's second may lie
+        // past K and is skipped)
+        const int nst2 = (nk + 1) / 2;
+        for (int j = 0; j < nst2; ++j, ++it) {
+            const int s = static_cast<int>(it % nst);
+            if (!mbar_wait(&full[s], static_cast<uint32_t>(it / nst) & 1u, abort_flag, p.status, lim)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const int nc = min(2, nk - 2 * j);
+            for (int cc = 0; cc < nc; ++cc) {
+                const uint32_t a_addr = smem_u32(smem + s * stb + cc * (kPairABytes / 2));
+                const uint64_t ad = umma_desc_sw128(a_addr);
+                const uint64_t bd = umma_desc_sw128(smem_u32(smem + s * stb + ab + cc * 128 * kBlockK * 2));
+#pragma unroll
+                for (int k = 0; k < kBlockK / 16; ++k)
+                    umma_bf16_pair(d, ad + 2 * k, bd + 2 * k, idesc_base, (j | cc | k) != 0 ? 1u : 0u);
+            }
+            umma_commit_pair(&empty[s], 3);
+        }
+        if (!ok) break;
+        if (p.has_lora) {
+            const int nu = pair_union_count(p, tc.b);
+            for (int i = 0; i < nu; ++i, ++it) {
+                const int s = static_cast<int>(it % nst);
+                if (!mbar_wait(&full[s], static_cast<uint32_t>(it / nst) & 1u, abort_flag, p.status, lim)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a_addr = smem_u32(smem + s * stb);
+                const uint64_t ad = umma_desc_sw128(a_addr);
+                const uint64_t bd = umma_desc_sw128(a_addr + ab);
+                for (int k = 0; k < lora_ksteps; ++k) umma_bf16_pair(d, ad + 2 * k, bd + 2 * k, idesc_base, 1u);
+                umma_commit_pair(&empty[s], 3);
+            }
+            if (!ok) break;
+        }
+        umma_commit_pair(&tfull[acc], 3);
+    }
+    // every MMA issued above (into both CTAs' tensor memory) completes
+    // before either CTA releases it
+    umma_commit_pair(drain, 1);
+    drain_wait(drain, 0, lim);
+}
+
 // Epilogue (warps 2-5): drains the TMEM accumulators, writes shrink tiles,
-// act rows or slot rows and publishes the per-block counters.
-template <bool kMx>
+// act rows or slot rows and publishes the per-block counters.  In a CTA
+// pair each CTA drains its own accumulator rows (its own block) and reports
+// the tile ring and the accumulator as read to the even CTA.
+template <bool kMx, bool kPair>
 __device__ __forceinline__ void epilogue(const Ctx& c) {
     const GemmParams& p = *c.p;
     uint64_t* const tfull = c.L.tfull;
@@ -626,7 +1078,6 @@ __device__ __forceinline__ void epilogue(const Ctx& c) {
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const long long lim = c.lim;
-    const int nblocks = c.nblocks;
     const int ns = c.ns;
     const Geom& gm = c.gm;
     const Phases& ph = c.ph;
@@ -637,16 +1088,30 @@ __device__ __forceinline__ void epilogue(const Ctx& c) {
     uint32_t npub = 0;
     for (int lt = 0;; ++lt) {
         const int ts = lt % kTileRing;
-        if (!mbar_wait(&tile_full[ts], static_cast<uint32_t>(lt / kTileRing) & 1u, abort_flag, p.status, lim)) break;
+        const uint32_t tph = static_cast<uint32_t>(lt / kTileRing) & 1u;
+        if (!(kPair ? mbar_wait_cluster(&tile_full[ts], tph, abort_flag, p.status, lim)
+                    : mbar_wait(&tile_full[ts], tph, abort_flag, p.status, lim)))
+            break;
         const long tile = tile_ring[ts];
         __syncwarp();
-        if (lane == 0) mbar_arrive(&tile_empty[ts]);
+        if (lane == 0) {
+            if (kPair)
+                mbar_arrive_cluster(mapa_shared(&tile_empty[ts], 0));
+            else
+                mbar_arrive(&tile_empty[ts]);
+        }
         if (tile < 0) break;
-        const Tile tc = decode_tile(p, gm, tile, ph, ns, nblocks);
+        const Tile tc = decode_tile(p, gm, tile, ph, ns, c.nunits, kPair ? 1 : 0, c.rank);
         const GemmSide& sd = p.side[tc.side];
         const int acc = lt & 1;
         if (!mbar_wait(&tfull[acc], static_cast<uint32_t>(lt >> 1) & 1u, abort_flag, p.status, lim)) break;
         tc_fence_after();
+        if (kPair && tc.rowless) {
+            // the odd CTA of a shrink tile: its accumulator rows are unused
+            tc_fence_before();
+            mbar_arrive_cluster(mapa_shared(&tempty[acc], 0));
+            continue;
+        }
         const uint32_t tb = tmem_base + static_cast<uint32_t>(acc * (kMx ? kMxAccCols : kAccCols)) +
                             (static_cast<uint32_t>(q * 32) << 16);
         const int prow = tc.b * kBlockM + row;
@@ -754,7 +1219,10 @@ __device__ __forceinline__ void epilogue(const Ctx& c) {
             }
         }
         tc_fence_before();
-        mbar_arrive(&tempty[acc]);
+        if (kPair)
+            mbar_arrive_cluster(mapa_shared(&tempty[acc], 0));
+        else
+            mbar_arrive(&tempty[acc]);
         if (publish) {
             // other CTAs read what this tile wrote with TMA: every thread
             // orders its writes for the async proxy and arrives
@@ -774,7 +1242,7 @@ __device__ __forceinline__ void epilogue(const Ctx& c) {
     }
 }
 
-template <bool kMx>
+template <bool kMx, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_constant__ GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -796,15 +1264,18 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
+        // a pair: the even CTA's accumulator barriers count both CTAs'
+        // epilogue threads, its tile-ring barriers the readers of both
+        // (MMA lane + 4 epilogue warps; producer + 4 epilogue warps)
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
-            mbar_init(&tempty[a], 128);
+            mbar_init(&tempty[a], kPair ? 256 : 128);
         }
         mbar_init(drain, 1);
         mbar_init(pub, 128);
         for (int r = 0; r < kTileRing; ++r) {
             mbar_init(&tile_full[r], 1);
-            mbar_init(&tile_empty[r], 1 + 4);
+            mbar_init(&tile_empty[r], kPair ? 10 : 1 + 4);
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -817,9 +1288,13 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
             if (!kMx)
                 for (int wc = 0; wc < kTileWidths; ++wc) prefetch_tensormap(&p.side[sd].tm_b[wc]);
             if (kMx) {
-                prefetch_tensormap(&p.side[sd].tm_aq);
-                prefetch_tensormap(&p.side[sd].tm_aq_full);
-                prefetch_tensormap(&p.side[sd].tm_bq);
+                prefetch_tensormap(&p.side[sd].tm_ax);
+                prefetch_tensormap(&p.side[sd].tm_ax_full);
+                prefetch_tensormap(&p.side[sd].tm_bx);
+            }
+            if (kPair && p.side[sd].K >= 2 * kBlockK) {
+                prefetch_tensormap(&p.side[sd].tm_ax_full);
+                prefetch_tensormap(&p.side[sd].tm_bx);
             }
             if (p.has_lora) {
                 prefetch_tensormap(&p.side[sd].tm_sa);
@@ -830,10 +1305,16 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
         }
     }
     if (warp == 1) {
-        tmem_alloc(tmem_holder, kTmemCols);
+        if (kPair)
+            tmem_alloc_pair(tmem_holder, kTmemCols);
+        else
+            tmem_alloc(tmem_holder, kTmemCols);
         tc_fence_before();
     }
     __syncthreads();
+    // a pair: both CTAs' barriers initialised and tensor memory allocated
+    // before either touches the other's
+    if (kPair) cluster_barrier();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
     // everything above overlapped the previous kernel in the stream
@@ -843,7 +1324,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
     // another kernel keeps waiting for an SM holds no tile that others
     // depend on), before the loads below so that the latencies overlap
     long first_tile = -1;
-    if (threadIdx.x == 0) first_tile = atomicAdd(p.tile_next, 1);
+    if (threadIdx.x == 0 && (!kPair || cluster_ctarank() == 0)) first_tile = atomicAdd(p.tile_next, 1);
     const Ctx c(p, smem, tmem_base);
     // ring geometry of this launch (the same in every CTA): when no expert
     // has more than one 32-row box of slots, A stages shrink to 4 KiB and
@@ -855,26 +1336,39 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
     constexpr uint32_t stb_f = kMx ? kMxStageBytes : kStageBytes;
     if (warp == 0) {
         if ((threadIdx.x & 31) == 0) {
-            if (small_a)
+            if constexpr (kPair)
+                producer_pair<kPairStages, kPairStageBytes, kPairABytes>(c, first_tile);
+            else if (small_a)
                 producer<nst_s, stb_s, kSmallATileBytes, kMx>(c, first_tile);
             else
                 producer<nst_f, stb_f, kATileBytes, kMx>(c, first_tile);
         }
     } else if (warp == 1) {
         if ((threadIdx.x & 31) == 0) {
-            if (small_a)
+            if constexpr (kPair) {
+                if (c.rank == 0) mma_issuer_pair<kPairStages, kPairStageBytes, kPairABytes>(c);
+            } else if (small_a) {
                 mma_issuer<nst_s, stb_s, kSmallATileBytes, kMx>(c);
-            else
+            } else {
                 mma_issuer<nst_f, stb_f, kATileBytes, kMx>(c);
+            }
         }
     } else {
-        epilogue<kMx>(c);
+        epilogue<kMx, kPair>(c);
     }
 
+    tc_fence_before();
     __syncthreads();
+    // a pair: the even CTA's MMAs into the odd CTA's tensor memory and the
+    // odd CTA's copies and arrivals on the even CTA's barriers are over
+    // before either CTA releases its tensor memory or exits
+    if (kPair) cluster_barrier();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, kTmemCols);
+        if (kPair)
+            tmem_dealloc_pair(tmem_base, kTmemCols);
+        else
+            tmem_dealloc(tmem_base, kTmemCols);
     }
 }
 
@@ -882,23 +1376,53 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
 
 cudaError_t launch_experts(const GemmParams& p, long max_tiles, cudaStream_t s) {
     if (max_tiles <= 0) return cudaSuccess;
-    static std::atomic<unsigned long long> attr_done[2];  // one bit per device (shared by host threads)
+    // per variant (bf16, MXFP8, bf16 pairs): one bit per device whose
+    // shared-memory attribute is set, and the pairs a device keeps resident
+    static std::atomic<unsigned long long> attr_done[3];
+    static std::atomic<int> resident_pairs[64];
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
-    const int v = p.mx ? 1 : 0;
+    const int v = p.pair ? 2 : p.mx ? 1 : 0;
+    void (*const kernel)(GemmParams) =
+        p.pair ? experts_kernel<false, true> : p.mx ? experts_kernel<true, false> : experts_kernel<false, false>;
     if (!(attr_done[v].load(std::memory_order_relaxed) & bit) || !bit) {
-        err = cudaFuncSetAttribute(p.mx ? experts_kernel<true> : experts_kernel<false>,
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (err != cudaSuccess) return err;
         attr_done[v].fetch_or(bit, std::memory_order_relaxed);
     }
-    long grid = device_sm_count();
+    const long sms = device_sm_count();
+    if (p.pair) {
+        // one cluster of two CTAs per pair of SMs, as many as fit at once
+        int pairs = dev >= 0 && dev < 64 ? resident_pairs[dev].load(std::memory_order_relaxed) : 0;
+        if (pairs <= 0) {
+            cudaLaunchConfig_t cfg{};
+            cfg.gridDim = dim3(static_cast<unsigned>(sms / 2 * 2));
+            cfg.blockDim = dim3(kThreads);
+            cfg.dynamicSmemBytes = kSmemBytes;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 2;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            if (cudaOccupancyMaxActiveClusters(&pairs, kernel, &cfg) != cudaSuccess || pairs <= 0) {
+                (void)cudaGetLastError();
+                pairs = static_cast<int>(sms / 2);
+            }
+            if (pairs > sms / 2) pairs = static_cast<int>(sms / 2);
+            if (pairs < 1) pairs = 1;
+            if (dev >= 0 && dev < 64) resident_pairs[dev].store(pairs, std::memory_order_relaxed);
+        }
+        long grid = 2L * pairs;
+        if (grid > 2 * max_tiles) grid = 2 * max_tiles;
+        return launch_pdl_cluster(kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads), kSmemBytes, s, 2u, p);
+    }
+    long grid = sms;
     if (grid > max_tiles) grid = max_tiles;
-    if (p.mx)
-        return launch_pdl(experts_kernel<true>, dim3(static_cast<unsigned>(grid)), dim3(kThreads), kSmemBytes, s, p);
-    return launch_pdl(experts_kernel<false>, dim3(static_cast<unsigned>(grid)), dim3(kThreads), kSmemBytes, s, p);
+    return launch_pdl(kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads), kSmemBytes, s, p);
 }
 
 }  // namespace mlora

@@ -113,6 +113,10 @@ struct Sizes {
     long max_lt;
     bool mx;          // MXFP8 expert weights
     int nkc0, nkc1;   // K-chunks of 128 of H and of I (MXFP8)
+    // CTA-pair experts tiles (pair_mode): every expert's blocks padded to
+    // an even count, so that blocks 2u and 2u+1 always share an expert;
+    // max_padded then counts padding up to 2 * kBlockM per expert
+    bool pair;
 };
 
 Sizes make_sizes(int M, int H, int I, int E_tot, int K_total, int L, int rank, bool mx = false);
@@ -140,6 +144,7 @@ struct AlignExtra {
     int32_t* gt_block;
     int32_t* gt_first;
     int32_t* gt_total;
+    int pair_pad;    // pad every expert's blocks to an even count (empty blocks: 0 rows)
 };
 
 cudaError_t launch_route(const float* logits, const float* bias, int M, int E, int top_k, int scoring,
@@ -178,7 +183,10 @@ struct alignas(128) GemmSide {
     CUtensorMap tm_a;       // token rows [rows, K] (x in sorted order / act), box {64, kRowBox}
     CUtensorMap tm_a_full;  // the same with box {64, 128}: one box per full block
     // weight rows: w13 view {H, I, 2, E_tot} / w2 view {I, H, E_tot}, one
-    // map per tile width (256, 192, 128 weight rows; gate_up boxes take half)
+    // map per tile width (256, 192, 128 weight rows; a gate_up box takes
+    // half the rows from the gate and half from the up half, gate first).
+    // A CTA-pair launch (256-row tiles only) holds the 128-row box of one
+    // gate_up half in width class 1's slot, here and in tm_lb.
     CUtensorMap tm_b[kTileWidths];
     CUtensorMap tm_sa;      // LoRA shrink weights: A13 / A2 view {K, rank, L*E_tot}
     // LoRA expand weights: B13 view {rank, I, 2, L*E_tot} / B2 view {rank, H, L*E_tot},
@@ -186,13 +194,20 @@ struct alignas(128) GemmSide {
     CUtensorMap tm_lb[kTileWidths];
     CUtensorMap tm_t;       // this side's LoRA tiles [tiles*128, 64], box {64, kRowBox}
     CUtensorMap tm_t_full;  // box {64, 128}
-    // MXFP8 layer only: E4M3 token rows (x codes / act codes [rows, K]),
-    // box {128, kRowBox} and {128, 128}; E4M3 weight rows (w13 codes view
-    // {H, I, 2, E_tot}, box {128, 96, 1, 1} / w2 codes {I, H, E_tot}, box
-    // {128, 192, 1})
-    CUtensorMap tm_aq;
-    CUtensorMap tm_aq_full;
-    CUtensorMap tm_bq;
+    // Maps of the launch kind.  MXFP8 layer: E4M3 token rows (x codes / act
+    // codes [rows, K]), box {128, kRowBox} (tm_ax) and {128, 128}
+    // (tm_ax_full); E4M3 weight rows (tm_bx: w13 codes view {H, I, 2,
+    // E_tot}, box {128, 96, 2, 1} / w2 codes {I, H, E_tot}, box {128, 192,
+    // 1}).  CTA-pair launch (bf16): two K-chunks of 64 per copy -- token rows
+    // viewed as {64, rows, K/64} (chunk stride 128 B), box {64, 128, 2}
+    // (tm_ax_full), and one CTA's half of a weight slab, w13 viewed as {64,
+    // I, 2, E_tot, H/64}, box {64, 128, 1, 1, 2} / w2 as {64, H, E_tot,
+    // I/64}, box {64, 128, 1, 2} (tm_bx); both land as [chunk][row][64].
+    // A view covers only the whole chunks of K (a partial last chunk is
+    // loaded with the 2D maps).
+    CUtensorMap tm_ax;
+    CUtensorMap tm_ax_full;
+    CUtensorMap tm_bx;
     const uint8_t* a_scales;  // token-row scale atoms [max_blocks][nkc][512]
     const uint8_t* b_scales;  // packed weight scales [E_tot][slabs][nkc][1024]
     uint8_t* out_q;           // gate_up side: act codes [rows, I]
@@ -234,6 +249,7 @@ struct alignas(128) GemmParams {
     int S;              // sentinel slot value M*K'
     int has_lora;
     int mx;             // MXFP8 expert weights (fixed 192-row tiles)
+    int pair;           // CTA-pair tiles over blocks (2u, 2u+1): clusters of 2, 256-row MMAs
     // tuned tile width class per block-count bucket (-1: the rule, choose_width)
     int8_t width_table[kWidthBuckets];
     float scaling;
@@ -255,6 +271,10 @@ cudaError_t launch_mx_gather(const void* x, int H, int K_total, const int32_t* s
 
 int device_sm_count();
 
+// Whether a bf16 layer runs its experts kernel as CTA pairs: only when the
+// calling thread asked for it (mlora_set_pair_mode); the MXFP8 layer never.
+bool use_pair_mode(bool mx);
+
 // Launch with programmatic stream serialisation (see griddep_wait in ptx.cuh).
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
@@ -269,6 +289,27 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// The same as clusters of `cluster` CTAs along x (grid.x a multiple of it).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                               unsigned cluster, Args&&... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 

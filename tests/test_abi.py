@@ -157,6 +157,28 @@ def test_tile_config_rule_and_hook(lib):
     assert lib.mlora_set_tile_config(0, 5) == 1
 
 
+def test_pair_mode_switch_and_workspace(lib):
+    """Pair mode is off unless the thread turns it on; while on, the bf16
+    workspace holds padding up to two blocks per expert (the MXFP8 layer
+    never pairs)."""
+    assert not ml.mlora_pair_mode()
+    args = (64, 2880, 2880, 32, 4, 8, 16)
+    plain = ml.mlora_moe_workspace_size(*args)
+    mx = ml.mlora_moe_workspace_size_mxfp8(*args)
+    try:
+        ml.mlora_set_pair_mode(True)
+        assert ml.mlora_pair_mode()
+        # up to 255 padding rows per expert instead of 127
+        assert ml.mlora_moe_workspace_size(*args) > plain
+        assert ml.mlora_moe_workspace_size_mxfp8(*args) == mx
+    finally:
+        ml.mlora_set_pair_mode(False)
+    assert not ml.mlora_pair_mode()
+    assert ml.mlora_moe_workspace_size(*args) == plain
+    assert lib.mlora_set_pair_mode(2) == 1
+    assert lib.mlora_set_pair_mode(-1) == 1
+
+
 def test_tuned_table_rows_are_valid():
     """Every row of the compiled-in tuned table names width classes in
     range (or -1) and a group size the rank allows; the library reports the

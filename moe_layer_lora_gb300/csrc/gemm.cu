@@ -44,10 +44,11 @@
 // the down GEMM fills the gate_up tail.  (The pages overlap the shrink and
 // expand kernels with PDL; here they share one grid.)
 //
-// Roles (192 threads): warp 0 issues TMA loads into a ring of smem stages
-// (A tile 128 x 64 bf16: one 128-row box for a full block, 32-row boxes
-// covering only the real rows of a partial one; B tile 256 x 64 bf16; both
-// K-major with 128-byte swizzle); warp 1 allocates TMEM and one lane issues
+// Roles (224 threads): warps 0 and 6 issue TMA loads into a ring of smem
+// stages, warp 0 the weight operand (B tile 256 x 64 bf16) and warp 6 the
+// token rows (A tile 128 x 64 bf16: one 128-row box for a full block,
+// 32-row boxes covering only the real rows of a partial one; both K-major
+// with 128-byte swizzle); warp 1 allocates TMEM and one lane issues
 // tcgen05.mma (M = 128, K = 16 per instruction, fp32 accumulate) and
 // tcgen05.commit; warps 2..5 drain the double-buffered TMEM accumulator with
 // tcgen05.ld while the next tile's MMAs run.  Grid: at most one CTA per SM.
@@ -63,7 +64,9 @@
 namespace mlora {
 namespace {
 
-constexpr int kThreads = 192;
+// 9 warps: weight producer (even stages, tiles), MMA, 4 epilogue, row
+// producer (even stages), weight producer (odd), row producer (odd)
+constexpr int kThreads = 288;
 constexpr int kBN = 256;                                         // weight rows per wide tile (MMA N)
 // The shared-memory ring: 4 stages of 48 KiB (A 16 KiB + B 32 KiB); when
 // no block has more than 32 real rows (decode-like batches) the A part of a
@@ -314,11 +317,27 @@ struct Ctx {
     }
 };
 
-// TMA producer (one thread): claims tiles, hands them on through the tile
-// ring and streams their operands into a ring of nst stages of stb bytes,
-// the first ab of each holding A rows.
-template <int nst, uint32_t stb, uint32_t ab, bool kMx>
-__device__ __forceinline__ void producer(const Ctx& c, long first_tile) {
+// TMA producers, four threads in four warps over one ring of nst stages of
+// stb bytes (the first ab of each holding A rows).  An issuing thread
+// stalls for a while on every TMA copy it issues (a streaming probe: two
+// copies a stage from one thread take ~600 ns, from two threads ~330 ns),
+// so each stage's two operands come from two threads, and each operand's
+// stages alternate between two threads (`par`: the stages it issues, by the
+// parity of the stage count):
+//  * the weight producer (kRows = false; warp 0) claims the tiles, hands
+//    them to the other roles through the tile ring and streams each
+//    stage's weight operand (B): expert weight rows, the adapters' B rows
+//    of the expand stages, the adapters' A rows of the shrink stages;
+//  * the row producer (kRows = true; warp 6) reads the tiles from the ring,
+//    waits for the rows' producers (a down-side tile for the block's act
+//    rows, an expand for the block's shrink tiles) and streams the
+//    token-row operand (A): x or act rows, the LoRA tiles of the expands.
+// Each announces its own bytes on the stage's full barrier (two arrivals),
+// so the weight stream runs ahead of the row stream's waits by up to the
+// ring's depth.  Only the even weight producer claims and hands out tiles;
+// the other three read them from the ring.
+template <int nst, uint32_t stb, uint32_t ab, bool kMx, bool kRows>
+__device__ __forceinline__ void producer(const Ctx& c, long first_tile, int par) {
     const GemmParams& p = *c.p;
     uint64_t* const full = c.L.full;
     uint64_t* const empty = c.L.empty;
@@ -341,24 +360,42 @@ __device__ __forceinline__ void producer(const Ctx& c, long first_tile) {
     // claim at the start of a tile hands work to CTAs that will be busy
     // for a whole tile while others idle), early enough that the atomic's
     // latency hides behind the last loads
+    const bool master = !kRows && par == 0;
     auto claim = [&]() {
-        if (next < 0) next = atomicAdd(p.tile_next, 1);
+        if (master && next < 0) next = atomicAdd(p.tile_next, 1);
+    };
+    // whether this thread issues stage `it`
+    auto mine = [&]() { return static_cast<int>(it & 1) == par; };
+    // waits for the next free stage; false after an abort
+    auto stage_free = [&](int s) {
+        return mbar_wait(&empty[s], (static_cast<uint32_t>(it / nst) & 1u) ^ 1u, abort_flag, p.status, lim);
     };
     // test hook: a wait on a flag that nothing sets, which must end
     // in a reported timeout and a clean exit
-    if (p.stall_flag && !wait_counter(p.stall_flag, 1, abort_flag, p.status, lim)) ok = false;
+    if (master && p.stall_flag && !wait_counter(p.stall_flag, 1, abort_flag, p.status, lim)) ok = false;
     for (int jt = 0; ok; ++jt, tile = next, next = -1) {
-        // hand the tile (or the end mark) to the MMA lane and the epilogue
         const int ts = jt % kTileRing;
-        if (!mbar_wait(&tile_empty[ts], (static_cast<uint32_t>(jt / kTileRing) & 1u) ^ 1u, abort_flag,
-                       p.status, lim)) {
-            ok = false;
-            break;
+        const uint32_t tph = static_cast<uint32_t>(jt / kTileRing) & 1u;
+        if (master) {
+            // hand the tile (or the end mark) to the row producer, the MMA
+            // lane and the epilogue
+            if (!mbar_wait(&tile_empty[ts], tph ^ 1u, abort_flag, p.status, lim)) {
+                ok = false;
+                break;
+            }
+            const bool have = tile >= 0 && tile < ntiles;
+            tile_ring[ts] = have ? tile : -1;
+            mbar_arrive(&tile_full[ts]);
+            if (!have) break;
+        } else {
+            if (!mbar_wait(&tile_full[ts], tph, abort_flag, p.status, lim)) {
+                ok = false;
+                break;
+            }
+            tile = tile_ring[ts];
+            mbar_arrive(&tile_empty[ts]);
+            if (tile < 0) break;
         }
-        const bool have = tile >= 0 && tile < ntiles;
-        tile_ring[ts] = have ? tile : -1;
-        mbar_arrive(&tile_full[ts]);
-        if (!have) break;
         const Tile tc = decode_tile(p, gm, tile, ph, ns, c.nunits, 0, 0u);
         const GemmSide& sd = p.side[tc.side];
         const int row0 = tc.b * kBlockM;
@@ -371,76 +408,11 @@ __device__ __forceinline__ void producer(const Ctx& c, long first_tile) {
         const int nk = (sd.K + kBlockK - 1) / kBlockK;
         // base tiles of the MXFP8 layer: K-chunks of 128 E4M3
         const int nk_base = kMx ? sd.nkc : nk;
-        const CUtensorMap* bmap = &sd.tm_b[gm.wc];
-        const CUtensorMap* lbmap = &sd.tm_lb[gm.wc];
-        // a base stage: the tile's weight rows of K-chunk kb (B; in the
-        // MXFP8 layer E4M3 rows of 128 bytes, then the chunk's packed
-        // weight scales) and the block's token rows (A; MXFP8: then the
-        // chunk's scale atom of the activations)
-        const long ncb = tc.side ? gm.ncb1 : gm.ncb0;
-        const uint8_t* b_scales = kMx ? sd.b_scales + (static_cast<size_t>(tc.e) * ncb + tc.cb) * sd.nkc * kMxTileScaleBytes
-                                      : nullptr;
-        const uint32_t b_stage = kMx ? gm.bn * kMxChunk + kMxTileScaleBytes : gm.bn * kBlockK * 2;
-        const uint32_t a_stage = kMx ? a_bytes + kMxAtom : a_bytes;
-        auto load_b = [&](int s, int kb) {
-            uint8_t* sb = smem + s * stb + ab;
-            const CUtensorMap* map = kMx ? &sd.tm_bx : bmap;
-            const int k0 = kb * (kMx ? kMxChunk : kBlockK);
-            if (tc.kind == kGateUp) {
-                // one box over the slab's gate rows and then its up rows
-                tma_load_4d(sb, map, &full[s], k0, tc.cb * gm.half, 0, tc.e);
-            } else {
-                tma_load_3d(sb, map, &full[s], k0, tc.cb * gm.bn, tc.e);
-            }
-            if (kMx)
-                bulk_load(sb + kMxBBytes + kMxAtom, b_scales + static_cast<size_t>(kb) * kMxTileScaleBytes,
-                          kMxTileScaleBytes, &full[s]);
-        };
-        auto load_a = [&](int s, int kb) {
-            uint8_t* sa = smem + s * stb;
-            const int k0 = kb * (kMx ? kMxChunk : kBlockK);
-            const CUtensorMap* full_map = kMx ? &sd.tm_ax_full : &sd.tm_a_full;
-            const CUtensorMap* box_map = kMx ? &sd.tm_ax : &sd.tm_a;
-            if (full_block)
-                tma_load_2d(sa, full_map, &full[s], k0, row0);
-            else
-                for (int i = 0; i < nbox; ++i)
-                    tma_load_2d(sa + i * kRowBox * 128, box_map, &full[s], k0, row0 + i * kRowBox);
-            if (kMx)
-                bulk_load(sa + ab + kMxBBytes, sd.a_scales + (static_cast<size_t>(tc.b) * sd.nkc + kb) * kMxAtom, kMxAtom,
-                          &full[s]);
-        };
-        // stages whose weight rows went out before the act wait below
-        int pre = 0;
-        if (tc.side == 1) {
-            // the down side reads act rows, complete once the block's
-            // gate_up tiles all are; the weight rows do not depend on
-            // them, so while the block's last gate_up tiles finish, the
-            // first stages' weight rows stream into the ring (an L2
-            // prefetch of the rest measured slower: prefetches ahead of
-            // the ring cut the stream rate of every SM by a quarter)
-            const int32_t* act_done = p.act_done + tc.b;
-            if (!tc.shrink && !counter_reached(act_done, gm.ncb0)) {
-                const int npre = min(nk_base, nst);
-                for (; pre < npre; ++pre) {
-                    const long j = it + pre;
-                    const int s = static_cast<int>(j % nst);
-                    if (!mbar_wait(&empty[s], (static_cast<uint32_t>(j / nst) & 1u) ^ 1u, abort_flag, p.status, lim)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_expect_tx(&full[s], b_stage);
-                    load_b(s, pre);
-                }
-            }
-            if (ok && !wait_counter(act_done, gm.ncb0, abort_flag, p.status, lim)) ok = false;
-            if (!ok) {
-                // the stages armed above complete once their weight rows
-                // land, so the drain below finds every issued copy
-                for (int q = 0; q < pre; ++q) mbar_arrive(&full[(it + q) % nst]);
-                it += pre;
-                break;
-            }
+        // the down side reads act rows, complete once the block's gate_up
+        // tiles all are (the weight rows do not depend on them)
+        if (kRows && tc.side == 1 && !wait_counter(p.act_done + tc.b, gm.ncb0, abort_flag, p.status, lim)) {
+            ok = false;
+            break;
         }
         if (tc.shrink) {
             // several K-chunks per stage: the shrink's operands are
@@ -451,85 +423,116 @@ __device__ __forceinline__ void producer(const Ctx& c, long first_tile) {
             const int cps = shrink_chunks(a_bytes, b_bytes, stb);
             for (int kb0 = 0; kb0 < nk; kb0 += cps, ++it) {
                 const int s = static_cast<int>(it % nst);
-                const uint32_t phs = static_cast<uint32_t>(it / nst) & 1u;
-                if (!mbar_wait(&empty[s], phs ^ 1u, abort_flag, p.status, lim)) {
+                const int nc = min(cps, nk - kb0);
+                if (kb0 + nc >= nk) claim();
+                if (!mine()) continue;
+                if (!stage_free(s)) {
                     ok = false;
                     break;
                 }
-                const int nc = min(cps, nk - kb0);
-                if (kb0 + nc >= nk) claim();
-                mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(nc) * chunk);
-                for (int c = 0; c < nc; ++c) {
-                    uint8_t* ca = smem + s * stb + c * chunk;
-                    uint8_t* cb = ca + a_bytes;
-                    const int k0 = (kb0 + c) * kBlockK;
-                    for (int i = 0; i < tc.g; ++i)
-                        tma_load_3d(cb + i * rp * kBlockK * 2, &sd.tm_sa, &full[s], k0, 0,
-                                    lora_list[tc.i0 + i] * p.E_tot + tc.e);
-                    if (full_block)
+                mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(nc) * (kRows ? a_bytes : b_bytes));
+                for (int cc = 0; cc < nc; ++cc) {
+                    uint8_t* ca = smem + s * stb + cc * chunk;
+                    const int k0 = (kb0 + cc) * kBlockK;
+                    if (!kRows) {
+                        for (int i = 0; i < tc.g; ++i)
+                            tma_load_3d(ca + a_bytes + i * rp * kBlockK * 2, &sd.tm_sa, &full[s], k0, 0,
+                                        lora_list[tc.i0 + i] * p.E_tot + tc.e);
+                    } else if (full_block) {
                         tma_load_2d(ca, &sd.tm_a_full, &full[s], k0, row0);
-                    else
+                    } else {
                         for (int i = 0; i < nbox; ++i)
-                            tma_load_2d(ca + i * kRowBox * kBlockK * 2, &sd.tm_a, &full[s], k0,
-                                        row0 + i * kRowBox);
+                            tma_load_2d(ca + i * kRowBox * kBlockK * 2, &sd.tm_a, &full[s], k0, row0 + i * kRowBox);
+                    }
                 }
             }
             continue;
         }
+        // a base stage: the tile's weight rows of K-chunk kb (B; in the
+        // MXFP8 layer E4M3 rows of 128 bytes, then the chunk's packed
+        // weight scales) and the block's token rows (A; MXFP8: then the
+        // chunk's scale atom of the activations)
         for (int kb = 0; kb < nk_base; ++kb, ++it) {
             const int s = static_cast<int>(it % nst);
-            const uint32_t phs = static_cast<uint32_t>(it / nst) & 1u;
-            if (kb >= pre && !mbar_wait(&empty[s], phs ^ 1u, abort_flag, p.status, lim)) {
+            if (kb + 3 >= nk_base) claim();
+            if (!mine()) continue;
+            if (!stage_free(s)) {
                 ok = false;
                 break;
             }
-            if (kb + 3 >= nk_base) claim();
-            if (kb < pre) {
-                mbar_arrive_expect_tx(&full[s], a_stage);
+            const int k0 = kb * (kMx ? kMxChunk : kBlockK);
+            if (!kRows) {
+                uint8_t* sb = smem + s * stb + ab;
+                const CUtensorMap* map = kMx ? &sd.tm_bx : &sd.tm_b[gm.wc];
+                mbar_arrive_expect_tx(&full[s], kMx ? gm.bn * kMxChunk + kMxTileScaleBytes : gm.bn * kBlockK * 2);
+                if (tc.kind == kGateUp)
+                    // one box over the slab's gate rows and then its up rows
+                    tma_load_4d(sb, map, &full[s], k0, tc.cb * gm.half, 0, tc.e);
+                else
+                    tma_load_3d(sb, map, &full[s], k0, tc.cb * gm.bn, tc.e);
+                if (kMx) {
+                    const long ncb = tc.side ? gm.ncb1 : gm.ncb0;
+                    bulk_load(sb + kMxBBytes + kMxAtom,
+                              sd.b_scales + ((static_cast<size_t>(tc.e) * ncb + tc.cb) * sd.nkc + kb) * kMxTileScaleBytes,
+                              kMxTileScaleBytes, &full[s]);
+                }
             } else {
-                mbar_arrive_expect_tx(&full[s], a_stage + b_stage);
-                load_b(s, kb);
+                uint8_t* sa = smem + s * stb;
+                mbar_arrive_expect_tx(&full[s], kMx ? a_bytes + kMxAtom : a_bytes);
+                const CUtensorMap* full_map = kMx ? &sd.tm_ax_full : &sd.tm_a_full;
+                const CUtensorMap* box_map = kMx ? &sd.tm_ax : &sd.tm_a;
+                if (full_block)
+                    tma_load_2d(sa, full_map, &full[s], k0, row0);
+                else
+                    for (int i = 0; i < nbox; ++i)
+                        tma_load_2d(sa + i * kRowBox * 128, box_map, &full[s], k0, row0 + i * kRowBox);
+                if (kMx)
+                    bulk_load(sa + ab + kMxBBytes, sd.a_scales + (static_cast<size_t>(tc.b) * sd.nkc + kb) * kMxAtom,
+                              kMxAtom, &full[s]);
             }
-            load_a(s, kb);
         }
-
         if (!ok || !p.has_lora) continue;
         const int nad = p.blk_nad[tc.b];
         if (nad == 0) continue;
         // the expand needs every shrink tile of this block and side
-        if (!wait_counter(sd.done + tc.b, (nad + p.gsize - 1) / p.gsize, abort_flag, p.status, lim)) {
+        if (kRows && !wait_counter(sd.done + tc.b, (nad + p.gsize - 1) / p.gsize, abort_flag, p.status, lim)) {
             ok = false;
             break;
         }
         const int lt0 = p.blk_lt_start[tc.b];
         for (int i = 0; i < nad; ++i, ++it) {
             const int s = static_cast<int>(it % nst);
-            const uint32_t phs = static_cast<uint32_t>(it / nst) & 1u;
-            if (!mbar_wait(&empty[s], phs ^ 1u, abort_flag, p.status, lim)) {
+            if (!mine()) continue;
+            if (!stage_free(s)) {
                 ok = false;
                 break;
             }
             uint8_t* sa = smem + s * stb;
-            uint8_t* sb = sa + ab;
-            const int le = lora_list[i] * p.E_tot + tc.e;
-            mbar_arrive_expect_tx(&full[s], a_bytes + gm.bn * kBlockK * 2);
-            if (tc.kind == kGateUp) {
-                tma_load_4d(sb, lbmap, &full[s], 0, tc.cb * gm.half, 0, le);
+            if (!kRows) {
+                const int le = lora_list[i] * p.E_tot + tc.e;
+                const CUtensorMap* lbmap = &sd.tm_lb[gm.wc];
+                mbar_arrive_expect_tx(&full[s], gm.bn * kBlockK * 2);
+                if (tc.kind == kGateUp)
+                    tma_load_4d(sa + ab, lbmap, &full[s], 0, tc.cb * gm.half, 0, le);
+                else
+                    tma_load_3d(sa + ab, lbmap, &full[s], 0, tc.cb * gm.bn, le);
             } else {
-                tma_load_3d(sb, lbmap, &full[s], 0, tc.cb * gm.bn, le);
+                mbar_arrive_expect_tx(&full[s], a_bytes);
+                if (full_block)
+                    tma_load_2d(sa, &sd.tm_t_full, &full[s], 0, (lt0 + i) * kBlockM);
+                else
+                    for (int j = 0; j < nbox; ++j)
+                        tma_load_2d(sa + j * kRowBox * kBlockK * 2, &sd.tm_t, &full[s], 0,
+                                    (lt0 + i) * kBlockM + j * kRowBox);
             }
-            if (full_block)
-                tma_load_2d(sa, &sd.tm_t_full, &full[s], 0, (lt0 + i) * kBlockM);
-            else
-                for (int j = 0; j < nbox; ++j)
-                    tma_load_2d(sa + j * kRowBox * kBlockK * 2, &sd.tm_t, &full[s], 0,
-                                (lt0 + i) * kBlockM + j * kRowBox);
         }
     }
     if (!ok) {
-        // the last min(it, nst) stages issued, walking back from the ring position
+        // this thread's stages among the last min(it, nst), walking back
+        // from the ring position (a stage whose other operand never went
+        // out ends the bounded wait)
         for (long j = it > nst ? it - nst : 0; j < it; ++j)
-            drain_wait(&full[j % nst], static_cast<uint32_t>(j / nst) & 1u, lim);
+            if (static_cast<int>(j & 1) == par) drain_wait(&full[j % nst], static_cast<uint32_t>(j / nst) & 1u, lim);
     }
 }
 
@@ -1260,13 +1263,16 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
 
     const int warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
+        // a stage is full once both producers' copies landed (a pair: the
+        // even CTA's one arrival counts both CTAs' bytes)
         for (int s = 0; s < kMaxStages; ++s) {
-            mbar_init(&full[s], 1);
+            mbar_init(&full[s], kPair ? 1 : 2);
             mbar_init(&empty[s], 1);
         }
         // a pair: the even CTA's accumulator barriers count both CTAs'
         // epilogue threads, its tile-ring barriers the readers of both
-        // (MMA lane + 4 epilogue warps; producer + 4 epilogue warps)
+        // (MMA lane + 4 epilogue warps; producer + 4 epilogue warps); one
+        // CTA: MMA lane, 4 epilogue warps and three producers
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
             mbar_init(&tempty[a], kPair ? 256 : 128);
@@ -1275,7 +1281,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
         mbar_init(pub, 128);
         for (int r = 0; r < kTileRing; ++r) {
             mbar_init(&tile_full[r], 1);
-            mbar_init(&tile_empty[r], kPair ? 10 : 1 + 4);
+            mbar_init(&tile_empty[r], kPair ? 10 : 1 + 4 + 3);
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -1334,14 +1340,27 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
     constexpr int nst_s = kMx ? kMxSmallStages : kSmallStages, nst_f = kMx ? kMxStages : kStages;
     constexpr uint32_t stb_s = kMx ? kMxSmallStageBytes : kSmallStageBytes;
     constexpr uint32_t stb_f = kMx ? kMxStageBytes : kStageBytes;
-    if (warp == 0) {
+    if (warp == 0 || warp >= 6) {
         if ((threadIdx.x & 31) == 0) {
-            if constexpr (kPair)
-                producer_pair<kPairStages, kPairStageBytes, kPairABytes>(c, first_tile);
-            else if (small_a)
-                producer<nst_s, stb_s, kSmallATileBytes, kMx>(c, first_tile);
-            else
-                producer<nst_f, stb_f, kATileBytes, kMx>(c, first_tile);
+            if constexpr (kPair) {
+                if (warp == 0) producer_pair<kPairStages, kPairStageBytes, kPairABytes>(c, first_tile);
+            } else {
+                // warps 0 / 7: weight operand, even / odd stages; 6 / 8: rows
+                const bool rows = warp == 6 || warp == 8;
+                const int par = warp >= 7 ? 1 : 0;
+                const long ft = warp == 0 ? first_tile : -1;
+                if (small_a) {
+                    if (rows)
+                        producer<nst_s, stb_s, kSmallATileBytes, kMx, true>(c, ft, par);
+                    else
+                        producer<nst_s, stb_s, kSmallATileBytes, kMx, false>(c, ft, par);
+                } else {
+                    if (rows)
+                        producer<nst_f, stb_f, kATileBytes, kMx, true>(c, ft, par);
+                    else
+                        producer<nst_f, stb_f, kATileBytes, kMx, false>(c, ft, par);
+                }
+            }
         }
     } else if (warp == 1) {
         if ((threadIdx.x & 31) == 0) {

@@ -145,13 +145,6 @@ __device__ bool wait_counter(const int32_t* flag, int target, volatile int* abor
     }
 }
 
-// One look at a counter, no ordering: whether a wait on it would pass now.
-__device__ __forceinline__ bool counter_reached(const int32_t* flag, int target) {
-    int v;
-    asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
-    return v >= target;
-}
-
 struct Tile {
     int kind;
     int side;  // 0: gate_up projection, 1: down projection
@@ -364,7 +357,11 @@ __device__ __forceinline__ void producer(const Ctx& c, long first_tile, int par)
     auto claim = [&]() {
         if (master && next < 0) next = atomicAdd(p.tile_next, 1);
     };
-    // whether this thread issues stage `it`
+    // whether this thread issues stage `it`.  It skips the other parity's
+    // stages without waiting on them: its own wait two stages back (for
+    // stage it - 2 - nst) already keeps it less than a ring cycle ahead of
+    // the MMA lane, so a parity wait on a slot always refers to the slot's
+    // latest use (nst >= 2)
     auto mine = [&]() { return static_cast<int>(it & 1) == par; };
     // waits for the next free stage; false after an abort
     auto stage_free = [&](int s) {
@@ -696,18 +693,23 @@ __device__ __forceinline__ int pair_union_count(const GemmParams& p, int b0) {
     return n;
 }
 
-// TMA producer of a CTA pair (one thread in each CTA).  The even CTA claims
-// the tiles and hands each to the rings of both CTAs.  Each CTA streams its
-// own block's token rows (A) and its 128 of the tile's 256 weight rows (B:
-// the gate rows of a gate_up slab in the even CTA, the up rows in the odd
-// one; the first or second half of a down slab) into its own stage ring;
-// every copy completes on the even CTA's stage barrier, whose one arrival
-// (the even CTA's) announces the bytes of both.  Shrink tiles: the even CTA
-// holds the block's rows, the adapters' rank rows are split between the two
-// (a group of odd size gets a zero adapter in the odd CTA).  Expand stages
-// run over the union of the two blocks' adapters; a block without the
-// stage's adapter loads zero rows (a box at a negative row reads as zero).
-template <int nst, uint32_t stb, uint32_t ab>
+// TMA producers of a CTA pair: in each CTA a weight producer (kRows =
+// false; warp 0) and a row producer (kRows = true; warp 6), as in the
+// one-CTA kernel.  The even CTA's weight producer claims the tiles and
+// hands each to the rings of both CTAs.  Each CTA streams its own block's
+// token rows (A) and its 128 of the tile's 256 weight rows (B: the gate
+// rows of a gate_up slab in the even CTA, the up rows in the odd one; the
+// first or second half of a down slab) into its own stage ring; every copy
+// completes on the even CTA's stage barrier, on which all four producers
+// arrive (the odd CTA's remotely), each announcing its own bytes before it
+// issues them -- so that the barrier's transaction count never runs below
+// zero, whichever CTA's copies land first.  Shrink
+// tiles: the even CTA holds the block's rows, the adapters' rank rows are
+// split between the two (a group of odd size gets a zero adapter in the odd
+// CTA).  Expand stages run over the union of the two blocks' adapters; a
+// block without the stage's adapter loads zero rows (a box at a negative
+// row reads as zero).
+template <int nst, uint32_t stb, uint32_t ab, bool kRows>
 __device__ __forceinline__ void producer_pair(const Ctx& c, long first_tile) {
     const GemmParams& p = *c.p;
     uint64_t* const full = c.L.full;
@@ -723,17 +725,29 @@ __device__ __forceinline__ void producer_pair(const Ctx& c, long first_tile) {
     uint8_t* const smem = c.smem;
     const uint32_t rank = c.rank;
     const bool lead = rank == 0;
-    long it = 0;  // stages issued
+    const bool master = lead && !kRows;
+    constexpr uint32_t kChunkB = 128 * kBlockK * 2;  // a CTA's weight rows of one K-chunk
+    long it = 0;  // stages passed
     bool ok = true;
     long tile = first_tile, next = -1;
     auto claim = [&]() {
-        if (lead && next < 0) next = atomicAdd(p.tile_next, 1);
+        if (master && next < 0) next = atomicAdd(p.tile_next, 1);
     };
-    if (p.stall_flag && !wait_counter(p.stall_flag, 1, abort_flag, p.status, lim)) ok = false;
+    auto stage_free = [&](int s) {
+        return mbar_wait(&empty[s], (static_cast<uint32_t>(it / nst) & 1u) ^ 1u, abort_flag, p.status, lim);
+    };
+    // this producer's arrival on stage s of the even CTA, with its bytes
+    auto arrive_stage = [&](int s, uint32_t fb, uint32_t bytes) {
+        if (lead)
+            mbar_arrive_expect_tx(&full[s], bytes);
+        else
+            mbar_arrive_expect_tx_cluster(fb, bytes);
+    };
+    if (master && p.stall_flag && !wait_counter(p.stall_flag, 1, abort_flag, p.status, lim)) ok = false;
     for (int jt = 0; ok; ++jt, tile = next, next = -1) {
         const int ts = jt % kTileRing;
         const uint32_t tph = static_cast<uint32_t>(jt / kTileRing) & 1u;
-        if (lead) {
+        if (master) {
             // the slot is free once its readers in both CTAs arrived
             if (!mbar_wait_cluster(&tile_empty[ts], tph ^ 1u, abort_flag, p.status, lim)) {
                 ok = false;
@@ -761,7 +775,8 @@ __device__ __forceinline__ void producer_pair(const Ctx& c, long first_tile) {
         const int32_t* lora_list = p.blk_lora + static_cast<long>(tc.b) * p.cap;
         if (tc.shrink) {
             // the down shrink reads act rows (the even CTA's)
-            if (tc.side == 1 && lead && !wait_counter(p.act_done + tc.b, gm.ncb0, abort_flag, p.status, lim)) {
+            if (kRows && lead && tc.side == 1 &&
+                !wait_counter(p.act_done + tc.b, gm.ncb0, abort_flag, p.status, lim)) {
                 ok = false;
                 break;
             }
@@ -775,29 +790,34 @@ __device__ __forceinline__ void producer_pair(const Ctx& c, long first_tile) {
             const int cps = shrink_chunks(a0, bh, stb);
             for (int kb0 = 0; kb0 < nk; kb0 += cps, ++it) {
                 const int s = static_cast<int>(it % nst);
-                if (!mbar_wait(&empty[s], (static_cast<uint32_t>(it / nst) & 1u) ^ 1u, abort_flag, p.status, lim)) {
+                const int nc = min(cps, nk - kb0);
+                if (kb0 + nc >= nk) claim();
+                // every producer waits for every stage it passes, so that
+                // it never runs a whole ring ahead of the MMA lane (a parity
+                // wait cannot tell a phase two behind from a finished one)
+                if (!stage_free(s)) {
                     ok = false;
                     break;
                 }
-                const int nc = min(cps, nk - kb0);
-                if (kb0 + nc >= nk) claim();
-                if (lead) mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(nc) * (a0 + 2 * bh));
                 const uint32_t fb = mapa_shared(&full[s], 0);
+                // (the odd CTA holds no rows of a shrink tile)
+                arrive_stage(s, fb, kRows ? (lead ? static_cast<uint32_t>(nc) * a0 : 0u)
+                                                        : static_cast<uint32_t>(nc) * bh);
+                if (kRows && !lead) continue;
                 for (int cc = 0; cc < nc; ++cc) {
                     uint8_t* ca = smem + s * stb + cc * chunk;
                     const int k0 = (kb0 + cc) * kBlockK;
-                    for (int i = 0; i < g2; ++i) {
-                        const int ai = static_cast<int>(rank) * g2 + i;
-                        const int le = ai < tc.g ? lora_list[tc.i0 + ai] * p.E_tot + tc.e : -1;
-                        tma_load_3d_pair(ca + a0 + i * rp * kBlockK * 2, &sd.tm_sa, fb, k0, 0, le);
-                    }
-                    if (lead) {
-                        if (full_block)
-                            tma_load_2d_pair(ca, &sd.tm_a_full, fb, k0, row0);
-                        else
-                            for (int i = 0; i < nbox; ++i)
-                                tma_load_2d_pair(ca + i * kRowBox * kBlockK * 2, &sd.tm_a, fb, k0,
-                                                 row0 + i * kRowBox);
+                    if (!kRows) {
+                        for (int i = 0; i < g2; ++i) {
+                            const int ai = static_cast<int>(rank) * g2 + i;
+                            const int le = ai < tc.g ? lora_list[tc.i0 + ai] * p.E_tot + tc.e : -1;
+                            tma_load_3d_pair(ca + a0 + i * rp * kBlockK * 2, &sd.tm_sa, fb, k0, 0, le);
+                        }
+                    } else if (full_block) {
+                        tma_load_2d_pair(ca, &sd.tm_a_full, fb, k0, row0);
+                    } else {
+                        for (int i = 0; i < nbox; ++i)
+                            tma_load_2d_pair(ca + i * kRowBox * kBlockK * 2, &sd.tm_a, fb, k0, row0 + i * kRowBox);
                     }
                 }
             }
@@ -805,9 +825,6 @@ __device__ __forceinline__ void producer_pair(const Ctx& c, long first_tile) {
         }
         const int b0 = tc.b & ~1;  // the pair's blocks: b0 (even CTA), b0 + 1
         const uint32_t a_mine = block_a_bytes(p, tc.b);
-        constexpr uint32_t kChunkB = 128 * kBlockK * 2;  // a CTA's weight rows of one K-chunk
-        // a stage: two chunks of both CTAs' token rows and weight halves
-        const uint32_t stage_bytes = 2 * (block_a_bytes(p, b0) + block_a_bytes(p, b0 + 1) + 2 * kChunkB);
         const int nbox = static_cast<int>(a_mine / (kRowBox * kBlockK * 2));
         const bool full_block = nbox * kRowBox == kBlockM;
         const int row0 = tc.b * kBlockM;
@@ -821,86 +838,68 @@ __device__ __forceinline__ void producer_pair(const Ctx& c, long first_tile) {
             const int c1 = 2 * j + 1;
             return kwhole >= 2 && (c1 < kwhole || (c1 == kwhole && kwhole == nk));
         };
-        // (a pair launch keeps the 128-row half boxes of the gate_up weights
-        // and expand weights in width class 1's map slot)
-        auto load_b = [&](int s, int j, uint32_t fb) {
-            uint8_t* sb = smem + s * stb + ab;
-            if (view_ok(j)) {
-                if (tc.kind == kGateUp)
-                    tma_load_5d_pair(sb, &sd.tm_bx, fb, 0, tc.cb * 128, static_cast<int>(rank), tc.e, 2 * j);
-                else
-                    tma_load_4d_pair(sb, &sd.tm_bx, fb, 0, tc.cb * 256 + static_cast<int>(rank) * 128, tc.e, 2 * j);
-                return;
-            }
-            for (int cc = 0; cc < 2; ++cc) {
-                const int k0 = (2 * j + cc) * kBlockK;
-                if (tc.kind == kGateUp)
-                    tma_load_4d_pair(sb + cc * kChunkB, &sd.tm_b[1], fb, k0, tc.cb * 128, static_cast<int>(rank),
-                                     tc.e);
-                else
-                    tma_load_3d_pair(sb + cc * kChunkB, &sd.tm_b[2], fb, k0,
-                                     tc.cb * 256 + static_cast<int>(rank) * 128, tc.e);
-            }
-        };
-        auto load_a = [&](int s, int j, uint32_t fb) {
-            uint8_t* sa = smem + s * stb;
-            if (nbox == 0) return;
-            if (full_block && view_ok(j)) {
-                tma_load_3d_pair(sa, &sd.tm_ax_full, fb, 0, row0, 2 * j);
-                return;
-            }
-            for (int cc = 0; cc < 2; ++cc) {
-                const int k0 = (2 * j + cc) * kBlockK;
-                uint8_t* ca = sa + cc * (kPairABytes / 2);
-                if (full_block)
-                    tma_load_2d_pair(ca, &sd.tm_a_full, fb, k0, row0);
-                else
-                    for (int i = 0; i < nbox; ++i)
-                        tma_load_2d_pair(ca + i * kRowBox * kBlockK * 2, &sd.tm_a, fb, k0, row0 + i * kRowBox);
-            }
-        };
-        int pre = 0;  // stages whose weight rows went out before the act wait
-        if (tc.side == 1) {
-            const int32_t* act_done = p.act_done + tc.b;
-            if (!counter_reached(act_done, gm.ncb0)) {
-                const int npre = min(nst2, nst);
-                for (; pre < npre; ++pre) {
-                    const long j = it + pre;
-                    const int s = static_cast<int>(j % nst);
-                    if (!mbar_wait(&empty[s], (static_cast<uint32_t>(j / nst) & 1u) ^ 1u, abort_flag, p.status, lim)) {
-                        ok = false;
-                        break;
-                    }
-                    if (lead) mbar_arrive_expect_tx(&full[s], stage_bytes);
-                    load_b(s, pre, mapa_shared(&full[s], 0));
-                }
-            }
-            if (ok && !wait_counter(act_done, gm.ncb0, abort_flag, p.status, lim)) ok = false;
-            if (!ok) {
-                it += pre;
-                break;
-            }
+        // the down side reads act rows, complete once the block's gate_up
+        // tiles all are (the weight rows do not depend on them)
+        if (kRows && tc.side == 1 && !wait_counter(p.act_done + tc.b, gm.ncb0, abort_flag, p.status, lim)) {
+            ok = false;
+            break;
         }
         for (int j = 0; j < nst2; ++j, ++it) {
             const int s = static_cast<int>(it % nst);
-            const uint32_t fb = mapa_shared(&full[s], 0);
-            if (j >= pre) {
-                if (!mbar_wait(&empty[s], (static_cast<uint32_t>(it / nst) & 1u) ^ 1u, abort_flag, p.status, lim)) {
-                    ok = false;
-                    break;
-                }
-                if (lead) mbar_arrive_expect_tx(&full[s], stage_bytes);
-                load_b(s, j, fb);
-            }
             if (j + 2 >= nst2) claim();
-            load_a(s, j, fb);
+            if (!stage_free(s)) {
+                ok = false;
+                break;
+            }
+            const uint32_t fb = mapa_shared(&full[s], 0);
+            if (!kRows) {
+                // (a pair launch keeps the 128-row half boxes of the gate_up
+                // weights and expand weights in width class 1's map slot)
+                arrive_stage(s, fb, 2 * kChunkB);
+                uint8_t* sb = smem + s * stb + ab;
+                if (view_ok(j)) {
+                    if (tc.kind == kGateUp)
+                        tma_load_5d_pair(sb, &sd.tm_bx, fb, 0, tc.cb * 128, static_cast<int>(rank), tc.e, 2 * j);
+                    else
+                        tma_load_4d_pair(sb, &sd.tm_bx, fb, 0, tc.cb * 256 + static_cast<int>(rank) * 128, tc.e,
+                                         2 * j);
+                } else {
+                    for (int cc = 0; cc < 2; ++cc) {
+                        const int k0 = (2 * j + cc) * kBlockK;
+                        if (tc.kind == kGateUp)
+                            tma_load_4d_pair(sb + cc * kChunkB, &sd.tm_b[1], fb, k0, tc.cb * 128,
+                                             static_cast<int>(rank), tc.e);
+                        else
+                            tma_load_3d_pair(sb + cc * kChunkB, &sd.tm_b[2], fb, k0,
+                                             tc.cb * 256 + static_cast<int>(rank) * 128, tc.e);
+                    }
+                }
+            } else {
+                arrive_stage(s, fb, 2 * a_mine);
+                uint8_t* sa = smem + s * stb;
+                if (nbox == 0) {
+                } else if (full_block && view_ok(j)) {
+                    tma_load_3d_pair(sa, &sd.tm_ax_full, fb, 0, row0, 2 * j);
+                } else {
+                    for (int cc = 0; cc < 2; ++cc) {
+                        const int k0 = (2 * j + cc) * kBlockK;
+                        uint8_t* ca = sa + cc * (kPairABytes / 2);
+                        if (full_block)
+                            tma_load_2d_pair(ca, &sd.tm_a_full, fb, k0, row0);
+                        else
+                            for (int i = 0; i < nbox; ++i)
+                                tma_load_2d_pair(ca + i * kRowBox * kBlockK * 2, &sd.tm_a, fb, k0, row0 + i * kRowBox);
+                    }
+                }
+            }
         }
         if (!ok || !p.has_lora) continue;
         const int n0 = p.blk_nad[b0], n1 = p.blk_nad[b0 + 1];
         if (n0 + n1 == 0) continue;
         // this block's LoRA tiles: every shrink tile of the block and side
         const int nmine = rank ? n1 : n0;
-        if (nmine > 0 && !wait_counter(sd.done + tc.b, (nmine + p.gsize - 1) / p.gsize, abort_flag, p.status, lim)) {
+        if (kRows && nmine > 0 &&
+            !wait_counter(sd.done + tc.b, (nmine + p.gsize - 1) / p.gsize, abort_flag, p.status, lim)) {
             ok = false;
             break;
         }
@@ -914,32 +913,37 @@ __device__ __forceinline__ void producer_pair(const Ctx& c, long first_tile) {
             const int l = min(a, b);
             const int mine = rank ? (b == l ? i1 : -1) : (a == l ? i0 : -1);
             const int s = static_cast<int>(it % nst);
-            if (!mbar_wait(&empty[s], (static_cast<uint32_t>(it / nst) & 1u) ^ 1u, abort_flag, p.status, lim)) {
+            if (!stage_free(s)) {
                 ok = false;
                 break;
             }
             const uint32_t fb = mapa_shared(&full[s], 0);
-            if (lead) mbar_arrive_expect_tx(&full[s], block_a_bytes(p, b0) + block_a_bytes(p, b0 + 1) + 2 * kChunkB);
             uint8_t* sa = smem + s * stb;
-            const int le = l * p.E_tot + tc.e;
-            if (tc.kind == kGateUp)
-                tma_load_4d_pair(sa + ab, lb, fb, 0, tc.cb * 128, static_cast<int>(rank), le);
-            else
-                tma_load_3d_pair(sa + ab, lb, fb, 0, tc.cb * 256 + static_cast<int>(rank) * 128, le);
-            if (full_block)
-                tma_load_2d_pair(sa, &sd.tm_t_full, fb, 0, mine >= 0 ? (lt0 + mine) * kBlockM : -kBlockM);
-            else
-                for (int j = 0; j < nbox; ++j)
-                    tma_load_2d_pair(sa + j * kRowBox * kBlockK * 2, &sd.tm_t, fb, 0,
-                                     mine >= 0 ? (lt0 + mine) * kBlockM + j * kRowBox : -kRowBox);
+            if (!kRows) {
+                arrive_stage(s, fb, kChunkB);
+                const int le = l * p.E_tot + tc.e;
+                if (tc.kind == kGateUp)
+                    tma_load_4d_pair(sa + ab, lb, fb, 0, tc.cb * 128, static_cast<int>(rank), le);
+                else
+                    tma_load_3d_pair(sa + ab, lb, fb, 0, tc.cb * 256 + static_cast<int>(rank) * 128, le);
+            } else {
+                arrive_stage(s, fb, a_mine);
+                if (full_block)
+                    tma_load_2d_pair(sa, &sd.tm_t_full, fb, 0, mine >= 0 ? (lt0 + mine) * kBlockM : -kBlockM);
+                else
+                    for (int j = 0; j < nbox; ++j)
+                        tma_load_2d_pair(sa + j * kRowBox * kBlockK * 2, &sd.tm_t, fb, 0,
+                                         mine >= 0 ? (lt0 + mine) * kBlockM + j * kRowBox : -kRowBox);
+            }
             i0 += a == l;
             i1 += b == l;
             ++it;
         }
     }
-    // after an abort the even CTA waits (bounded) for the stages issued: each
-    // barrier counts the bytes of both CTAs' copies; the odd CTA's copies
-    // land before the pair passes its final cluster barrier
+    // after an abort the even CTA's producers wait (bounded) for the stages
+    // issued: each barrier counts the bytes of both CTAs' copies (a stage
+    // whose other operand never went out ends the bounded wait); the odd
+    // CTA's copies land before the pair passes its final cluster barrier
     if (!ok && lead) {
         for (long j = it > nst ? it - nst : 0; j < it; ++j)
             drain_wait(&full[j % nst], static_cast<uint32_t>(j / nst) & 1u, lim);
@@ -1264,15 +1268,16 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
     const int warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
         // a stage is full once both producers' copies landed (a pair: the
-        // even CTA's one arrival counts both CTAs' bytes)
+        // even CTA's barrier counts the four producers of both CTAs)
         for (int s = 0; s < kMaxStages; ++s) {
-            mbar_init(&full[s], kPair ? 1 : 2);
+            mbar_init(&full[s], kPair ? 4 : 2);
             mbar_init(&empty[s], 1);
         }
         // a pair: the even CTA's accumulator barriers count both CTAs'
         // epilogue threads, its tile-ring barriers the readers of both
-        // (MMA lane + 4 epilogue warps; producer + 4 epilogue warps); one
-        // CTA: MMA lane, 4 epilogue warps and three producers
+        // (MMA lane + 4 epilogue warps + row producer; 2 producers + 4
+        // epilogue warps); one CTA: MMA lane, 4 epilogue warps and three
+        // producers
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
             mbar_init(&tempty[a], kPair ? 256 : 128);
@@ -1281,7 +1286,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
         mbar_init(pub, 128);
         for (int r = 0; r < kTileRing; ++r) {
             mbar_init(&tile_full[r], 1);
-            mbar_init(&tile_empty[r], kPair ? 10 : 1 + 4 + 3);
+            mbar_init(&tile_empty[r], kPair ? 12 : 1 + 4 + 3);
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -1343,7 +1348,8 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(const __grid_const
     if (warp == 0 || warp >= 6) {
         if ((threadIdx.x & 31) == 0) {
             if constexpr (kPair) {
-                if (warp == 0) producer_pair<kPairStages, kPairStageBytes, kPairABytes>(c, first_tile);
+                if (warp == 0) producer_pair<kPairStages, kPairStageBytes, kPairABytes, false>(c, first_tile);
+                if (warp == 6) producer_pair<kPairStages, kPairStageBytes, kPairABytes, true>(c, -1);
             } else {
                 // warps 0 / 7: weight operand, even / odd stages; 6 / 8: rows
                 const bool rows = warp == 6 || warp == 8;

@@ -278,6 +278,14 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// arrive (relaxed, cluster scope) on a barrier given by its cluster address,
+// raising its transaction count by `bytes` first: for a stage barrier,
+// where the bytes arrive through the async proxy and need no ordering
+__device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.relaxed.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
 __device__ __forceinline__ void st_cluster_s64(uint32_t addr, long long v) {
     asm volatile("st.shared::cluster.s64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
 }

@@ -4,7 +4,8 @@ Every computed index into a workspace or output buffer is checked before the
 store; a bad one would set MLORA_DEV_BOUNDS in the device status word and
 skip the store instead of faulting.  These tests run the layer through that
 build on shapes that exercise every tile kind, the narrow and wide tiles,
-both align methods and ragged edges: the status word must stay clean and
+both align methods, ragged edges, the CTA-pair kernel and the MXFP8 layer:
+the status word must stay clean and
 the outputs must still match the oracle.  (A stand-in for a memory checker,
 which this GPU pool does not offer.)"""
 import numpy as np
@@ -80,3 +81,52 @@ def test_mid_width_ragged():
 
 def test_shared_one_token():
     _run(wl.spec("shared", M=1))
+
+
+def _run_pair(spec, rows=None):
+    ml.mlora_set_pair_mode(True)
+    try:
+        _run(spec, rows)
+    finally:
+        ml.mlora_set_pair_mode(False)
+
+
+@pytest.mark.parametrize("over", [
+    dict(M=700, H=256, I=256, E=8, top_k=2, L=5, r=16, seed=501),             # pairs with adapters
+    dict(M=300, H=160, I=224, E=5, top_k=3, L=3, r=24, seed=502),             # partial chunks and slabs
+    dict(M=1, H=512, I=384, E=8, top_k=4, L=2, r=16, seed=506),               # every second block empty
+    dict(M=500, H=96, I=64, E=4, top_k=2, L=2, r=8, seed=508),                # chunk-by-chunk copies only
+])
+def test_pair_small_layers(over):
+    """The CTA-pair kernel (clusters of two, 256-row MMAs) through the
+    bounds-checked build."""
+    _run_pair(wl.spec("tiny", **over))
+
+
+def test_pair_prefill_sampled():
+    s = wl.spec("prefill")
+    _run_pair(s, rows=np.linspace(0, s.M - 1, 16).round().astype(np.int64))
+
+
+@pytest.mark.parametrize("name,over", [
+    ("tiny", dict(M=37, H=160, I=224, E=5, top_k=3, L=3, r=24, seed=401)),    # ragged slabs and K-chunks
+    ("decode", dict()),
+    ("shared", dict(M=1)),
+])
+def test_mxfp8_layers(name, over):
+    """The MXFP8 layer (E4M3 weights and rows, E8M0 scales) through the
+    bounds-checked build, against the oracle's MXFP8 layer."""
+    from test_gpu_mxfp8 import MxLayer
+    s = wl.spec(name, **over)
+    L = MxLayer(s)
+    ids, w = gu.gpu_route(L.d)
+    ws = torch.empty(ml.mlora_moe_workspace_size_mxfp8(s.M, s.H, s.I, s.E_tot, s.K_total,
+                                                       s.L if s.has_lora else 0, s.r if s.has_lora else 0),
+                     dtype=torch.uint8, device="cuda")
+    y = L.forward(ids, w, workspace=ws)
+    torch.cuda.synchronize()
+    status = ml.mlora_moe_read_status(ws)
+    assert not status & ml.DEV_BOUNDS, f"{name}: an index left its buffer (status {status:#x})"
+    assert status == 0
+    ids_ref, w_ref = gu.oracle_route(L.inp)
+    gu.check_y(y, L.oracle(ids_ref, w_ref), f"mxfp8 {name} (bounds-checked build)")

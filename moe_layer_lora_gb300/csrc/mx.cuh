@@ -79,41 +79,61 @@ __device__ __forceinline__ uint8_t mx_quantize32(const float (&v)[32], uint4& q0
 // each lane takes whole blocks of 32 of the bf16 row `src`, writes their
 // E4M3 codes to q_row and their scale bytes into the block's atoms
 // (atoms[kc * 512 + ...], kc = the K-chunk); the bf16 row is copied to
-// bf_row too when it is set.  Blocks of the last K-chunk past H get a zero
-// scale byte (their data reads as zero), never a stale one.
+// bf_row too when it is set.  The loads of two blocks per lane are issued
+// before either is converted; the four scale bytes of a K-chunk (lanes
+// 4j..4j+3 of one pass) go out as one 32-bit word.  Blocks of the last
+// K-chunk past H get a zero scale byte (their data reads as zero), never a
+// stale one.  Every lane of the warp must call it.
 __device__ __forceinline__ void mx_gather_row(const uint4* __restrict__ src, int H, int r, uint8_t* __restrict__ q_row,
                                               uint8_t* __restrict__ atoms, uint4* __restrict__ bf_row, int lane) {
     const int nblk = H / kMxBlock;
-    const int per_chunk = kMxChunk / kMxBlock;
-    for (int b = lane; b < nblk; b += 32) {
-        uint4 raw[4];
+    const int nchunk = (H + kMxChunk - 1) / kMxChunk;
+    const int passes = (nblk + 31) / 32;
+    const int word_off = (r % 32) * 16 + (r / 32) * 4;  // the row's 4 scale bytes in an atom
+    constexpr int kGroup = 2;
+    for (int i0 = 0; i0 < passes; i0 += kGroup) {
+        uint4 raw[kGroup][4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) raw[q] = __ldg(src + b * 4 + q);
-        if (bf_row) {
+        for (int u = 0; u < kGroup; ++u) {
+            const int b = (i0 + u) * 32 + lane;
+            if (i0 + u < passes && b < nblk) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) bf_row[b * 4 + q] = raw[q];
-        }
-        float v[32];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw[q]);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float2 t = __bfloat1622float2(h[i]);
-                v[8 * q + 2 * i] = t.x;
-                v[8 * q + 2 * i + 1] = t.y;
+                for (int q = 0; q < 4; ++q) raw[u][q] = __ldg(src + b * 4 + q);
             }
         }
-        uint4 q0, q1;
-        const uint8_t sc = mx_quantize32(v, q0, q1);
-        uint4* dq = reinterpret_cast<uint4*>(q_row + b * kMxBlock);
-        dq[0] = q0;
-        dq[1] = q1;
-        atoms[(b / per_chunk) * kMxAtom + mx_atom_byte(r, b % per_chunk)] = sc;
-    }
-    if (lane == 0) {
-        const int nchunk = (H + kMxChunk - 1) / kMxChunk;
-        for (int b = nblk; b < nchunk * per_chunk; ++b) atoms[(b / per_chunk) * kMxAtom + mx_atom_byte(r, b % per_chunk)] = 0;
+#pragma unroll
+        for (int u = 0; u < kGroup; ++u) {
+            if (i0 + u >= passes) break;  // the same for every lane
+            const int b = (i0 + u) * 32 + lane;
+            uint32_t sc = 0;
+            if (b < nblk) {
+                if (bf_row) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) bf_row[b * 4 + q] = raw[u][q];
+                }
+                float v[32];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw[u][q]);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float2 t = __bfloat1622float2(h[i]);
+                        v[8 * q + 2 * i] = t.x;
+                        v[8 * q + 2 * i + 1] = t.y;
+                    }
+                }
+                uint4 q0, q1;
+                sc = mx_quantize32(v, q0, q1);
+                uint4* dq = reinterpret_cast<uint4*>(q_row + b * kMxBlock);
+                dq[0] = q0;
+                dq[1] = q1;
+            }
+            uint32_t word = sc << (8 * (lane & 3));
+            word |= __shfl_xor_sync(0xffffffffu, word, 1);
+            word |= __shfl_xor_sync(0xffffffffu, word, 2);
+            const int kc = b / (kMxChunk / kMxBlock);
+            if ((lane & 3) == 0 && kc < nchunk) *reinterpret_cast<uint32_t*>(atoms + kc * kMxAtom + word_off) = word;
+        }
     }
 }
 #endif

@@ -24,20 +24,27 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
     const int lane = threadIdx.x & 31;
     const int warps = blockDim.x >> 5;
     const int np = *n_pad;
-    for (int p = blockIdx.x * warps + (threadIdx.x >> 5); p < np; p += gridDim.x * warps) {
+    const int stride = gridDim.x * warps;
+    int p = blockIdx.x * warps + (threadIdx.x >> 5);
+    // the next row's source slot is read one row ahead, so that its latency
+    // overlaps the current row's copy
+    int f_next = p < np && p < max_padded ? sorted[p] : S;
+    for (; p < np; p += stride) {
         if (!MLORA_IN_BOUNDS(p < max_padded, status)) break;
-        const int f = sorted[p];
+        const int f = f_next;
+        const int pn = p + stride;
+        f_next = pn < np && pn < max_padded ? sorted[pn] : S;
         if (f >= S) continue;  // padding row: never stored downstream
         const uint4* src = x + static_cast<size_t>(f / K_total) * H8;
         uint4* dst = x_perm + static_cast<size_t>(p) * H8;
-        // four independent 16-byte loads in flight per lane
-        for (int i0 = lane; i0 < H8; i0 += 128) {
-            uint4 v[4];
+        // eight independent 16-byte loads in flight per lane
+        for (int i0 = lane; i0 < H8; i0 += 256) {
+            uint4 v[8];
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
+            for (int j = 0; j < 8; ++j)
                 if (i0 + 32 * j < H8) v[j] = __ldg(src + i0 + 32 * j);
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
+            for (int j = 0; j < 8; ++j)
                 if (i0 + 32 * j < H8) dst[i0 + 32 * j] = v[j];
         }
     }

@@ -1232,18 +1232,18 @@ __device__ __forceinline__ void epilogue(const Ctx& c) {
             mbar_arrive(&tempty[acc]);
         if (publish) {
             // other CTAs read what this tile wrote with TMA: every thread
-            // orders its writes for the async proxy and arrives
-            // (release, CTA scope); one thread waits (bounded, acquire)
-            // for all 128, then a GPU-scope fence -- cumulative over the
-            // writes it has synchronised with -- and the counter bump
+            // orders its writes for the async proxy, arrives (release, CTA
+            // scope) and waits (bounded, acquire) for all 128; then one
+            // thread bumps the counter with a GPU-scope release, cumulative
+            // over the writes it has synchronised with.  Every thread
+            // waits, not only the one that publishes: a warp that ran on
+            // to its next published tile would otherwise lend that tile's
+            // arrival to this phase, completing it before a slower warp's
+            // rows are written.
             asm volatile("fence.proxy.async.global;" ::: "memory");
             mbar_arrive(pub);
-            if (warp == 2 && lane == 0) {
-                if (mbar_wait(pub, npub & 1u, abort_flag, p.status, lim)) {
-                    __threadfence();
-                    atomicAdd(publish, 1);
-                }
-            }
+            const bool all_written = mbar_wait(pub, npub & 1u, abort_flag, p.status, lim);
+            if (all_written && warp == 2 && lane == 0) red_add_release_gpu(publish, 1);
             ++npub;
         }
     }

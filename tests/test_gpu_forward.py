@@ -349,6 +349,29 @@ def test_ring_geometry_boundary(M, E, n_hot):
     gu.check_y(y, gu.oracle_forward(inp, ids, w), f"busiest expert {n_hot} slots")
 
 
+def test_poisoned_workspace_never_leaks():
+    """Every forward writes whatever it reads: with the workspace filled
+    with NaN bytes before each of eight calls, every output matches the
+    oracle.  A block whose rows another CTA consumes (the act rows of the
+    down projection, the LoRA tiles of the expands) is published only once
+    all four epilogue warps wrote their rows, whichever warp runs ahead."""
+    M, E, k = 1024, 128, 2
+    s = wl.spec("tiny", M=M, H=64, I=136, E=E, top_k=k, L=3, r=16, seed=131)
+    inp = wl.make(s, device="cuda")
+    d = gu.DeviceInputs(inp)
+    ids_h, w_h = _hot_expert_ids(M, E, k, 32, seed=1)
+    ids, w = torch.from_numpy(ids_h).cuda(), torch.from_numpy(w_h).cuda()
+    y_ref = gu.oracle_forward(inp, ids_h, w_h)
+    ws = torch.empty(ml.mlora_moe_workspace_size(M, s.H, s.I, s.E_tot, s.K_total, s.L, s.r), dtype=torch.uint8,
+                     device="cuda")
+    for call in range(8):
+        ws.fill_(0xFF)
+        y = gu.gpu_forward(d, ids, w, workspace=ws)
+        torch.cuda.synchronize()
+        assert ml.mlora_moe_read_status(ws) == 0, call
+        gu.check_y(y, y_ref, f"poisoned workspace, call {call}")
+
+
 def test_graph_replay_switches_tile_geometry():
     """One captured forward, replayed on routings that move the kernel
     between its tile widths (wide/narrow, chosen from the padded block

@@ -140,6 +140,34 @@ def test_mxfp8_decode_full():
     _check_layer(wl.spec("decode"))
 
 
+def test_mxfp8_poisoned_workspace_never_leaks():
+    """The MXFP8 layer on a workspace filled with NaN bytes before each of
+    eight calls (128 experts, the busiest with 32 slots): every output
+    matches the oracle, so no call reads a row before it is published."""
+    M, E, k = 1024, 128, 2
+    L = MxLayer(wl.spec("tiny", M=M, H=128, I=160, E=E, top_k=k, L=3, r=16, seed=132))
+    ids_h = ((np.arange(M)[:, None] * k + np.arange(k)[None, :]) % 64).astype(np.int32)
+    w_h = np.full((M, k), 1.0 / k, np.float32)
+    ids, w = torch.from_numpy(ids_h).cuda(), torch.from_numpy(w_h).cuda()
+    y_ref = L.oracle(ids_h, w_h)
+    s = L.spec
+    ws = torch.empty(ml.mlora_moe_workspace_size_mxfp8(M, s.H, s.I, s.E_tot, s.K_total, s.L, s.r),
+                     dtype=torch.uint8, device="cuda")
+    for call in range(8):
+        ws.fill_(0xFF)
+        y = L.forward(ids, w, workspace=ws)
+        torch.cuda.synchronize()
+        assert ml.mlora_moe_read_status(ws) == 0, call
+        gu.check_y(y, y_ref, f"mxfp8 poisoned workspace, call {call}")
+
+
+@pytest.mark.parametrize("M", [2, 7])
+def test_mxfp8_decode_few_tokens(M):
+    """A handful of tokens on the decode layer: blocks of one or two rows,
+    a 192-row tile per slab, adapters on most slots."""
+    _check_layer(wl.spec("decode", M=M), label=f"mxfp8 decode M={M}")
+
+
 @pytest.mark.parametrize("M", [1, 32, 128])
 def test_mxfp8_shared_full(M):
     _check_layer(wl.spec("shared", M=M))

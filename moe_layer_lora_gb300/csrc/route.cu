@@ -9,7 +9,7 @@
 // "교훈" item 2).  Ranking: descending key, ties to the lower expert id.
 //
 // Each lane holds experts lane, lane+32, ... in registers (coalesced row
-// read); every selection step is one butterfly arg-max over the warp.
+// read); every selection step is one arg-max over the warp.
 // Non-finite input never yields an id outside [0, E): a NaN key ranks
 // last (ties among them to the lower id); the weights of such a token are
 // then NaN as well.
@@ -23,6 +23,13 @@ namespace {
 
 __device__ __forceinline__ bool better(float ka, int ia, float kb, int ib) {
     return ka > kb || (ka == kb && ia < ib);
+}
+
+// A non-NaN float as an unsigned integer of the same order (-0 folded into
+// +0, which compare equal as floats), for the warp's integer max reduction.
+__device__ __forceinline__ unsigned ordered(float k) {
+    const unsigned u = __float_as_uint(k == 0.0f ? 0.0f : k);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
 template <int VPL>
@@ -72,15 +79,11 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ lo
                 bi = e;
             }
         }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const float ok = __shfl_xor_sync(0xffffffffu, bk, off);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-            if (better(ok, oi, bk, bi)) {
-                bk = ok;
-                bi = oi;
-            }
-        }
+        // the warp's arg-max: the largest key, then the lowest id among
+        // the lanes holding it (two warp reductions)
+        const unsigned ok = ordered(bk);
+        const unsigned kmax = __reduce_max_sync(0xffffffffu, ok);
+        bi = static_cast<int>(__reduce_min_sync(0xffffffffu, ok == kmax ? static_cast<unsigned>(bi) : 0x7fffffffu));
         const int owner = bi & 31, vsel = bi >> 5;
         float r = 0.f;
 #pragma unroll

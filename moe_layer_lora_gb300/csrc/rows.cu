@@ -62,19 +62,21 @@ __global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__
         const int m = static_cast<int>(idx / H8);
         const int c = static_cast<int>(idx - static_cast<long>(m) * H8);
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        // slots in groups of four: their loads are issued together, the sum
-        // still runs over k in ascending order
-        for (int k0 = 0; k0 < K_total; k0 += 4) {
-            float4 raw[4][2];
-            float wk[4];
-            bool live[4];
+        // slots in groups of eight, every load of a group issued at once --
+        // ids, weights and slot rows, so that a group costs one memory
+        // round trip (a dropped slot's row lies inside y_slot as well; it is
+        // read and left out of the sum); the sum still runs over k in
+        // ascending order
+        for (int k0 = 0; k0 < K_total; k0 += 8) {
+            float4 raw[8][2];
+            float wk[8];
+            int e[8];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < 8; ++j) {
                 const long f = static_cast<long>(m) * K_total + k0 + j;
-                const int e = k0 + j < K_total ? __ldg(topk_ids + f) : -1;
-                live[j] = static_cast<unsigned>(e) < static_cast<unsigned>(E_tot);  // else a dropped slot
-                wk[j] = 0.f;
-                if (live[j]) {
+                e[j] = -1;
+                if (k0 + j < K_total) {
+                    e[j] = __ldg(topk_ids + f);
                     wk[j] = __ldg(topk_w + f);
                     const float4* src = y_slot + (f * H8 + c) * 2;
                     raw[j][0] = __ldcs(src);
@@ -82,8 +84,9 @@ __global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__
                 }
             }
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                if (!live[j]) continue;
+            for (int j = 0; j < 8; ++j) {
+                // a dropped slot (id outside [0, E_tot)) adds nothing
+                if (static_cast<unsigned>(e[j]) >= static_cast<unsigned>(E_tot)) continue;
                 const float v[8] = {raw[j][0].x, raw[j][0].y, raw[j][0].z, raw[j][0].w,
                                     raw[j][1].x, raw[j][1].y, raw[j][1].z, raw[j][1].w};
 #pragma unroll

@@ -71,6 +71,30 @@ def test_pair_equals_single_cta(over):
                f"pair {over}")
 
 
+def test_pair_poisoned_workspace_never_leaks():
+    """Pair mode on a workspace filled with NaN bytes before each of eight
+    calls (adapters, many small blocks): every call equals the single-CTA
+    kernel on a clean workspace, so no CTA of either kind reads a block's
+    act rows or LoRA tiles before all four epilogue warps wrote them."""
+    s = wl.spec("tiny", M=700, H=256, I=256, E=8, top_k=2, L=5, r=16, seed=501)
+    inp = wl.make(s, device="cuda")
+    d = gu.DeviceInputs(inp)
+    ids, w = gu.gpu_route(d)
+    y_single = _forward(d, ids, w, False)
+    ml.mlora_set_pair_mode(True)
+    try:
+        ws = torch.empty(ml.mlora_moe_workspace_size(s.M, s.H, s.I, s.E_tot, s.K_total, s.L, s.r),
+                         dtype=torch.uint8, device="cuda")
+        for call in range(8):
+            ws.fill_(0xFF)
+            y = gu.gpu_forward(d, ids, w, workspace=ws)
+            torch.cuda.synchronize()
+            assert ml.mlora_moe_read_status(ws) == 0, call
+            assert torch.equal(y, y_single), call
+    finally:
+        ml.mlora_set_pair_mode(False)
+
+
 def test_prefill_in_pairs_equals_single_cta():
     """The prefill layer (32 768 slots over 32 experts, adapters) in pair
     mode gives the single-CTA kernel's bits, which the full-row prefill test

@@ -37,7 +37,7 @@ constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kRounds = kSmallMaxSlots / kThreads;  // slots per thread
 constexpr int kMaxSmem = 227 * 1024;
-constexpr int kScratch = 64;  // ints: scan scratch [0, 17), flags [48], largest count [49], gather list length [50]
+constexpr int kScratch = 64;  // ints: scan scratch [0, 34), flags [48], largest count [49], gather list length [50]
 static_assert(kRounds * kThreads == kSmallMaxSlots, "slots per thread");
 
 // Exclusive scan of one int per thread over the CTA; the CTA total goes to
@@ -70,6 +70,86 @@ __device__ int cta_exclusive_scan(int v, int* scratch, int* total) {
     return excl;
 }
 
+// The same for two values at once (one set of barriers); scratch holds
+// 2 * (kWarps + 1) ints.
+__device__ void cta_exclusive_scan2(int va, int vb, int* scratch, int* ea, int* eb, int* ta, int* tb) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int ia = va, ib = vb;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int na = __shfl_up_sync(0xffffffffu, ia, off);
+        const int nb = __shfl_up_sync(0xffffffffu, ib, off);
+        if (lane >= off) {
+            ia += na;
+            ib += nb;
+        }
+    }
+    int* sa = scratch;
+    int* sb = scratch + kWarps + 1;
+    if (lane == 31) {
+        sa[warp] = ia;
+        sb[warp] = ib;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const int a = lane < kWarps ? sa[lane] : 0;
+        const int b = lane < kWarps ? sb[lane] : 0;
+        int xa = a, xb = b;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int na = __shfl_up_sync(0xffffffffu, xa, off);
+            const int nb = __shfl_up_sync(0xffffffffu, xb, off);
+            if (lane >= off) {
+                xa += na;
+                xb += nb;
+            }
+        }
+        if (lane < kWarps) {
+            sa[lane] = xa - a;
+            sb[lane] = xb - b;
+        }
+        if (lane == kWarps - 1) {
+            sa[kWarps] = xa;
+            sb[kWarps] = xb;
+        }
+    }
+    __syncthreads();
+    *ea = sa[warp] + ia - va;
+    *eb = sb[warp] + ib - vb;
+    *ta = sa[kWarps];
+    *tb = sb[kWarps];
+    __syncthreads();
+}
+
+// x / block_m and rounding up to a multiple of it, for x >= 0: a shift when
+// block_m is a power of two (the forward's 128), else a division.
+struct BlockDiv {
+    int bm, sh;
+    __device__ int div(int x) const { return sh >= 0 ? x >> sh : x / bm; }
+    __device__ int up(int x) const { return div(x + bm - 1) * bm; }
+};
+
+__device__ __forceinline__ BlockDiv block_div(int b) { return BlockDiv{b, (b & (b - 1)) == 0 ? __ffs(b) - 1 : -1}; }
+
+// Position of the j-th (from 0) set bit of m; j < popc(m).  A binary search
+// over halves of the remaining window by their population counts.
+__device__ __forceinline__ int nth_set_bit(unsigned m, int j) {
+    int pos = 0;
+#pragma unroll
+    for (int w = 16; w > 0; w >>= 1) {
+        const unsigned low = m & ((1u << w) - 1u);
+        const int c = __popc(low);
+        if (j >= c) {
+            j -= c;
+            m >>= w;
+            pos += w;
+        } else {
+            m = low;
+        }
+    }
+    return pos;
+}
+
 template <bool kWithLora, bool kGather>
 __global__ void __launch_bounds__(kThreads, 1)
     align_small_kernel(const int32_t* __restrict__ ids, int S, int E_tot, int BM, int max_padded,
@@ -83,8 +163,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     int* first = tot + E_tot;            // [E_tot] padded start of each expert
     int* scratch = first + E_tot;        // [kScratch]
     int* nad_s = scratch + kScratch;     // with adapters: [max_padded / BM] adapters per block
-    int* glist = nad_s + (kWithLora ? max_padded / BM : 0);  // gather: [2 * S] (position, token) of this CTA's rows
-    uint16_t* st_sorted = reinterpret_cast<uint16_t*>(glist + (kGather ? 2 * S : 0));  // [max_padded]
+    const BlockDiv bd = block_div(BM);
+    const int max_blocks = bd.div(max_padded);
+    int* glist = nad_s + (kWithLora ? max_blocks : 0);  // gather: [2 * S] (position, token) of this CTA's rows
+    int* ints_end = glist + (kGather ? 2 * S : 0);
+    // (8-byte aligned: the output sweep reads four entries at a time)
+    uint16_t* st_sorted = reinterpret_cast<uint16_t*>(ints_end + ((ints_end - smem_i) & 1));  // [max_padded]
     int16_t* st_lora = reinterpret_cast<int16_t*>(st_sorted + max_padded);            // with adapters: [max_padded]
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const bool writer = blockIdx.x == 0;  // CTA-uniform: the CTA that writes the sort's outputs
@@ -112,8 +196,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         scratch[50] = 0;
     }
     // the forward's status word, counts and per-block counters start at zero
-    if (writer)
+    if (writer) {
         for (int i = tid; i < ex.zero_words; i += kThreads) ex.zero[i] = 0u;
+        // every position starts as padding (the sentinel id S, no adapter);
+        // the slots' positions are written over it below
+        if ((max_padded & 1) == 0) {
+            uint32_t* ss2 = reinterpret_cast<uint32_t*>(st_sorted);
+            for (int i = tid; i < max_padded / 2; i += kThreads) ss2[i] = static_cast<uint32_t>(S) * 0x10001u;
+            if (kWithLora) {
+                uint32_t* sl2 = reinterpret_cast<uint32_t*>(st_lora);
+                for (int i = tid; i < max_padded / 2; i += kThreads) sl2[i] = 0xFFFFFFFFu;
+            }
+        } else {
+            for (int i = tid; i < max_padded; i += kThreads) {
+                st_sorted[i] = static_cast<uint16_t>(S);
+                if (kWithLora) st_lora[i] = -1;
+            }
+        }
+    }
     __syncthreads();
 
     // 1. ranks within the warp, round by round in slot order
@@ -135,23 +235,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncthreads();
 
-    // 2. per expert: each warp's first offset (exclusive over warps, in
-    //    place), the total and the padded size; thread t takes experts 2t
-    //    and 2t+1 (E_tot <= 1024), then one scan of the padded sizes
+    // 2. per expert: each warp's first offset (exclusive over the warps
+    //    that hold slots, in place; all of an expert's counts read before
+    //    any is written), the total and the padded size; thread t takes
+    //    experts 2t and 2t+1 (E_tot <= 1024), then one scan of the padded
+    //    sizes
+    const int nw = min(kWarps, (S + per_warp - 1) / per_warp);  // warps holding slots
     int c_e[2] = {0, 0}, pad_e[2] = {0, 0};
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
         const int e = 2 * tid + q;
         if (e < E_tot) {
+            int t[kWarps];
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) t[w] = w < nw ? wcnt[w * E_tot + e] : 0;
             int run = 0;
+#pragma unroll
             for (int w = 0; w < kWarps; ++w) {
-                const int t = wcnt[w * E_tot + e];
-                wcnt[w * E_tot + e] = run;
-                run += t;
+                if (w < nw) wcnt[w * E_tot + e] = run;
+                run += t[w];
             }
             tot[e] = run;
             c_e[q] = run;
-            pad_e[q] = (run + BM - 1) / BM * BM;
+            pad_e[q] = bd.up(run);
             if (run > 0) atomicMax(&scratch[49], run);
         }
     }
@@ -165,10 +271,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         first[e] = s_e;
         if (writer) {
             // the block -> expert map and the real rows of each block
-            for (int b = s_e / BM; b < (s_e + pad_e[q]) / BM; ++b) {
-                if (!MLORA_IN_BOUNDS(b < max_padded / BM, status)) break;
+            const int b0 = bd.div(s_e);
+            for (int b = b0; b < bd.div(s_e + pad_e[q]); ++b) {
+                if (!MLORA_IN_BOUNDS(b < max_blocks, status)) break;
                 expert_ids[b] = e;
-                if (ex.blk_rows) ex.blk_rows[b] = min(BM, c_e[q] - (b - s_e / BM) * BM);
+                if (ex.blk_rows) ex.blk_rows[b] = min(BM, c_e[q] - (b - b0) * BM);
             }
         }
     }
@@ -177,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             *n_pad_out = total;
             if (ex.max_rows) *ex.max_rows = min(scratch[49], BM);
         }
-        for (int b = total / BM + tid; b < max_padded / BM; b += kThreads) expert_ids[b] = -1;
+        for (int b = bd.div(total) + tid; b < max_blocks; b += kThreads) expert_ids[b] = -1;
     }
     __syncthreads();
 
@@ -208,17 +315,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             glist[2 * i + 1] = f / K_total;
         }
     }
-    // the padding of each expert's last block, one warp per expert
-    if (writer)
-        for (int e = warp; e < E_tot; e += kWarps) {
-            const int n = tot[e];
-            const int pad_end = first[e] + (n + BM - 1) / BM * BM;
-            for (int p = first[e] + n + lane; p < pad_end; p += 32) {
-                if (!MLORA_IN_BOUNDS(p < max_padded, status)) break;
-                st_sorted[p] = static_cast<uint16_t>(S);
-                if (kWithLora) st_lora[p] = -1;
-            }
-        }
     __syncthreads();
 
     // 4. this CTA's x rows into their sorted positions: one warp per row,
@@ -253,21 +349,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (!writer) return;
 
-    // 5. the sorted ids (and adapters) out in one coalesced sweep, the
-    //    sentinel tail
-    for (int p = tid; p < total; p += kThreads) {
-        sorted[p] = st_sorted[p];
-        if (kWithLora) ex.lora_of[p] = st_lora[p];
+    // 5. the sorted ids (padding and the tail past the last block
+    //    included) and the adapters of the used positions out in coalesced
+    //    sweeps, four entries per thread and step where alignment allows
+    const bool vec = (max_padded & 3) == 0 && (total & 3) == 0 &&
+                     ((reinterpret_cast<uintptr_t>(sorted) |
+                       (kWithLora ? reinterpret_cast<uintptr_t>(ex.lora_of) : uintptr_t(0))) & 15) == 0;
+    if (vec) {
+        const uint2* s4 = reinterpret_cast<const uint2*>(st_sorted);
+        for (int i = tid; i < max_padded / 4; i += kThreads) {
+            const uint2 v = s4[i];
+            reinterpret_cast<int4*>(sorted)[i] = make_int4(static_cast<int>(v.x & 0xFFFFu), static_cast<int>(v.x >> 16),
+                                                           static_cast<int>(v.y & 0xFFFFu), static_cast<int>(v.y >> 16));
+        }
+        if (kWithLora) {
+            const uint2* l4 = reinterpret_cast<const uint2*>(st_lora);
+            for (int i = tid; i < total / 4; i += kThreads) {
+                const uint2 v = l4[i];
+                reinterpret_cast<int4*>(ex.lora_of)[i] =
+                    make_int4(static_cast<int16_t>(v.x & 0xFFFFu), static_cast<int16_t>(v.x >> 16),
+                              static_cast<int16_t>(v.y & 0xFFFFu), static_cast<int16_t>(v.y >> 16));
+            }
+        }
+    } else {
+        for (int p = tid; p < max_padded; p += kThreads) {
+            sorted[p] = st_sorted[p];
+            if (kWithLora && p < total) ex.lora_of[p] = st_lora[p];
+        }
     }
-    for (int p = total + tid; p < max_padded; p += kThreads) sorted[p] = S;
     if (!kWithLora) {
         if (tid == 0 && *flags && status) atomicOr(status, static_cast<uint32_t>(*flags));
         return;
     }
 
-    // 6. distinct adapters of each block (ascending), one warp per block
+    // 6. distinct adapters of each block (ascending), one warp per block:
+    //    with at most 64 adapters the block's set as a 64-bit mask, whose
+    //    j-th member lane j writes; else one warp minimum per adapter
     constexpr int kMaxPerLane = MLORA_FORWARD_BLOCK_M / 32;
-    const int nblocks = total / BM;
+    const int nblocks = bd.div(total);
     for (int b = warp; b < nblocks; b += kWarps) {
         int mine[kMaxPerLane];
 #pragma unroll
@@ -275,19 +394,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int r = lane + 32 * i;
             mine[i] = r >= BM ? -1 : st_lora[b * BM + r];
         }
-        int prev = -1, count = 0;
-        for (;;) {
-            int cand = 0x7fffffff;
+        int count = 0;
+        if (ex.L <= 64) {
+            unsigned lo = 0u, hi = 0u;
 #pragma unroll
-            for (int i = 0; i < kMaxPerLane; ++i)
-                if (mine[i] > prev && mine[i] < cand) cand = mine[i];
+            for (int i = 0; i < kMaxPerLane; ++i) {
+                const int l = mine[i];
+                if (l >= 0 && l < 32) lo |= 1u << l;
+                if (l >= 32) hi |= 1u << (l - 32);
+            }
+            lo = __reduce_or_sync(0xffffffffu, lo);
+            hi = __reduce_or_sync(0xffffffffu, hi);
+            const int nlo = __popc(lo);
+            count = nlo + __popc(hi);
+            if (!MLORA_IN_BOUNDS(count <= ex.cap, status)) count = ex.cap;
+            for (int j = lane; j < count; j += 32)
+                ex.blk_lora[static_cast<long>(b) * ex.cap + j] = j < nlo ? nth_set_bit(lo, j) : 32 + nth_set_bit(hi, j - nlo);
+        } else {
+            int prev = -1;
+            for (;;) {
+                int cand = 0x7fffffff;
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) cand = min(cand, __shfl_xor_sync(0xffffffffu, cand, off));
-            if (cand == 0x7fffffff) break;
-            if (!MLORA_IN_BOUNDS(count < ex.cap, status)) break;
-            if (lane == 0) ex.blk_lora[static_cast<long>(b) * ex.cap + count] = cand;
-            ++count;
-            prev = cand;
+                for (int i = 0; i < kMaxPerLane; ++i)
+                    if (mine[i] > prev && mine[i] < cand) cand = mine[i];
+                cand = static_cast<int>(__reduce_min_sync(0xffffffffu, static_cast<unsigned>(cand)));
+                if (cand == 0x7fffffff) break;
+                if (!MLORA_IN_BOUNDS(count < ex.cap, status)) break;
+                if (lane == 0) ex.blk_lora[static_cast<long>(b) * ex.cap + count] = cand;
+                ++count;
+                prev = cand;
+            }
         }
         if (lane == 0) {
             ex.blk_nad[b] = count;
@@ -304,9 +440,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int b = cb + tid;
         const int v = b < nblocks ? nad_s[b] : 0;
         const int ng = (v + ex.gsize - 1) / ex.gsize;
-        int lt_chunk, gt_chunk;
-        const int lt_excl = cta_exclusive_scan(v, scratch, &lt_chunk);
-        const int gt_excl = cta_exclusive_scan(ng, scratch, &gt_chunk);
+        int lt_chunk, gt_chunk, lt_excl, gt_excl;
+        cta_exclusive_scan2(v, ng, scratch, &lt_excl, &gt_excl, &lt_chunk, &gt_chunk);
         if (b < nblocks) {
             ex.blk_lt_start[b] = run_lt + lt_excl;
             for (int j = 0; j < ng; ++j) {
@@ -344,9 +479,10 @@ cudaError_t launch_variant(int variant, const cudaLaunchConfig_t& cfg, const int
 }  // namespace
 
 size_t align_small_smem(long S, int E_tot, int block_m, long max_padded, bool with_lora, bool gather) {
-    return sizeof(int) * (static_cast<size_t>(kWarps + 2) * E_tot + kScratch +
-                          (with_lora ? static_cast<size_t>(max_padded / block_m) : 0) +
-                          (gather ? 2 * static_cast<size_t>(S) : 0)) +
+    size_t ints = static_cast<size_t>(kWarps + 2) * E_tot + kScratch +
+                  (with_lora ? static_cast<size_t>(max_padded / block_m) : 0) + (gather ? 2 * static_cast<size_t>(S) : 0);
+    ints += ints & 1;  // the staged ids start on an 8-byte boundary
+    return sizeof(int) * ints +
            (sizeof(uint16_t) + (with_lora ? sizeof(int16_t) : 0)) * static_cast<size_t>(max_padded);
 }
 

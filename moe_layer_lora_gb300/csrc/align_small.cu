@@ -173,6 +173,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const bool writer = blockIdx.x == 0;  // CTA-uniform: the CTA that writes the sort's outputs
     int* flags = scratch + 48;
+    if (kGather) {
+        // the x rows this CTA copies are known before the ids are (slot f
+        // reads token f / K_total): start them into L2 while the routing
+        // kernel still runs (a prefetch reads nothing stale into a result)
+        const int lines = (H8 * 16 + 127) / 128;
+        const int nrows = (S - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
+        for (int i = tid; i < nrows * lines; i += kThreads) {
+            const int f = static_cast<int>(blockIdx.x) + (i / lines) * static_cast<int>(gridDim.x);
+            const char* line = reinterpret_cast<const char*>(x + static_cast<size_t>(f / K_total) * H8) + (i % lines) * 128;
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(line));
+        }
+    }
     griddep_wait();
     griddep_launch_dependents();
 

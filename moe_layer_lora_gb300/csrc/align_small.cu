@@ -22,7 +22,11 @@
 // The grid has several CTAs when the forward asks for the row gather: each
 // CTA computes the same (cheap) sort, CTA 0 alone writes the sort's outputs,
 // and every CTA copies the x rows of its share of the slots into their
-// sorted positions -- one launch and one dependency instead of two.
+// sorted positions -- one launch and one dependency instead of two.  Those
+// rows depend on slot numbers only, so each CTA starts them into L2 before
+// its grid wait, while the routing kernel still runs.  With adapters, a
+// block's distinct adapters come from a 64-bit set when there are at most
+// 64 adapters (one warp minimum per adapter otherwise).
 #include <algorithm>
 #include <atomic>
 

@@ -156,6 +156,24 @@ def test_wait_timeout_is_reported_and_the_context_recovers():
     gu.check_y(y, gu.oracle_forward(inp, ids_ref, w_ref), "after a timed-out forward")
 
 
+@pytest.mark.parametrize("L", [64, 65])
+def test_block_adapter_sets_word_edges(L):
+    """Blocks holding adapters on both sides of the 32-adapter word boundary
+    and the last adapter id, with tokens without an adapter between them:
+    a block's adapter list comes from a 64-bit set when there are at most 64
+    adapters, and from one warp minimum per adapter beyond."""
+    s = wl.spec("tiny", M=40, H=64, I=64, E=2, top_k=1, L=L, r=8, seed=611 + L)
+    inp = wl.make(s, device="cuda")
+    gu.assert_unambiguous(inp)
+    idx = np.array([(0, 31, 32, L - 1, -1, 1, 30, 33)[i % 8] for i in range(s.M)], np.int32)
+    d = gu.DeviceInputs(inp)
+    ids, w = gu.gpu_route(d)
+    y = gu.gpu_forward(d, ids, w, idx=torch.from_numpy(idx).cuda())
+    torch.cuda.synchronize()
+    ids_ref, w_ref = gu.oracle_route(inp)
+    gu.check_y(y, gu.oracle_forward(inp, ids_ref, w_ref, idx=idx), f"adapter sets L={L}")
+
+
 def test_bad_device_values_are_flagged():
     """Out-of-range adapter ids act as 'no adapter', out-of-range expert ids
     drop their slot; both set a bit of the device status word."""

@@ -65,35 +65,97 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ lo
     int32_t* oid = ids + static_cast<size_t>(token) * KT;
     float* ow = w + static_cast<size_t>(token) * KT;
 
-    uint32_t taken = 0;
     float my_raw[2] = {0.f, 0.f};  // raw logit of slots k = lane and k = lane + 32
     int my_id[2] = {0, 0};
-    for (int k = 0; k < top_k; ++k) {
-        float bk = -INFINITY;
-        int bi = 0x7fffffff;
+    if constexpr (VPL <= 8) {
+        // each lane's candidates as a queue, best first (descending key,
+        // then ascending id; ids ascend with v, so a stable sort keeps equal
+        // keys in id order).  A selection is the head of the lane whose head
+        // is the warp's best -- the largest key, then (only when lanes tie)
+        // the lowest id -- and only that lane's queue moves.  Slots past E
+        // rank below every key.
+        unsigned q_ok[VPL];
+        int q_id[VPL];
+        float q_raw[VPL];
 #pragma unroll
         for (int v = 0; v < VPL; ++v) {
             const int e = lane + 32 * v;
-            if (e < E && !((taken >> v) & 1u) && better(key[v], e, bk, bi)) {
-                bk = key[v];
-                bi = e;
+            q_ok[v] = e < E ? ordered(key[v]) : 0u;
+            q_id[v] = e;
+            q_raw[v] = raw[v];
+        }
+#pragma unroll
+        for (int i = 1; i < VPL; ++i) {
+#pragma unroll
+            for (int j = i; j > 0; --j) {
+                if (q_ok[j] > q_ok[j - 1]) {
+                    const unsigned to = q_ok[j];
+                    const int ti = q_id[j];
+                    const float tr = q_raw[j];
+                    q_ok[j] = q_ok[j - 1];
+                    q_id[j] = q_id[j - 1];
+                    q_raw[j] = q_raw[j - 1];
+                    q_ok[j - 1] = to;
+                    q_id[j - 1] = ti;
+                    q_raw[j - 1] = tr;
+                }
             }
         }
-        // the warp's arg-max: the largest key, then the lowest id among
-        // the lanes holding it (two warp reductions)
-        const unsigned ok = ordered(bk);
-        const unsigned kmax = __reduce_max_sync(0xffffffffu, ok);
-        bi = static_cast<int>(__reduce_min_sync(0xffffffffu, ok == kmax ? static_cast<unsigned>(bi) : 0x7fffffffu));
-        const int owner = bi & 31, vsel = bi >> 5;
-        float r = 0.f;
+        for (int k = 0; k < top_k; ++k) {
+            const unsigned kmax = __reduce_max_sync(0xffffffffu, q_ok[0]);
+            const unsigned tied = __ballot_sync(0xffffffffu, q_ok[0] == kmax);
+            int owner;
+            if (__popc(tied) == 1)  // the same for every lane
+                owner = __ffs(tied) - 1;
+            else
+                owner = static_cast<int>(
+                    __reduce_min_sync(0xffffffffu, q_ok[0] == kmax ? static_cast<unsigned>(q_id[0]) : 0xffffffffu) &
+                    31u);
+            const int sid = __shfl_sync(0xffffffffu, q_id[0], owner);
+            const float sraw = __shfl_sync(0xffffffffu, q_raw[0], owner);
+            if ((k & 31) == lane) {
+                my_raw[k >> 5] = sraw;
+                my_id[k >> 5] = sid;
+            }
+            if (lane == owner) {
 #pragma unroll
-        for (int v = 0; v < VPL; ++v)
-            if (v == vsel) r = raw[v];
-        r = __shfl_sync(0xffffffffu, r, owner);
-        if (lane == owner) taken |= 1u << vsel;
-        if ((k & 31) == lane) {
-            my_raw[k >> 5] = r;
-            my_id[k >> 5] = bi;
+                for (int v = 0; v + 1 < VPL; ++v) {
+                    q_ok[v] = q_ok[v + 1];
+                    q_id[v] = q_id[v + 1];
+                    q_raw[v] = q_raw[v + 1];
+                }
+                q_ok[VPL - 1] = 0u;
+            }
+        }
+    } else {
+        uint32_t taken = 0;
+        for (int k = 0; k < top_k; ++k) {
+            float bk = -INFINITY;
+            int bi = 0x7fffffff;
+#pragma unroll
+            for (int v = 0; v < VPL; ++v) {
+                const int e = lane + 32 * v;
+                if (e < E && !((taken >> v) & 1u) && better(key[v], e, bk, bi)) {
+                    bk = key[v];
+                    bi = e;
+                }
+            }
+            // the warp's arg-max: the largest key, then the lowest id among
+            // the lanes holding it (two warp reductions)
+            const unsigned ok = ordered(bk);
+            const unsigned kmax = __reduce_max_sync(0xffffffffu, ok);
+            bi = static_cast<int>(__reduce_min_sync(0xffffffffu, ok == kmax ? static_cast<unsigned>(bi) : 0x7fffffffu));
+            const int owner = bi & 31, vsel = bi >> 5;
+            float r = 0.f;
+#pragma unroll
+            for (int v = 0; v < VPL; ++v)
+                if (v == vsel) r = raw[v];
+            r = __shfl_sync(0xffffffffu, r, owner);
+            if (lane == owner) taken |= 1u << vsel;
+            if ((k & 31) == lane) {
+                my_raw[k >> 5] = r;
+                my_id[k >> 5] = bi;
+            }
         }
     }
 
